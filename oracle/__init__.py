@@ -1,0 +1,251 @@
+"""fp64 CPU oracle for exact softmax attention -- TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, the smoke check and the benchmark's CPU-baseline leg may
+import this package.  The library's compute path never does, and nothing here
+imports the library.
+
+``oracle.c`` holds the arithmetic (see its header for the definition it
+follows); this module compiles it with gcc, loads it with ctypes, widens the
+rounded bf16/fp16 inputs to float64 exactly and marshals arrays.  It also
+holds the oracle's own conversion of a packed variable-length batch into the
+padded batch plus key_padding_mask that the pages' MHA module takes
+(lei6393.com training-integration page, §2.5): the oracle evaluates the padded
+form, an independent route to the packed result the CUDA path produces.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import List, Optional, Sequence, Tuple
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(_HERE, "oracle.c")
+LIB = os.path.join(_HERE, "liboracle.so")
+
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False, src: str = SRC, out: str = LIB) -> str:
+    """Compile ``src`` into the shared library ``out`` (gcc, OpenMP if present)."""
+    if not force and out == LIB and os.path.exists(out) and os.path.getmtime(out) >= os.path.getmtime(src):
+        return out
+    base = ["gcc", "-O2", "-fPIC", "-shared", "-std=c11", "-Wall", "-o", out, src, "-lm"]
+    try:
+        subprocess.run(base[:1] + ["-fopenmp"] + base[1:], check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base, check=True, capture_output=True)
+    return out
+
+
+def _load(path: str = LIB):
+    lib = ctypes.CDLL(path)
+    dp = ctypes.POINTER(ctypes.c_double)
+    u8p = ctypes.POINTER(ctypes.c_ubyte)
+    ip = ctypes.POINTER(ctypes.c_int)
+    I, D = ctypes.c_int, ctypes.c_double
+    lib.oracle_attention.argtypes = [dp, dp, dp, u8p, dp, dp, dp, I, I, I, I, I, I, I, D]
+    lib.oracle_attention.restype = I
+    lib.oracle_attention_rows.argtypes = [dp, dp, dp, u8p, ip, I, dp, dp, I, I, I, I, I, I, I, D]
+    lib.oracle_attention_rows.restype = I
+    lib.oracle_online_rows.argtypes = [dp, dp, dp, u8p, ip, I, dp, dp, I, I, I, I, I, I, I, D, I, I, dp]
+    lib.oracle_online_rows.restype = I
+    lib.oracle_num_threads.argtypes = []
+    lib.oracle_num_threads.restype = I
+    return lib
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            _lib = _load()
+    return _lib
+
+
+def load_variant(path: str):
+    """Load another build of the oracle source (used to plant mistakes)."""
+    return _load(path)
+
+
+def num_threads() -> int:
+    return int(lib().oracle_num_threads())
+
+
+# --------------------------------------------------------------------------
+# marshalling
+# --------------------------------------------------------------------------
+
+def f64(x) -> np.ndarray:
+    """Widen a tensor or array to a contiguous float64 numpy array.  bf16 and
+    fp16 values are exactly representable in float64."""
+    try:
+        import torch
+
+        if isinstance(x, torch.Tensor):
+            return np.ascontiguousarray(x.detach().to("cpu", torch.float64).numpy())
+    except ImportError:  # pragma: no cover
+        pass
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _dp(a: Optional[np.ndarray]):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _u8(a: Optional[np.ndarray]):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_ubyte))
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise ValueError(f"{what}: oracle returned {rc}")
+
+
+def _dims(q: np.ndarray, k: np.ndarray):
+    B, Lq, Hq, d = q.shape
+    Bk, Lk, Hkv, dk = k.shape
+    if Bk != B or dk != d:
+        raise ValueError("q and k disagree on batch or head_dim")
+    return B, Hq, Hkv, Lq, Lk, d
+
+
+def attention(q, k, v, causal: bool = False, scale: Optional[float] = None,
+              key_padding_mask=None, with_probs: bool = False, _lib=None):
+    """O (B,Lq,Hq,d) and lse (B,Hq,Lq) in float64 (and P (B,Hq,Lq,Lk) if asked)."""
+    L = _lib or lib()
+    q, k, v = f64(q), f64(k), f64(v)
+    B, Hq, Hkv, Lq, Lk, d = _dims(q, k)
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    kpm = None if key_padding_mask is None else np.ascontiguousarray(np.asarray(key_padding_mask, dtype=np.uint8))
+    o = np.empty((B, Lq, Hq, d), np.float64)
+    lse = np.empty((B, Hq, Lq), np.float64)
+    p = np.empty((B, Hq, Lq, Lk), np.float64) if with_probs else None
+    rc = L.oracle_attention(_dp(q), _dp(k), _dp(v), _u8(kpm), _dp(o), _dp(lse), _dp(p),
+                            B, Hq, Hkv, Lq, Lk, d, int(bool(causal)), float(scale))
+    _check(rc, "oracle_attention")
+    return (o, lse, p) if with_probs else (o, lse)
+
+
+def attention_rows(q, k, v, rows: Sequence[Tuple[int, int, int]], causal: bool = False,
+                   scale: Optional[float] = None, key_padding_mask=None, _lib=None):
+    """O and lse of the selected (b, h, i) rows only: (n, d) and (n,)."""
+    L = _lib or lib()
+    q, k, v = f64(q), f64(k), f64(v)
+    B, Hq, Hkv, Lq, Lk, d = _dims(q, k)
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    kpm = None if key_padding_mask is None else np.ascontiguousarray(np.asarray(key_padding_mask, dtype=np.uint8))
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 3))
+    n = r.shape[0]
+    o = np.empty((n, d), np.float64)
+    lse = np.empty((n,), np.float64)
+    rc = L.oracle_attention_rows(_dp(q), _dp(k), _dp(v), _u8(kpm),
+                                 r.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), n,
+                                 _dp(o), _dp(lse), B, Hq, Hkv, Lq, Lk, d, int(bool(causal)), float(scale))
+    _check(rc, "oracle_attention_rows")
+    return o, lse
+
+
+def online_rows(q, k, v, rows: Sequence[Tuple[int, int, int]], beta: int, form: int = 0,
+                causal: bool = False, scale: Optional[float] = None, key_padding_mask=None,
+                trace: bool = False, _lib=None):
+    """The blocked online-softmax recurrence over key blocks of size ``beta``.
+
+    form 0: (m, l, u, r) recurrence; form 1: normalised-o recurrence.  With
+    ``trace`` it also returns the (m, l, u[0]) state after every block for the
+    first row (o[0] in place of u[0] for form 1)."""
+    L = _lib or lib()
+    q, k, v = f64(q), f64(k), f64(v)
+    B, Hq, Hkv, Lq, Lk, d = _dims(q, k)
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    kpm = None if key_padding_mask is None else np.ascontiguousarray(np.asarray(key_padding_mask, dtype=np.uint8))
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 3))
+    n = r.shape[0]
+    o = np.empty((n, d), np.float64)
+    lse = np.empty((n,), np.float64)
+    nblk = (Lk + beta - 1) // beta
+    tr = np.full((max(nblk, 1), 3), np.nan, np.float64) if trace else None
+    rc = L.oracle_online_rows(_dp(q), _dp(k), _dp(v), _u8(kpm),
+                              r.ctypes.data_as(ctypes.POINTER(ctypes.c_int)), n,
+                              _dp(o), _dp(lse), B, Hq, Hkv, Lq, Lk, d, int(bool(causal)), float(scale),
+                              int(beta), int(form), _dp(tr))
+    _check(rc, "oracle_online_rows")
+    return (o, lse, tr) if trace else (o, lse)
+
+
+# --------------------------------------------------------------------------
+# packed variable-length batches, evaluated through the padded form
+# --------------------------------------------------------------------------
+
+def pad_packed(packed, lengths: Sequence[int], max_len: Optional[int] = None):
+    """Packed (total, H, d) -> padded (B, max_len, H, d) float64 plus the
+    key_padding_mask (B, max_len) with True = keep and the padding at the end
+    of each row (lei6393.com training page, §2.5)."""
+    x = f64(packed)
+    B = len(lengths)
+    T = max_len if max_len is not None else (max(lengths) if B else 0)
+    out = np.zeros((B, T) + x.shape[1:], np.float64)
+    mask = np.zeros((B, T), np.uint8)
+    off = 0
+    for b, n in enumerate(lengths):
+        out[b, :n] = x[off:off + n]
+        mask[b, :n] = 1
+        off += n
+    return out, mask
+
+
+def varlen_attention(q, k, v, lengths: Sequence[int], causal: bool = False,
+                     scale: Optional[float] = None):
+    """Packed varlen attention via the padded batch + key_padding_mask.
+
+    Returns O packed as (total, Hq, d) and lse as (Hq, total)."""
+    lengths = [int(n) for n in lengths]
+    qp, mask = pad_packed(q, lengths)
+    kp, _ = pad_packed(k, lengths)
+    vp, _ = pad_packed(v, lengths)
+    o, lse = attention(qp, kp, vp, causal=causal, scale=scale, key_padding_mask=mask)
+    total = sum(lengths)
+    Hq, d = o.shape[2], o.shape[3]
+    o_packed = np.empty((total, Hq, d), np.float64)
+    lse_packed = np.empty((Hq, total), np.float64)
+    off = 0
+    for b, n in enumerate(lengths):
+        o_packed[off:off + n] = o[b, :n]
+        lse_packed[:, off:off + n] = lse[b, :, :n]
+        off += n
+    return o_packed, lse_packed
+
+
+def varlen_rows(q, k, v, lengths: Sequence[int], rows: Sequence[Tuple[int, int, int]],
+                causal: bool = False, scale: Optional[float] = None):
+    """Selected (b, h, i) rows of a packed varlen batch, via the padded form."""
+    lengths = [int(n) for n in lengths]
+    qp, mask = pad_packed(q, lengths)
+    kp, _ = pad_packed(k, lengths)
+    vp, _ = pad_packed(v, lengths)
+    return attention_rows(qp, kp, vp, rows, causal=causal, scale=scale, key_padding_mask=mask)
+
+
+def standard_attention_traffic_bytes(L: int, d: int, io_bytes: int = 2, score_bytes: int = 4) -> dict:
+    """Byte count of the materialising (standard) attention for one head, as
+    the clxhxhhr.top S23-J17 §3 table accounts it: Q, K, V read and O written
+    once in the I/O dtype; S and P (L x L in fp32) each written once and read
+    once."""
+    qkvo = 4 * L * d * io_bytes
+    s = L * L * score_bytes
+    p = L * L * score_bytes
+    return {"q_each": L * d * io_bytes, "s": s, "p": p, "qkvo": qkvo,
+            "intermediate": 2 * s + 2 * p, "total": qkvo + 2 * s + 2 * p}
