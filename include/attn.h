@@ -1,0 +1,178 @@
+/*
+ * attn.h -- C ABI of the tiled attention forward library (libattn.so).
+ *
+ * The library computes exact softmax attention
+ *
+ *     O = softmax(scale * Q K^T [+ causal mask]) V
+ *
+ * tile by tile with the online-softmax running statistics: the row max m,
+ * the exp-sum l relative to m, the value accumulator u weighted the same
+ * way, and the rescale factor r = exp(m_old - m_new) applied to l and u
+ * whenever m grows (page S23-J17, clxhxhhr.top/posts/5544, §3.1 "在线
+ * Softmax 只需三个量"; the same recurrence in normalised form is the
+ * online-softmax pseudocode of the ans20xx.com day14 page).  The L x L score
+ * and probability matrices never reach global memory: only O and the per-row
+ * log-sum-exp leave the kernel (S23-J17 §3 accounts the 1 GiB of S/P traffic
+ * this avoids at L = 8192, d = 128).
+ *
+ * Problem statement (lei6393.com flash-attention training-integration page):
+ *   - multi-head and grouped-query attention (§2.3: query head h reads KV
+ *     head h / (Hq / Hkv), i.e. consecutive groups of Hq/Hkv query heads
+ *     share one KV head);
+ *   - causal or not (§2.2); causal keeps key j for query i iff
+ *     j <= i + (Lk - Lq), the diagonal included;
+ *   - padded batches given as packed variable-length sequences (§2.5: the
+ *     key_padding_mask keeps a prefix of each row, which the MHA module
+ *     unpads into a packed batch described by cumulative lengths);
+ *   - softmax_scale defaults to 1/sqrt(head_dim) (§8.5); here it is always
+ *     passed explicitly.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers on the current CUDA device,
+ *     owned by the caller; the library neither frees nor retains them past
+ *     the call's completion on `stream`.
+ *   - Work is enqueued on `stream`; no entry point except attn_get_error()
+ *     synchronises.  Arguments are validated on the host before anything is
+ *     enqueued; a non-zero return means nothing was launched.
+ *   - The library allocates, once per device and lazily, its own small
+ *     buffers: cached TMA descriptors, a tile schedule per problem shape and
+ *     a split-KV workspace that is grown on demand.  These live until the
+ *     process exits.
+ *   - Calls that share a device may run concurrently on different streams
+ *     only if they do not share a problem shape that uses split-KV (the
+ *     workspace of a shape is shared).
+ */
+#ifndef ATTN_H
+#define ATTN_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st *cudaStream_t;
+
+/* ---- return codes ------------------------------------------------------ */
+#define ATTN_OK 0
+#define ATTN_EINVAL (-1)       /* bad argument: null pointer, non-positive size, Hq % Hkv != 0,
+                                  pointer not 16-byte aligned, size out of range */
+#define ATTN_EUNSUPPORTED (-2) /* valid but not built: head_dim other than 64 or 128, or a
+                                  device that is not sm_103 */
+#define ATTN_ELAUNCH (-3)      /* a CUDA runtime or driver call failed */
+#define ATTN_ENOMEM (-4)       /* the library could not allocate its workspace */
+#define ATTN_EDEVICE (-5)      /* returned by attn_get_error(): a kernel reported an error */
+
+/* Device-side error codes, reported through attn_get_error() (as
+ * ATTN_EDEVICE) and readable with attn_last_device_error(). */
+#define ATTN_DEVERR_WAIT_TIMEOUT 0x100  /* a pipeline barrier wait ran past its time limit;
+                                           low byte names the wait site */
+#define ATTN_DEVERR_BAD_SEQLENS 0x200   /* cu_seqlens not non-decreasing from 0, or its last
+                                           entry exceeds the packed length */
+
+/*
+ * attn_fwd -- attention forward, bf16 inputs and outputs, fp32 accumulation.
+ *
+ *   q    (B, Lq, Hq, d) bf16, contiguous            [dense]
+ *        (Lq, Hq, d) packed rows                    [varlen, cu_seqlens != NULL]
+ *   k, v (B, Lk, Hkv, d) bf16, contiguous           [dense]
+ *        (Lk, Hkv, d) packed rows                   [varlen]
+ *   o    same shape and dtype as q; written
+ *   lse  float32 log-sum-exp of the scaled scores (natural log), written:
+ *        (B, Hq, Lq) [dense] or (Hq, Lq) indexed by packed row [varlen].
+ *        A row that sees no key gets O = 0 and lse = -inf.
+ *   B, Hq, Hkv   batch (number of sequences for varlen), query heads and KV
+ *                heads; Hq must be a multiple of Hkv.
+ *   Lq, Lk       dense: query and key length of every sequence.
+ *                varlen: number of packed rows in q/o and in k/v (the
+ *                buffers' extents); self-attention only, so Lq == Lk.
+ *   d            head_dim, 64 or 128.
+ *   causal       0 or 1 (mask described above; for varlen it applies within
+ *                each sequence).
+ *   scale        softmax scale applied to Q K^T (usually 1/sqrt(d)); finite.
+ *   cu_seqlens_or_null
+ *                NULL for dense inputs; else a DEVICE int32 array of B+1
+ *                cumulative sequence lengths, cu[0] = 0, non-decreasing,
+ *                cu[B] <= Lq, shared by queries and keys.  The host never
+ *                reads it; a malformed array is reported through
+ *                attn_get_error() and its rows are left unwritten.
+ *   stream       CUDA stream to enqueue on (NULL = legacy default stream).
+ *
+ * All of q, k, v, o must be 16-byte aligned and lse 4-byte aligned.
+ * Returns ATTN_OK or a negative code; see attn_strerror().
+ */
+int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+             int B, int Hq, int Hkv, int Lq, int Lk, int d, int causal,
+             float scale, const int *cu_seqlens_or_null, cudaStream_t stream);
+
+/* attn_fwd_fp16 -- the same operation and argument rules with fp16 q, k, v
+ * and o (the SDPA experiment of the ans20xx.com day14 page, 实验 2, runs in
+ * float16). */
+int attn_fwd_fp16(const void *q, const void *k, const void *v, void *o, float *lse,
+                  int B, int Hq, int Hkv, int Lq, int Lk, int d, int causal,
+                  float scale, const int *cu_seqlens_or_null, cudaStream_t stream);
+
+/* attn_get_error -- synchronises `stream`, then returns ATTN_EDEVICE if any
+ * kernel of this library on the current device has reported an error since
+ * the last call (and clears it), ATTN_ELAUNCH if the stream itself failed,
+ * else ATTN_OK. */
+int attn_get_error(cudaStream_t stream);
+
+/* attn_last_device_error -- the device error code (ATTN_DEVERR_*) that the
+ * last attn_get_error() call cleared, or 0. Host-only, no synchronisation. */
+int attn_last_device_error(void);
+
+/* attn_strerror -- static text for a return code. */
+const char *attn_strerror(int code);
+
+/* attn_set_wait_timeout_ns -- time limit of every pipeline barrier wait in
+ * the kernels launched afterwards by this process (default 2e9 ns).  A wait
+ * that runs out records ATTN_DEVERR_WAIT_TIMEOUT and the kernel returns
+ * early with its outputs incomplete.  Values below 1000 are raised to 1000. */
+void attn_set_wait_timeout_ns(unsigned long long ns);
+
+/* attn_selftest_wait_timeout -- launches one CTA that waits on a barrier no
+ * thread ever arrives on, under the current time limit, so that the
+ * failure path (error word, early exit) can be checked on a GPU without a
+ * fault or a hang.  Returns ATTN_OK if the launch was enqueued; the caller
+ * then expects attn_get_error() to return ATTN_EDEVICE. */
+int attn_selftest_wait_timeout(cudaStream_t stream);
+
+/*
+ * attn_plan -- the host-side persistent-kernel schedule for a dense problem,
+ * exposed for inspection and tests (no GPU needed).  Writes up to
+ * `max_units` work units to `units` as 8 ints each:
+ *     { b*Hq + h, m_block, kv_begin, kv_end, split, n_split, partial_slot, cta }
+ * where m_block indexes 256-row query blocks, [kv_begin, kv_end) is the
+ * range of 128-key tiles the unit covers, split/n_split identify a split-KV
+ * piece (n_split = 1: no split), partial_slot is its workspace slot (-1 if
+ * none) and cta the persistent CTA that runs it.  `*n_units` receives the
+ * unit count, `*n_ctas` the grid size and `*n_partials` the number of
+ * workspace slots.  Returns ATTN_OK, ATTN_EINVAL, or ATTN_ENOMEM if
+ * max_units is too small (then *n_units still holds the required count).
+ */
+int attn_plan(int B, int Hq, int Hkv, int Lq, int Lk, int d, int causal, int num_sms,
+              int *units, int max_units, int *n_units, int *n_ctas, int *n_partials);
+
+/* attn_launch_count -- number of kernels this library has launched in this
+ * process (all devices), counted on the host at each successful launch. */
+unsigned long long attn_launch_count(void);
+
+/*
+ * Per-call kernel timing, for benchmarks.  attn_profile_enable(n) makes the
+ * next n forward calls on any stream record CUDA events around their kernels:
+ * before the main kernel, after it, and after the split-KV combine (when one
+ * runs).  attn_profile_read() synchronises on the recorded events and writes,
+ * for up to `max` recorded calls, the main kernel's duration and the whole
+ * call's duration in milliseconds; *n receives the number of calls recorded.
+ * Enabling again discards earlier records.  Returns ATTN_OK, ATTN_ENOMEM or
+ * ATTN_ELAUNCH.
+ */
+int attn_profile_enable(int n);
+int attn_profile_read(float *main_ms, float *call_ms, int max, int *n);
+void attn_profile_disable(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_H */

@@ -10,3 +10,12 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+
+
+@pytest.fixture(scope="session")
+def attn_lib():
+    """libattn.so, built in-tree on first use (nvcc cross-compiles without a GPU)."""
+    from tiled_attention_attn_gb300 import build, attn
+
+    build.build()
+    return attn.lib()

@@ -1,0 +1,63 @@
+"""The C ABI library loads, exports every symbol include/attn.h declares and
+rejects bad arguments on the host, before anything reaches CUDA."""
+
+import ctypes
+
+import pytest
+
+from tiled_attention_attn_gb300 import attn
+
+
+def test_header_declares_the_entry_points():
+    names = attn.declared_functions()
+    for n in ("attn_fwd", "attn_fwd_fp16", "attn_get_error", "attn_strerror", "attn_plan",
+              "attn_set_wait_timeout_ns", "attn_selftest_wait_timeout", "attn_last_device_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(attn_lib):
+    for name in attn.declared_functions():
+        assert hasattr(attn_lib, name), name
+
+
+def test_strerror(attn_lib):
+    assert attn.strerror(attn.ATTN_OK) == "ok"
+    assert "invalid" in attn.strerror(attn.ATTN_EINVAL)
+    assert "unsupported" in attn.strerror(attn.ATTN_EUNSUPPORTED)
+    assert attn.strerror(12345) == "unknown error"
+
+
+def _call(L, q=16, k=16, v=16, o=16, lse=16, B=1, Hq=2, Hkv=1, Lq=8, Lk=8, d=64, causal=0,
+          scale=0.125, cu=None, fn="attn_fwd"):
+    f = getattr(L, fn)
+    return f(q, k, v, o, lse, B, Hq, Hkv, Lq, Lk, d, causal, ctypes.c_float(scale), cu, None)
+
+
+@pytest.mark.parametrize("fn", ["attn_fwd", "attn_fwd_fp16"])
+@pytest.mark.parametrize("bad", [
+    dict(q=None), dict(k=None), dict(v=None), dict(o=None), dict(lse=None),
+    dict(q=8), dict(o=24), dict(lse=2),                      # misaligned pointers
+    dict(B=0), dict(Hq=0), dict(Hkv=0), dict(Lq=-1), dict(Lk=-1),
+    dict(Hq=3, Hkv=2),                                       # Hq % Hkv != 0
+    dict(causal=2), dict(scale=float("nan")), dict(scale=float("inf")), dict(scale=-1.0),
+    dict(cu=16, Lq=8, Lk=9),                                 # varlen is self-attention
+    dict(cu=16, B=5000),                                     # too many sequences
+    dict(B=1 << 20, Lq=1 << 12, Hq=1 << 10, Hkv=1 << 10),    # rows overflow 32-bit coordinates
+])
+def test_bad_arguments_rejected_on_host(attn_lib, fn, bad):
+    assert _call(attn_lib, fn=fn, **bad) == attn.ATTN_EINVAL
+
+
+@pytest.mark.parametrize("d", [32, 80, 96, 256])
+def test_unsupported_head_dim(attn_lib, d):
+    assert _call(attn_lib, d=d) == attn.ATTN_EUNSUPPORTED
+
+
+def test_empty_query_is_a_no_op(attn_lib):
+    # Lq = 0: nothing to compute, nothing enqueued, no CUDA call
+    assert _call(attn_lib, Lq=0) == attn.ATTN_OK
+
+
+def test_timeout_setter_accepts_values(attn_lib):
+    attn.set_wait_timeout_ns(10)
+    attn.set_wait_timeout_ns(2_000_000_000)

@@ -1,0 +1,221 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Bar (stated for this method): max |O_gpu - O_ref| <= 1e-2 with bf16/fp16
+output and fp32 accumulation on unit-normal inputs, and max |lse_gpu -
+lse_ref| <= 1e-3; rows that see no key must give O = 0 and lse = -inf on both
+sides.  Small shapes are compared element by element; the full-size
+workloads, run exactly as the benchmark runs them, are compared on sampled
+rows the oracle evaluates one by one.
+"""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tiled_attention_attn_gb300 import attn
+from tiled_attention_attn_gb300.inputs import WORKLOADS, Workload, generate, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+O_TOL = 1e-2
+LSE_TOL = 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(attn_lib):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    attn.set_wait_timeout_ns(2_000_000_000)
+    return attn_lib
+
+
+def run(inp, causal, scale=None):
+    dev = torch.device("cuda", 0)
+    q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
+    cu = inp.cu_seqlens.to(dev) if inp.cu_seqlens is not None else None
+    o, lse = attn.attn_fwd(q, k, v, causal=causal, scale=scale, cu_seqlens=cu)
+    assert attn.get_error() == attn.ATTN_OK
+    return o.float().cpu().double().numpy(), lse.cpu().double().numpy()
+
+
+def check(o, lse, o_ref, lse_ref, what=""):
+    assert o.shape == o_ref.shape and lse.shape == lse_ref.shape
+    inf_ref = np.isneginf(lse_ref)
+    assert np.array_equal(np.isneginf(lse), inf_ref), f"{what}: -inf rows differ"
+    err_o = np.max(np.abs(o - o_ref)) if o.size else 0.0
+    fin = ~inf_ref
+    err_l = np.max(np.abs(lse[fin] - lse_ref[fin])) if fin.any() else 0.0
+    assert np.all(np.isfinite(o)), f"{what}: non-finite output"
+    assert err_o <= O_TOL, f"{what}: max |dO| = {err_o:.3e}"
+    assert err_l <= LSE_TOL, f"{what}: max |dlse| = {err_l:.3e}"
+    return err_o, err_l
+
+
+# ---------------------------------------------------------------------------
+# the worked example: scores [0, ln 2], values [1, 3] -> 7/3
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_worked_example(dtype):
+    d = 64
+    q = torch.zeros(1, 1, 1, d)
+    q[0, 0, 0, 0] = 1.0
+    k = torch.zeros(1, 2, 1, d)
+    k[0, 1, 0, 0] = 1.0
+    v = torch.zeros(1, 2, 1, d)
+    v[0, 0, 0, 0] = 1.0
+    v[0, 1, 0, 0] = 3.0
+    dev = torch.device("cuda", 0)
+    o, lse = attn.attn_fwd(q.to(dev, dtype), k.to(dev, dtype), v.to(dev, dtype), scale=math.log(2.0))
+    assert attn.get_error() == attn.ATTN_OK
+    assert abs(float(o[0, 0, 0, 0]) - 7.0 / 3.0) < O_TOL
+    assert torch.all(o[0, 0, 0, 1:] == 0)
+    assert abs(float(lse[0, 0, 0]) - math.log(3.0)) < LSE_TOL
+
+
+# ---------------------------------------------------------------------------
+# small shapes, every element
+# ---------------------------------------------------------------------------
+
+SMALL = [
+    # B, Hq, Hkv, Lq, Lk, d, dtype, causal
+    (1, 2, 2, 256, 256, 64, "bf16", False),
+    (1, 2, 2, 256, 256, 64, "bf16", True),
+    (2, 4, 2, 300, 300, 128, "bf16", True),     # ragged tail, GQA
+    (2, 4, 2, 300, 300, 128, "fp16", False),
+    (1, 3, 1, 129, 700, 128, "bf16", False),    # Lq != Lk
+    (1, 2, 1, 100, 333, 64, "bf16", True),      # causal, bottom-right, Lq < Lk
+    (1, 2, 2, 300, 100, 64, "fp16", True),      # causal, Lq > Lk: rows without keys
+    (2, 2, 2, 1, 1, 64, "bf16", False),
+    (1, 1, 1, 1, 5, 128, "bf16", True),
+    (1, 2, 2, 640, 640, 64, "fp16", True),
+    (3, 8, 8, 77, 77, 128, "bf16", True),
+    (1, 8, 2, 512, 1024, 128, "bf16", False),
+]
+
+
+@pytest.mark.parametrize("shape", SMALL, ids=lambda s: "-".join(map(str, s)))
+def test_small_shapes_full(shape):
+    B, Hq, Hkv, Lq, Lk, d, dt, causal = shape
+    wl = Workload("small", B=B, Hq=Hq, Hkv=Hkv, Lq=Lq, Lk=Lk, d=d, dtype=dt, causal=causal, seed=11)
+    inp = generate(wl)
+    o, lse = run(inp, causal)
+    o_ref, lse_ref = oracle.attention(inp.q, inp.k, inp.v, causal=causal, scale=wl.softmax_scale)
+    check(o, lse, o_ref, lse_ref, str(shape))
+
+
+def test_config_mha_l256_d64_full():
+    wl = WORKLOADS["mha_l256_d64"]
+    inp = generate(wl)
+    o, lse = run(inp, wl.causal)
+    o_ref, lse_ref = oracle.attention(inp.q, inp.k, inp.v, causal=wl.causal, scale=wl.softmax_scale)
+    check(o, lse, o_ref, lse_ref, wl.name)
+
+
+def test_config_varlen_full():
+    wl = WORKLOADS["varlen_b16_h12_d64"]
+    inp = generate(wl)
+    o, lse = run(inp, wl.causal)
+    o_ref, lse_ref = oracle.varlen_attention(inp.q, inp.k, inp.v, inp.lengths, causal=wl.causal,
+                                             scale=wl.softmax_scale)
+    check(o, lse, o_ref, lse_ref, wl.name)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("lengths", [[0, 1, 255, 256, 257, 600, 3], [513], [1, 1, 1], [700, 0, 0, 129]])
+def test_varlen_edges_full(lengths, causal):
+    wl = Workload("varlen_edges", B=len(lengths), Hq=4, Hkv=2, Lq=0, Lk=0, d=128, dtype="bf16",
+                  causal=causal, seed=5, varlen=True)
+    inp = generate(wl, lengths=lengths)
+    o, lse = run(inp, causal)
+    o_ref, lse_ref = oracle.varlen_attention(inp.q, inp.k, inp.v, inp.lengths, causal=causal,
+                                             scale=wl.softmax_scale)
+    check(o, lse, o_ref, lse_ref, f"varlen {lengths}")
+
+
+def test_split_kv_small():
+    # a long causal single head is split along the key range by the schedule
+    B, H, L, d = 1, 1, 4096, 64
+    n_sms = torch.cuda.get_device_properties(0).multi_processor_count
+    _, _, n_part = attn.plan(B, H, H, L, L, d, True, n_sms)
+    assert n_part > 0
+    wl = Workload("split", B=B, Hq=H, Hkv=H, Lq=L, Lk=L, d=d, dtype="bf16", causal=True, seed=3)
+    inp = generate(wl)
+    o, lse = run(inp, True)
+    rows = sample_rows(wl, 160)
+    o_ref, lse_ref = oracle.attention_rows(inp.q, inp.k, inp.v, rows, causal=True, scale=wl.softmax_scale)
+    idx = np.array(rows)
+    check(o[idx[:, 0], idx[:, 2], idx[:, 1]], lse[idx[:, 0], idx[:, 1], idx[:, 2]], o_ref, lse_ref, "split")
+
+
+# ---------------------------------------------------------------------------
+# the full-size workloads, sampled rows
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["single_head_l8192_d128_causal", "mha_b2_h16_l2048_d64_fp16_causal",
+                                  "gqa_b2_hq32_hkv8_l4096_d128_causal"])
+def test_full_size_sampled(name):
+    wl = WORKLOADS[name]
+    inp = generate(wl)
+    o, lse = run(inp, wl.causal)
+    rows = sample_rows(wl, 256)
+    o_ref, lse_ref = oracle.attention_rows(inp.q, inp.k, inp.v, rows, causal=wl.causal, scale=wl.softmax_scale)
+    idx = np.array(rows)
+    check(o[idx[:, 0], idx[:, 2], idx[:, 1]], lse[idx[:, 0], idx[:, 1], idx[:, 2]], o_ref, lse_ref, name)
+    if wl.causal:
+        # causal row 0 sees only key 0: O equals V[0] exactly
+        g = np.arange(wl.Hq) // (wl.Hq // wl.Hkv)
+        v0 = inp.v[:, 0].double().numpy()[:, g]
+        assert np.array_equal(o[:, 0], v0)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+
+
+# ---------------------------------------------------------------------------
+# properties and degenerate cases
+# ---------------------------------------------------------------------------
+
+def test_zero_scale_is_mean_of_values():
+    wl = Workload("zs", B=1, Hq=2, Hkv=2, Lq=200, Lk=200, d=64, dtype="bf16", causal=True, seed=8)
+    inp = generate(wl)
+    o, lse = run(inp, True, scale=0.0)
+    v = inp.v.double().numpy()
+    ref = np.cumsum(v, axis=1) / np.arange(1, 201)[None, :, None, None]
+    assert np.max(np.abs(o - ref)) <= O_TOL
+    assert np.max(np.abs(lse - np.log(np.arange(1, 201))[None, None, :])) <= LSE_TOL
+
+
+def test_repeat_is_bitwise_identical():
+    wl = WORKLOADS["single_head_l8192_d128_causal"]
+    inp = generate(wl)
+    dev = torch.device("cuda", 0)
+    q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
+    o1, l1 = attn.attn_fwd(q, k, v, causal=True)
+    o2, l2 = attn.attn_fwd(q, k, v, causal=True)
+    assert attn.get_error() == attn.ATTN_OK
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_wait_timeout_is_reported_and_context_survives():
+    attn.set_wait_timeout_ns(1_000_000)   # 1 ms
+    try:
+        assert attn.selftest_wait_timeout() == attn.ATTN_OK
+        assert attn.get_error() == attn.ATTN_EDEVICE
+        assert attn.last_device_error() & 0xF00 == attn.ATTN_DEVERR_WAIT_TIMEOUT
+    finally:
+        attn.set_wait_timeout_ns(2_000_000_000)
+    assert attn.get_error() == attn.ATTN_OK
+    test_worked_example(torch.bfloat16)
+
+
+def test_malformed_cu_seqlens_reported():
+    dev = torch.device("cuda", 0)
+    q = torch.randn(300, 2, 64, device=dev, dtype=torch.bfloat16)
+    for bad in ([0, 200, 100, 300], [5, 100, 300], [0, 100, 301]):
+        cu = torch.tensor(bad, dtype=torch.int32, device=dev)
+        attn.attn_fwd(q, q, q, cu_seqlens=cu)
+        assert attn.get_error() == attn.ATTN_EDEVICE
+        assert attn.last_device_error() == attn.ATTN_DEVERR_BAD_SEQLENS
+    assert attn.get_error() == attn.ATTN_OK

@@ -1,0 +1,227 @@
+"""ctypes binding of libattn.so (include/attn.h), argument marshalling only.
+
+Every step of the forward pass runs in the library's CUDA kernels; this module
+checks tensor shapes, allocates outputs with torch, passes raw device pointers
+and the current stream, and turns return codes into exceptions.  There is no
+other implementation behind it: if the library is missing, calls fail.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+from . import build as _build
+
+ATTN_OK = 0
+ATTN_EINVAL = -1
+ATTN_EUNSUPPORTED = -2
+ATTN_ELAUNCH = -3
+ATTN_ENOMEM = -4
+ATTN_EDEVICE = -5
+ATTN_DEVERR_WAIT_TIMEOUT = 0x100
+ATTN_DEVERR_BAD_SEQLENS = 0x200
+
+HEADER = os.path.join(_build.ROOT, "include", "attn.h")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {strerror(code) if _lib is not None else code} (code {code})")
+        self.code = code
+
+
+def declared_functions() -> list:
+    """Names of the functions include/attn.h declares."""
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"\b(attn_\w+)\s*\(", text)
+
+
+def lib(path: Optional[str] = None):
+    """Load libattn.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or _build.LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"{p} is missing: build it with tiled_attention_attn_gb300.build.build()")
+        L = ctypes.CDLL(p)
+        vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        fwd_args = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp, vp]
+        for name in ("attn_fwd", "attn_fwd_fp16"):
+            fn = getattr(L, name)
+            fn.argtypes = fwd_args
+            fn.restype = i
+        L.attn_get_error.argtypes = [vp]
+        L.attn_get_error.restype = i
+        L.attn_last_device_error.argtypes = []
+        L.attn_last_device_error.restype = i
+        L.attn_strerror.argtypes = [i]
+        L.attn_strerror.restype = ctypes.c_char_p
+        L.attn_set_wait_timeout_ns.argtypes = [ctypes.c_ulonglong]
+        L.attn_set_wait_timeout_ns.restype = None
+        L.attn_selftest_wait_timeout.argtypes = [vp]
+        L.attn_selftest_wait_timeout.restype = i
+        L.attn_launch_count.argtypes = []
+        L.attn_launch_count.restype = ctypes.c_ulonglong
+        L.attn_profile_enable.argtypes = [i]
+        L.attn_profile_enable.restype = i
+        L.attn_profile_disable.argtypes = []
+        L.attn_profile_disable.restype = None
+        fp = ctypes.POINTER(ctypes.c_float)
+        L.attn_profile_read.argtypes = [fp, fp, i, ctypes.POINTER(ctypes.c_int)]
+        L.attn_profile_read.restype = i
+        ip = ctypes.POINTER(ctypes.c_int)
+        L.attn_plan.argtypes = [i, i, i, i, i, i, i, i, ip, i, ip, ip, ip]
+        L.attn_plan.restype = i
+        if path is None:
+            _lib = L
+        return L
+
+
+def strerror(code: int) -> str:
+    return lib().attn_strerror(int(code)).decode()
+
+
+def _stream_handle(device: torch.device, stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return int(s.cuda_stream)
+
+
+def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+             scale: Optional[float] = None, cu_seqlens: Optional[torch.Tensor] = None,
+             out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+             stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """O = softmax(scale * Q K^T [+ causal mask]) V and the row log-sum-exp.
+
+    Dense: q (B, Lq, Hq, d), k and v (B, Lk, Hkv, d); returns O like q and
+    lse (B, Hq, Lq) float32.  Varlen (``cu_seqlens`` given, int32 on the
+    device, B+1 entries): q, k, v packed (total, H, d); lse is (Hq, total).
+    ``scale`` defaults to 1/sqrt(d).
+    """
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError("q, k, v must be bfloat16 or float16")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must share one dtype")
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k and v must be CUDA tensors")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k and v must be contiguous")
+    if k.shape != v.shape:
+        raise ValueError("k and v must have the same shape")
+    d = q.shape[-1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if cu_seqlens is not None:
+        if q.dim() != 3 or k.dim() != 3:
+            raise ValueError("varlen q, k, v are (total, H, d)")
+        if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda:
+            raise ValueError("cu_seqlens must be an int32 CUDA tensor")
+        B = cu_seqlens.numel() - 1
+        Lq, Hq, _ = q.shape
+        Lk, Hkv, _ = k.shape
+        lse_shape = (Hq, Lq)
+        cu_ptr = cu_seqlens.data_ptr()
+    else:
+        if q.dim() != 4 or k.dim() != 4:
+            raise ValueError("dense q is (B, Lq, Hq, d) and k, v are (B, Lk, Hkv, d)")
+        B, Lq, Hq, _ = q.shape
+        _, Lk, Hkv, _ = k.shape
+        lse_shape = (B, Hq, Lq)
+        cu_ptr = None
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(lse_shape, dtype=torch.float32, device=q.device)
+    if out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor shaped like q")
+    if tuple(lse.shape) != lse_shape or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError(f"lse must be a contiguous float32 tensor of shape {lse_shape}")
+    L = lib()
+    fn = L.attn_fwd if q.dtype == torch.bfloat16 else L.attn_fwd_fp16
+    with torch.cuda.device(q.device):
+        rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                int(B), int(Hq), int(Hkv), int(Lq), int(Lk), int(d), int(bool(causal)),
+                ctypes.c_float(float(scale)), cu_ptr, _stream_handle(q.device, stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd")
+    return out, lse
+
+
+def get_error(stream: Optional[torch.cuda.Stream] = None, device=None) -> int:
+    """Synchronise the stream and return (and clear) the library's device error status."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        return int(lib().attn_get_error(_stream_handle(dev, stream)))
+
+
+def last_device_error() -> int:
+    return int(lib().attn_last_device_error())
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    lib().attn_set_wait_timeout_ns(int(ns))
+
+
+def selftest_wait_timeout(stream: Optional[torch.cuda.Stream] = None, device=None) -> int:
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        return int(lib().attn_selftest_wait_timeout(_stream_handle(dev, stream)))
+
+
+def plan(B: int, Hq: int, Hkv: int, Lq: int, Lk: int, d: int, causal: bool, num_sms: int):
+    """The persistent-kernel schedule for a dense problem (host only).
+
+    Returns (units, n_ctas, n_partials) with units an (n, 8) int tensor of
+    (b*Hq+h, m_block, kv_begin, kv_end, split, n_split, slot, cta)."""
+    L = lib()
+    n_units, n_ctas, n_part = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    rc = L.attn_plan(B, Hq, Hkv, Lq, Lk, d, int(bool(causal)), num_sms, None, 0,
+                     ctypes.byref(n_units), ctypes.byref(n_ctas), ctypes.byref(n_part))
+    if rc not in (ATTN_OK, ATTN_ENOMEM):
+        raise AttnError(rc, "attn_plan")
+    buf = (ctypes.c_int * (8 * max(n_units.value, 1)))()
+    rc = L.attn_plan(B, Hq, Hkv, Lq, Lk, d, int(bool(causal)), num_sms, buf, n_units.value,
+                     ctypes.byref(n_units), ctypes.byref(n_ctas), ctypes.byref(n_part))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_plan")
+    units = torch.tensor(list(buf)[: 8 * n_units.value], dtype=torch.int64).reshape(-1, 8)
+    return units, n_ctas.value, n_part.value
+
+
+def launch_count() -> int:
+    """Kernels this library has launched in this process."""
+    return int(lib().attn_launch_count())
+
+
+def profile_enable(n: int) -> None:
+    rc = lib().attn_profile_enable(int(n))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_profile_enable")
+
+
+def profile_disable() -> None:
+    lib().attn_profile_disable()
+
+
+def profile_read(max_calls: int):
+    """(main-kernel ms, whole-call ms) of the profiled calls, as two lists."""
+    main = (ctypes.c_float * max(max_calls, 1))()
+    call = (ctypes.c_float * max(max_calls, 1))()
+    n = ctypes.c_int(0)
+    rc = lib().attn_profile_read(main, call, int(max_calls), ctypes.byref(n))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_profile_read")
+    k = min(n.value, max_calls)
+    return list(main)[:k], list(call)[:k]

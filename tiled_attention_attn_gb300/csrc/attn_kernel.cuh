@@ -1,0 +1,660 @@
+// sm_103a attention forward: TMA-fed, tcgen05 tensor cores accumulating in
+// TMEM, online softmax in registers, persistent over a schedule of work units.
+//
+// Method (page S23-J17, clxhxhhr.top/posts/5544, §3.1): per query row keep the
+// running max m, the exp-sum l relative to m and the value accumulator u with
+// the same weights; when m grows, r = exp(m_old - m_new) rescales l and u.
+// The score tile S and probability tile P live only in TMEM and registers.
+//
+// CTA layout (320 threads, one CTA per SM):
+//   warps 0-3  softmax warpgroup for query sub-tile 0 (rows 0..127 of the block)
+//   warps 4-7  softmax warpgroup for query sub-tile 1 (rows 128..255)
+//   warp 8     TMA producer: Q block once per unit, K and V tiles through rings
+//   warp 9     TMEM allocator and single-thread tcgen05.mma issuer
+// TMEM (512 columns x 128 lanes, fp32): S_t at columns [128t, 128t+128); P_t
+// (16-bit, two per column) overwrites the first 64 columns of S_t; the
+// accumulator u_t (= O before normalisation) at [256+128t, 256+128t+D).
+// Lane i of TMEM is query row i of a sub-tile, owned by one softmax thread.
+//
+// Rescaling of u is skipped while the running max grows by at most 2^8 in
+// exp2 units (the exponentials then stay <= 256); the final O = u / l uses
+// the same stale max in both numerator and denominator, so the result is
+// unchanged.  This is the conditional rescale of the published
+// FlashAttention-4 write-up; the pages' recurrence rescales on every change.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "attn_params.h"
+#include "ptx.cuh"
+
+namespace attn {
+
+template <int D>
+struct Cfg {
+  static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+  static constexpr int kChunks = D / 64;                  // 128-byte swizzle atoms per row
+  static constexpr int kTile = kBM * D * 2;               // bytes of one 128-row tile
+  static constexpr int kNK = (D == 128) ? 2 : 4;          // K ring stages
+  static constexpr int kNV = (D == 128) ? 2 : 4;          // V ring stages
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kNSub * kTile;
+  static constexpr int kOffV = kOffK + kNK * kTile;
+  static constexpr int kOffBar = kOffV + kNV * kTile;
+  // barriers: q_full, q_empty, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV],
+  //           s_full[2], p_full[2], o_done[2], drain
+  static constexpr int kNBars = 2 + 2 * kNK + 2 * kNV + 7;
+  static constexpr int kOffMisc = kOffBar + kNBars * 8;   // tmem slot, abort flag, bad flag
+  static constexpr int kOffVarlen = kOffMisc + 64;        // varlen unit prefix table
+  static constexpr int kSmemDense = kOffVarlen + 1024;    // + alignment slack
+  static constexpr int kSmemVarlen = kOffVarlen + 4 * (kVarlenMaxB + 1) + 1024;
+  static constexpr uint32_t kTmemCols = 512;
+};
+
+template <bool BF16>
+struct IO;
+template <>
+struct IO<true> {
+  using T = __nv_bfloat16;
+  static constexpr bool bf16 = true;
+};
+template <>
+struct IO<false> {
+  using T = __half;
+  static constexpr bool bf16 = false;
+};
+
+// One scheduled work unit, decoded identically by every role.
+struct Unit {
+  int b, h, g;
+  int q_row0;            // first query row of the 256-row block (within the sequence)
+  int q_len, k_len;      // sequence lengths
+  int row_q, row_k;      // TMA row coordinate of the sequence start
+  int bcoord;            // TMA batch coordinate
+  int kv_begin, kv_end;  // 128-key tiles covered
+  int split, n_split, slot;
+  int kv_last[2];
+};
+
+template <bool CAUSAL, bool VARLEN>
+__device__ __forceinline__ bool decode_unit(const FwdParams& p, const int* vl_pref, int u, Unit& U) {
+  if constexpr (!VARLEN) {
+    const int* e = p.units + u * kUnitInts;
+    const int bh = e[0];
+    U.b = bh / p.Hq;
+    U.h = bh - U.b * p.Hq;
+    U.q_row0 = e[1] * kBlockRows;
+    U.kv_begin = e[2];
+    U.kv_end = e[3];
+    U.split = e[4];
+    U.n_split = e[5];
+    U.slot = e[6];
+    U.q_len = p.Lq;
+    U.k_len = p.Lk;
+    U.row_q = 0;
+    U.row_k = 0;
+    U.bcoord = U.b;
+  } else {
+    // binary search: largest b with vl_pref[b] <= u
+    int lo = 0, hi = p.B;   // vl_pref[0] = 0 <= u < vl_pref[B]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (vl_pref[mid] <= u) lo = mid; else hi = mid;
+    }
+    U.b = lo;
+    const int local = u - vl_pref[lo];
+    const int mb = local / p.Hq;
+    U.h = local - mb * p.Hq;
+    U.q_row0 = mb * kBlockRows;
+    const int s0 = __ldg(p.cu_seqlens + lo);
+    const int len = __ldg(p.cu_seqlens + lo + 1) - s0;
+    U.q_len = len;
+    U.k_len = len;
+    U.row_q = s0;
+    U.row_k = s0;
+    U.bcoord = 0;
+    U.split = 0;
+    U.n_split = 1;
+    U.slot = -1;
+    U.kv_begin = 0;
+    U.kv_end = 0;
+  }
+  U.g = U.h / p.group;
+  U.kv_last[0] = kv_last_tile(U.q_row0, 0, U.q_len, U.k_len, CAUSAL);
+  U.kv_last[1] = kv_last_tile(U.q_row0, 1, U.q_len, U.k_len, CAUSAL);
+  const int end = max(U.kv_last[0], U.kv_last[1]) + 1;
+  if constexpr (VARLEN) {
+    U.kv_end = end;
+  } else {
+    U.kv_end = min(U.kv_end, end);
+  }
+  return true;
+}
+
+__device__ __forceinline__ bool unit_active(const Unit& U, int t, int j) { return j <= U.kv_last[t]; }
+
+// ---------------------------------------------------------------------------
+// softmax of one S tile for the calling thread's row
+// ---------------------------------------------------------------------------
+struct RowState {
+  float m;     // running max in scaled exp2 units (scale * log2(e) * max score); -inf if none
+  float l;     // exp-sum relative to m
+};
+
+// Loads S (128 fp32) of this thread's row, masks keys beyond `lim` when
+// MASK, updates (m, l), writes P to TMEM and, when the max moved by more than
+// 2^8, rescales u in TMEM (after the in-flight P.V of the previous tile has
+// completed; the P.V of this tile is issued only after this thread arrives).
+template <bool MASK, bool BF16, int D>
+__device__ __forceinline__ bool softmax_tile(uint32_t t_s, uint32_t t_o, int lim, float c_log2, RowState& st,
+                                             bool first, uint32_t o_done_bar, uint32_t o_parity,
+                                             const WaitCtl& wc) {
+  float s[128];
+  {
+    uint32_t r0[32], r1[32], r2[32], r3[32];
+    tmem_ld_32x32b_x32(t_s + 0, r0);
+    tmem_ld_32x32b_x32(t_s + 32, r1);
+    tmem_ld_32x32b_x32(t_s + 64, r2);
+    tmem_ld_32x32b_x32(t_s + 96, r3);
+    tmem_wait_ld(r0);
+    tmem_wait_ld(r1);
+    tmem_wait_ld(r2);
+    tmem_wait_ld(r3);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      s[i] = __uint_as_float(r0[i]);
+      s[32 + i] = __uint_as_float(r1[i]);
+      s[64 + i] = __uint_as_float(r2[i]);
+      s[96 + i] = __uint_as_float(r3[i]);
+    }
+  }
+  if constexpr (MASK) {
+#pragma unroll
+    for (int i = 0; i < 128; ++i) s[i] = (i <= lim) ? s[i] : -INFINITY;
+  }
+  // row max (raw scores)
+  float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+  for (int i = 4; i < 128; i += 4) {
+    mx0 = fmaxf(mx0, s[i]);
+    mx1 = fmaxf(mx1, s[i + 1]);
+    mx2 = fmaxf(mx2, s[i + 2]);
+    mx3 = fmaxf(mx3, s[i + 3]);
+  }
+  const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+  const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * c_log2;
+  const float m_old = st.m;
+  bool resc = false;
+  if (m_tile > m_old && (first || m_old == -INFINITY || m_tile - m_old > 8.0f)) {
+    resc = true;
+    st.m = m_tile;
+  }
+  const float moff = (st.m == -INFINITY) ? 0.0f : st.m;
+  // p = exp2(s * c - m), packed to 16-bit pairs 16 columns at a time
+  float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int c0 = q * 32 + 2 * i;
+      float a = ex2_approx(fmaf(s[c0], c_log2, -moff));
+      float b = ex2_approx(fmaf(s[c0 + 1], c_log2, -moff));
+      if constexpr (MASK) {
+        a = (c0 <= lim) ? a : 0.0f;
+        b = (c0 + 1 <= lim) ? b : 0.0f;
+      }
+      sum0 += a;
+      sum1 += b;
+      pk[i] = pack2<BF16>(a, b);
+    }
+    tmem_st_32x32b_x16(t_s + q * 16, pk);
+  }
+  // rescale l and, when anything is accumulated, u
+  const float r = resc ? ((m_old == -INFINITY) ? 0.0f : ex2_approx(m_old - st.m)) : 1.0f;
+  st.l = st.l * r + (sum0 + sum1);
+  if (!first && __any_sync(0xffffffffu, resc)) {
+    if (!mbar_wait_warp(o_done_bar, o_parity, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteODone))) return false;
+    tc_fence_after();
+#pragma unroll
+    for (int c = 0; c < D / 16; ++c) {
+      uint32_t o[16];
+      tmem_ld_32x32b_x16(t_o + c * 16, o);
+      tmem_wait_ld(o);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * r);
+      tmem_st_32x32b_x16(t_o + c * 16, o);
+    }
+  }
+  tmem_wait_st();
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+template <int D, bool BF16, bool CAUSAL, bool VARLEN>
+__global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
+  using C = Cfg<D>;
+  using T = typename IO<BF16>::T;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sQ = sbase + C::kOffQ;
+  const uint32_t sK = sbase + C::kOffK;
+  const uint32_t sV = sbase + C::kOffV;
+  const uint32_t bar0 = sbase + C::kOffBar;
+  const uint32_t b_q_full = bar0;
+  const uint32_t b_q_empty = bar0 + 8;
+  auto b_k_full = [&](int s) { return bar0 + 16 + 8 * s; };
+  auto b_k_empty = [&](int s) { return bar0 + 16 + 8 * (C::kNK + s); };
+  auto b_v_full = [&](int s) { return bar0 + 16 + 8 * (2 * C::kNK + s); };
+  auto b_v_empty = [&](int s) { return bar0 + 16 + 8 * (2 * C::kNK + C::kNV + s); };
+  const uint32_t bar_sp = bar0 + 16 + 8 * (2 * C::kNK + 2 * C::kNV);
+  auto b_s_full = [&](int t) { return bar_sp + 8 * t; };
+  auto b_p_full = [&](int t) { return bar_sp + 16 + 8 * t; };
+  auto b_o_done = [&](int t) { return bar_sp + 32 + 8 * t; };
+  const uint32_t b_drain = bar_sp + 48;
+
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+  volatile int* bad_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 8);
+  int* vl_pref = reinterpret_cast<int*>(smem + C::kOffVarlen);
+
+  WaitCtl wc{p.err, abort_flag, p.timeout_ns};
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    *bad_flag = 0;
+    mbar_init(b_q_full, 1);
+    mbar_init(b_q_empty, 1);
+    for (int s = 0; s < C::kNK; ++s) {
+      mbar_init(b_k_full(s), 1);
+      mbar_init(b_k_empty(s), 1);
+    }
+    for (int s = 0; s < C::kNV; ++s) {
+      mbar_init(b_v_full(s), 1);
+      mbar_init(b_v_empty(s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(b_s_full(t), 1);
+      mbar_init(b_p_full(t), kBM);
+      mbar_init(b_o_done(t), 1);
+    }
+    mbar_init(b_drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == kWarpMMA) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kWarpTMA && lane == 0) {
+    tma_prefetch_desc(&p.tm_q);
+    tma_prefetch_desc(&p.tm_k);
+    tma_prefetch_desc(&p.tm_v);
+  }
+
+  // varlen: validate cu_seqlens and build the prefix table of units per sequence
+  int n_units = 0, u_first = 0, u_step = 1;
+  if constexpr (VARLEN) {
+    if (warp == 0) {
+      int carry = 0;
+      bool bad = false;
+      if (lane == 0 && __ldg(p.cu_seqlens) != 0) bad = true;
+      for (int b0 = 0; b0 < p.B; b0 += 32) {
+        const int b = b0 + lane;
+        int cnt = 0;
+        if (b < p.B) {
+          const int a = __ldg(p.cu_seqlens + b), e = __ldg(p.cu_seqlens + b + 1);
+          if (e < a || e > p.Lq) bad = true;
+          const int len = e - a;
+          cnt = (len > 0) ? ((len + kBlockRows - 1) / kBlockRows) * p.Hq : 0;
+        }
+        int x = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += y;
+        }
+        if (b < p.B) vl_pref[b + 1] = carry + x;
+        carry += __shfl_sync(0xffffffffu, x, 31);
+      }
+      if (lane == 0) vl_pref[0] = 0;
+      if (__any_sync(0xffffffffu, bad) && lane == 0) {
+        *bad_flag = 1;
+        atomicCAS(p.err, 0, ATTN_DEVERR_BAD_SEQLENS);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if constexpr (VARLEN) {
+    n_units = (*bad_flag) ? 0 : vl_pref[p.B];
+    u_first = blockIdx.x;
+    u_step = gridDim.x;
+  } else {
+    u_first = p.cta_off[blockIdx.x];
+    n_units = p.cta_off[blockIdx.x + 1];
+    u_step = 1;
+  }
+
+  if (warp == kWarpTMA) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t q_cnt = 0, k_cnt = 0, v_cnt = 0;
+      for (int u = u_first; u < n_units; u += u_step) {
+        Unit U;
+        decode_unit<CAUSAL, VARLEN>(p, vl_pref, u, U);
+        if (U.kv_end <= U.kv_begin) continue;
+        if (!mbar_wait(b_q_empty, (q_cnt & 1) ^ 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteQEmpty))) break;
+        mbar_arrive_expect_tx(b_q_full, kNSub * C::kTile);
+#pragma unroll
+        for (int t = 0; t < kNSub; ++t)
+#pragma unroll
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_4d(sQ + t * C::kTile + c * 16384, &p.tm_q, b_q_full, c * 64, U.h,
+                        U.row_q + U.q_row0 + t * kBM, U.bcoord);
+        ++q_cnt;
+        bool ok = true;
+        for (int j = U.kv_begin; j < U.kv_end && ok; ++j) {
+          const int ks = k_cnt % C::kNK;
+          if (!mbar_wait(b_k_empty(ks), ((k_cnt / C::kNK) & 1) ^ 1, wc,
+                         ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKEmpty))) { ok = false; break; }
+          mbar_arrive_expect_tx(b_k_full(ks), C::kTile);
+#pragma unroll
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_4d(sK + ks * C::kTile + c * 16384, &p.tm_k, b_k_full(ks), c * 64, U.g,
+                        U.row_k + j * kBN, U.bcoord);
+          ++k_cnt;
+          const int vs = v_cnt % C::kNV;
+          if (!mbar_wait(b_v_empty(vs), ((v_cnt / C::kNV) & 1) ^ 1, wc,
+                         ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteVEmpty))) { ok = false; break; }
+          mbar_arrive_expect_tx(b_v_full(vs), C::kTile);
+#pragma unroll
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_4d(sV + vs * C::kTile + c * 16384, &p.tm_v, b_v_full(vs), c * 64, U.g,
+                        U.row_k + j * kBN, U.bcoord);
+          ++v_cnt;
+        }
+        if (!ok) break;
+      }
+      // On an abort, let loads already issued land before the CTA exits.
+      if (*abort_flag) {
+        for (int s = 0; s < C::kNK; ++s) {
+          const uint32_t n = (k_cnt + C::kNK - 1 - s) / C::kNK;   // loads issued into stage s
+          if (n > 0) mbar_wait(b_k_full(s), (n - 1) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteDrain), false);
+        }
+        for (int s = 0; s < C::kNV; ++s) {
+          const uint32_t n = (v_cnt + C::kNV - 1 - s) / C::kNV;
+          if (n > 0) mbar_wait(b_v_full(s), (n - 1) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteDrain), false);
+        }
+      }
+    }
+  } else if (warp == kWarpMMA) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdescO = idesc_f16_f32acc(kBM, D, BF16, true);
+      constexpr uint32_t kIdescS = idesc_f16_f32acc(kBM, kBN, BF16, false);
+      // descriptor bases (start address field is addr >> 4 in the low bits)
+      const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024);
+      const uint64_t dk0 = sdesc_sw128(sK, 16, 1024);
+      const uint64_t dv0 = sdesc_sw128(sV, 16384, 1024);
+      uint32_t q_cnt = 0, k_cnt = 0, v_cnt = 0;
+      uint32_t p_cnt[2] = {0, 0};
+      auto issue_s = [&](int t, int ks) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          const uint64_t a = dq0 + ((t * C::kTile + off) >> 4);
+          const uint64_t b = dk0 + ((ks * C::kTile + off) >> 4);
+          umma_ss(tmem + t * 128, a, b, kIdescS, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(b_s_full(t));
+      };
+      bool ok = true;
+      for (int u = u_first; u < n_units && ok; u += u_step) {
+        Unit U;
+        decode_unit<CAUSAL, VARLEN>(p, vl_pref, u, U);
+        if (U.kv_end <= U.kv_begin) continue;
+        if (!mbar_wait(b_q_full, q_cnt & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteQFull))) break;
+        tc_fence_after();
+        bool first_pv[2] = {true, true};
+        // S for the first tile
+        {
+          const int ks = k_cnt % C::kNK;
+          if (!mbar_wait(b_k_full(ks), (k_cnt / C::kNK) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull))) break;
+          tc_fence_after();
+          for (int t = 0; t < kNSub; ++t)
+            if (unit_active(U, t, U.kv_begin)) issue_s(t, ks);
+          umma_commit(b_k_empty(ks));
+          ++k_cnt;
+        }
+        for (int j = U.kv_begin; j < U.kv_end; ++j) {
+          const int vs = v_cnt % C::kNV;
+          if (!mbar_wait(b_v_full(vs), (v_cnt / C::kNV) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteVFull))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const bool have_next = j + 1 < U.kv_end;
+          const int ks = k_cnt % C::kNK;
+          bool k_ready = false;
+          for (int t = 0; t < kNSub && ok; ++t) {
+            if (unit_active(U, t, j)) {
+              if (!mbar_wait(b_p_full(t), p_cnt[t] & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSitePFull))) {
+                ok = false;
+                break;
+              }
+              ++p_cnt[t];
+              tc_fence_after();
+#pragma unroll
+              for (int kk = 0; kk < kBN / 16; ++kk) {
+                const uint64_t b = dv0 + ((vs * C::kTile + kk * 2048) >> 4);
+                umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, b, kIdescO,
+                        (first_pv[t] && kk == 0) ? 0u : 1u);
+              }
+              umma_commit(b_o_done(t));
+              first_pv[t] = false;
+            }
+            if (have_next && unit_active(U, t, j + 1)) {
+              if (!k_ready) {
+                if (!mbar_wait(b_k_full(ks), (k_cnt / C::kNK) & 1, wc,
+                               ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull))) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                k_ready = true;
+              }
+              issue_s(t, ks);
+            }
+          }
+          if (!ok) break;
+          if (have_next) {
+            if (!k_ready) {   // keep the K ring's phases in step even if no sub-tile used the tile
+              if (!mbar_wait(b_k_full(ks), (k_cnt / C::kNK) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull))) break;
+              tc_fence_after();
+            }
+            umma_commit(b_k_empty(ks));
+            ++k_cnt;
+          }
+          umma_commit(b_v_empty(vs));
+          ++v_cnt;
+        }
+        umma_commit(b_q_empty);
+        ++q_cnt;
+      }
+      // every MMA issued by this thread has completed once the drain barrier fires
+      umma_commit(b_drain);
+      mbar_wait(b_drain, 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteDrain), false);
+    }
+  } else {
+    // ------------------------------------------------------------------ softmax warpgroups
+    const int t = warp >> 2;                 // query sub-tile
+    const int quarter = warp & 3;            // TMEM lane quarter of this warp
+    const int row = quarter * 32 + lane;     // row within the sub-tile
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + t * 128;
+    const uint32_t t_o = tmem + lane_off + 256 + t * 128;
+    const float c_log2 = p.scale_log2;
+    uint32_t s_cnt = 0, pv_cnt = 0;
+    T* out = reinterpret_cast<T*>(p.o);
+    for (int u = u_first; u < n_units; u += u_step) {
+      Unit U;
+      decode_unit<CAUSAL, VARLEN>(p, vl_pref, u, U);
+      const int qrow = U.q_row0 + t * kBM + row;        // query row within the sequence
+      const bool row_valid = qrow < U.q_len;
+      // allowed keys of this row: key <= lim_key
+      int lim_key = U.k_len - 1;
+      if constexpr (CAUSAL) lim_key = min(lim_key, qrow + (U.k_len - U.q_len));
+      RowState st{-INFINITY, 0.0f};
+      int n_act = 0;
+      bool ok = true;
+      for (int j = U.kv_begin; j < U.kv_end; ++j) {
+        if (!unit_active(U, t, j)) break;
+        if (!mbar_wait_warp(b_s_full(t), s_cnt & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteSFull))) { ok = false; break; }
+        ++s_cnt;
+        tc_fence_after();
+        const int lim = lim_key - j * kBN;
+        const bool mask_tile = (j * kBN + kBN - 1 > U.k_len - 1) ||
+                               (CAUSAL && j * kBN + kBN - 1 > U.q_row0 + t * kBM + (U.k_len - U.q_len));
+        const uint32_t o_par = (pv_cnt - 1) & 1;
+        bool r;
+        if (mask_tile)
+          r = softmax_tile<true, BF16, D>(t_s, t_o, lim, c_log2, st, n_act == 0, b_o_done(t), o_par, wc);
+        else
+          r = softmax_tile<false, BF16, D>(t_s, t_o, lim, c_log2, st, n_act == 0, b_o_done(t), o_par, wc);
+        if (!r) { ok = false; break; }
+        tc_fence_before();
+        mbar_arrive(b_p_full(t));
+        ++pv_cnt;
+        ++n_act;
+      }
+      if (!ok) break;
+      const bool split = U.n_split > 1;
+      if (n_act > 0) {
+        if (!mbar_wait_warp(b_o_done(t), (pv_cnt - 1) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteODone))) break;
+        tc_fence_after();
+      }
+      if (!split) {
+        // O = u / l, lse = m / log2(e) + ln l
+        const float inv_l = (st.l > 0.0f) ? 1.0f / st.l : 0.0f;
+        const size_t orow = VARLEN ? static_cast<size_t>(U.row_q + qrow)
+                                   : static_cast<size_t>(U.b) * p.Lq + qrow;
+        T* dst = out + (orow * p.Hq + U.h) * D;
+        if (n_act > 0) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld_32x32b_x32(t_o + c * 32, o);
+            tmem_wait_ld(o);
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pk[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+            if (row_valid) {
+              uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            }
+          }
+        } else if (row_valid) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+          for (int i = 0; i < D / 8; ++i) d4[i] = make_uint4(0, 0, 0, 0);
+        }
+        if (row_valid) {
+          const float lse = (st.l > 0.0f) ? st.m * 0.69314718055994531f + __logf(st.l) : -INFINITY;
+          const size_t li = VARLEN ? static_cast<size_t>(U.h) * p.Lq + U.row_q + qrow
+                                   : (static_cast<size_t>(U.b) * p.Hq + U.h) * p.Lq + qrow;
+          p.lse[li] = lse;
+        }
+      } else {
+        // split-KV piece: store the unnormalised accumulator and (m, l)
+        const size_t prow = (static_cast<size_t>(U.slot) * kNSub + t) * kBM + row;
+        float* po = p.part_o + prow * D;
+        if (n_act > 0) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld_32x32b_x32(t_o + c * 32, o);
+            tmem_wait_ld(o);
+            float4* d4 = reinterpret_cast<float4*>(po + c * 32);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              d4[i] = make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
+                                  __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
+          }
+        }
+        float2* pml = reinterpret_cast<float2*>(p.part_ml) + prow;
+        *pml = make_float2(n_act > 0 ? st.m : -INFINITY, n_act > 0 ? st.l : 0.0f);
+      }
+      tc_fence_before();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMMA) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// split-KV combine: O = sum_s 2^(m_s - M) u_s / sum_s 2^(m_s - M) l_s
+// (the same r rescaling, applied across pieces instead of across tiles)
+// ---------------------------------------------------------------------------
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant__ CombineParams p) {
+  using T = typename IO<BF16>::T;
+  constexpr int kThreadsPerRow = D / 8;
+  constexpr int kRowsPerCta = 256 / kThreadsPerRow;
+  const int grp = blockIdx.x;
+  const int* ge = p.groups + grp * kGroupInts;
+  const int bh = ge[0], mb = ge[1], slot0 = ge[2], ns = ge[3];
+  const int r_all = blockIdx.y * kRowsPerCta + threadIdx.x / kThreadsPerRow;   // 0..255
+  const int chunk = threadIdx.x % kThreadsPerRow;
+  const int t = r_all / kBM, row = r_all % kBM;
+  const int qrow = mb * kBlockRows + r_all;
+  if (qrow >= p.Lq) return;
+  const int b = bh / p.Hq, h = bh % p.Hq;
+  float M = -INFINITY;
+  for (int s = 0; s < ns; ++s) {
+    const size_t prow = (static_cast<size_t>(slot0 + s) * kNSub + t) * kBM + row;
+    M = fmaxf(M, __ldcg(reinterpret_cast<const float2*>(p.part_ml) + prow).x);
+  }
+  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  float L = 0.0f;
+  if (M != -INFINITY) {
+    for (int s = 0; s < ns; ++s) {
+      const size_t prow = (static_cast<size_t>(slot0 + s) * kNSub + t) * kBM + row;
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + prow);
+      if (ml.x == -INFINITY) continue;
+      const float w = ex2_approx(ml.x - M);
+      L += w * ml.y;
+      const float4* src = reinterpret_cast<const float4*>(p.part_o + prow * D + chunk * 8);
+      const float4 a = __ldcg(src), c = __ldcg(src + 1);
+      acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
+      acc[4] += w * c.x; acc[5] += w * c.y; acc[6] += w * c.z; acc[7] += w * c.w;
+    }
+  }
+  const float inv = (L > 0.0f) ? 1.0f / L : 0.0f;
+  T* dst = reinterpret_cast<T*>(p.o) + ((static_cast<size_t>(b) * p.Lq + qrow) * p.Hq + h) * D + chunk * 8;
+  *reinterpret_cast<uint4*>(dst) = make_uint4(pack2<BF16>(acc[0] * inv, acc[1] * inv), pack2<BF16>(acc[2] * inv, acc[3] * inv),
+                                              pack2<BF16>(acc[4] * inv, acc[5] * inv), pack2<BF16>(acc[6] * inv, acc[7] * inv));
+  if (chunk == 0)
+    p.lse[(static_cast<size_t>(b) * p.Hq + h) * p.Lq + qrow] =
+        (L > 0.0f) ? M * 0.69314718055994531f + __logf(L) : -INFINITY;
+}
+
+}  // namespace attn

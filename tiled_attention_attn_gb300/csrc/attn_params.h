@@ -1,0 +1,82 @@
+// Parameters shared by the host launcher and the sm_103a kernels.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+
+#include "attn.h"
+
+#define ATTN_DEVERR_WAIT_TIMEOUT_SITE(site) (ATTN_DEVERR_WAIT_TIMEOUT | (site))
+
+#if defined(__CUDACC__)
+#define ATTN_HD __host__ __device__
+#else
+#define ATTN_HD
+#endif
+
+namespace attn {
+
+constexpr int kBM = 128;        // query rows per sub-tile (one TMEM lane per row)
+constexpr int kBN = 128;        // keys per KV tile
+constexpr int kNSub = 2;        // query sub-tiles per work unit (256 query rows)
+constexpr int kBlockRows = kBM * kNSub;
+constexpr int kThreads = 320;   // 8 softmax warps + 1 TMA warp + 1 MMA warp
+constexpr int kWarpTMA = 8;
+constexpr int kWarpMMA = 9;
+constexpr int kVarlenMaxB = 4096;   // sequences per varlen call (prefix table in smem)
+constexpr int kUnitInts = 8;        // ints per scheduled work unit
+constexpr int kGroupInts = 4;       // ints per split-KV group
+constexpr int kMaxSplits = 64;      // split pieces per group
+
+// Wait-site codes (low byte of ATTN_DEVERR_WAIT_TIMEOUT).
+enum WaitSite : int {
+  kSiteQEmpty = 1, kSiteKEmpty, kSiteVEmpty, kSiteQFull, kSiteKFull, kSiteVFull,
+  kSiteSFull, kSitePFull, kSiteODone, kSiteDrain, kSiteSelftest
+};
+
+struct FwdParams {
+  CUtensorMap tm_q;            // (d, Hq, L, B) or packed (d, Hq, total, 1); box 64 x 1 x 128 x 1
+  CUtensorMap tm_k;            // (d, Hkv, L, B) or packed
+  CUtensorMap tm_v;
+  void* o;                     // like q
+  float* lse;                  // (B, Hq, Lq) or (Hq, total)
+  const int* cu_seqlens;       // varlen only
+  const int* units;            // dense schedule, kUnitInts per unit, grouped by CTA
+  const int* cta_off;          // dense: first unit of every CTA, n_ctas + 1 entries
+  float* part_o;               // split-KV partial accumulators [slot][2][128][D] fp32
+  float* part_ml;              // split-KV partial (m, l) [slot][2][128][2]
+  int* err;                    // device error word
+  unsigned long long timeout_ns;
+  int B, Hq, Hkv, Lq, Lk, group;
+  float scale_log2;            // scale * log2(e)
+  float scale;
+};
+
+struct CombineParams {
+  const int* groups;           // kGroupInts per group: bh, m_block, slot_base, n_split
+  const float* part_o;
+  const float* part_ml;
+  void* o;
+  float* lse;
+  int Hq, Lq;
+};
+
+// Last 128-key tile (inclusive) that holds an allowed key for query sub-tile
+// `t` of the 256-row block starting at `q_row0`, or -1 if the sub-tile has no
+// valid query row or no allowed key.  Causal keeps key j for query i iff
+// j <= i + (k_len - q_len).
+ATTN_HD inline int kv_last_tile(int q_row0, int t, int q_len, int k_len, bool causal) {
+  const int first = q_row0 + t * kBM;
+  if (first >= q_len || k_len <= 0) return -1;
+  int last_row = first + kBM - 1;
+  if (last_row > q_len - 1) last_row = q_len - 1;
+  int last = (k_len + kBN - 1) / kBN - 1;
+  if (causal) {
+    const int max_key = last_row + (k_len - q_len);
+    if (max_key < 0) return -1;
+    const int lt = max_key / kBN;
+    if (lt < last) last = lt;
+  }
+  return last;
+}
+
+}  // namespace attn

@@ -1,0 +1,182 @@
+// Host-side schedule for the persistent forward kernel; see attn_plan.h.
+#include "attn_plan.h"
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <functional>
+#include <limits>
+#include <queue>
+#include <utility>
+
+#include "attn_params.h"
+
+namespace attn {
+namespace {
+
+struct Pair {
+  int bh, mb, kv_end, kl0, kl1;
+  long cost;   // tile pairs (sub-tile x key tile) the block computes
+};
+
+struct Cand {
+  int pair;      // index into pairs
+  int a, e;      // key-tile range
+  int split, n_split;
+  double cost;
+};
+
+long piece_cost(const Pair& p, int a, int e) {
+  const long c0 = std::max(0, std::min(e, p.kl0 + 1) - a);
+  const long c1 = std::max(0, std::min(e, p.kl1 + 1) - a);
+  return c0 + c1;
+}
+
+// Fixed per-unit cost in tile pairs (Q load, pipeline fill and drain,
+// epilogue), the extra store of a split piece, and the combine pass.
+struct CostModel {
+  double unit, split_extra, combine;
+};
+
+CostModel cost_model(int d) {
+  if (d == 128) return {2.0, 1.0, 3.0};
+  return {4.0, 2.0, 6.0};
+}
+
+double assign(std::vector<Cand>& units, int num_sms, std::vector<int>& cta_of, int& n_ctas) {
+  std::stable_sort(units.begin(), units.end(), [](const Cand& x, const Cand& y) { return x.cost > y.cost; });
+  n_ctas = std::max(1, std::min<int>(num_sms, static_cast<int>(units.size())));
+  using Slot = std::pair<double, int>;
+  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+  for (int c = 0; c < n_ctas; ++c) heap.push({0.0, c});
+  cta_of.assign(units.size(), 0);
+  double makespan = 0.0;
+  for (size_t i = 0; i < units.size(); ++i) {
+    Slot s = heap.top();
+    heap.pop();
+    cta_of[i] = s.second;
+    s.first += units[i].cost;
+    makespan = std::max(makespan, s.first);
+    heap.push(s);
+  }
+  return makespan;
+}
+
+void build_units(const std::vector<Pair>& pairs, double target, const CostModel& cm,
+                 std::vector<Cand>& units, bool& any_split) {
+  units.clear();
+  any_split = false;
+  for (size_t i = 0; i < pairs.size(); ++i) {
+    const Pair& p = pairs[i];
+    int n = 1;
+    if (p.kv_end > 1 && static_cast<double>(p.cost) > target) {
+      n = static_cast<int>(std::ceil(static_cast<double>(p.cost) / target));
+      n = std::min(n, std::min(p.kv_end, kMaxSplits));
+    }
+    if (n > 1) any_split = true;
+    for (int s = 0; s < n; ++s) {
+      const int a = static_cast<int>(static_cast<long>(s) * p.kv_end / n);
+      const int e = static_cast<int>(static_cast<long>(s + 1) * p.kv_end / n);
+      const double c = static_cast<double>(piece_cost(p, a, e)) + cm.unit + (n > 1 ? cm.split_extra : 0.0);
+      units.push_back({static_cast<int>(i), a, e, s, n, c});
+    }
+  }
+}
+
+}  // namespace
+
+bool make_plan(int B, int Hq, int Hkv, int Lq, int Lk, int d, bool causal, int num_sms, Plan& out) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Lq <= 0 || Lk < 0 || num_sms <= 0) return false;
+  if (d != 64 && d != 128) return false;
+  const int group = Hq / Hkv;
+  const int n_mb = (Lq + kBlockRows - 1) / kBlockRows;
+  const long long n_pairs = static_cast<long long>(B) * Hq * n_mb;
+  if (n_pairs > (1LL << 26) || static_cast<long long>(B) * Hq > std::numeric_limits<int>::max()) return false;
+
+  // query blocks in (batch, KV head, block, query head in group) order, so the
+  // query heads that share a KV head sit next to each other
+  std::vector<Pair> pairs;
+  pairs.reserve(static_cast<size_t>(n_pairs));
+  long total = 0, max_cost = 0;
+  for (int b = 0; b < B; ++b)
+    for (int g = 0; g < Hkv; ++g)
+      for (int mb = 0; mb < n_mb; ++mb)
+        for (int hh = 0; hh < group; ++hh) {
+          const int h = g * group + hh;
+          Pair p;
+          p.bh = b * Hq + h;
+          p.mb = mb;
+          p.kl0 = kv_last_tile(mb * kBlockRows, 0, Lq, Lk, causal);
+          p.kl1 = kv_last_tile(mb * kBlockRows, 1, Lq, Lk, causal);
+          p.kv_end = std::max(p.kl0, p.kl1) + 1;
+          p.cost = piece_cost(p, 0, p.kv_end);
+          total += p.cost;
+          max_cost = std::max(max_cost, p.cost);
+          pairs.push_back(p);
+        }
+
+  const CostModel cm = cost_model(d);
+  const double avg = (static_cast<double>(total) + cm.unit * static_cast<double>(pairs.size())) / num_sms;
+  std::vector<double> targets = {std::numeric_limits<double>::infinity()};
+  if (static_cast<double>(max_cost) > 0.75 * avg) {
+    for (double f : {0.375, 0.5, 0.625, 0.75, 0.875, 1.0, 1.25, 1.5, 2.0, 3.0})
+      if (f * avg >= 1.0) targets.push_back(f * avg);
+  }
+
+  double best = std::numeric_limits<double>::infinity();
+  std::vector<Cand> best_units;
+  std::vector<int> best_cta;
+  int best_ctas = 0;
+  for (double tgt : targets) {
+    std::vector<Cand> units;
+    bool any_split = false;
+    build_units(pairs, tgt, cm, units, any_split);
+    std::vector<int> cta_of;
+    int n_ctas = 0;
+    double ms = assign(units, num_sms, cta_of, n_ctas);
+    if (any_split) ms += cm.combine;
+    if (ms < best - 1e-9 || (std::fabs(ms - best) <= 1e-9 && units.size() < best_units.size())) {
+      best = ms;
+      best_units = std::move(units);
+      best_cta = std::move(cta_of);
+      best_ctas = n_ctas;
+    }
+  }
+
+  // workspace slots for split groups, in pair order
+  std::vector<int> slot_base(pairs.size(), -1);
+  out = Plan();
+  int n_slots = 0;
+  {
+    std::vector<int> nsplit(pairs.size(), 1);
+    for (const Cand& c : best_units) nsplit[c.pair] = c.n_split;
+    for (size_t i = 0; i < pairs.size(); ++i)
+      if (nsplit[i] > 1) {
+        slot_base[i] = n_slots;
+        out.groups.push_back({pairs[i].bh, pairs[i].mb, n_slots, nsplit[i]});
+        n_slots += nsplit[i];
+      }
+  }
+
+  // per-CTA lists, each in assignment order (longest first)
+  out.n_ctas = best_ctas;
+  out.n_partials = n_slots;
+  out.makespan = best;
+  std::vector<std::vector<int>> per_cta(best_ctas);
+  for (size_t i = 0; i < best_units.size(); ++i) per_cta[best_cta[i]].push_back(static_cast<int>(i));
+  out.cta_off.assign(best_ctas + 1, 0);
+  out.units.reserve(best_units.size());
+  for (int c = 0; c < best_ctas; ++c) {
+    out.cta_off[c] = static_cast<int>(out.units.size());
+    for (int i : per_cta[c]) {
+      const Cand& u = best_units[i];
+      const Pair& p = pairs[u.pair];
+      const int slot = (u.n_split > 1) ? slot_base[u.pair] + u.split : -1;
+      out.units.push_back({p.bh, p.mb, u.a, u.e, u.split, u.n_split, slot, c});
+    }
+  }
+  out.cta_off[best_ctas] = static_cast<int>(out.units.size());
+  return true;
+}
+
+}  // namespace attn
