@@ -1,0 +1,484 @@
+#!/usr/bin/env python3
+"""Benchmark of the attention forward hot path on GB300.
+
+One step = one attn_fwd call through the C ABI (the persistent forward kernel
+plus, when the schedule splits key ranges, the combine kernel) over one batch
+of synthetic inputs already resident in HBM.  The default workload is the
+single-head L = 8192, d = 128 causal BF16 problem (page S23-J17 §3 table);
+``--workload`` picks another of tiled_attention_attn_gb300.inputs.WORKLOADS.
+
+Metric: attention forward TFLOP/s, causal-adjusted (4 * d * Hq * sum over
+sequences of Lq * Lk, halved when causal), and its fraction of the measured
+dense BF16 tensor peak.
+
+Timing: W warm-up steps, then K timed steps bracketed by a barrier and a
+device synchronisation.  The inputs (6 MiB for the default workload) fit in
+L2, so a 256 MiB buffer is written before every step and each step is timed
+with its own pair of CUDA events on the launching stream (the flush is
+outside the events).  Clocks are sampled with nvidia-smi during the timed
+steps.  Further legs: the main kernel's own duration (library profiling
+events) for the roofline; an end-to-end leg through pinned host buffers
+(host->device copies of q, k, v and device->host copies of O and lse inside
+the timed region); and, on rank 0 at N = 1, the fp64 CPU oracle timed on a
+bounded sample of the same workload.
+
+``--impl reference`` times the oracle alone, as the reference arm.
+N > 1 (torchrun): every rank runs an independent replica of the workload
+(the forward pass has no exchange step); value = all ranks' FLOPs / the
+slowest rank's time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from tiled_attention_attn_gb300.inputs import HEADLINE, WORKLOADS, generate  # noqa: E402
+
+METRIC = "attn fwd TFLOP/s (causal-adjusted) and % of GB300 dense BF16 tensor peak"
+UNIT = "TFLOP/s"
+FLUSH_BYTES = 256 * 1024 * 1024          # > 129 MB L2
+FALLBACK_PEAK = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "attn_fwd_kernel_l8192_d128_causal.ncu.txt")
+
+
+# ---------------------------------------------------------------------------
+# workload accounting
+# ---------------------------------------------------------------------------
+
+def workload_flops(wl, lengths=None) -> float:
+    """Causal-adjusted FLOPs: 4 * d per (query, key) pair, pairs halved when causal."""
+    if wl.varlen:
+        pairs = sum(n * n for n in lengths)
+    else:
+        pairs = wl.B * wl.Lq * wl.Lk
+    if wl.causal:
+        pairs *= 0.5
+    return 4.0 * wl.d * wl.Hq * pairs
+
+
+def workload_bytes(wl, lengths=None) -> float:
+    """Algorithmic HBM bytes: Q, K, V read once, O written once (input dtype), lse (fp32)."""
+    rows_q = sum(lengths) if wl.varlen else wl.B * wl.Lq
+    rows_k = sum(lengths) if wl.varlen else wl.B * wl.Lk
+    return 2.0 * wl.d * (2 * rows_q * wl.Hq + 2 * rows_k * wl.Hkv) + 4.0 * rows_q * wl.Hq
+
+
+def sample_flops(wl, rows) -> float:
+    """Exact FLOPs of the oracle's work on sampled rows (4 * d per allowed key)."""
+    tot = 0
+    for (b, h, i) in rows:
+        n = wl.Lk if not wl.causal else min(wl.Lk, i + (wl.Lk - wl.Lq) + 1)
+        tot += max(n, 0)
+    return 4.0 * wl.d * tot
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"bf16_tflops": float(d["bf16_tflops"]), "hbm_gbs": float(d["hbm_gbs"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAK, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "tiled_attention_attn_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the main kernel from the committed ncu summary,
+    if it was taken on the current kernel sources (else None)."""
+    try:
+        kv = {}
+        with open(PROFILE_SUMMARY) as f:
+            for line in f:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_sha256") != kernel_source_hash():
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: str):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(1.0)   # nvidia-smi start-up
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        if which == "begin":
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sel = [l for (t, l) in self.lines if self.t0 is not None and self.t0 - 0.05 <= t <= self.t1 + 0.05]
+        mhz, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in sel:
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                mhz.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(mhz)}
+
+
+def gpu_index_for(local_rank: int) -> str:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [x.strip() for x in vis.split(",") if x.strip()]
+        if local_rank < len(ids):
+            return ids[local_rank]
+    return str(local_rank)
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ---------------------------------------------------------------------------
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        return dist, world, rank, local
+    return None, 1, 0, 0
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, x: float, device) -> float:
+    if dist is None:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle on a bounded sample
+# ---------------------------------------------------------------------------
+
+def oracle_sample(wl, inp, budget_s: float, max_rows: int = 4096, seed: int = 99):
+    """Times the oracle on sampled rows of the workload for about budget_s
+    seconds; returns (TFLOP/s, seconds, n_rows, threads)."""
+    import oracle
+
+    oracle.build()
+    q = oracle.f64(inp.q)
+    k = oracle.f64(inp.k)
+    v = oracle.f64(inp.v)
+    rng = np.random.default_rng(seed)
+
+    def rows_of(n):
+        b = rng.integers(0, wl.B, n)
+        h = rng.integers(0, wl.Hq, n)
+        i = rng.integers(0, wl.Lq, n)
+        return [(int(x), int(y), int(z)) for x, y, z in zip(b, h, i)]
+
+    threads = oracle.num_threads()
+    # calibrate on one batch of rows per thread
+    cal = rows_of(max(threads, 1))
+    t0 = time.perf_counter()
+    oracle.attention_rows(q, k, v, cal, causal=wl.causal, scale=wl.softmax_scale)
+    t_cal = max(time.perf_counter() - t0, 1e-6)
+    n = int(min(max_rows, max(threads, len(cal) * budget_s / t_cal)))
+    rows = rows_of(n)
+    t0 = time.perf_counter()
+    oracle.attention_rows(q, k, v, rows, causal=wl.causal, scale=wl.softmax_scale)
+    dt = time.perf_counter() - t0
+    return sample_flops(wl, rows) / dt / 1e12, dt, n, threads
+
+
+def workload_config(wl, lengths=None) -> dict:
+    cfg = {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
+           "causal": wl.causal, "scale": wl.softmax_scale}
+    if wl.varlen:
+        cfg.update({"varlen": True, "lengths": "U[%d,%d]" % (wl.len_lo, wl.len_hi), "total_tokens": sum(lengths)})
+    else:
+        cfg.update({"Lq": wl.Lq, "Lk": wl.Lk})
+    return cfg
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+
+def run_reference(args, wl):
+    dist, world, rank, local = dist_setup(args.gpus)
+    if rank != 0:
+        return 0
+    import oracle
+
+    inp = generate(wl)
+    oracle.build()
+    q, k, v = oracle.f64(inp.q), oracle.f64(inp.k), oracle.f64(inp.v)
+    rng = np.random.default_rng(7)
+    steps, warm = args.steps, args.warmup
+    # size each step's sample so that the whole run stays within a few minutes
+    budget_per_step = min(2.0, 150.0 / max(steps + warm, 1))
+    cal = [(0, 0, wl.Lq - 1)]
+    t0 = time.perf_counter()
+    oracle.attention_rows(q, k, v, cal, causal=wl.causal, scale=wl.softmax_scale)
+    t_row = max(time.perf_counter() - t0, 1e-6)
+    rows_per_step = max(1, int(budget_per_step / t_row))
+
+    def step():
+        b = rng.integers(0, wl.B, rows_per_step)
+        h = rng.integers(0, wl.Hq, rows_per_step)
+        i = rng.integers(0, wl.Lq, rows_per_step)
+        rows = [(int(x), int(y), int(z)) for x, y, z in zip(b, h, i)]
+        oracle.attention_rows(q, k, v, rows, causal=wl.causal, scale=wl.softmax_scale)
+        return sample_flops(wl, rows)
+
+    for _ in range(warm):
+        step()
+    t0 = time.perf_counter()
+    fl = 0.0
+    for _ in range(steps):
+        fl += step()
+    dt = time.perf_counter() - t0
+    value = fl / dt / 1e12
+    threads = oracle.num_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": steps, "warmup": warm, "ms_per_step": dt / steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(wl),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{rows_per_step} random query rows per step of {wl.name}, fp64, "
+                                   f"S and P rows materialised"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, wl):
+    from tiled_attention_attn_gb300 import attn, build
+
+    dist, world, rank, local = dist_setup(args.gpus)
+    build.build()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    inp = generate(wl)
+    q, k, v = inp.q.to(device), inp.k.to(device), inp.v.to(device)
+    cu = inp.cu_seqlens.to(device) if inp.cu_seqlens is not None else None
+    o = torch.empty_like(q)
+    lse_shape = (wl.Hq, q.shape[0]) if wl.varlen else (wl.B, wl.Hq, wl.Lq)
+    lse = torch.empty(lse_shape, dtype=torch.float32, device=device)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flops = workload_flops(wl, inp.lengths)
+    stream = torch.cuda.current_stream(device)
+
+    def call():
+        attn.attn_fwd(q, k, v, causal=wl.causal, scale=wl.softmax_scale, cu_seqlens=cu, out=o, lse=lse)
+
+    # warm-up
+    for _ in range(args.warmup):
+        flush.zero_()
+        call()
+    if attn.get_error() != attn.ATTN_OK:
+        raise RuntimeError(f"device error during warm-up: {attn.last_device_error():#x}")
+
+    # ---- headline: K steps, L2 flushed before each, per-step events
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    sampler = ClockSampler(gpu_index_for(local))
+    sampler.start()
+    barrier(dist)
+    torch.cuda.synchronize(device)
+    sampler.mark("begin")
+    lc0 = attn.launch_count()
+    for i in range(K):
+        flush.zero_()
+        starts[i].record(stream)
+        call()
+        ends[i].record(stream)
+    torch.cuda.synchronize(device)
+    barrier(dist)
+    sampler.mark("end")
+    launches = attn.launch_count() - lc0
+    clocks = sampler.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    total_ms = max_over_ranks(dist, total_ms, device)
+    if attn.get_error() != attn.ATTN_OK:
+        raise RuntimeError(f"device error in the timed region: {attn.last_device_error():#x}")
+    value = world * flops * K / (total_ms / 1e3) / 1e12
+
+    # ---- roofline: the main kernel's own duration (library profiling events)
+    KR = min(K, 2000)
+    attn.profile_enable(KR)
+    for _ in range(KR):
+        flush.zero_()
+        call()
+    main_ms, call_ms = attn.profile_read(KR)
+    attn.profile_disable()
+    main_avg = statistics.mean(main_ms)
+    peaks = measured_peaks()
+    achieved = flops / (main_avg / 1e3) / 1e12
+    traffic = profiled_traffic()
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
+                "kernel": "attn_fwd_kernel", "kernel_ms": main_avg,
+                "peak_source": f"{peaks['source']} bf16 burst (MEASURED_PEAKS.json)"
+                if peaks["source"] == "measured" else "fallback 1.9 PFLOP/s bf16",
+                "algorithmic_flops_per_launch": flops,
+                "algorithmic_bytes_per_launch": workload_bytes(wl, inp.lengths)}
+
+    # ---- end to end through pinned host buffers
+    KE = min(K, args.e2e_steps)
+    qh, kh, vh = (inp.q.pin_memory(), inp.k.pin_memory(), inp.v.pin_memory())
+    oh = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lh = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    cuh = inp.cu_seqlens.pin_memory() if inp.cu_seqlens is not None else None
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(KE)]
+    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(KE)]
+    barrier(dist)
+    torch.cuda.synchronize(device)
+    for i in range(KE):
+        flush.zero_()
+        e_s[i].record(stream)
+        q.copy_(qh, non_blocking=True)
+        k.copy_(kh, non_blocking=True)
+        v.copy_(vh, non_blocking=True)
+        if cu is not None:
+            cu.copy_(cuh, non_blocking=True)
+        call()
+        oh.copy_(o, non_blocking=True)
+        lh.copy_(lse, non_blocking=True)
+        e_e[i].record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = max_over_ranks(dist, sum(s.elapsed_time(e) for s, e in zip(e_s, e_e)), device)
+    h2d = sum(t.numel() * t.element_size() for t in (qh, kh, vh)) + (cuh.numel() * 4 if cuh is not None else 0)
+    d2h = oh.numel() * oh.element_size() + lh.numel() * lh.element_size()
+    e2e = {"value": world * flops * KE / (e2e_ms / 1e3) / 1e12, "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": KE}
+    if attn.get_error() != attn.ATTN_OK:
+        raise RuntimeError(f"device error in the e2e leg: {attn.last_device_error():#x}")
+
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tf, dt, n, threads = oracle_sample(wl, inp, args.cpu_budget_s)
+        cpu = {"value": tf, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": f"{n} random query rows of {wl.name} ({dt:.1f} s), fp64, S and P rows materialised"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": wl.dtype, "data": "synthetic",
+            "config": dict(workload_config(wl, inp.lengths), parallelism=f"replicas x{world}",
+                           l2="256 MiB buffer written before every step, outside the per-step CUDA events"),
+            "pct_of_peak": 100.0 * value / world / peaks["bf16_tflops"],
+            "clocks": clocks, "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=500)
+    ap.add_argument("--cpu-budget-s", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    wl = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
