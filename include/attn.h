@@ -61,6 +61,8 @@ typedef struct CUstream_st *cudaStream_t;
 #define ATTN_ELAUNCH (-3)      /* a CUDA runtime or driver call failed */
 #define ATTN_ENOMEM (-4)       /* the library could not allocate its workspace */
 #define ATTN_EDEVICE (-5)      /* returned by attn_get_error(): a kernel reported an error */
+#define ATTN_ETOOLARGE (-6)    /* attn_fwd_noalloc only: the problem's schedule or split-KV
+                                  partials exceed its static scratch buffer */
 
 /* Device-side error codes, reported through attn_get_error() (as
  * ATTN_EDEVICE) and readable with attn_last_device_error(). */
@@ -110,6 +112,41 @@ int attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
 int attn_fwd_fp16(const void *q, const void *k, const void *v, void *o, float *lse,
                   int B, int Hq, int Hkv, int Lq, int Lk, int d, int causal,
                   float scale, const int *cu_seqlens_or_null, cudaStream_t stream);
+
+/*
+ * attn_fwd_noalloc -- attn_fwd (bf16) for callers that cannot allocate
+ * device memory.  The paper has no counterpart: this is a deployment
+ * variant of the same operation, not part of the method.
+ *
+ * attn_fwd allocates on first use of a problem shape (its schedule) and
+ * grows a split-KV workspace with cudaMalloc/cudaFree.  Some callers cannot
+ * allow that: a process whose device memory is owned by a pool or caching
+ * allocator that has already reserved it (a surprise cudaMalloc may fail),
+ * or a latency-critical loop where cudaFree's implicit device-wide
+ * synchronisation would stall every other stream.  This entry point takes
+ * the same arguments and performs the same computation with the same
+ * kernels, but its scratch (the schedule and the split-KV partials) lives in
+ * one file-scope device array of ATTN_NOALLOC_SCRATCH_BYTES (24 MiB: 4 MiB
+ * for the schedule, 20 MiB for partials) that every GPU loading the library
+ * holds until the process exits.  It calls no cudaMalloc, cudaFree or other
+ * allocating routine.
+ *
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind; nothing in it needs to start at zero (every partial is written
+ *     before it is read).  Calls whose work overlaps on the GPU (for example
+ *     on two streams without an ordering between them) race on the array and
+ *     give wrong results: order them.
+ *   - A dense problem whose schedule exceeds 4 MiB or whose partials exceed
+ *     20 MiB returns ATTN_ETOOLARGE without launching anything; use attn_fwd.
+ *     Varlen calls use no scratch.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES (24u << 20)
+int attn_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
+                     int B, int Hq, int Hkv, int Lq, int Lk, int d, int causal,
+                     float scale, const int *cu_seqlens_or_null, cudaStream_t stream);
 
 /* attn_get_error -- synchronises `stream`, then returns ATTN_EDEVICE if any
  * kernel of this library on the current device has reported an error since

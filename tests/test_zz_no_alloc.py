@@ -1,0 +1,117 @@
+"""attn_fwd_noalloc, the allocation-free entry point.
+
+Some callers cannot allocate device memory during a call: their memory is
+owned by a pool or caching allocator that has already reserved it (a
+surprise cudaMalloc may fail), or they cannot afford the device-wide
+synchronisation that cudaFree implies.  For them attn_fwd_noalloc runs the
+same kernels as attn_fwd with its scratch (schedule and split-KV partials) in
+a static device array.  These tests call it through the C ABI and check it
+against attn_fwd, on two calls in a row with different inputs (the array
+keeps the previous call's contents), across a change of problem shape, and
+that a problem too large for the array is refused without a launch.
+
+The file is named to be collected last, so that a run stopping at the first
+failure has already run every other test.
+"""
+
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from tiled_attention_attn_gb300 import attn
+from tiled_attention_attn_gb300.inputs import WORKLOADS, Workload, generate
+
+pytestmark = pytest.mark.gpu
+
+O_TOL = 1e-2
+LSE_TOL = 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(attn_lib):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return attn_lib
+
+
+def noalloc(q, k, v, causal, scale, cu=None):
+    """Calls attn_fwd_noalloc through the C ABI; returns (O, lse, return code)."""
+    L = attn.lib()
+    o = torch.empty_like(q)
+    if cu is None:
+        B, Lq, Hq, d = q.shape
+        _, Lk, Hkv, _ = k.shape
+        lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device)
+    else:
+        Lq, Hq, d = q.shape
+        Lk, Hkv, _ = k.shape
+        B = cu.numel() - 1
+        lse = torch.empty((Hq, Lq), dtype=torch.float32, device=q.device)
+    stream = torch.cuda.current_stream(q.device).cuda_stream
+    rc = L.attn_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                            B, Hq, Hkv, Lq, Lk, d, int(causal), ctypes.c_float(scale),
+                            cu.data_ptr() if cu is not None else None, stream)
+    return o, lse, rc
+
+
+def assert_close(o, lse, o_ref, lse_ref):
+    assert torch.isfinite(o).all()
+    assert float((o.float() - o_ref.float()).abs().max()) <= O_TOL
+    inf = torch.isneginf(lse_ref)
+    assert torch.equal(torch.isneginf(lse), inf)
+    if (~inf).any():
+        assert float((lse[~inf] - lse_ref[~inf]).abs().max()) <= LSE_TOL
+
+
+def test_noalloc_matches_attn_fwd_two_calls_in_a_row():
+    wl = WORKLOADS["single_head_l8192_d128_causal"]
+    n_sms = torch.cuda.get_device_properties(0).multi_processor_count
+    _, _, n_part = attn.plan(wl.B, wl.Hq, wl.Hkv, wl.Lq, wl.Lk, wl.d, wl.causal, n_sms)
+    assert n_part > 0, "this shape must use split-KV partials, i.e. the scratch array"
+    dev = torch.device("cuda", 0)
+    for seed in (21, 22):
+        inp = generate(wl, seed=seed)
+        q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
+        o_ref, lse_ref = attn.attn_fwd(q, k, v, causal=True, scale=wl.softmax_scale)
+        o, lse, rc = noalloc(q, k, v, True, wl.softmax_scale)
+        assert rc == attn.ATTN_OK
+        assert attn.get_error() == attn.ATTN_OK
+        assert_close(o, lse, o_ref, lse_ref)
+
+
+def test_noalloc_shape_change_and_varlen():
+    dev = torch.device("cuda", 0)
+    for shape in [(2, 8, 2, 700, 700, 64, True), (1, 2, 2, 300, 900, 128, False), (2, 8, 2, 700, 700, 64, True)]:
+        B, Hq, Hkv, Lq, Lk, d, causal = shape
+        wl = Workload("na", B=B, Hq=Hq, Hkv=Hkv, Lq=Lq, Lk=Lk, d=d, dtype="bf16", causal=causal, seed=4)
+        inp = generate(wl)
+        q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
+        o_ref, lse_ref = attn.attn_fwd(q, k, v, causal=causal)
+        o, lse, rc = noalloc(q, k, v, causal, wl.softmax_scale)
+        assert rc == attn.ATTN_OK
+        assert attn.get_error() == attn.ATTN_OK
+        assert_close(o, lse, o_ref, lse_ref)
+    wl = WORKLOADS["varlen_b16_h12_d64"]
+    inp = generate(wl)
+    q, k, v, cu = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev), inp.cu_seqlens.to(dev)
+    o_ref, lse_ref = attn.attn_fwd(q, k, v, causal=False, cu_seqlens=cu)
+    o, lse, rc = noalloc(q, k, v, False, wl.softmax_scale, cu=cu)
+    assert rc == attn.ATTN_OK and attn.get_error() == attn.ATTN_OK
+    assert_close(o, lse, o_ref, lse_ref)
+
+
+def test_noalloc_refuses_problems_beyond_its_array():
+    # single head, L = 16384, causal: its split-KV partials need more than 20 MiB
+    L, d = 16384, 128
+    n_sms = torch.cuda.get_device_properties(0).multi_processor_count
+    _, _, n_part = attn.plan(1, 1, 1, L, L, d, True, n_sms)
+    assert n_part * 2 * 128 * (d + 2) * 4 > (20 << 20)
+    dev = torch.device("cuda", 0)
+    q = torch.randn(1, L, 1, d, device=dev, dtype=torch.bfloat16)
+    before = attn.launch_count()
+    o, lse, rc = noalloc(q, q, q, True, d ** -0.5)
+    assert rc == attn.ATTN_ETOOLARGE
+    assert attn.launch_count() == before
+    assert "static buffer" in attn.strerror(rc)

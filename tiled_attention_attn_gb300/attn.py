@@ -25,6 +25,7 @@ ATTN_EUNSUPPORTED = -2
 ATTN_ELAUNCH = -3
 ATTN_ENOMEM = -4
 ATTN_EDEVICE = -5
+ATTN_ETOOLARGE = -6
 ATTN_DEVERR_WAIT_TIMEOUT = 0x100
 ATTN_DEVERR_BAD_SEQLENS = 0x200
 
@@ -59,7 +60,7 @@ def lib(path: Optional[str] = None):
         L = ctypes.CDLL(p)
         vp, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
         fwd_args = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp, vp]
-        for name in ("attn_fwd", "attn_fwd_fp16"):
+        for name in ("attn_fwd", "attn_fwd_fp16", "attn_fwd_noalloc"):
             fn = getattr(L, name)
             fn.argtypes = fwd_args
             fn.restype = i

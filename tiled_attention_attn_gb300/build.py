@@ -21,7 +21,7 @@ BUILD_DIR = os.path.join(ROOT, "_build", "attn")
 LIB_PATH = os.path.join(PKG, "libattn.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["attn_host.cu", "attn_kernels_d64.cu", "attn_kernels_d128.cu", "attn_plan.cpp"]
+SOURCES = ["attn_host.cu", "attn_noalloc.cu", "attn_kernels_d64.cu", "attn_kernels_d128.cu", "attn_plan.cpp"]
 
 
 def nvcc() -> str:

@@ -15,6 +15,7 @@
 #include <vector>
 
 #include "attn.h"
+#include "attn_internal.h"
 #include "attn_launch.h"
 #include "attn_params.h"
 #include "attn_plan.h"
@@ -314,6 +315,38 @@ __global__ void selftest_wait_kernel(int* err, unsigned long long timeout_ns) {
 
 }  // namespace
 
+int device_info(int dev, DeviceInfo& out) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevState& st = g_dev[dev];
+  const int rc = init_device(dev, st);
+  if (rc) return rc;
+  out.sm_count = st.sm_count;
+  out.supported = st.supported;
+  out.err_word = st.err_word;
+  return ATTN_OK;
+}
+
+int encode_map(const void* ptr, bool bf16, int d, int H, int L, int B, CUtensorMap& out) {
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!get_encode()) return ATTN_ELAUNCH;
+  }
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(H) * d * 2,
+                                 static_cast<cuuint64_t>(L) * H * d * 2};
+  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kBM), 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  const CUresult r = g_encode(&out, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+                              const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? ATTN_OK : ATTN_EINVAL;
+}
+
+unsigned long long wait_timeout_ns() { return g_timeout_ns.load(); }
+void count_launch() { g_launches.fetch_add(1); }
+
 cudaError_t launch_selftest_wait(int* err_word, unsigned long long timeout_ns, cudaStream_t stream) {
   selftest_wait_kernel<<<1, 32, 0, stream>>>(err_word, timeout_ns);
   return cudaGetLastError();
@@ -357,6 +390,8 @@ const char* attn_strerror(int code) {
     case ATTN_ELAUNCH: return "CUDA launch or runtime failure";
     case ATTN_ENOMEM: return "workspace allocation failed";
     case ATTN_EDEVICE: return "a kernel reported a device-side error (see attn_last_device_error)";
+    case ATTN_ETOOLARGE:
+      return "problem needs more scratch than the static buffer of attn_fwd_noalloc holds; use attn_fwd";
     default: return "unknown error";
   }
 }

@@ -1,0 +1,26 @@
+// Internal helpers shared by the library's entry-point translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace attn {
+
+struct DeviceInfo {
+  int sm_count = 0;
+  bool supported = false;   // sm_103
+  int* err_word = nullptr;  // device address of the error word
+};
+
+// Queries (once per device, cached) the SM count, whether the device is an
+// sm_103 part, and the device address of the error word.  Allocates nothing.
+int device_info(int dev, DeviceInfo& out);
+
+// Encodes the 4-D TMA map over (d, H, L, B) of a contiguous (B, L, H, d)
+// 16-bit tensor, box 64 x 1 x 128 x 1, without caching.  Allocates nothing.
+int encode_map(const void* ptr, bool bf16, int d, int H, int L, int B, CUtensorMap& out);
+
+// Current barrier-wait time limit and the launch counter of attn_launch_count().
+unsigned long long wait_timeout_ns();
+void count_launch();
+
+}  // namespace attn
