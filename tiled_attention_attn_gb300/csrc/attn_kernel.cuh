@@ -172,17 +172,17 @@ __device__ __forceinline__ bool softmax_tile(uint32_t t_s, uint32_t t_o, int lim
 #pragma unroll
     for (int i = 0; i < 128; ++i) s[i] = (i <= lim) ? s[i] : -INFINITY;
   }
-  // row max (raw scores)
-  float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+  // row max (raw scores) over eight independent chains of two-input max
+  float mx[8];
 #pragma unroll
-  for (int i = 4; i < 128; i += 4) {
-    mx0 = fmaxf(mx0, s[i]);
-    mx1 = fmaxf(mx1, s[i + 1]);
-    mx2 = fmaxf(mx2, s[i + 2]);
-    mx3 = fmaxf(mx3, s[i + 3]);
-  }
-  const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-  const float m_tile = (mx == -INFINITY) ? -INFINITY : mx * c_log2;
+  for (int i = 0; i < 8; ++i) mx[i] = s[i];
+#pragma unroll
+  for (int i = 8; i < 128; i += 8)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], s[i + k]);
+  const float mx_all = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+  const float m_tile = (mx_all == -INFINITY) ? -INFINITY : mx_all * c_log2;
   const float m_old = st.m;
   bool resc = false;
   if (m_tile > m_old && (first || m_old == -INFINITY || m_tile - m_old > 8.0f)) {
@@ -190,29 +190,39 @@ __device__ __forceinline__ bool softmax_tile(uint32_t t_s, uint32_t t_o, int lim
     st.m = m_tile;
   }
   const float moff = (st.m == -INFINITY) ? 0.0f : st.m;
-  // p = exp2(s * c - m), packed to 16-bit pairs 16 columns at a time
-  float sum0 = 0.f, sum1 = 0.f;
+  // p = exp2(s * c - m): the argument with packed fp32x2 FMA, one ex2 per
+  // element, row sums with packed adds; P packed to 16-bit pairs and stored
+  // 32 columns at a time
+  const float2 c2 = make_float2(c_log2, c_log2);
+  const float2 nm2 = make_float2(-moff, -moff);
+  float2 sum_a = make_float2(0.f, 0.f), sum_b = make_float2(0.f, 0.f);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     uint32_t pk[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < 16; i += 2) {
       const int c0 = q * 32 + 2 * i;
-      float a = ex2_approx(fmaf(s[c0], c_log2, -moff));
-      float b = ex2_approx(fmaf(s[c0 + 1], c_log2, -moff));
+      const float2 x0 = ffma2(make_float2(s[c0], s[c0 + 1]), c2, nm2);
+      const float2 x1 = ffma2(make_float2(s[c0 + 2], s[c0 + 3]), c2, nm2);
+      float2 e0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
+      float2 e1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
       if constexpr (MASK) {
-        a = (c0 <= lim) ? a : 0.0f;
-        b = (c0 + 1 <= lim) ? b : 0.0f;
+        e0.x = (c0 <= lim) ? e0.x : 0.0f;
+        e0.y = (c0 + 1 <= lim) ? e0.y : 0.0f;
+        e1.x = (c0 + 2 <= lim) ? e1.x : 0.0f;
+        e1.y = (c0 + 3 <= lim) ? e1.y : 0.0f;
       }
-      sum0 += a;
-      sum1 += b;
-      pk[i] = pack2<BF16>(a, b);
+      sum_a = fadd2(sum_a, e0);
+      sum_b = fadd2(sum_b, e1);
+      pk[i] = pack2<BF16>(e0.x, e0.y);
+      pk[i + 1] = pack2<BF16>(e1.x, e1.y);
     }
     tmem_st_32x32b_x16(t_s + q * 16, pk);
   }
   // rescale l and, when anything is accumulated, u
   const float r = resc ? ((m_old == -INFINITY) ? 0.0f : ex2_approx(m_old - st.m)) : 1.0f;
-  st.l = st.l * r + (sum0 + sum1);
+  const float2 sum2 = fadd2(sum_a, sum_b);
+  st.l = st.l * r + (sum2.x + sum2.y);
   if (!first && __any_sync(0xffffffffu, resc)) {
     if (!mbar_wait_warp(o_done_bar, o_parity, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteODone))) return false;
     tc_fence_after();
@@ -335,6 +345,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the combine pass of split pieces may be scheduled now; it waits for this grid
+  grid_launch_dependents();
 
   if constexpr (VARLEN) {
     n_units = (*bad_flag) ? 0 : vl_pref[p.B];
@@ -408,14 +420,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       const uint64_t dk0 = sdesc_sw128(sK, 16, 1024);
       const uint64_t dv0 = sdesc_sw128(sV, 16384, 1024);
       uint32_t q_cnt = 0, k_cnt = 0, v_cnt = 0;
-      uint32_t p_cnt[2] = {0, 0};
+      uint32_t p_cnt0 = 0, p_cnt1 = 0;
       auto issue_s = [&](int t, int ks) {
+        const uint64_t a0 = dq0 + ((t * C::kTile) >> 4);
+        const uint64_t b0 = dk0 + ((ks * C::kTile) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          const uint64_t a = dq0 + ((t * C::kTile + off) >> 4);
-          const uint64_t b = dk0 + ((ks * C::kTile + off) >> 4);
-          umma_ss(tmem + t * 128, a, b, kIdescS, kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          umma_ss(tmem + t * 128, a0 + off, b0 + off, kIdescS, kk > 0 ? 1u : 0u);
         }
         umma_commit(b_s_full(t));
       };
@@ -426,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if (U.kv_end <= U.kv_begin) continue;
         if (!mbar_wait(b_q_full, q_cnt & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteQFull))) break;
         tc_fence_after();
-        bool first_pv[2] = {true, true};
+        bool first_pv0 = true, first_pv1 = true;
         // S for the first tile
         {
           const int ks = k_cnt % C::kNK;
@@ -447,22 +459,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           const bool have_next = j + 1 < U.kv_end;
           const int ks = k_cnt % C::kNK;
           bool k_ready = false;
-          for (int t = 0; t < kNSub && ok; ++t) {
+#pragma unroll
+          for (int t = 0; t < kNSub; ++t) {
+            if (!ok) break;
+            uint32_t& p_cnt = (t == 0) ? p_cnt0 : p_cnt1;
+            bool& first_pv = (t == 0) ? first_pv0 : first_pv1;
             if (unit_active(U, t, j)) {
-              if (!mbar_wait(b_p_full(t), p_cnt[t] & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSitePFull))) {
+              if (!mbar_wait(b_p_full(t), p_cnt & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSitePFull))) {
                 ok = false;
                 break;
               }
-              ++p_cnt[t];
+              ++p_cnt;
               tc_fence_after();
+              const uint64_t bv = dv0 + ((vs * C::kTile) >> 4);
 #pragma unroll
-              for (int kk = 0; kk < kBN / 16; ++kk) {
-                const uint64_t b = dv0 + ((vs * C::kTile + kk * 2048) >> 4);
-                umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, b, kIdescO,
-                        (first_pv[t] && kk == 0) ? 0u : 1u);
-              }
+              for (int kk = 0; kk < kBN / 16; ++kk)
+                umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, bv + ((kk * 2048) >> 4), kIdescO,
+                        (first_pv && kk == 0) ? 0u : 1u);
               umma_commit(b_o_done(t));
-              first_pv[t] = false;
+              first_pv = false;
             }
             if (have_next && unit_active(U, t, j + 1)) {
               if (!k_ready) {
@@ -578,22 +593,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           p.lse[li] = lse;
         }
       } else {
-        // split-KV piece: store the unnormalised accumulator and (m, l)
-        const size_t prow = (static_cast<size_t>(U.slot) * kNSub + t) * kBM + row;
-        float* po = p.part_o + prow * D;
+        // split-KV piece: store the unnormalised accumulator and (m, l).
+        // Layout [slot][t][D/4][row][4]: a warp's 32 rows of one 4-column
+        // group are 512 contiguous bytes.
+        const size_t pbase = (static_cast<size_t>(U.slot) * kNSub + t) * (D / 4);
+        float4* po = reinterpret_cast<float4*>(p.part_o);
         if (n_act > 0) {
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
             tmem_ld_32x32b_x32(t_o + c * 32, o);
             tmem_wait_ld(o);
-            float4* d4 = reinterpret_cast<float4*>(po + c * 32);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-              d4[i] = make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
-                                  __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
+              po[(pbase + c * 8 + i) * kBM + row] =
+                  make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
+                              __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
           }
         }
+        const size_t prow = (static_cast<size_t>(U.slot) * kNSub + t) * kBM + row;
         float2* pml = reinterpret_cast<float2*>(p.part_ml) + prow;
         *pml = make_float2(n_act > 0 ? st.m : -INFINITY, n_act > 0 ? st.l : 0.0f);
       }
@@ -612,47 +630,78 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
 // ---------------------------------------------------------------------------
 // split-KV combine: O = sum_s 2^(m_s - M) u_s / sum_s 2^(m_s - M) l_s
-// (the same r rescaling, applied across pieces instead of across tiles)
+// (the same r rescaling, applied across pieces instead of across tiles).
+// Grid (groups, 2 sub-tiles, D/16 column blocks), one thread per query row
+// and 16 columns; pieces are read four at a time so that their loads are in
+// flight together.  Launched as a programmatic dependent of the forward
+// kernel: it may be scheduled early and waits here until that grid has
+// completed and its writes are visible.
 // ---------------------------------------------------------------------------
 template <int D, bool BF16>
-__global__ void __launch_bounds__(256) attn_combine_kernel(const __grid_constant__ CombineParams p) {
+__global__ void __launch_bounds__(kBM) attn_combine_kernel(const __grid_constant__ CombineParams p) {
   using T = typename IO<BF16>::T;
-  constexpr int kThreadsPerRow = D / 8;
-  constexpr int kRowsPerCta = 256 / kThreadsPerRow;
-  const int grp = blockIdx.x;
-  const int* ge = p.groups + grp * kGroupInts;
-  const int bh = ge[0], mb = ge[1], slot0 = ge[2], ns = ge[3];
-  const int r_all = blockIdx.y * kRowsPerCta + threadIdx.x / kThreadsPerRow;   // 0..255
-  const int chunk = threadIdx.x % kThreadsPerRow;
-  const int t = r_all / kBM, row = r_all % kBM;
-  const int qrow = mb * kBlockRows + r_all;
+  const int* ge = p.groups + blockIdx.x * kGroupInts;
+  const int bh = __ldg(ge), mb = __ldg(ge + 1), slot0 = __ldg(ge + 2), ns = __ldg(ge + 3);
+  const int t = blockIdx.y, cb = blockIdx.z, row = threadIdx.x;
+  const int qrow = mb * kBlockRows + t * kBM + row;
   if (qrow >= p.Lq) return;
-  const int b = bh / p.Hq, h = bh % p.Hq;
+  const int b = bh / p.Hq, h = bh - b * p.Hq;
+  grid_wait_prerequisites();
+  const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
+  const float4* po = reinterpret_cast<const float4*>(p.part_o);
+  const size_t ml_base = static_cast<size_t>(slot0) * kNSub * kBM + t * kBM + row;
+  const size_t o_base = (static_cast<size_t>(slot0) * kNSub + t) * (D / 4) + cb * 4;
+  constexpr size_t kMlStride = kNSub * kBM;      // per piece, in float2
+  constexpr size_t kOStride = kNSub * (D / 4);   // per piece, in 4-column groups
   float M = -INFINITY;
-  for (int s = 0; s < ns; ++s) {
-    const size_t prow = (static_cast<size_t>(slot0 + s) * kNSub + t) * kBM + row;
-    M = fmaxf(M, __ldcg(reinterpret_cast<const float2*>(p.part_ml) + prow).x);
+  for (int s0 = 0; s0 < ns; s0 += 8) {
+    float mv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mv[i] = (s0 + i < ns) ? __ldcg(ml + ml_base + (s0 + i) * kMlStride).x : -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) M = fmaxf(M, mv[i]);
   }
-  float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  float acc[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
   float L = 0.0f;
   if (M != -INFINITY) {
-    for (int s = 0; s < ns; ++s) {
-      const size_t prow = (static_cast<size_t>(slot0 + s) * kNSub + t) * kBM + row;
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + prow);
-      if (ml.x == -INFINITY) continue;
-      const float w = ex2_approx(ml.x - M);
-      L += w * ml.y;
-      const float4* src = reinterpret_cast<const float4*>(p.part_o + prow * D + chunk * 8);
-      const float4 a = __ldcg(src), c = __ldcg(src + 1);
-      acc[0] += w * a.x; acc[1] += w * a.y; acc[2] += w * a.z; acc[3] += w * a.w;
-      acc[4] += w * c.x; acc[5] += w * c.y; acc[6] += w * c.z; acc[7] += w * c.w;
+    for (int s0 = 0; s0 < ns; s0 += 4) {
+      float2 mlv[4];
+      float4 x[4][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const bool in = s0 + i < ns;
+        mlv[i] = in ? __ldcg(ml + ml_base + (s0 + i) * kMlStride) : make_float2(-INFINITY, 0.0f);
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          x[i][c] = in ? __ldcg(po + (o_base + (s0 + i) * kOStride + c) * kBM + row) : make_float4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (mlv[i].x == -INFINITY) continue;   // an empty piece (its u was never written)
+        const float w = ex2_approx(mlv[i].x - M);
+        L += w * mlv[i].y;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          acc[4 * c] += w * x[i][c].x;
+          acc[4 * c + 1] += w * x[i][c].y;
+          acc[4 * c + 2] += w * x[i][c].z;
+          acc[4 * c + 3] += w * x[i][c].w;
+        }
+      }
     }
   }
   const float inv = (L > 0.0f) ? 1.0f / L : 0.0f;
-  T* dst = reinterpret_cast<T*>(p.o) + ((static_cast<size_t>(b) * p.Lq + qrow) * p.Hq + h) * D + chunk * 8;
-  *reinterpret_cast<uint4*>(dst) = make_uint4(pack2<BF16>(acc[0] * inv, acc[1] * inv), pack2<BF16>(acc[2] * inv, acc[3] * inv),
-                                              pack2<BF16>(acc[4] * inv, acc[5] * inv), pack2<BF16>(acc[6] * inv, acc[7] * inv));
-  if (chunk == 0)
+  T* dst = reinterpret_cast<T*>(p.o) + ((static_cast<size_t>(b) * p.Lq + qrow) * p.Hq + h) * D + cb * 16;
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+    d4[i] = make_uint4(pack2<BF16>(acc[8 * i] * inv, acc[8 * i + 1] * inv),
+                       pack2<BF16>(acc[8 * i + 2] * inv, acc[8 * i + 3] * inv),
+                       pack2<BF16>(acc[8 * i + 4] * inv, acc[8 * i + 5] * inv),
+                       pack2<BF16>(acc[8 * i + 6] * inv, acc[8 * i + 7] * inv));
+  if (cb == 0)
     p.lse[(static_cast<size_t>(b) * p.Hq + h) * p.Lq + qrow] =
         (L > 0.0f) ? M * 0.69314718055994531f + __logf(L) : -INFINITY;
 }
