@@ -195,6 +195,24 @@ int attn_plan(int B, int Hq, int Hkv, int Lq, int Lk, int d, int causal, int num
 unsigned long long attn_launch_count(void);
 
 /*
+ * attn_trace_enable -- phase trace of the forward kernel, for performance
+ * analysis.  Trace points are compiled only into the traced build of the
+ * library (libattn_trace.so, built with ATTN_TRACE=1) so that the default
+ * kernels carry none of their cost; the default build returns
+ * ATTN_EUNSUPPORTED.  With a non-null DEVICE buffer, every later forward
+ * launch records, per CTA, four event streams (TMA producer, MMA issuer, and
+ * one thread of each softmax warpgroup) of up to `events_per_stream` events.
+ * An event is two 64-bit words: a tag word (tag << 56 | sub-tile << 48 |
+ * unit << 24 | key tile) and the SM clock.  CTA c, stream s starts at word
+ * (c * 4 + s) * events_per_stream * 2; the buffer must hold
+ * grid * 4 * events_per_stream * 16 bytes, grid being at most the SM count.
+ * The caller owns the buffer and keeps it alive while traced launches run.
+ * A null buffer (or events_per_stream <= 0) turns tracing off.  Returns
+ * ATTN_OK, ATTN_EINVAL (buffer not 16-byte aligned) or ATTN_EUNSUPPORTED.
+ */
+int attn_trace_enable(void *dev_buf, int events_per_stream);
+
+/*
  * Per-call kernel timing, for benchmarks.  attn_profile_enable(n) makes the
  * next n forward calls on any stream record CUDA events around their kernels:
  * before the main kernel, after it, and after the split-KV combine (when one

@@ -54,7 +54,7 @@ def lib(path: Optional[str] = None):
     with _lock:
         if _lib is not None and path is None:
             return _lib
-        p = path or _build.LIB_PATH
+        p = path or os.environ.get("TILED_ATTN_LIB") or _build.LIB_PATH
         if not os.path.exists(p):
             raise RuntimeError(f"{p} is missing: build it with tiled_attention_attn_gb300.build.build()")
         L = ctypes.CDLL(p)
@@ -83,6 +83,8 @@ def lib(path: Optional[str] = None):
         fp = ctypes.POINTER(ctypes.c_float)
         L.attn_profile_read.argtypes = [fp, fp, i, ctypes.POINTER(ctypes.c_int)]
         L.attn_profile_read.restype = i
+        L.attn_trace_enable.argtypes = [vp, i]
+        L.attn_trace_enable.restype = i
         ip = ctypes.POINTER(ctypes.c_int)
         L.attn_plan.argtypes = [i, i, i, i, i, i, i, i, ip, i, ip, ip, ip]
         L.attn_plan.restype = i
@@ -226,3 +228,15 @@ def profile_read(max_calls: int):
         raise AttnError(rc, "attn_profile_read")
     k = min(n.value, max_calls)
     return list(main)[:k], list(call)[:k]
+
+
+def trace_enable(buf: Optional[torch.Tensor], events_per_stream: int = 0) -> None:
+    """Record the forward kernel's phase trace into ``buf`` (a CUDA tensor of at
+    least n_sms * 4 * events_per_stream * 16 bytes); ``None`` turns it off.
+    Needs the traced build (libattn_trace.so, selected with TILED_ATTN_LIB)."""
+    if buf is None:
+        rc = lib().attn_trace_enable(None, 0)
+    else:
+        rc = lib().attn_trace_enable(buf.data_ptr(), int(events_per_stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_trace_enable")

@@ -19,6 +19,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build", "attn")
 LIB_PATH = os.path.join(PKG, "libattn.so")
+TRACE_LIB_PATH = os.path.join(PKG, "libattn_trace.so")   # phase-trace points compiled in
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["attn_host.cu", "attn_noalloc.cu", "attn_kernels_d64.cu", "attn_kernels_d128.cu", "attn_plan.cpp"]
@@ -40,22 +41,27 @@ def _deps():
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+def up_to_date(path: str = LIB_PATH) -> bool:
+    if not os.path.exists(path):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, trace: bool = False) -> str:
+    """Build libattn.so, or with ``trace`` the phase-traced libattn_trace.so."""
+    out = TRACE_LIB_PATH if trace else LIB_PATH
+    if not force and up_to_date(out):
+        return out
+    bdir = BUILD_DIR + ("_trace" if trace else "")
+    os.makedirs(bdir, exist_ok=True)
     exe = nvcc()
     common = ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
+    if trace:
+        common += ["-DATTN_TRACE=1"]
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(bdir, os.path.splitext(src)[0] + ".o")
         cmd = [exe, "-c", os.path.join(CSRC, src), "-o", obj] + common + ARCH
         if src.endswith(".cu"):
             cmd += ["-Xptxas", "-v"] if verbose else []
@@ -68,16 +74,16 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB_PATH + ".tmp"
+    tmp = out + ".tmp"
     cmd = [exe, "-shared", "-o", tmp] + objs + ARCH
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":
     import sys
 
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, trace="--trace" in sys.argv))

@@ -30,6 +30,8 @@ namespace {
 
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
 std::atomic<unsigned long long> g_launches{0};
+unsigned long long* g_trace = nullptr;   // attn_trace_enable (traced build only)
+int g_trace_cap = 0;
 
 // per-call timing events (attn_profile_*)
 struct ProfileRec {
@@ -247,6 +249,8 @@ int fwd(bool bf16, const void* q, const void* k, const void* v, void* o, float* 
   p.lse = lse;
   p.cu_seqlens = cu;
   p.err = st.err_word;
+  p.trace = g_trace;
+  p.trace_cap = g_trace_cap;
   p.timeout_ns = g_timeout_ns.load();
   p.B = B;
   p.Hq = Hq;
@@ -410,6 +414,25 @@ int attn_selftest_wait_timeout(cudaStream_t stream) {
 }
 
 unsigned long long attn_launch_count(void) { return attn::g_launches.load(); }
+
+int attn_trace_enable(void* dev_buf, int events_per_stream) {
+#if !defined(ATTN_TRACE) || !ATTN_TRACE
+  (void)dev_buf;
+  (void)events_per_stream;
+  return ATTN_EUNSUPPORTED;   // trace points exist only in the traced build
+#else
+  std::lock_guard<std::mutex> lock(attn::g_mu);
+  if (dev_buf == nullptr || events_per_stream <= 0) {
+    attn::g_trace = nullptr;
+    attn::g_trace_cap = 0;
+    return ATTN_OK;
+  }
+  if (reinterpret_cast<uintptr_t>(dev_buf) % 16 != 0) return ATTN_EINVAL;
+  attn::g_trace = static_cast<unsigned long long*>(dev_buf);
+  attn::g_trace_cap = events_per_stream;
+  return ATTN_OK;
+#endif
+}
 
 int attn_profile_enable(int n) {
   std::lock_guard<std::mutex> lock(attn::g_mu);

@@ -133,6 +133,35 @@ __device__ __forceinline__ bool decode_unit(const FwdParams& p, const int* vl_pr
 
 __device__ __forceinline__ bool unit_active(const Unit& U, int t, int j) { return j <= U.kv_last[t]; }
 
+// Phase trace: one writer thread per stream; events beyond the capacity are
+// dropped.  Compiled in only when ATTN_TRACE is 1 (the library's traced
+// build); otherwise every call below compiles to nothing.
+#ifndef ATTN_TRACE
+#define ATTN_TRACE 0
+#endif
+struct Tracer {
+  unsigned long long* base;   // this CTA's region of this stream, or null
+  int cap, n;
+  __device__ __forceinline__ void init(const FwdParams& p, int stream) {
+    base = (ATTN_TRACE && p.trace)
+               ? p.trace + (static_cast<size_t>(blockIdx.x) * kTrStreams + stream) * p.trace_cap * 2
+               : nullptr;
+    cap = p.trace_cap;
+    n = 0;
+  }
+  __device__ __forceinline__ void off() { base = nullptr; }
+  __device__ __forceinline__ void rec(int tag, int t, int a, int b) {
+    if (ATTN_TRACE && base != nullptr && n < cap) {
+      base[2 * n] = (static_cast<unsigned long long>(tag) << 56) |
+                    (static_cast<unsigned long long>(t & 0xff) << 48) |
+                    (static_cast<unsigned long long>(a & 0xffffff) << 24) |
+                    static_cast<unsigned long long>(b & 0xffffff);
+      base[2 * n + 1] = clock64();
+      ++n;
+    }
+  }
+};
+
 // ---------------------------------------------------------------------------
 // softmax of one S tile for the calling thread's row
 // ---------------------------------------------------------------------------
@@ -361,6 +390,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   if (warp == kWarpTMA) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
+      Tracer tr;
+      tr.init(p, kTrProducer);
       uint32_t q_cnt = 0, k_cnt = 0, v_cnt = 0;
       for (int u = u_first; u < n_units; u += u_step) {
         Unit U;
@@ -374,6 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_4d(sQ + t * C::kTile + c * 16384, &p.tm_q, b_q_full, c * 64, U.h,
                         U.row_q + U.q_row0 + t * kBM, U.bcoord);
+        tr.rec(kTagQIssue, 0, u, 0);
         ++q_cnt;
         bool ok = true;
         for (int j = U.kv_begin; j < U.kv_end && ok; ++j) {
@@ -385,6 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_4d(sK + ks * C::kTile + c * 16384, &p.tm_k, b_k_full(ks), c * 64, U.g,
                         U.row_k + j * kBN, U.bcoord);
+          tr.rec(kTagKIssue, 0, u, j);
           ++k_cnt;
           const int vs = v_cnt % C::kNV;
           if (!mbar_wait(b_v_empty(vs), ((v_cnt / C::kNV) & 1) ^ 1, wc,
@@ -394,6 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_4d(sV + vs * C::kTile + c * 16384, &p.tm_v, b_v_full(vs), c * 64, U.g,
                         U.row_k + j * kBN, U.bcoord);
+          tr.rec(kTagVIssue, 0, u, j);
           ++v_cnt;
         }
         if (!ok) break;
@@ -419,6 +453,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024);
       const uint64_t dk0 = sdesc_sw128(sK, 16, 1024);
       const uint64_t dv0 = sdesc_sw128(sV, 16384, 1024);
+      Tracer tr;
+      tr.init(p, kTrMMA);
+      tr.rec(kTagStart, 0, 0, 0);
       uint32_t q_cnt = 0, k_cnt = 0, v_cnt = 0;
       uint32_t p_cnt0 = 0, p_cnt1 = 0;
       auto issue_s = [&](int t, int ks) {
@@ -437,25 +474,29 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         decode_unit<CAUSAL, VARLEN>(p, vl_pref, u, U);
         if (U.kv_end <= U.kv_begin) continue;
         if (!mbar_wait(b_q_full, q_cnt & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteQFull))) break;
-        tc_fence_after();
+        tr.rec(kTagQFull, 0, u, 0);
         bool first_pv0 = true, first_pv1 = true;
         // S for the first tile
         {
           const int ks = k_cnt % C::kNK;
           if (!mbar_wait(b_k_full(ks), (k_cnt / C::kNK) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull))) break;
-          tc_fence_after();
+          tr.rec(kTagKFull, 0, u, U.kv_begin);
           for (int t = 0; t < kNSub; ++t)
-            if (unit_active(U, t, U.kv_begin)) issue_s(t, ks);
+            if (unit_active(U, t, U.kv_begin)) {
+              issue_s(t, ks);
+              tr.rec(kTagSIssue, t, u, U.kv_begin);
+            }
           umma_commit(b_k_empty(ks));
           ++k_cnt;
         }
         for (int j = U.kv_begin; j < U.kv_end; ++j) {
           const int vs = v_cnt % C::kNV;
+          tr.rec(kTagVWait, 0, u, j);
           if (!mbar_wait(b_v_full(vs), (v_cnt / C::kNV) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteVFull))) {
             ok = false;
             break;
           }
-          tc_fence_after();
+          tr.rec(kTagVFull, 0, u, j);
           const bool have_next = j + 1 < U.kv_end;
           const int ks = k_cnt % C::kNK;
           bool k_ready = false;
@@ -465,18 +506,26 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             uint32_t& p_cnt = (t == 0) ? p_cnt0 : p_cnt1;
             bool& first_pv = (t == 0) ? first_pv0 : first_pv1;
             if (unit_active(U, t, j)) {
+              tr.rec(kTagPWait, t, u, j);
               if (!mbar_wait(b_p_full(t), p_cnt & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSitePFull))) {
                 ok = false;
                 break;
               }
               ++p_cnt;
+              // P was written into TMEM by the softmax threads (tcgen05.st):
+              // this fence orders that before the MMA that reads it.  Waits on
+              // TMA-filled barriers need no tcgen05 fence (the transaction
+              // count makes the data visible), and each such fence costs the
+              // issuing thread a drain of its MMAs in flight.
               tc_fence_after();
+              tr.rec(kTagPFull, t, u, j);
               const uint64_t bv = dv0 + ((vs * C::kTile) >> 4);
 #pragma unroll
               for (int kk = 0; kk < kBN / 16; ++kk)
                 umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, bv + ((kk * 2048) >> 4), kIdescO,
                         (first_pv && kk == 0) ? 0u : 1u);
               umma_commit(b_o_done(t));
+              tr.rec(kTagPVIssue, t, u, j);
               first_pv = false;
             }
             if (have_next && unit_active(U, t, j + 1)) {
@@ -486,17 +535,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                   ok = false;
                   break;
                 }
-                tc_fence_after();
+                tr.rec(kTagKFull, 0, u, j + 1);
                 k_ready = true;
               }
               issue_s(t, ks);
+              tr.rec(kTagSIssue, t, u, j + 1);
             }
           }
           if (!ok) break;
           if (have_next) {
             if (!k_ready) {   // keep the K ring's phases in step even if no sub-tile used the tile
               if (!mbar_wait(b_k_full(ks), (k_cnt / C::kNK) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull))) break;
-              tc_fence_after();
             }
             umma_commit(b_k_empty(ks));
             ++k_cnt;
@@ -505,6 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           ++v_cnt;
         }
         umma_commit(b_q_empty);
+        tr.rec(kTagUnitEnd, 0, u, 0);
         ++q_cnt;
       }
       // every MMA issued by this thread has completed once the drain barrier fires
@@ -522,6 +572,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const float c_log2 = p.scale_log2;
     uint32_t s_cnt = 0, pv_cnt = 0;
     T* out = reinterpret_cast<T*>(p.o);
+    Tracer tr;
+    tr.init(p, t == 0 ? kTrSoftmax0 : kTrSoftmax1);
+    if (row != 0) tr.off();
     for (int u = u_first; u < n_units; u += u_step) {
       Unit U;
       decode_unit<CAUSAL, VARLEN>(p, vl_pref, u, U);
@@ -533,11 +586,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       RowState st{-INFINITY, 0.0f};
       int n_act = 0;
       bool ok = true;
+      tr.rec(kTagUnitBegin, t, u, 0);
       for (int j = U.kv_begin; j < U.kv_end; ++j) {
         if (!unit_active(U, t, j)) break;
         if (!mbar_wait_warp(b_s_full(t), s_cnt & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteSFull))) { ok = false; break; }
         ++s_cnt;
         tc_fence_after();
+        tr.rec(kTagSFull, t, u, j);
         const int lim = lim_key - j * kBN;
         const bool mask_tile = (j * kBN + kBN - 1 > U.k_len - 1) ||
                                (CAUSAL && j * kBN + kBN - 1 > U.q_row0 + t * kBM + (U.k_len - U.q_len));
@@ -550,6 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if (!r) { ok = false; break; }
         tc_fence_before();
         mbar_arrive(b_p_full(t));
+        tr.rec(kTagPArrive, t, u, j);
         ++pv_cnt;
         ++n_act;
       }
@@ -558,6 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       if (n_act > 0) {
         if (!mbar_wait_warp(b_o_done(t), (pv_cnt - 1) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteODone))) break;
         tc_fence_after();
+        tr.rec(kTagODone, t, u, 0);
       }
       if (!split) {
         // O = u / l, lse = m / log2(e) + ln l
@@ -615,6 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         float2* pml = reinterpret_cast<float2*>(p.part_ml) + prow;
         *pml = make_float2(n_act > 0 ? st.m : -INFINITY, n_act > 0 ? st.l : 0.0f);
       }
+      tr.rec(kTagEpiDone, t, u, 0);
       tc_fence_before();
     }
   }

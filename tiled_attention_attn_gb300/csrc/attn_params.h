@@ -27,6 +27,16 @@ constexpr int kUnitInts = 8;        // ints per scheduled work unit
 constexpr int kGroupInts = 4;       // ints per split-KV group
 constexpr int kMaxSplits = 64;      // split pieces per group
 
+// Phase trace streams and tags (attn_trace_enable).  An event is two 64-bit
+// words: (tag << 56 | sub-tile << 48 | unit << 24 | key tile) and the SM clock.
+enum TraceStream : int { kTrProducer = 0, kTrMMA = 1, kTrSoftmax0 = 2, kTrSoftmax1 = 3, kTrStreams = 4 };
+enum TraceTag : int {
+  kTagStart = 1, kTagQIssue = 2, kTagKIssue = 3, kTagVIssue = 4,
+  kTagQFull = 10, kTagSIssue = 11, kTagPFull = 12, kTagPVIssue = 13, kTagKFull = 14, kTagVFull = 15,
+  kTagUnitEnd = 16, kTagVWait = 17, kTagPWait = 18,
+  kTagSFull = 20, kTagPArrive = 21, kTagODone = 23, kTagEpiDone = 24, kTagUnitBegin = 25,
+};
+
 // Wait-site codes (low byte of ATTN_DEVERR_WAIT_TIMEOUT).
 enum WaitSite : int {
   kSiteQEmpty = 1, kSiteKEmpty, kSiteVEmpty, kSiteQFull, kSiteKFull, kSiteVFull,
@@ -45,6 +55,8 @@ struct FwdParams {
   float* part_o;               // split-KV partial accumulators [slot][2][128][D] fp32
   float* part_ml;              // split-KV partial (m, l) [slot][2][128][2]
   int* err;                    // device error word
+  unsigned long long* trace;   // optional phase trace (traced build, attn_trace_enable), else null
+  int trace_cap;               // events per stream per CTA
   unsigned long long timeout_ns;
   int B, Hq, Hkv, Lq, Lk, group;
   float scale_log2;            // scale * log2(e)

@@ -72,7 +72,7 @@ __device__ __forceinline__ void report_error(const WaitCtl& w, int code) {
 // Waits for the phase with parity `parity` of barrier `bar` to complete.
 // Bounded: gives up after w.timeout_ns (checked every 64 polls) or, when
 // `honor_abort`, as soon as another thread of the CTA has aborted.
-static __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& w, int code,
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& w, int code,
                                        bool honor_abort = true) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
