@@ -87,6 +87,7 @@ using PlanKey = std::tuple<int, int, int, int, int, int, int>;   // B, Hq, Hkv, 
 
 struct DevPlan {
   Plan host;
+  std::vector<int> flat_units;   // kUnitInts per unit, the layout the kernel reads
   int* d_units = nullptr;
   int* d_cta_off = nullptr;
   int* d_groups = nullptr;
@@ -99,7 +100,7 @@ struct DevState {
   int* err_word = nullptr;
   std::map<MapKey, CUtensorMap> maps;
   std::map<PlanKey, std::unique_ptr<DevPlan>> plans;
-  float* part_o = nullptr;
+  void* part_o = nullptr;
   float* part_ml = nullptr;
   size_t part_o_bytes = 0, part_ml_bytes = 0;
 };
@@ -162,6 +163,7 @@ int get_plan(DevState& st, int B, int Hq, int Hkv, int Lq, int Lk, int d, bool c
     const int e[kUnitInts] = {u.bh, u.m_block, u.kv_begin, u.kv_end, u.split, u.n_split, u.slot, u.cta};
     std::memcpy(&units[i * kUnitInts], e, sizeof(e));
   }
+  dp->flat_units = units;
   std::vector<int> groups(pl.groups.size() * kGroupInts);
   for (size_t i = 0; i < pl.groups.size(); ++i) {
     const PlanGroup& g = pl.groups[i];
@@ -187,7 +189,7 @@ int get_plan(DevState& st, int B, int Hq, int Hkv, int Lq, int Lk, int d, bool c
 }
 
 int ensure_workspace(DevState& st, int n_partials, int d) {
-  const size_t need_o = static_cast<size_t>(n_partials) * kNSub * kBM * d * sizeof(float);
+  const size_t need_o = static_cast<size_t>(n_partials) * kNSub * kBM * d * 2;   // fp16
   const size_t need_ml = static_cast<size_t>(n_partials) * kNSub * kBM * 2 * sizeof(float);
   if (need_o > st.part_o_bytes) {
     if (st.part_o) cudaFree(st.part_o);
@@ -274,6 +276,11 @@ int fwd(bool bf16, const void* q, const void* k, const void* v, void* o, float* 
     }
     p.units = plan->d_units;
     p.cta_off = plan->d_cta_off;
+    if (static_cast<int>(plan->host.units.size()) <= kInlineUnits && plan->host.n_ctas <= kInlineCtas) {
+      p.n_inline = 1;
+      std::memcpy(p.units_inline, plan->flat_units.data(), plan->flat_units.size() * sizeof(int));
+      std::memcpy(p.cta_off_inline, plan->host.cta_off.data(), plan->host.cta_off.size() * sizeof(int));
+    }
     grid = plan->host.n_ctas;
   } else {
     // units = sum over sequences of Hq * ceil(len / 256) <= Hq * (B + ceil(total / 256))

@@ -79,7 +79,7 @@ struct Unit {
 template <bool CAUSAL, bool VARLEN>
 __device__ __forceinline__ bool decode_unit(const FwdParams& p, const int* vl_pref, int u, Unit& U) {
   if constexpr (!VARLEN) {
-    const int* e = p.units + u * kUnitInts;
+    const int* e = (p.n_inline ? p.units_inline : p.units) + u * kUnitInts;
     const int bh = e[0];
     U.b = bh / p.Hq;
     U.h = bh - U.b * p.Hq;
@@ -382,8 +382,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     u_first = blockIdx.x;
     u_step = gridDim.x;
   } else {
-    u_first = p.cta_off[blockIdx.x];
-    n_units = p.cta_off[blockIdx.x + 1];
+    const int* off = p.n_inline ? p.cta_off_inline : p.cta_off;
+    u_first = off[blockIdx.x];
+    n_units = off[blockIdx.x + 1];
     u_step = 1;
   }
 
@@ -650,22 +651,27 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           p.lse[li] = lse;
         }
       } else {
-        // split-KV piece: store the unnormalised accumulator and (m, l).
-        // Layout [slot][t][D/4][row][4]: a warp's 32 rows of one 4-column
-        // group are 512 contiguous bytes.
-        const size_t pbase = (static_cast<size_t>(U.slot) * kNSub + t) * (D / 4);
-        float4* po = reinterpret_cast<float4*>(p.part_o);
+        // split-KV piece: store its own normalised output O_s = u_s / l_s in
+        // fp16 and (m, l) in fp32; the combine pass forms the convex mix
+        // sum_s w_s O_s / sum_s w_s, so the fp16 rounding error stays below
+        // 2^-12 |O|.  Layout [slot][t][D/8][row][8]: a warp's 32 rows of one
+        // 8-column group are 512 contiguous bytes.
+        const size_t pbase = (static_cast<size_t>(U.slot) * kNSub + t) * (D / 8);
+        uint4* po = reinterpret_cast<uint4*>(p.part_o);
         if (n_act > 0) {
+          const float inv_l = 1.0f / st.l;
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
             tmem_ld_32x32b_x32(t_o + c * 32, o);
             tmem_wait_ld(o);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              po[(pbase + c * 8 + i) * kBM + row] =
-                  make_float4(__uint_as_float(o[4 * i]), __uint_as_float(o[4 * i + 1]),
-                              __uint_as_float(o[4 * i + 2]), __uint_as_float(o[4 * i + 3]));
+            for (int i = 0; i < 4; ++i)
+              po[(pbase + c * 4 + i) * kBM + row] =
+                  make_uint4(pack2<false>(__uint_as_float(o[8 * i]) * inv_l, __uint_as_float(o[8 * i + 1]) * inv_l),
+                             pack2<false>(__uint_as_float(o[8 * i + 2]) * inv_l, __uint_as_float(o[8 * i + 3]) * inv_l),
+                             pack2<false>(__uint_as_float(o[8 * i + 4]) * inv_l, __uint_as_float(o[8 * i + 5]) * inv_l),
+                             pack2<false>(__uint_as_float(o[8 * i + 6]) * inv_l, __uint_as_float(o[8 * i + 7]) * inv_l));
           }
         }
         const size_t prow = (static_cast<size_t>(U.slot) * kNSub + t) * kBM + row;
@@ -687,10 +693,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 }
 
 // ---------------------------------------------------------------------------
-// split-KV combine: O = sum_s 2^(m_s - M) u_s / sum_s 2^(m_s - M) l_s
-// (the same r rescaling, applied across pieces instead of across tiles).
+// split-KV combine.  Piece s holds O_s = u_s / l_s (fp16) and (m_s, l_s);
+// with M = max_s m_s and w_s = 2^(m_s - M) l_s (the same r rescaling as
+// across tiles), O = sum_s w_s O_s / sum_s w_s and lse = M ln 2 + ln sum_s w_s.
 // Grid (groups, 2 sub-tiles, D/16 column blocks), one thread per query row
-// and 16 columns; pieces are read four at a time so that their loads are in
+// and 16 columns; pieces are read four at a time so their loads are in
 // flight together.  Launched as a programmatic dependent of the forward
 // kernel: it may be scheduled early and waits here until that grid has
 // completed and its writes are visible.
@@ -706,11 +713,11 @@ __global__ void __launch_bounds__(kBM) attn_combine_kernel(const __grid_constant
   const int b = bh / p.Hq, h = bh - b * p.Hq;
   grid_wait_prerequisites();
   const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
-  const float4* po = reinterpret_cast<const float4*>(p.part_o);
+  const uint4* po = reinterpret_cast<const uint4*>(p.part_o);
   const size_t ml_base = static_cast<size_t>(slot0) * kNSub * kBM + t * kBM + row;
-  const size_t o_base = (static_cast<size_t>(slot0) * kNSub + t) * (D / 4) + cb * 4;
+  const size_t o_base = (static_cast<size_t>(slot0) * kNSub + t) * (D / 8) + cb * 2;
   constexpr size_t kMlStride = kNSub * kBM;      // per piece, in float2
-  constexpr size_t kOStride = kNSub * (D / 4);   // per piece, in 4-column groups
+  constexpr size_t kOStride = kNSub * (D / 8);   // per piece, in 8-column groups
   float M = -INFINITY;
   for (int s0 = 0; s0 < ns; s0 += 8) {
     float mv[8];
@@ -726,26 +733,29 @@ __global__ void __launch_bounds__(kBM) attn_combine_kernel(const __grid_constant
   if (M != -INFINITY) {
     for (int s0 = 0; s0 < ns; s0 += 4) {
       float2 mlv[4];
-      float4 x[4][4];
+      uint4 x[4][2];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const bool in = s0 + i < ns;
         mlv[i] = in ? __ldcg(ml + ml_base + (s0 + i) * kMlStride) : make_float2(-INFINITY, 0.0f);
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          x[i][c] = in ? __ldcg(po + (o_base + (s0 + i) * kOStride + c) * kBM + row) : make_float4(0, 0, 0, 0);
+        for (int c = 0; c < 2; ++c)
+          x[i][c] = in ? __ldcg(po + (o_base + (s0 + i) * kOStride + c) * kBM + row) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        if (mlv[i].x == -INFINITY) continue;   // an empty piece (its u was never written)
-        const float w = ex2_approx(mlv[i].x - M);
-        L += w * mlv[i].y;
+        if (mlv[i].x == -INFINITY) continue;   // an empty piece (its O_s was never written)
+        const float w = ex2_approx(mlv[i].x - M) * mlv[i].y;
+        L += w;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          acc[4 * c] += w * x[i][c].x;
-          acc[4 * c + 1] += w * x[i][c].y;
-          acc[4 * c + 2] += w * x[i][c].z;
-          acc[4 * c + 3] += w * x[i][c].w;
+        for (int c = 0; c < 2; ++c) {
+          const uint32_t wds[4] = {x[i][c].x, x[i][c].y, x[i][c].z, x[i][c].w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wds[k]));
+            acc[8 * c + 2 * k] += w * f.x;
+            acc[8 * c + 2 * k + 1] += w * f.y;
+          }
         }
       }
     }

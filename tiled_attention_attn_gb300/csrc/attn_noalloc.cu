@@ -147,7 +147,7 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
       st.off_cta = align256(st.units.size() * sizeof(int));
       st.off_groups = st.off_cta + align256(pl.cta_off.size() * sizeof(int));
       const size_t sched = st.off_groups + align256(st.groups.size() * sizeof(int));
-      st.off_ml = align256(static_cast<size_t>(pl.n_partials) * kNSub * kBM * d * sizeof(float));
+      st.off_ml = align256(static_cast<size_t>(pl.n_partials) * kNSub * kBM * d * 2);   // fp16 partials
       const size_t part = st.off_ml + static_cast<size_t>(pl.n_partials) * kNSub * kBM * 2 * sizeof(float);
       if (sched > kSchedBytes || part > kPartBytes) return ATTN_ETOOLARGE;
       st.key = key;
@@ -168,7 +168,7 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
     }
     p.units = reinterpret_cast<const int*>(st.scratch);
     p.cta_off = reinterpret_cast<const int*>(st.scratch + st.off_cta);
-    p.part_o = reinterpret_cast<float*>(st.scratch + kSchedBytes);
+    p.part_o = st.scratch + kSchedBytes;
     p.part_ml = reinterpret_cast<float*>(st.scratch + kSchedBytes + st.off_ml);
     grid = st.plan.n_ctas;
     combine = !st.plan.groups.empty();

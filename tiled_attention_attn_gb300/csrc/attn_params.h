@@ -26,6 +26,8 @@ constexpr int kVarlenMaxB = 4096;   // sequences per varlen call (prefix table i
 constexpr int kUnitInts = 8;        // ints per scheduled work unit
 constexpr int kGroupInts = 4;       // ints per split-KV group
 constexpr int kMaxSplits = 64;      // split pieces per group
+constexpr int kInlineUnits = 200;   // schedules up to this size travel in the kernel parameters
+constexpr int kInlineCtas = 160;
 
 // Phase trace streams and tags (attn_trace_enable).  An event is two 64-bit
 // words: (tag << 56 | sub-tile << 48 | unit << 24 | key tile) and the SM clock.
@@ -52,7 +54,7 @@ struct FwdParams {
   const int* cu_seqlens;       // varlen only
   const int* units;            // dense schedule, kUnitInts per unit, grouped by CTA
   const int* cta_off;          // dense: first unit of every CTA, n_ctas + 1 entries
-  float* part_o;               // split-KV partial accumulators [slot][2][128][D] fp32
+  void* part_o;                // split-KV partial outputs O_s = u_s / l_s, fp16 [slot][2][D/8][128][8]
   float* part_ml;              // split-KV partial (m, l) [slot][2][128][2]
   int* err;                    // device error word
   unsigned long long* trace;   // optional phase trace (traced build, attn_trace_enable), else null
@@ -61,11 +63,17 @@ struct FwdParams {
   int B, Hq, Hkv, Lq, Lk, group;
   float scale_log2;            // scale * log2(e)
   float scale;
+  // A small schedule is copied here so that a CTA learns its first unit from
+  // the launch itself instead of a global-memory read (n_inline = 0: use
+  // units / cta_off).
+  int n_inline;
+  int cta_off_inline[kInlineCtas + 1];
+  int units_inline[kInlineUnits * kUnitInts];
 };
 
 struct CombineParams {
   const int* groups;           // kGroupInts per group: bh, m_block, slot_base, n_split
-  const float* part_o;
+  const void* part_o;
   const float* part_ml;
   void* o;
   float* lse;
