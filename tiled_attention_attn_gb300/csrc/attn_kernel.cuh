@@ -9,7 +9,7 @@
 // CTA layout (320 threads, one CTA per SM):
 //   warps 0-3  softmax warpgroup for query sub-tile 0 (rows 0..127 of the block)
 //   warps 4-7  softmax warpgroup for query sub-tile 1 (rows 128..255)
-//   warp 8     TMA producer: Q block once per unit, K and V tiles through rings
+//   warp 8     TMA producer: Q block once per unit, K and V tiles through one ring
 //   warp 9     TMEM allocator and single-thread tcgen05.mma issuer
 // TMEM (512 columns x 128 lanes, fp32): S_t at columns [128t, 128t+128); P_t
 // (16-bit, two per column) overwrites the first 64 columns of S_t; the
@@ -35,15 +35,18 @@ struct Cfg {
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
   static constexpr int kChunks = D / 64;                  // 128-byte swizzle atoms per row
   static constexpr int kTile = kBM * D * 2;               // bytes of one 128-row tile
-  static constexpr int kNK = (D == 128) ? 2 : 4;          // K ring stages
-  static constexpr int kNV = (D == 128) ? 2 : 4;          // V ring stages
+  // Ring of key/value stages.  Stage use i of a unit holds K tile
+  // kv_begin + i and V tile kv_begin + i - 1 (the first use K only, the last
+  // V only): the P.V of tile j and the S of tile j + 1 read one stage, which
+  // is then released with a single commit.
+  static constexpr int kNS = (D == 128) ? 2 : 4;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kNSub * kTile;
-  static constexpr int kOffV = kOffK + kNK * kTile;
-  static constexpr int kOffBar = kOffV + kNV * kTile;
-  // barriers: q_full, q_empty, k_full[NK], k_empty[NK], v_full[NV], v_empty[NV],
-  //           s_full[2], p_full[2], o_done[2], drain
-  static constexpr int kNBars = 2 + 2 * kNK + 2 * kNV + 7;
+  static constexpr int kOffV = kOffK + kNS * kTile;
+  static constexpr int kOffBar = kOffV + kNS * kTile;
+  // barriers: q_full, q_empty, kv_full[NS], kv_empty[NS], s_full[2], p_full[2],
+  //           o_done[2], drain
+  static constexpr int kNBars = 2 + 2 * kNS + 7;
   static constexpr int kOffMisc = kOffBar + kNBars * 8;   // tmem slot, abort flag, bad flag
   static constexpr int kOffVarlen = kOffMisc + 64;        // varlen unit prefix table
   static constexpr int kSmemDense = kOffVarlen + 1024;    // + alignment slack
@@ -172,12 +175,12 @@ struct RowState {
 
 // Loads S (128 fp32) of this thread's row, masks keys beyond `lim` when
 // MASK, updates (m, l), writes P to TMEM and, when the max moved by more than
-// 2^8, rescales u in TMEM (after the in-flight P.V of the previous tile has
-// completed; the P.V of this tile is issued only after this thread arrives).
+// 2^8, rescales u in TMEM.  The previous tile's P.V has completed by then
+// (the commit that signalled this S was issued after it), and this tile's P.V
+// is issued only after this thread arrives.
 template <bool MASK, bool BF16, int D>
-__device__ __forceinline__ bool softmax_tile(uint32_t t_s, uint32_t t_o, int lim, float c_log2, RowState& st,
-                                             bool first, uint32_t o_done_bar, uint32_t o_parity,
-                                             const WaitCtl& wc) {
+__device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, int lim, float c_log2, RowState& st,
+                                             bool first) {
   float s[128];
   {
     uint32_t r0[32], r1[32], r2[32], r3[32];
@@ -253,8 +256,6 @@ __device__ __forceinline__ bool softmax_tile(uint32_t t_s, uint32_t t_o, int lim
   const float2 sum2 = fadd2(sum_a, sum_b);
   st.l = st.l * r + (sum2.x + sum2.y);
   if (!first && __any_sync(0xffffffffu, resc)) {
-    if (!mbar_wait_warp(o_done_bar, o_parity, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteODone))) return false;
-    tc_fence_after();
 #pragma unroll
     for (int c = 0; c < D / 16; ++c) {
       uint32_t o[16];
@@ -266,7 +267,6 @@ __device__ __forceinline__ bool softmax_tile(uint32_t t_s, uint32_t t_o, int lim
     }
   }
   tmem_wait_st();
-  return true;
 }
 
 // ---------------------------------------------------------------------------
@@ -290,11 +290,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   const uint32_t bar0 = sbase + C::kOffBar;
   const uint32_t b_q_full = bar0;
   const uint32_t b_q_empty = bar0 + 8;
-  auto b_k_full = [&](int s) { return bar0 + 16 + 8 * s; };
-  auto b_k_empty = [&](int s) { return bar0 + 16 + 8 * (C::kNK + s); };
-  auto b_v_full = [&](int s) { return bar0 + 16 + 8 * (2 * C::kNK + s); };
-  auto b_v_empty = [&](int s) { return bar0 + 16 + 8 * (2 * C::kNK + C::kNV + s); };
-  const uint32_t bar_sp = bar0 + 16 + 8 * (2 * C::kNK + 2 * C::kNV);
+  auto b_kv_full = [&](int s) { return bar0 + 16 + 8 * s; };
+  auto b_kv_empty = [&](int s) { return bar0 + 16 + 8 * (C::kNS + s); };
+  const uint32_t bar_sp = bar0 + 16 + 16 * C::kNS;
   auto b_s_full = [&](int t) { return bar_sp + 8 * t; };
   auto b_p_full = [&](int t) { return bar_sp + 16 + 8 * t; };
   auto b_o_done = [&](int t) { return bar_sp + 32 + 8 * t; };
@@ -312,13 +310,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     *bad_flag = 0;
     mbar_init(b_q_full, 1);
     mbar_init(b_q_empty, 1);
-    for (int s = 0; s < C::kNK; ++s) {
-      mbar_init(b_k_full(s), 1);
-      mbar_init(b_k_empty(s), 1);
-    }
-    for (int s = 0; s < C::kNV; ++s) {
-      mbar_init(b_v_full(s), 1);
-      mbar_init(b_v_empty(s), 1);
+    for (int s = 0; s < C::kNS; ++s) {
+      mbar_init(b_kv_full(s), 1);
+      mbar_init(b_kv_empty(s), 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(b_s_full(t), 1);
@@ -393,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     if (lane == 0) {
       Tracer tr;
       tr.init(p, kTrProducer);
-      uint32_t q_cnt = 0, k_cnt = 0, v_cnt = 0;
+      uint32_t q_cnt = 0, kv_cnt = 0;
       for (int u = u_first; u < n_units; u += u_step) {
         Unit U;
         decode_unit<CAUSAL, VARLEN>(p, vl_pref, u, U);
@@ -409,39 +403,36 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         tr.rec(kTagQIssue, 0, u, 0);
         ++q_cnt;
         bool ok = true;
-        for (int j = U.kv_begin; j < U.kv_end && ok; ++j) {
-          const int ks = k_cnt % C::kNK;
-          if (!mbar_wait(b_k_empty(ks), ((k_cnt / C::kNK) & 1) ^ 1, wc,
+        const int n = U.kv_end - U.kv_begin;
+        for (int i = 0; i <= n; ++i) {
+          const int st = kv_cnt % C::kNS;
+          if (!mbar_wait(b_kv_empty(st), ((kv_cnt / C::kNS) & 1) ^ 1, wc,
                          ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKEmpty))) { ok = false; break; }
-          mbar_arrive_expect_tx(b_k_full(ks), C::kTile);
+          const bool hk = i < n, hv = i > 0;
+          mbar_arrive_expect_tx(b_kv_full(st), (hk && hv ? 2 : 1) * C::kTile);
+          if (hk) {
 #pragma unroll
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_load_4d(sK + ks * C::kTile + c * 16384, &p.tm_k, b_k_full(ks), c * 64, U.g,
-                        U.row_k + j * kBN, U.bcoord);
-          tr.rec(kTagKIssue, 0, u, j);
-          ++k_cnt;
-          const int vs = v_cnt % C::kNV;
-          if (!mbar_wait(b_v_empty(vs), ((v_cnt / C::kNV) & 1) ^ 1, wc,
-                         ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteVEmpty))) { ok = false; break; }
-          mbar_arrive_expect_tx(b_v_full(vs), C::kTile);
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_4d(sK + st * C::kTile + c * 16384, &p.tm_k, b_kv_full(st), c * 64, U.g,
+                          U.row_k + (U.kv_begin + i) * kBN, U.bcoord);
+            tr.rec(kTagKIssue, 0, u, U.kv_begin + i);
+          }
+          if (hv) {
 #pragma unroll
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_load_4d(sV + vs * C::kTile + c * 16384, &p.tm_v, b_v_full(vs), c * 64, U.g,
-                        U.row_k + j * kBN, U.bcoord);
-          tr.rec(kTagVIssue, 0, u, j);
-          ++v_cnt;
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_4d(sV + st * C::kTile + c * 16384, &p.tm_v, b_kv_full(st), c * 64, U.g,
+                          U.row_k + (U.kv_begin + i - 1) * kBN, U.bcoord);
+            tr.rec(kTagVIssue, 0, u, U.kv_begin + i - 1);
+          }
+          ++kv_cnt;
         }
         if (!ok) break;
       }
       // On an abort, let loads already issued land before the CTA exits.
       if (*abort_flag) {
-        for (int s = 0; s < C::kNK; ++s) {
-          const uint32_t n = (k_cnt + C::kNK - 1 - s) / C::kNK;   // loads issued into stage s
-          if (n > 0) mbar_wait(b_k_full(s), (n - 1) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteDrain), false);
-        }
-        for (int s = 0; s < C::kNV; ++s) {
-          const uint32_t n = (v_cnt + C::kNV - 1 - s) / C::kNV;
-          if (n > 0) mbar_wait(b_v_full(s), (n - 1) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteDrain), false);
+        for (int s = 0; s < C::kNS; ++s) {
+          const uint32_t n = (kv_cnt + C::kNS - 1 - s) / C::kNS;   // fills issued into stage s
+          if (n > 0) mbar_wait(b_kv_full(s), (n - 1) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteDrain), false);
         }
       }
     }
@@ -457,11 +448,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       Tracer tr;
       tr.init(p, kTrMMA);
       tr.rec(kTagStart, 0, 0, 0);
-      uint32_t q_cnt = 0, k_cnt = 0, v_cnt = 0;
+      uint32_t q_cnt = 0, kv_cnt = 0;
       uint32_t p_cnt0 = 0, p_cnt1 = 0;
-      auto issue_s = [&](int t, int ks) {
+      auto issue_s = [&](int t, int st) {
         const uint64_t a0 = dq0 + ((t * C::kTile) >> 4);
-        const uint64_t b0 = dk0 + ((ks * C::kTile) >> 4);
+        const uint64_t b0 = dk0 + ((st * C::kTile) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
@@ -477,35 +468,38 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if (!mbar_wait(b_q_full, q_cnt & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteQFull))) break;
         tr.rec(kTagQFull, 0, u, 0);
         bool first_pv0 = true, first_pv1 = true;
-        // S for the first tile
+        // first stage use: K of the first tile, S for it
         {
-          const int ks = k_cnt % C::kNK;
-          if (!mbar_wait(b_k_full(ks), (k_cnt / C::kNK) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull))) break;
+          const int st = kv_cnt % C::kNS;
+          if (!mbar_wait(b_kv_full(st), (kv_cnt / C::kNS) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull))) break;
           tr.rec(kTagKFull, 0, u, U.kv_begin);
           for (int t = 0; t < kNSub; ++t)
             if (unit_active(U, t, U.kv_begin)) {
-              issue_s(t, ks);
+              issue_s(t, st);
               tr.rec(kTagSIssue, t, u, U.kv_begin);
             }
-          umma_commit(b_k_empty(ks));
-          ++k_cnt;
+          umma_commit(b_kv_empty(st));
+          ++kv_cnt;
         }
+        // Per tile j: O_t += P_t(j) V(j), then S_t(j+1) = Q_t K(j+1)^T, for
+        // t = 0, 1.  The S of a sub-tile is issued after its P.V, so the
+        // commit that signals S_t(j+1) also covers P_t(j) V(j): the softmax
+        // of tile j+1 may read and rescale u_t.  o_done is committed once per
+        // unit and sub-tile, after its last P.V, for the epilogue.
         for (int j = U.kv_begin; j < U.kv_end; ++j) {
-          const int vs = v_cnt % C::kNV;
+          const int st = kv_cnt % C::kNS;
           tr.rec(kTagVWait, 0, u, j);
-          if (!mbar_wait(b_v_full(vs), (v_cnt / C::kNV) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteVFull))) {
+          if (!mbar_wait(b_kv_full(st), (kv_cnt / C::kNS) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteVFull))) {
             ok = false;
             break;
           }
           tr.rec(kTagVFull, 0, u, j);
           const bool have_next = j + 1 < U.kv_end;
-          const int ks = k_cnt % C::kNK;
-          bool k_ready = false;
 #pragma unroll
           for (int t = 0; t < kNSub; ++t) {
-            if (!ok) break;
             uint32_t& p_cnt = (t == 0) ? p_cnt0 : p_cnt1;
             bool& first_pv = (t == 0) ? first_pv0 : first_pv1;
+            const bool next_s = have_next && unit_active(U, t, j + 1);
             if (unit_active(U, t, j)) {
               tr.rec(kTagPWait, t, u, j);
               if (!mbar_wait(b_p_full(t), p_cnt & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSitePFull))) {
@@ -514,46 +508,28 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
               }
               ++p_cnt;
               // P was written into TMEM by the softmax threads (tcgen05.st):
-              // this fence orders that before the MMA that reads it.  Waits on
-              // TMA-filled barriers need no tcgen05 fence (the transaction
-              // count makes the data visible), and each such fence costs the
-              // issuing thread a drain of its MMAs in flight.
+              // this fence orders that before the MMA that reads it.
               tc_fence_after();
               tr.rec(kTagPFull, t, u, j);
-              const uint64_t bv = dv0 + ((vs * C::kTile) >> 4);
+              const uint64_t bv = dv0 + ((st * C::kTile) >> 4);
 #pragma unroll
               for (int kk = 0; kk < kBN / 16; ++kk)
                 umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, bv + ((kk * 2048) >> 4), kIdescO,
                         (first_pv && kk == 0) ? 0u : 1u);
-              umma_commit(b_o_done(t));
+              if (!next_s) umma_commit(b_o_done(t));
               tr.rec(kTagPVIssue, t, u, j);
               first_pv = false;
             }
-            if (have_next && unit_active(U, t, j + 1)) {
-              if (!k_ready) {
-                if (!mbar_wait(b_k_full(ks), (k_cnt / C::kNK) & 1, wc,
-                               ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull))) {
-                  ok = false;
-                  break;
-                }
-                tr.rec(kTagKFull, 0, u, j + 1);
-                k_ready = true;
-              }
-              issue_s(t, ks);
+            if (next_s) {
+              issue_s(t, st);
               tr.rec(kTagSIssue, t, u, j + 1);
             }
           }
           if (!ok) break;
-          if (have_next) {
-            if (!k_ready) {   // keep the K ring's phases in step even if no sub-tile used the tile
-              if (!mbar_wait(b_k_full(ks), (k_cnt / C::kNK) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull))) break;
-            }
-            umma_commit(b_k_empty(ks));
-            ++k_cnt;
-          }
-          umma_commit(b_v_empty(vs));
-          ++v_cnt;
+          umma_commit(b_kv_empty(st));
+          ++kv_cnt;
         }
+        if (!ok) break;
         umma_commit(b_q_empty);
         tr.rec(kTagUnitEnd, 0, u, 0);
         ++q_cnt;
@@ -571,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const uint32_t t_s = tmem + lane_off + t * 128;
     const uint32_t t_o = tmem + lane_off + 256 + t * 128;
     const float c_log2 = p.scale_log2;
-    uint32_t s_cnt = 0, pv_cnt = 0;
+    uint32_t s_cnt = 0, o_cnt = 0;   // s_full phases seen; units with an o_done commit
     T* out = reinterpret_cast<T*>(p.o);
     Tracer tr;
     tr.init(p, t == 0 ? kTrSoftmax0 : kTrSoftmax1);
@@ -597,23 +573,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         const int lim = lim_key - j * kBN;
         const bool mask_tile = (j * kBN + kBN - 1 > U.k_len - 1) ||
                                (CAUSAL && j * kBN + kBN - 1 > U.q_row0 + t * kBM + (U.k_len - U.q_len));
-        const uint32_t o_par = (pv_cnt - 1) & 1;
-        bool r;
         if (mask_tile)
-          r = softmax_tile<true, BF16, D>(t_s, t_o, lim, c_log2, st, n_act == 0, b_o_done(t), o_par, wc);
+          softmax_tile<true, BF16, D>(t_s, t_o, lim, c_log2, st, n_act == 0);
         else
-          r = softmax_tile<false, BF16, D>(t_s, t_o, lim, c_log2, st, n_act == 0, b_o_done(t), o_par, wc);
-        if (!r) { ok = false; break; }
+          softmax_tile<false, BF16, D>(t_s, t_o, lim, c_log2, st, n_act == 0);
         tc_fence_before();
         mbar_arrive(b_p_full(t));
         tr.rec(kTagPArrive, t, u, j);
-        ++pv_cnt;
         ++n_act;
       }
       if (!ok) break;
       const bool split = U.n_split > 1;
       if (n_act > 0) {
-        if (!mbar_wait_warp(b_o_done(t), (pv_cnt - 1) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteODone))) break;
+        if (!mbar_wait_warp(b_o_done(t), o_cnt & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteODone))) break;
+        ++o_cnt;
         tc_fence_after();
         tr.rec(kTagODone, t, u, 0);
       }
