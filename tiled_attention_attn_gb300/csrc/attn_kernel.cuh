@@ -181,39 +181,53 @@ struct RowState {
 template <bool MASK, bool BF16, int D>
 __device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, int lim, float c_log2, RowState& st,
                                              bool first) {
+  // S in two halves: the second half loads while the first half's max is
+  // taken.  Row max over eight chains of three-input max.
   float s[128];
+  float mx[8];
   {
-    uint32_t r0[32], r1[32], r2[32], r3[32];
+    uint32_t r0[32], r1[32];
     tmem_ld_32x32b_x32(t_s + 0, r0);
     tmem_ld_32x32b_x32(t_s + 32, r1);
-    tmem_ld_32x32b_x32(t_s + 64, r2);
-    tmem_ld_32x32b_x32(t_s + 96, r3);
     tmem_wait_ld(r0);
     tmem_wait_ld(r1);
-    tmem_wait_ld(r2);
-    tmem_wait_ld(r3);
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
       s[i] = __uint_as_float(r0[i]);
       s[32 + i] = __uint_as_float(r1[i]);
+    }
+  }
+  {
+    uint32_t r2[32], r3[32];
+    tmem_ld_32x32b_x32(t_s + 64, r2);
+    tmem_ld_32x32b_x32(t_s + 96, r3);
+    if constexpr (MASK) {
+#pragma unroll
+      for (int i = 0; i < 64; ++i) s[i] = (i <= lim) ? s[i] : -INFINITY;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) mx[k] = fmaxf(s[k], s[k + 8]);
+#pragma unroll
+    for (int i = 16; i < 64; i += 16)
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx[k] = fmax3(mx[k], s[i + k], s[i + 8 + k]);
+    tmem_wait_ld(r2);
+    tmem_wait_ld(r3);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
       s[64 + i] = __uint_as_float(r2[i]);
       s[96 + i] = __uint_as_float(r3[i]);
     }
   }
   if constexpr (MASK) {
 #pragma unroll
-    for (int i = 0; i < 128; ++i) s[i] = (i <= lim) ? s[i] : -INFINITY;
+    for (int i = 64; i < 128; ++i) s[i] = (i <= lim) ? s[i] : -INFINITY;
   }
-  // row max (raw scores) over eight independent chains of two-input max
-  float mx[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) mx[i] = s[i];
+  for (int i = 64; i < 128; i += 16)
 #pragma unroll
-  for (int i = 8; i < 128; i += 8)
-#pragma unroll
-    for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], s[i + k]);
-  const float mx_all = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+    for (int k = 0; k < 8; ++k) mx[k] = fmax3(mx[k], s[i + k], s[i + 8 + k]);
+  const float mx_all = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
   const float m_tile = (mx_all == -INFINITY) ? -INFINITY : mx_all * c_log2;
   const float m_old = st.m;
   bool resc = false;
@@ -316,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(b_s_full(t), 1);
-      mbar_init(b_p_full(t), kBM);
+      mbar_init(b_p_full(t), kBM / 32);   // one arrival per softmax warp
       mbar_init(b_o_done(t), 1);
     }
     mbar_init(b_drain, 1);
@@ -578,7 +592,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         else
           softmax_tile<false, BF16, D>(t_s, t_o, lim, c_log2, st, n_act == 0);
         tc_fence_before();
-        mbar_arrive(b_p_full(t));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_p_full(t));
         tr.rec(kTagPArrive, t, u, j);
         ++n_act;
       }

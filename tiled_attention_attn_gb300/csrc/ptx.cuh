@@ -202,6 +202,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// Three-input maximum (one instruction on sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // Packed two-lane fp32 fused multiply-add and add (one instruction per pair;
 // half-rate on the FMA pipe, so two warps running them leave issue slots to a
 // third, e.g. the MMA issuer on the same sub-partition).
