@@ -103,15 +103,19 @@ def test_noalloc_shape_change_and_varlen():
 
 
 def test_noalloc_refuses_problems_beyond_its_array():
-    # single head, L = 16384, causal: its split-KV partials need more than 20 MiB
-    L, d = 16384, 128
+    # 133120 one-block units (B 1040, 128 query heads on one KV head, L 256,
+    # d 64): the schedule (32 bytes per unit) exceeds the array's 4 MiB
+    # schedule region.  The tensors are allocated at full size (uninitialised)
+    # so that even a launch by mistake would stay inside them.
+    B, Hq, Hkv, L, d = 1040, 128, 1, 256, 64
     n_sms = torch.cuda.get_device_properties(0).multi_processor_count
-    _, _, n_part = attn.plan(1, 1, 1, L, L, d, True, n_sms)
-    assert n_part * 2 * 128 * (2 * d + 8) > (20 << 20)   # fp16 partial outputs + fp32 (m, l)
+    units, _, _ = attn.plan(B, Hq, Hkv, L, L, d, False, n_sms)
+    assert units.shape[0] * 8 * 4 > (4 << 20)
     dev = torch.device("cuda", 0)
-    q = torch.randn(1, L, 1, d, device=dev, dtype=torch.bfloat16)
+    q = torch.empty(B, L, Hq, d, device=dev, dtype=torch.bfloat16)
+    kv = torch.empty(B, L, Hkv, d, device=dev, dtype=torch.bfloat16)
     before = attn.launch_count()
-    o, lse, rc = noalloc(q, q, q, True, d ** -0.5)
+    o, lse, rc = noalloc(q, kv, kv, False, d ** -0.5)
     assert rc == attn.ATTN_ETOOLARGE
     assert attn.launch_count() == before
     assert "static buffer" in attn.strerror(rc)

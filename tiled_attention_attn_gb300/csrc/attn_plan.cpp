@@ -119,7 +119,9 @@ bool make_plan(int B, int Hq, int Hkv, int Lq, int Lk, int d, bool causal, int n
   const double avg = (static_cast<double>(total) + cm.unit * static_cast<double>(pairs.size())) / num_sms;
   std::vector<double> targets = {std::numeric_limits<double>::infinity()};
   if (static_cast<double>(max_cost) > 0.75 * avg) {
-    for (double f : {0.375, 0.5, 0.625, 0.75, 0.875, 1.0, 1.25, 1.5, 2.0, 3.0})
+    // piece sizes are whole key tiles, so the best target can sit anywhere:
+    // a fine grid of fractions of the average CTA load
+    for (double f = 0.25; f <= 3.0 + 1e-9; f += 0.03125)
       if (f * avg >= 1.0) targets.push_back(f * avg);
   }
 
