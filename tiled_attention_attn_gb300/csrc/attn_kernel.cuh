@@ -685,8 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 // with M = max_s m_s and w_s = 2^(m_s - M) l_s (the same r rescaling as
 // across tiles), O = sum_s w_s O_s / sum_s w_s and lse = M ln 2 + ln sum_s w_s.
 // Grid (groups, 2 sub-tiles, D/16 column blocks), one thread per query row
-// and 16 columns; pieces are read four at a time so their loads are in
-// flight together.  Launched as a programmatic dependent of the forward
+// and 16 columns.  Launched as a programmatic dependent of the forward
 // kernel: it may be scheduled early and waits here until that grid has
 // completed and its writes are visible.
 // ---------------------------------------------------------------------------
@@ -706,44 +705,47 @@ __global__ void __launch_bounds__(kBM) attn_combine_kernel(const __grid_constant
   const size_t o_base = (static_cast<size_t>(slot0) * kNSub + t) * (D / 8) + cb * 2;
   constexpr size_t kMlStride = kNSub * kBM;      // per piece, in float2
   constexpr size_t kOStride = kNSub * (D / 8);   // per piece, in 8-column groups
-  float M = -INFINITY;
-  for (int s0 = 0; s0 < ns; s0 += 8) {
-    float mv[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) mv[i] = (s0 + i < ns) ? __ldcg(ml + ml_base + (s0 + i) * kMlStride).x : -INFINITY;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) M = fmaxf(M, mv[i]);
-  }
+  // Pieces in batches of eight: every load of a batch ((m, l) and this
+  // thread's 16 columns of O_s) is issued before any is used, so a batch
+  // costs one L2 round trip.  Batches merge with a running max, the same
+  // r rescaling again.
+  float M = -INFINITY, L = 0.0f;
   float acc[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
-  float L = 0.0f;
-  if (M != -INFINITY) {
-    for (int s0 = 0; s0 < ns; s0 += 4) {
-      float2 mlv[4];
-      uint4 x[4][2];
+  for (int s0 = 0; s0 < ns; s0 += 8) {
+    float2 mlv[8];
+    uint4 x[8][2];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const bool in = s0 + i < ns;
-        mlv[i] = in ? __ldcg(ml + ml_base + (s0 + i) * kMlStride) : make_float2(-INFINITY, 0.0f);
+    for (int i = 0; i < 8; ++i) {
+      const bool in = s0 + i < ns;
+      mlv[i] = in ? __ldcg(ml + ml_base + (s0 + i) * kMlStride) : make_float2(-INFINITY, 0.0f);
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
-          x[i][c] = in ? __ldcg(po + (o_base + (s0 + i) * kOStride + c) * kBM + row) : make_uint4(0, 0, 0, 0);
-      }
+      for (int c = 0; c < 2; ++c)
+        x[i][c] = in ? __ldcg(po + (o_base + (s0 + i) * kOStride + c) * kBM + row) : make_uint4(0, 0, 0, 0);
+    }
+    float mb = M;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        if (mlv[i].x == -INFINITY) continue;   // an empty piece (its O_s was never written)
-        const float w = ex2_approx(mlv[i].x - M) * mlv[i].y;
-        L += w;
+    for (int i = 0; i < 8; ++i) mb = fmaxf(mb, mlv[i].x);
+    if (mb == -INFINITY) continue;   // no piece so far saw a key
+    const float r = (M == -INFINITY) ? 0.0f : ex2_approx(M - mb);
+    M = mb;
+    L *= r;
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const uint32_t wds[4] = {x[i][c].x, x[i][c].y, x[i][c].z, x[i][c].w};
+    for (int i = 0; i < 16; ++i) acc[i] *= r;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wds[k]));
-            acc[8 * c + 2 * k] += w * f.x;
-            acc[8 * c + 2 * k + 1] += w * f.y;
-          }
+    for (int i = 0; i < 8; ++i) {
+      if (mlv[i].x == -INFINITY) continue;   // an empty piece (its O_s was never written)
+      const float w = ex2_approx(mlv[i].x - M) * mlv[i].y;
+      L += w;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        const uint32_t wds[4] = {x[i][c].x, x[i][c].y, x[i][c].z, x[i][c].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wds[k]));
+          acc[8 * c + 2 * k] += w * f.x;
+          acc[8 * c + 2 * k + 1] += w * f.y;
         }
       }
     }
