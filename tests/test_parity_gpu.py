@@ -151,6 +151,23 @@ def test_split_kv_small():
     check(o[idx[:, 0], idx[:, 2], idx[:, 1]], lse[idx[:, 0], idx[:, 1], idx[:, 2]], o_ref, lse_ref, "split")
 
 
+def test_split_kv_more_than_one_merge_batch():
+    # a query block split into more than eight pieces: the merge reads pieces
+    # in batches of eight and rescales across batches (single head, causal,
+    # d 128; L = 12288 gives 10-12 pieces for SM counts from 132 to 160)
+    n_sms = torch.cuda.get_device_properties(0).multi_processor_count
+    L = next((x for x in (12288, 14336, 16384) if attn.plan(1, 1, 1, x, x, 128, True, n_sms)[0][:, 5].max() > 8),
+             None)
+    assert L is not None, "no candidate length splits a block into more than 8 pieces"
+    wl = Workload("split9", B=1, Hq=1, Hkv=1, Lq=L, Lk=L, d=128, dtype="bf16", causal=True, seed=11)
+    inp = generate(wl)
+    o, lse = run(inp, True)
+    rows = sample_rows(wl, 192)
+    o_ref, lse_ref = oracle.attention_rows(inp.q, inp.k, inp.v, rows, causal=True, scale=wl.softmax_scale)
+    idx = np.array(rows)
+    check(o[idx[:, 0], idx[:, 2], idx[:, 1]], lse[idx[:, 0], idx[:, 1], idx[:, 2]], o_ref, lse_ref, "split > 8")
+
+
 # ---------------------------------------------------------------------------
 # the full-size workloads, sampled rows
 # ---------------------------------------------------------------------------

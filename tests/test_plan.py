@@ -94,7 +94,9 @@ def test_headline_plan_is_balanced(attn_lib):
     total = sum(load.values())
     assert total == 2080
     assert n_ctas <= 152
-    assert max(load.values()) <= 1.6 * total / 152
+    # pieces are whole key tiles (two tile pairs): the busiest CTA carries at
+    # most one tile more than the mean load rounded up to whole tiles
+    assert max(load.values()) <= 2 * math.ceil(total / 152 / 2) + 2
     assert n_part > 0   # the longest rows are split along the key range
 
 
