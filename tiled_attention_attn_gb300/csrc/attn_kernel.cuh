@@ -186,21 +186,15 @@ __device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, int lim
   float s[128];
   float mx[8];
   {
-    uint32_t r0[32], r1[32];
-    tmem_ld_32x32b_x32(t_s + 0, r0);
-    tmem_ld_32x32b_x32(t_s + 32, r1);
+    uint32_t r0[64];
+    tmem_ld_32x32b_x64(t_s + 0, r0);
     tmem_wait_ld(r0);
-    tmem_wait_ld(r1);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      s[i] = __uint_as_float(r0[i]);
-      s[32 + i] = __uint_as_float(r1[i]);
-    }
+    for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(r0[i]);
   }
   {
-    uint32_t r2[32], r3[32];
-    tmem_ld_32x32b_x32(t_s + 64, r2);
-    tmem_ld_32x32b_x32(t_s + 96, r3);
+    uint32_t r2[64];
+    tmem_ld_32x32b_x64(t_s + 64, r2);
     if constexpr (MASK) {
 #pragma unroll
       for (int i = 0; i < 64; ++i) s[i] = (i <= lim) ? s[i] : -INFINITY;
@@ -212,12 +206,8 @@ __device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, int lim
 #pragma unroll
       for (int k = 0; k < 8; ++k) mx[k] = fmax3(mx[k], s[i + k], s[i + 8 + k]);
     tmem_wait_ld(r2);
-    tmem_wait_ld(r3);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      s[64 + i] = __uint_as_float(r2[i]);
-      s[96 + i] = __uint_as_float(r3[i]);
-    }
+    for (int i = 0; i < 64; ++i) s[64 + i] = __uint_as_float(r2[i]);
   }
   if constexpr (MASK) {
 #pragma unroll
