@@ -148,6 +148,48 @@ int attn_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float
                      int B, int Hq, int Hkv, int Lq, int Lk, int d, int causal,
                      float scale, const int *cu_seqlens_or_null, cudaStream_t stream);
 
+/*
+ * Padded batches around the varlen forward (the flash-attention
+ * training-integration page, §2.5: drop the padded positions, run the
+ * variable-length call, put the outputs back).  Each call enqueues device
+ * kernels on `stream` and returns without synchronising; device pointers
+ * throughout, owned by the caller.
+ *
+ * attn_unpad_index -- from a key-padding mask (B, L) of bytes, nonzero =
+ *   keep, writes cu_seqlens (B+1 int32: cu[0] = 0, cu[b+1] = cu[b] + kept
+ *   tokens of row b) and indices (B*L int32 slots: indices[cu[b] + k] =
+ *   b*L + i for the k-th kept position i of row b, in order; slots from
+ *   cu[B] on are left untouched).  Kept tokens need not form a prefix.
+ *   Returns ATTN_EINVAL (null pointer, B or L <= 0, B*L >= 2^31) or
+ *   ATTN_ELAUNCH.
+ *
+ * attn_gather_rows -- dst row r = src row indices[r] for r < min(n_max,
+ *   *n_dev) (n_dev is a DEVICE int, e.g. cu_seqlens + B, so no host sync
+ *   is needed; dst must hold n_max rows).  Rows are row_bytes long (a
+ *   multiple of 16); src has src_rows rows and an index outside
+ *   [0, src_rows) moves nothing.  src and dst 16-byte aligned.
+ *
+ * attn_scatter_rows -- dst row indices[r] = src row r for r < min(n_max,
+ *   *n_dev); dst has dst_rows rows (indices outside are skipped) and its
+ *   other rows are left as they are (fill them first, e.g. with zeros).
+ *
+ * attn_scatter_lse -- lse of a varlen call, (Hq, n_max) fp32 (n_max = the
+ *   packed row count passed to attn_fwd), to the padded (B, Hq, L):
+ *   dst[b, h, i] = src[h, r] where indices[r] = b*L + i, r < min(n_max,
+ *   *n_dev); other entries left as they are (fill with -inf first).
+ *
+ * The three return ATTN_OK, ATTN_EINVAL (null pointer, negative count,
+ * row_bytes not a positive multiple of 16, misaligned row pointer, or a
+ * padded extent of 2^31 rows or more) or ATTN_ELAUNCH.
+ */
+int attn_unpad_index(const unsigned char *mask, int B, int L, int *cu_seqlens, int *indices, cudaStream_t stream);
+int attn_gather_rows(const void *src, int src_rows, const int *indices, int n_max, const int *n_dev, int row_bytes,
+                     void *dst, cudaStream_t stream);
+int attn_scatter_rows(const void *src, const int *indices, int n_max, const int *n_dev, int row_bytes, void *dst,
+                      int dst_rows, cudaStream_t stream);
+int attn_scatter_lse(const float *src, const int *indices, int n_max, const int *n_dev, int Hq, int B, int L,
+                     float *dst, cudaStream_t stream);
+
 /* attn_get_error -- synchronises `stream`, then returns ATTN_EDEVICE if any
  * kernel of this library on the current device has reported an error since
  * the last call (and clears it), ATTN_ELAUNCH if the stream itself failed,

@@ -10,7 +10,9 @@ rounded bf16/fp16 inputs to float64 exactly and marshals arrays.  It also
 holds the oracle's own conversion of a packed variable-length batch into the
 padded batch plus key_padding_mask that the pages' MHA module takes
 (lei6393.com training-integration page, §2.5): the oracle evaluates the padded
-form, an independent route to the packed result the CUDA path produces.
+form, an independent route to the packed result the CUDA path produces.  The
+unpad / pad steps of that section (index of the kept tokens, row gather and
+scatter) are written out here too, as plain definitions.
 """
 
 from __future__ import annotations
@@ -237,6 +239,59 @@ def varlen_rows(q, k, v, lengths: Sequence[int], rows: Sequence[Tuple[int, int, 
     kp, _ = pad_packed(k, lengths)
     vp, _ = pad_packed(v, lengths)
     return attention_rows(qp, kp, vp, rows, causal=causal, scale=scale, key_padding_mask=mask)
+
+
+# --------------------------------------------------------------------------
+# padded <-> packed: the unpad / pad steps around the variable-length call
+# (lei6393.com training-integration page, §2.5).  Plain definitions.
+# --------------------------------------------------------------------------
+
+def unpad_index(mask):
+    """Kept tokens of a key-padding mask (B, L), nonzero = keep.
+
+    Returns (cu_seqlens, indices): indices lists b*L + i for every kept
+    position, row by row and in order within a row; cu_seqlens (B+1) holds
+    the running count of kept tokens before each row (cu[0] = 0)."""
+    m = np.asarray(mask) != 0
+    B, L = m.shape
+    cu = [0]
+    idx = []
+    for b in range(B):
+        kept = np.nonzero(m[b])[0]
+        idx.extend(int(b * L + i) for i in kept)
+        cu.append(cu[-1] + len(kept))
+    return np.asarray(cu, np.int64), np.asarray(idx, np.int64)
+
+
+def gather_rows(src, indices):
+    """Rows indices[0], indices[1], ... of src (first axis), stacked."""
+    src = np.asarray(src)
+    out = np.empty((len(indices),) + src.shape[1:], src.dtype)
+    for r, i in enumerate(indices):
+        out[r] = src[int(i)]
+    return out
+
+
+def scatter_rows(src, indices, n_rows: int, fill=0):
+    """An array of n_rows rows of ``fill`` with row indices[r] = src[r]."""
+    src = np.asarray(src)
+    out = np.full((n_rows,) + src.shape[1:], fill, src.dtype)
+    for r, i in enumerate(indices):
+        out[int(i)] = src[r]
+    return out
+
+
+def padded_attention(q, k, v, mask, causal: bool = False, scale: Optional[float] = None):
+    """Attention of a padded self-attention batch (B, L, H, d) with its
+    key-padding mask, as the padded module returns it: kept query rows
+    attend to the kept keys (causal: to those at or before them); padded
+    query positions give O = 0 and lse = -inf (the padded output is filled
+    with zeros around the kept rows)."""
+    m = np.asarray(mask) != 0
+    o, lse = attention(q, k, v, causal=causal, scale=scale, key_padding_mask=m.astype(np.uint8))
+    o[~m] = 0.0
+    lse = np.where(m[:, None, :], lse, -np.inf)
+    return o, lse
 
 
 def standard_attention_traffic_bytes(L: int, d: int, io_bytes: int = 2, score_bytes: int = 4) -> dict:

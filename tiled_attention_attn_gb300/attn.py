@@ -88,6 +88,14 @@ def lib(path: Optional[str] = None):
         ip = ctypes.POINTER(ctypes.c_int)
         L.attn_plan.argtypes = [i, i, i, i, i, i, i, i, ip, i, ip, ip, ip]
         L.attn_plan.restype = i
+        L.attn_unpad_index.argtypes = [vp, i, i, vp, vp, vp]
+        L.attn_unpad_index.restype = i
+        L.attn_gather_rows.argtypes = [vp, i, vp, i, vp, i, vp, vp]
+        L.attn_gather_rows.restype = i
+        L.attn_scatter_rows.argtypes = [vp, vp, i, vp, i, vp, i, vp]
+        L.attn_scatter_rows.restype = i
+        L.attn_scatter_lse.argtypes = [vp, vp, i, vp, i, i, i, vp, vp]
+        L.attn_scatter_lse.restype = i
         if path is None:
             _lib = L
         return L
@@ -160,6 +168,113 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = F
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd")
     return out, lse
+
+
+# ---------------------------------------------------------------------------
+# padded batches around the varlen forward (include/attn.h, attn_unpad_index
+# and the row gather / scatter kernels)
+# ---------------------------------------------------------------------------
+
+def _check_cuda(*ts):
+    for t in ts:
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def unpad_index(key_padding_mask: torch.Tensor, stream: Optional[torch.cuda.Stream] = None):
+    """(cu_seqlens (B+1,), indices (B*L,)) int32 on the mask's device for a
+    (B, L) key-padding mask (True / nonzero = keep); indices[cu[B]:] are
+    unspecified.  No host synchronisation."""
+    if key_padding_mask.dim() != 2:
+        raise ValueError("key_padding_mask is (B, L)")
+    m = key_padding_mask.contiguous()
+    if m.dtype == torch.bool:
+        m = m.view(torch.uint8)
+    if m.dtype != torch.uint8:
+        raise TypeError("key_padding_mask must be bool or uint8")
+    _check_cuda(m)
+    B, L = m.shape
+    cu = torch.empty(B + 1, dtype=torch.int32, device=m.device)
+    idx = torch.empty(B * L, dtype=torch.int32, device=m.device)
+    with torch.cuda.device(m.device):
+        rc = lib().attn_unpad_index(m.data_ptr(), int(B), int(L), cu.data_ptr(), idx.data_ptr(),
+                                    _stream_handle(m.device, stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_unpad_index")
+    return cu, idx
+
+
+def gather_rows(src: torch.Tensor, indices: torch.Tensor, n_dev: torch.Tensor, n_max: int,
+                out: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """out[r] = src[indices[r]] for r < min(n_max, n_dev[0]) along the first axis."""
+    _check_cuda(src, indices, n_dev)
+    if out is None:
+        out = torch.empty((n_max,) + tuple(src.shape[1:]), dtype=src.dtype, device=src.device)
+    _check_cuda(out)
+    row_bytes = src[0].numel() * src.element_size() if src.shape[0] else 0
+    with torch.cuda.device(src.device):
+        rc = lib().attn_gather_rows(src.data_ptr(), int(src.shape[0]), indices.data_ptr(), int(n_max),
+                                    n_dev.data_ptr(), int(row_bytes), out.data_ptr(),
+                                    _stream_handle(src.device, stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_gather_rows")
+    return out
+
+
+def scatter_rows(src: torch.Tensor, indices: torch.Tensor, n_dev: torch.Tensor, out: torch.Tensor,
+                 stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """out[indices[r]] = src[r] for r < min(src rows, n_dev[0]); other rows of out untouched."""
+    _check_cuda(src, indices, n_dev, out)
+    row_bytes = src[0].numel() * src.element_size() if src.shape[0] else 0
+    with torch.cuda.device(src.device):
+        rc = lib().attn_scatter_rows(src.data_ptr(), indices.data_ptr(), int(src.shape[0]), n_dev.data_ptr(),
+                                     int(row_bytes), out.data_ptr(), int(out.shape[0]),
+                                     _stream_handle(src.device, stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_scatter_rows")
+    return out
+
+
+def scatter_lse(src: torch.Tensor, indices: torch.Tensor, n_dev: torch.Tensor, out: torch.Tensor,
+                stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Varlen lse (Hq, n_max) into the padded out (B, Hq, L); other entries untouched."""
+    _check_cuda(src, indices, n_dev, out)
+    Hq, n_max = src.shape
+    B, _, L = out.shape
+    with torch.cuda.device(src.device):
+        rc = lib().attn_scatter_lse(src.data_ptr(), indices.data_ptr(), int(n_max), n_dev.data_ptr(), int(Hq),
+                                    int(B), int(L), out.data_ptr(), _stream_handle(src.device, stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_scatter_lse")
+    return out
+
+
+def attn_fwd_padded(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, key_padding_mask: torch.Tensor,
+                    causal: bool = False, scale: Optional[float] = None,
+                    stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Self-attention of a padded batch (B, L, H, d) with its key-padding mask
+    (B, L), True = keep: the kept tokens are gathered into the packed layout,
+    the varlen forward runs on them, and O (zero at padded positions) and lse
+    (B, Hq, L; -inf at padded positions) are scattered back.  The packed
+    buffers are sized B*L rows, so no step waits for the host."""
+    B, L, Hq, d = q.shape
+    Hkv = k.shape[2]
+    if k.shape != (B, L, Hkv, d) or v.shape != k.shape:
+        raise ValueError("k and v must be (B, L, Hkv, d) like q")
+    if tuple(key_padding_mask.shape) != (B, L):
+        raise ValueError("key_padding_mask must be (B, L)")
+    cu, idx = unpad_index(key_padding_mask, stream)
+    n_dev = cu[B:]
+    N = B * L
+    qp = gather_rows(q.view(N, Hq, d), idx, n_dev, N, stream=stream)
+    kp = gather_rows(k.view(N, Hkv, d), idx, n_dev, N, stream=stream)
+    vp = gather_rows(v.view(N, Hkv, d), idx, n_dev, N, stream=stream)
+    op, lsep = attn_fwd(qp, kp, vp, causal=causal, scale=scale, cu_seqlens=cu, stream=stream)
+    o = torch.zeros_like(q)
+    scatter_rows(op, idx, n_dev, o.view(N, Hq, d), stream=stream)
+    lse = torch.full((B, Hq, L), float("-inf"), dtype=torch.float32, device=q.device)
+    scatter_lse(lsep, idx, n_dev, lse, stream=stream)
+    return o, lse
 
 
 def get_error(stream: Optional[torch.cuda.Stream] = None, device=None) -> int:
