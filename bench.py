@@ -237,7 +237,7 @@ def max_over_ranks(dist, x: float, device) -> float:
 # the CPU oracle on a bounded sample
 # ---------------------------------------------------------------------------
 
-def oracle_sample(wl, inp, budget_s: float, max_rows: int = 4096, seed: int = 99):
+def oracle_sample(wl, inp, budget_s: float, max_rows: int = 400000, seed: int = 99):
     """Times the oracle on sampled rows of the workload for about budget_s
     seconds; returns (TFLOP/s, seconds, n_rows, threads)."""
     import oracle
@@ -330,6 +330,51 @@ def run_reference(args, wl):
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+PAD_SHAPE = (64, 4096, 16, 128)   # B, L, H, d of the padded-batch leg: 1 GiB of bf16, larger than L2
+
+
+def pad_leg(attn, device, stream, peaks, iters: int = 20):
+    """The padded-batch kernels on a padded bf16 batch (B 64, L 4096, H 16,
+    d 128; lengths uniform in [L/2, L] from a fixed seed): the unpad index,
+    the gather of the kept rows into the packed layout and the scatter back.
+    Bound: HBM.  Algorithmic bytes of a gather or scatter: each kept row read
+    once and written once, plus its 4-byte index."""
+    B, L, H, d = PAD_SHAPE
+    g = torch.Generator().manual_seed(77)
+    lengths = torch.randint(L // 2, L + 1, (B,), generator=g)
+    mask = (torch.arange(L)[None, :] < lengths[:, None]).to(device)
+    x = torch.randn(B * L, H, d, device=device, dtype=torch.bfloat16)
+    cu, idx = attn.unpad_index(mask, stream)
+    n_dev = cu[B:]
+    packed = torch.empty_like(x)
+    back = torch.zeros_like(x)
+    kept = int(lengths.sum())
+    row = H * d * 2
+    moved = kept * (2 * row + 4)
+
+    def timed(fn):
+        fn()
+        torch.cuda.synchronize(device)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(iters):
+            fn()
+        e.record(stream)
+        torch.cuda.synchronize(device)
+        return s.elapsed_time(e) / iters
+
+    t_idx = timed(lambda: attn.unpad_index(mask, stream))
+    t_g = timed(lambda: attn.gather_rows(x, idx, n_dev, B * L, out=packed, stream=stream))
+    t_s = timed(lambda: attn.scatter_rows(packed, idx, n_dev, back, stream=stream))
+    gbs_g = moved / (t_g / 1e3) / 1e9
+    gbs_s = moved / (t_s / 1e3) / 1e9
+    return {"workload": f"padded bf16 B{B} L{L} H{H} d{d}, {kept} kept rows of {B * L}",
+            "bound": "hbm", "unit": "GB/s", "peak": peaks["hbm_gbs"],
+            "gather": {"achieved": gbs_g, "frac": gbs_g / peaks["hbm_gbs"], "ms": t_g},
+            "scatter": {"achieved": gbs_s, "frac": gbs_s / peaks["hbm_gbs"], "ms": t_s},
+            "unpad_index_ms": t_idx, "algorithmic_bytes_per_launch": moved}
 
 
 def run_ours(args, wl):
@@ -437,6 +482,11 @@ def run_ours(args, wl):
     if attn.get_error() != attn.ATTN_OK:
         raise RuntimeError(f"device error in the e2e leg: {attn.last_device_error():#x}")
 
+    # ---- padded batches: unpad index and row gather / scatter (HBM-bound)
+    pad = None
+    if not args.no_pad_leg:
+        pad = pad_leg(attn, device, stream, peaks)
+
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -453,7 +503,7 @@ def run_ours(args, wl):
                            l2="256 MiB buffer written before every step, outside the per-step CUDA events"),
             "pct_of_peak": 100.0 * value / world / peaks["bf16_tflops"],
             "clocks": clocks, "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
-            "cpu_baseline": cpu,
+            "cpu_baseline": cpu, "pad_unpad": pad,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -471,6 +521,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=500)
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-pad-leg", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
