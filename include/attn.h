@@ -149,6 +149,25 @@ int attn_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float
                      float scale, const int *cu_seqlens_or_null, cudaStream_t stream);
 
 /*
+ * attn_fwd_varlen -- the packed (varlen) forward with separate query and key
+ * offsets: cross-attention between packed batches, and queries that extend a
+ * key/value cache (training page §2.4 cross-attention; §4, rotary offsets
+ * from the cache length during generation).  q, o are (total_q, Hq, d), k, v
+ * are (total_k, Hkv, d); sequence b has queries cu_seqlens_q[b] ..
+ * cu_seqlens_q[b+1] - 1 and keys cu_seqlens_k[b] .. cu_seqlens_k[b+1] - 1 (both
+ * device int32 arrays of B+1 entries, 0 first, non-decreasing, last entry
+ * at most the total; checked by the kernel as for attn_fwd).  Causal aligns
+ * bottom-right per sequence: query i of a sequence with Lq_b queries and Lk_b
+ * keys sees key j iff j <= i + Lk_b - Lq_b (the queries are the last Lq_b
+ * positions, as when a cache of Lk_b - Lq_b tokens precedes them); a query
+ * that sees no key gives O = 0, lse = -inf.  lse is (Hq, total_q).  fp16 = 0
+ * selects bf16 tensors, 1 fp16.  B <= 4096.  Return codes as attn_fwd.
+ */
+int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv,
+                    int total_q, int total_k, int d, int causal, float scale, const int *cu_seqlens_q,
+                    const int *cu_seqlens_k, int fp16, cudaStream_t stream);
+
+/*
  * Padded batches around the varlen forward (the flash-attention
  * training-integration page, §2.5: drop the padded positions, run the
  * variable-length call, put the outputs back).  Each call enqueues device

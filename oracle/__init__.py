@@ -241,6 +241,31 @@ def varlen_rows(q, k, v, lengths: Sequence[int], rows: Sequence[Tuple[int, int, 
     return attention_rows(qp, kp, vp, rows, causal=causal, scale=scale, key_padding_mask=mask)
 
 
+def varlen_cross_attention(q, k, v, lengths_q: Sequence[int], lengths_k: Sequence[int], causal: bool = False,
+                           scale: Optional[float] = None):
+    """Packed varlen attention with separate query and key lengths
+    (cross-attention, or queries extending a key/value cache: training page
+    §2.4, §4), one dense call per sequence.  q packed (total_q, Hq, d); k, v
+    packed (total_k, Hkv, d).  Causal aligns each sequence bottom-right (its
+    queries are the last Lq_b of Lk_b positions).  Returns O (total_q, Hq, d)
+    and lse (Hq, total_q); a query with no key gives O = 0, lse = -inf."""
+    q, k, v = f64(q), f64(k), f64(v)
+    Hq, d = q.shape[1], q.shape[2]
+    o = np.zeros((q.shape[0], Hq, d), np.float64)
+    lse = np.full((Hq, q.shape[0]), -np.inf, np.float64)
+    oq = ok = 0
+    for nq, nk in zip(lengths_q, lengths_k):
+        nq, nk = int(nq), int(nk)
+        if nq > 0 and nk > 0:
+            ob, lb = attention(q[None, oq:oq + nq], k[None, ok:ok + nk], v[None, ok:ok + nk], causal=causal,
+                               scale=scale)
+            o[oq:oq + nq] = ob[0]
+            lse[:, oq:oq + nq] = lb[0]
+        oq += nq
+        ok += nk
+    return o, lse
+
+
 # --------------------------------------------------------------------------
 # padded <-> packed: the unpad / pad steps around the variable-length call
 # (lei6393.com training-integration page, §2.5).  Plain definitions.

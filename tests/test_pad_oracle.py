@@ -62,3 +62,4 @@ def test_padded_attention_prefix_mask_equals_varlen():
         assert np.allclose(oracle.gather_rows(o_pad.reshape(-1, H, d), idx), o_var, atol=1e-13)
         assert np.all(o_pad[mask == 0] == 0.0)
         assert np.all(np.isneginf(lse_pad.transpose(0, 2, 1)[mask == 0]))
+

@@ -64,6 +64,8 @@ def lib(path: Optional[str] = None):
             fn = getattr(L, name)
             fn.argtypes = fwd_args
             fn.restype = i
+        L.attn_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp, vp, i, vp]
+        L.attn_fwd_varlen.restype = i
         L.attn_get_error.argtypes = [vp]
         L.attn_get_error.restype = i
         L.attn_last_device_error.argtypes = []
@@ -113,13 +115,16 @@ def _stream_handle(device: torch.device, stream: Optional[torch.cuda.Stream]) ->
 def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
              scale: Optional[float] = None, cu_seqlens: Optional[torch.Tensor] = None,
              out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-             stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+             stream: Optional[torch.cuda.Stream] = None,
+             cu_seqlens_k: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor]:
     """O = softmax(scale * Q K^T [+ causal mask]) V and the row log-sum-exp.
 
     Dense: q (B, Lq, Hq, d), k and v (B, Lk, Hkv, d); returns O like q and
     lse (B, Hq, Lq) float32.  Varlen (``cu_seqlens`` given, int32 on the
     device, B+1 entries): q, k, v packed (total, H, d); lse is (Hq, total).
-    ``scale`` defaults to 1/sqrt(d).
+    With ``cu_seqlens_k`` as well, the keys have their own offsets (k, v
+    packed as (total_k, Hkv, d)): cross-attention or a key/value cache, causal
+    aligned bottom-right per sequence.  ``scale`` defaults to 1/sqrt(d).
     """
     if q.dtype not in (torch.bfloat16, torch.float16):
         raise TypeError("q, k, v must be bfloat16 or float16")
@@ -134,11 +139,16 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = F
     d = q.shape[-1]
     if scale is None:
         scale = 1.0 / math.sqrt(d)
+    if cu_seqlens_k is not None and cu_seqlens is None:
+        raise ValueError("cu_seqlens_k needs cu_seqlens")
     if cu_seqlens is not None:
         if q.dim() != 3 or k.dim() != 3:
             raise ValueError("varlen q, k, v are (total, H, d)")
         if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda:
             raise ValueError("cu_seqlens must be an int32 CUDA tensor")
+        if cu_seqlens_k is not None and (cu_seqlens_k.dtype != torch.int32 or not cu_seqlens_k.is_cuda
+                                         or cu_seqlens_k.numel() != cu_seqlens.numel()):
+            raise ValueError("cu_seqlens_k must be an int32 CUDA tensor with as many entries as cu_seqlens")
         B = cu_seqlens.numel() - 1
         Lq, Hq, _ = q.shape
         Lk, Hkv, _ = k.shape
@@ -160,11 +170,17 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = F
     if tuple(lse.shape) != lse_shape or lse.dtype != torch.float32 or not lse.is_contiguous():
         raise ValueError(f"lse must be a contiguous float32 tensor of shape {lse_shape}")
     L = lib()
-    fn = L.attn_fwd if q.dtype == torch.bfloat16 else L.attn_fwd_fp16
     with torch.cuda.device(q.device):
-        rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                int(B), int(Hq), int(Hkv), int(Lq), int(Lk), int(d), int(bool(causal)),
-                ctypes.c_float(float(scale)), cu_ptr, _stream_handle(q.device, stream))
+        if cu_seqlens_k is not None:
+            rc = L.attn_fwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                   int(B), int(Hq), int(Hkv), int(Lq), int(Lk), int(d), int(bool(causal)),
+                                   ctypes.c_float(float(scale)), cu_ptr, cu_seqlens_k.data_ptr(),
+                                   int(q.dtype == torch.float16), _stream_handle(q.device, stream))
+        else:
+            fn = L.attn_fwd if q.dtype == torch.bfloat16 else L.attn_fwd_fp16
+            rc = fn(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                    int(B), int(Hq), int(Hkv), int(Lq), int(Lk), int(d), int(bool(causal)),
+                    ctypes.c_float(float(scale)), cu_ptr, _stream_handle(q.device, stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd")
     return out, lse

@@ -211,7 +211,7 @@ int ensure_workspace(DevState& st, int n_partials, int d) {
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int fwd(bool bf16, const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
-        int Lq, int Lk, int d, int causal, float scale, const int* cu, cudaStream_t stream) {
+        int Lq, int Lk, int d, int causal, float scale, const int* cu, const int* cu_k, cudaStream_t stream) {
   // ---- host-side argument checks (nothing is enqueued on failure)
   if (!q || !k || !v || !o || !lse) return ATTN_EINVAL;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4)) return ATTN_EINVAL;
@@ -221,8 +221,12 @@ int fwd(bool bf16, const void* q, const void* k, const void* v, void* o, float* 
   if (!std::isfinite(scale) || scale < 0.0f) return ATTN_EINVAL;
   if (d != 64 && d != 128) return ATTN_EUNSUPPORTED;
   const bool varlen = cu != nullptr;
+  if (!varlen && cu_k != nullptr) return ATTN_EINVAL;
   if (varlen) {
-    if (Lq != Lk || B > kVarlenMaxB) return ATTN_EINVAL;
+    // one offsets array serves queries and keys (self-attention) unless the
+    // keys have their own (cross-attention, a key/value cache)
+    if ((cu_k == nullptr && Lq != Lk) || B > kVarlenMaxB) return ATTN_EINVAL;
+    if (cu_k == nullptr) cu_k = cu;
   }
   // sizes: TMA coordinates and the kernel's row arithmetic are 32-bit
   const long long rows_q = varlen ? static_cast<long long>(Lq) : static_cast<long long>(B) * Lq;
@@ -250,6 +254,7 @@ int fwd(bool bf16, const void* q, const void* k, const void* v, void* o, float* 
   p.o = o;
   p.lse = lse;
   p.cu_seqlens = cu;
+  p.cu_seqlens_k = cu_k;
   p.err = st.err_word;
   p.trace = g_trace;
   p.trace_cap = g_trace_cap;
@@ -369,13 +374,22 @@ extern "C" {
 
 int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Lq,
              int Lk, int d, int causal, float scale, const int* cu_seqlens_or_null, cudaStream_t stream) {
-  return attn::fwd(true, q, k, v, o, lse, B, Hq, Hkv, Lq, Lk, d, causal, scale, cu_seqlens_or_null, stream);
+  return attn::fwd(true, q, k, v, o, lse, B, Hq, Hkv, Lq, Lk, d, causal, scale, cu_seqlens_or_null, nullptr, stream);
 }
 
 int attn_fwd_fp16(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                   int Lq, int Lk, int d, int causal, float scale, const int* cu_seqlens_or_null,
                   cudaStream_t stream) {
-  return attn::fwd(false, q, k, v, o, lse, B, Hq, Hkv, Lq, Lk, d, causal, scale, cu_seqlens_or_null, stream);
+  return attn::fwd(false, q, k, v, o, lse, B, Hq, Hkv, Lq, Lk, d, causal, scale, cu_seqlens_or_null, nullptr,
+                   stream);
+}
+
+int attn_fwd_varlen(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                    int total_q, int total_k, int d, int causal, float scale, const int* cu_seqlens_q,
+                    const int* cu_seqlens_k, int fp16, cudaStream_t stream) {
+  if (!cu_seqlens_q || !cu_seqlens_k || (fp16 != 0 && fp16 != 1)) return ATTN_EINVAL;
+  return attn::fwd(fp16 == 0, q, k, v, o, lse, B, Hq, Hkv, total_q, total_k, d, causal, scale, cu_seqlens_q,
+                   cu_seqlens_k, stream);
 }
 
 int attn_get_error(cudaStream_t stream) {

@@ -111,10 +111,11 @@ __device__ __forceinline__ bool decode_unit(const FwdParams& p, const int* vl_pr
     U.q_row0 = mb * kBlockRows;
     const int s0 = __ldg(p.cu_seqlens + lo);
     const int len = __ldg(p.cu_seqlens + lo + 1) - s0;
+    const int s0k = __ldg(p.cu_seqlens_k + lo);
     U.q_len = len;
-    U.k_len = len;
+    U.k_len = __ldg(p.cu_seqlens_k + lo + 1) - s0k;
     U.row_q = s0;
-    U.row_k = s0;
+    U.row_k = s0k;
     U.bcoord = 0;
     U.split = 0;
     U.n_split = 1;
@@ -336,19 +337,21 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     tma_prefetch_desc(&p.tm_v);
   }
 
-  // varlen: validate cu_seqlens and build the prefix table of units per sequence
+  // varlen: validate cu_seqlens (queries) and cu_seqlens_k (keys) and build
+  // the prefix table of units per sequence
   int n_units = 0, u_first = 0, u_step = 1;
   if constexpr (VARLEN) {
     if (warp == 0) {
       int carry = 0;
       bool bad = false;
-      if (lane == 0 && __ldg(p.cu_seqlens) != 0) bad = true;
+      if (lane == 0 && (__ldg(p.cu_seqlens) != 0 || __ldg(p.cu_seqlens_k) != 0)) bad = true;
       for (int b0 = 0; b0 < p.B; b0 += 32) {
         const int b = b0 + lane;
         int cnt = 0;
         if (b < p.B) {
           const int a = __ldg(p.cu_seqlens + b), e = __ldg(p.cu_seqlens + b + 1);
-          if (e < a || e > p.Lq) bad = true;
+          const int ak = __ldg(p.cu_seqlens_k + b), ek = __ldg(p.cu_seqlens_k + b + 1);
+          if (e < a || e > p.Lq || ek < ak || ek > p.Lk) bad = true;
           const int len = e - a;
           cnt = (len > 0) ? ((len + kBlockRows - 1) / kBlockRows) * p.Hq : 0;
         }

@@ -112,6 +112,7 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
   p.o = o;
   p.lse = lse;
   p.cu_seqlens = cu;
+  p.cu_seqlens_k = cu;   // self-attention: queries and keys share the offsets
   p.err = st.info.err_word;
   p.timeout_ns = wait_timeout_ns();
   p.B = B;

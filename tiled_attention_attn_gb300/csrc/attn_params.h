@@ -51,7 +51,8 @@ struct FwdParams {
   CUtensorMap tm_v;
   void* o;                     // like q
   float* lse;                  // (B, Hq, Lq) or (Hq, total)
-  const int* cu_seqlens;       // varlen only
+  const int* cu_seqlens;       // varlen only: query row offsets (B+1)
+  const int* cu_seqlens_k;     // varlen only: key row offsets (B+1); the same array for self-attention
   const int* units;            // dense schedule, kUnitInts per unit, grouped by CTA
   const int* cta_off;          // dense: first unit of every CTA, n_ctas + 1 entries
   void* part_o;                // split-KV partial outputs O_s = u_s / l_s, fp16 [slot][2][D/8][128][8]
