@@ -255,8 +255,8 @@ def oracle_sample(wl, inp, budget_s: float, max_rows: int = 400000, seed: int = 
         return [(int(x), int(y), int(z)) for x, y, z in zip(b, h, i)]
 
     threads = oracle.num_threads()
-    # calibrate on one batch of rows per thread
-    cal = rows_of(max(threads, 1))
+    # calibrate on 32 rows per thread (fewer leave the call overhead dominant)
+    cal = rows_of(max(threads, 1) * 32)
     t0 = time.perf_counter()
     oracle.attention_rows(q, k, v, cal, causal=wl.causal, scale=wl.softmax_scale)
     t_cal = max(time.perf_counter() - t0, 1e-6)
@@ -377,6 +377,46 @@ def pad_leg(attn, device, stream, peaks, iters: int = 20):
             "unpad_index_ms": t_idx, "algorithmic_bytes_per_launch": moved}
 
 
+CACHE_SHAPE = (16, 16, 4, 128)   # B, Hq, Hkv, d of the key/value-cache leg
+
+
+def cache_leg(attn, device, stream, peaks, iters: int = 20):
+    """Queries extending a key/value cache through attn_fwd_varlen: B 16
+    sequences of Lq_b ~ U[64, 512] new tokens over Lk_b = Lq_b + cache_b keys
+    (cache_b ~ U[0, 4096]), GQA 16/4, d 128, bf16, causal (bottom-right).
+    FLOPs: 4 * d * Hq * (allowed query-key pairs, counted exactly).  Inputs
+    (~21 MB) fit in L2, so each timed call follows a 256 MiB buffer write."""
+    B, Hq, Hkv, d = CACHE_SHAPE
+    g = torch.Generator().manual_seed(88)
+    lq = torch.randint(64, 513, (B,), generator=g)
+    cache = torch.randint(0, 4097, (B,), generator=g)
+    lk = lq + cache
+    q = torch.randn(int(lq.sum()), Hq, d, generator=g).to(torch.bfloat16).to(device)
+    k = torch.randn(int(lk.sum()), Hkv, d, generator=g).to(torch.bfloat16).to(device)
+    v = torch.randn(int(lk.sum()), Hkv, d, generator=g).to(torch.bfloat16).to(device)
+    cu_q = torch.tensor([0] + torch.cumsum(lq, 0).tolist(), dtype=torch.int32, device=device)
+    cu_k = torch.tensor([0] + torch.cumsum(lk, 0).tolist(), dtype=torch.int32, device=device)
+    pairs = sum(int(a) * int(c) + int(a) * (int(a) + 1) // 2 for a, c in zip(lq, cache))
+    flops = 4.0 * d * Hq * pairs
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    o, lse = attn.attn_fwd(q, k, v, causal=True, cu_seqlens=cu_q, cu_seqlens_k=cu_k, stream=stream)
+    torch.cuda.synchronize(device)
+    ms = []
+    for _ in range(iters):
+        flush.zero_()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        attn.attn_fwd(q, k, v, causal=True, cu_seqlens=cu_q, cu_seqlens_k=cu_k, out=o, lse=lse, stream=stream)
+        e.record(stream)
+        torch.cuda.synchronize(device)
+        ms.append(s.elapsed_time(e))
+    t = statistics.median(ms)
+    tf = flops / (t / 1e3) / 1e12
+    return {"workload": f"kv cache: B{B} Hq{Hq} Hkv{Hkv} d{d} bf16 causal, Lq~U[64,512], cache~U[0,4096]",
+            "value": tf, "unit": "TFLOP/s", "frac": tf / peaks["bf16_tflops"], "ms": t,
+            "flops_per_call": flops, "query_tokens": int(lq.sum()), "key_tokens": int(lk.sum())}
+
+
 def run_ours(args, wl):
     from tiled_attention_attn_gb300 import attn, build
 
@@ -483,9 +523,10 @@ def run_ours(args, wl):
         raise RuntimeError(f"device error in the e2e leg: {attn.last_device_error():#x}")
 
     # ---- padded batches: unpad index and row gather / scatter (HBM-bound)
-    pad = None
+    pad = cache = None
     if not args.no_pad_leg:
         pad = pad_leg(attn, device, stream, peaks)
+        cache = cache_leg(attn, device, stream, peaks)
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1)
     cpu = None
@@ -503,7 +544,7 @@ def run_ours(args, wl):
                            l2="256 MiB buffer written before every step, outside the per-step CUDA events"),
             "pct_of_peak": 100.0 * value / world / peaks["bf16_tflops"],
             "clocks": clocks, "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
-            "cpu_baseline": cpu, "pad_unpad": pad,
+            "cpu_baseline": cpu, "pad_unpad": pad, "kv_cache": cache,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -521,7 +562,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=500)
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-pad-leg", action="store_true")
+    ap.add_argument("--no-pad-leg", action="store_true", help="skip the padded-batch and kv-cache legs")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
