@@ -168,6 +168,25 @@ int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float 
                     const int *cu_seqlens_k, int fp16, cudaStream_t stream);
 
 /*
+ * attn_rotary -- rotary position embedding of a Q or K tensor (training
+ * page §4: rotary dimension, base frequency, GPT-NeoX or GPT-J pairing, and a
+ * position offset that starts new tokens at the cache length).  x and y are
+ * (B, L, H, d) (dense) or packed (total, H, d) with cu_seqlens (device, B+1);
+ * y may be x (in place) or a disjoint buffer (a partial overlap is
+ * ATTN_EINVAL).  Token i of sequence b sits at position i + offsets[b]
+ * (offsets: device int32 array of B, or null for 0).  For pair p <
+ * rot_dim/2 (the features (p, p + rot_dim/2), or (2p, 2p+1) when
+ * interleaved), with a = position * base^(-2p / rot_dim), (x1, x2) becomes
+ * (x1 cos a - x2 sin a, x1 sin a + x2 cos a); features from rot_dim on are
+ * copied.  rot_dim even, 0 < rot_dim <= d; base > 1; fp16 = 0 bf16, 1 fp16.
+ * fp32 arithmetic, result rounded to the tensor's type.  Returns ATTN_OK,
+ * ATTN_EINVAL or ATTN_ELAUNCH.
+ */
+int attn_rotary(const void *x, void *y, int B, int L, int H, int d, int rot_dim, float base, int interleaved,
+                const int *cu_seqlens_or_null, int total, const int *offsets_or_null, int fp16,
+                cudaStream_t stream);
+
+/*
  * Padded batches around the varlen forward (the flash-attention
  * training-integration page, §2.5: drop the padded positions, run the
  * variable-length call, put the outputs back).  Each call enqueues device

@@ -319,6 +319,26 @@ def padded_attention(q, k, v, mask, causal: bool = False, scale: Optional[float]
     return o, lse
 
 
+def rotary(x, positions, rot_dim: int, base: float = 10000.0, interleaved: bool = False):
+    """Rotary position embedding in float64 (training page §4): x (N, H, d)
+    with one position per row N.  Pair p < rot_dim/2 is (p, p + rot_dim/2)
+    (GPT-NeoX) or (2p, 2p+1) (GPT-J); with a = position * base^(-2p/rot_dim)
+    it becomes (x1 cos a - x2 sin a, x1 sin a + x2 cos a).  Features from
+    rot_dim on are unchanged."""
+    x = f64(x)
+    pos = np.asarray(positions, np.float64)
+    out = x.copy()
+    half = rot_dim // 2
+    for p in range(half):
+        a = pos * base ** (-2.0 * p / rot_dim)
+        c, s = np.cos(a)[:, None], np.sin(a)[:, None]
+        i1, i2 = (2 * p, 2 * p + 1) if interleaved else (p, p + half)
+        x1, x2 = x[:, :, i1], x[:, :, i2]
+        out[:, :, i1] = x1 * c - x2 * s
+        out[:, :, i2] = x1 * s + x2 * c
+    return out
+
+
 def standard_attention_traffic_bytes(L: int, d: int, io_bytes: int = 2, score_bytes: int = 4) -> dict:
     """Byte count of the materialising (standard) attention for one head, as
     the clxhxhhr.top S23-J17 §3 table accounts it: Q, K, V read and O written

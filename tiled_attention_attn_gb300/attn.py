@@ -90,6 +90,8 @@ def lib(path: Optional[str] = None):
         ip = ctypes.POINTER(ctypes.c_int)
         L.attn_plan.argtypes = [i, i, i, i, i, i, i, i, ip, i, ip, ip, ip]
         L.attn_plan.restype = i
+        L.attn_rotary.argtypes = [vp, vp, i, i, i, i, i, f, i, vp, i, vp, i, vp]
+        L.attn_rotary.restype = i
         L.attn_unpad_index.argtypes = [vp, i, i, vp, vp, vp]
         L.attn_unpad_index.restype = i
         L.attn_gather_rows.argtypes = [vp, i, vp, i, vp, i, vp, vp]
@@ -291,6 +293,48 @@ def attn_fwd_padded(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, key_paddi
     lse = torch.full((B, Hq, L), float("-inf"), dtype=torch.float32, device=q.device)
     scatter_lse(lsep, idx, n_dev, lse, stream=stream)
     return o, lse
+
+
+def rotary(x: torch.Tensor, rot_dim: Optional[int] = None, base: float = 10000.0, interleaved: bool = False,
+           cu_seqlens: Optional[torch.Tensor] = None, offsets: Optional[torch.Tensor] = None,
+           out: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Rotary position embedding of x: (B, L, H, d), or packed (total, H, d)
+    with ``cu_seqlens``.  Token i of sequence b is at position i + offsets[b]
+    (``offsets``: int32 CUDA tensor of B, e.g. cache lengths).  ``out`` may be
+    x itself (in place); default a new tensor."""
+    if x.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError("x must be bfloat16 or float16")
+    _check_cuda(x)
+    d = x.shape[-1]
+    rot = d if rot_dim is None else int(rot_dim)
+    if cu_seqlens is not None:
+        if x.dim() != 3:
+            raise ValueError("packed x is (total, H, d)")
+        _check_cuda(cu_seqlens)
+        B, L, H, total = cu_seqlens.numel() - 1, 0, x.shape[1], x.shape[0]
+    else:
+        if x.dim() != 4:
+            raise ValueError("dense x is (B, L, H, d)")
+        B, L, H = x.shape[0], x.shape[1], x.shape[2]
+        total = 0
+    if offsets is not None:
+        _check_cuda(offsets)
+        if offsets.dtype != torch.int32 or offsets.numel() != B:
+            raise ValueError("offsets must be int32 with one entry per sequence")
+    if out is None:
+        out = torch.empty_like(x)
+    if out.shape != x.shape or out.dtype != x.dtype:
+        raise ValueError("out must be shaped like x")
+    _check_cuda(out)
+    with torch.cuda.device(x.device):
+        rc = lib().attn_rotary(x.data_ptr(), out.data_ptr(), int(B), int(L), int(H), int(d), rot,
+                               ctypes.c_float(float(base)), int(bool(interleaved)),
+                               cu_seqlens.data_ptr() if cu_seqlens is not None else None, int(total),
+                               offsets.data_ptr() if offsets is not None else None,
+                               int(x.dtype == torch.float16), _stream_handle(x.device, stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_rotary")
+    return out
 
 
 def get_error(stream: Optional[torch.cuda.Stream] = None, device=None) -> int:

@@ -1,0 +1,148 @@
+// Rotary position embedding of Q or K (training-integration page
+// inference.lei6393.com, 07-usage-tutorial/02-training-integration, §4:
+// rotary dimension, base frequency, GPT-NeoX or GPT-J pairing, and a position
+// offset that starts new tokens at the cache length).  For pair i of the
+// first rot_dim features (i < rot_dim / 2) the angle is
+//   a = position * base^(-2 i / rot_dim)
+// and the pair (x1, x2) becomes (x1 cos a - x2 sin a, x1 sin a + x2 cos a);
+// the pair is (i, i + rot_dim/2) for GPT-NeoX and (2i, 2i+1) for GPT-J;
+// features from rot_dim on are copied.  fp32 arithmetic on 16-bit data;
+// bound by HBM.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "attn.h"
+#include "attn_internal.h"
+
+namespace attn {
+namespace {
+
+constexpr int kThreads = 256;
+
+template <bool BF16>
+__device__ __forceinline__ float ld16(const uint16_t* p) {
+  const uint16_t v = *p;
+  if constexpr (BF16) return __bfloat162float(__ushort_as_bfloat16(v));
+  return __half2float(__ushort_as_half(v));
+}
+template <bool BF16>
+__device__ __forceinline__ void st16(uint16_t* p, float x) {
+  if constexpr (BF16) *p = __bfloat16_as_ushort(__float2bfloat16_rn(x));
+  else *p = __half_as_ushort(__float2half_rn(x));
+}
+
+// token r of a (rows, H, d) tensor: its sequence b and position in it
+__device__ __forceinline__ int position_of(int r, int L, const int* cu, int B, const int* offset) {
+  int b, i;
+  if (cu == nullptr) {
+    b = r / L;
+    i = r - b * L;
+  } else {
+    int lo = 0, hi = B;   // largest b with cu[b] <= r
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(cu + mid) <= r) lo = mid; else hi = mid;
+    }
+    b = lo;
+    i = r - __ldg(cu + b);
+  }
+  return i + (offset ? __ldg(offset + b) : 0);
+}
+
+// Work items per (token, head): groups of 4 rotated pairs, then groups of 8
+// copied tail features (none when rotating in place).  A thread owns whole
+// pairs (it loads both members before it stores either), so y == x is safe.
+template <bool BF16, bool GPTJ>
+__global__ void __launch_bounds__(kThreads) rotary_kernel(const uint16_t* x, uint16_t* y,
+                                                          long long rows, int L, int H, int d, int rot,
+                                                          float log2_base, const int* __restrict__ cu, int B,
+                                                          const int* __restrict__ offset, bool in_place) {
+  const int half = rot / 2;
+  const int pair_groups = (half + 3) / 4;
+  const int tail_groups = in_place ? 0 : (d - rot + 7) / 8;
+  const int per = pair_groups + tail_groups;
+  const long long items = rows * H * per;
+  for (long long it = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; it < items;
+       it += static_cast<long long>(gridDim.x) * kThreads) {
+    const long long th = it / per;
+    const int g = static_cast<int>(it - th * per);
+    const long long r = th / H;
+    const uint16_t* xs = x + th * d;
+    uint16_t* ys = y + th * d;
+    if (g >= pair_groups) {   // unrotated features
+      const int c0 = rot + (g - pair_groups) * 8;
+      for (int c = c0; c < min(c0 + 8, d); ++c) ys[c] = xs[c];
+      continue;
+    }
+    const float pos = static_cast<float>(position_of(static_cast<int>(r), L, cu, B, offset));
+    float x1[4], x2[4];
+    int c1[4], c2[4];
+    const int i0 = g * 4;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = i0 + e;
+      c1[e] = GPTJ ? 2 * i : i;
+      c2[e] = GPTJ ? 2 * i + 1 : i + half;
+      if (i < half) {
+        x1[e] = ld16<BF16>(xs + c1[e]);
+        x2[e] = ld16<BF16>(xs + c2[e]);
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = i0 + e;
+      if (i >= half) break;
+      const float theta = exp2f(-2.0f * static_cast<float>(i) / static_cast<float>(rot) * log2_base);
+      float sn, cs;
+      sincosf(pos * theta, &sn, &cs);
+      st16<BF16>(ys + c1[e], x1[e] * cs - x2[e] * sn);
+      st16<BF16>(ys + c2[e], x1[e] * sn + x2[e] * cs);
+    }
+  }
+}
+
+}  // namespace
+}  // namespace attn
+
+extern "C" int attn_rotary(const void* x, void* y, int B, int L, int H, int d, int rot_dim, float base,
+                           int interleaved, const int* cu_seqlens_or_null, int total, const int* offsets_or_null,
+                           int fp16, cudaStream_t stream) {
+  using namespace attn;
+  if (!x || !y || B <= 0 || H <= 0 || d <= 0 || (fp16 != 0 && fp16 != 1)) return ATTN_EINVAL;
+  if (rot_dim <= 0 || rot_dim > d || (rot_dim & 1) || !(base > 1.0f) || !std::isfinite(base)) return ATTN_EINVAL;
+  if (interleaved != 0 && interleaved != 1) return ATTN_EINVAL;
+  const bool varlen = cu_seqlens_or_null != nullptr;
+  if (varlen ? total < 0 : L < 0) return ATTN_EINVAL;
+  const long long rows = varlen ? static_cast<long long>(total) : static_cast<long long>(B) * L;
+  if (rows * H * d > (1LL << 40) || rows > (1LL << 31) - 1) return ATTN_EINVAL;
+  // x and y either the same tensor or disjoint: a partial overlap would race
+  const uintptr_t xa = reinterpret_cast<uintptr_t>(x), ya = reinterpret_cast<uintptr_t>(y);
+  const uintptr_t bytes = static_cast<uintptr_t>(rows * H * d * 2);
+  if (xa != ya && xa < ya + bytes && ya < xa + bytes) return ATTN_EINVAL;
+  if (rows == 0) return ATTN_OK;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return ATTN_ELAUNCH;
+  const bool in_place = xa == ya;
+  const long long items = rows * H * ((rot_dim / 2 + 3) / 4 + (in_place ? 0 : (d - rot_dim + 7) / 8));
+  const long long blocks = (items + kThreads - 1) / kThreads;
+  const int grid = static_cast<int>(blocks < 8LL * sms ? blocks : 8LL * sms);
+  const float lb = std::log2(base);
+  auto* xs = static_cast<const uint16_t*>(x);
+  auto* ys = static_cast<uint16_t*>(y);
+  const int Lr = varlen ? 1 : L;
+  if (fp16 == 0) {
+    if (interleaved) rotary_kernel<true, true><<<grid, kThreads, 0, stream>>>(xs, ys, rows, Lr, H, d, rot_dim, lb, cu_seqlens_or_null, B, offsets_or_null, in_place);
+    else rotary_kernel<true, false><<<grid, kThreads, 0, stream>>>(xs, ys, rows, Lr, H, d, rot_dim, lb, cu_seqlens_or_null, B, offsets_or_null, in_place);
+  } else {
+    if (interleaved) rotary_kernel<false, true><<<grid, kThreads, 0, stream>>>(xs, ys, rows, Lr, H, d, rot_dim, lb, cu_seqlens_or_null, B, offsets_or_null, in_place);
+    else rotary_kernel<false, false><<<grid, kThreads, 0, stream>>>(xs, ys, rows, Lr, H, d, rot_dim, lb, cu_seqlens_or_null, B, offsets_or_null, in_place);
+  }
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
+  count_launch();
+  return ATTN_OK;
+}
