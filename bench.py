@@ -378,6 +378,29 @@ def pad_leg(attn, device, stream, peaks, iters: int = 20):
 
 
 CACHE_SHAPE = (16, 16, 4, 128)   # B, Hq, Hkv, d of the key/value-cache leg
+ROTARY_SHAPE = (2, 8192, 32, 128)   # B, L, H, d of the rotary leg: 128 MiB of bf16
+
+
+def rotary_leg(attn, device, stream, peaks, iters: int = 20):
+    """attn_rotary in place on a (B 2, L 8192, H 32, d 128) bf16 tensor with
+    full rotary dimension (GPT-NeoX pairing).  Bound: HBM; algorithmic bytes
+    = the tensor read once and written once."""
+    B, L, H, d = ROTARY_SHAPE
+    x = torch.randn(B, L, H, d, device=device, dtype=torch.bfloat16)
+    attn.rotary(x, out=x, stream=stream)
+    torch.cuda.synchronize(device)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(iters):
+        attn.rotary(x, out=x, stream=stream)
+    e.record(stream)
+    torch.cuda.synchronize(device)
+    ms = s.elapsed_time(e) / iters
+    moved = 2 * x.numel() * x.element_size()
+    gbs = moved / (ms / 1e3) / 1e9
+    return {"workload": f"rotary in place, bf16 B{B} L{L} H{H} d{d}", "bound": "hbm", "achieved": gbs,
+            "unit": "GB/s", "peak": peaks["hbm_gbs"], "frac": gbs / peaks["hbm_gbs"], "ms": ms,
+            "algorithmic_bytes_per_launch": moved}
 
 
 def cache_leg(attn, device, stream, peaks, iters: int = 20):
@@ -523,10 +546,11 @@ def run_ours(args, wl):
         raise RuntimeError(f"device error in the e2e leg: {attn.last_device_error():#x}")
 
     # ---- padded batches: unpad index and row gather / scatter (HBM-bound)
-    pad = cache = None
+    pad = cache = rot = None
     if not args.no_pad_leg:
         pad = pad_leg(attn, device, stream, peaks)
         cache = cache_leg(attn, device, stream, peaks)
+        rot = rotary_leg(attn, device, stream, peaks)
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1)
     cpu = None
@@ -544,7 +568,7 @@ def run_ours(args, wl):
                            l2="256 MiB buffer written before every step, outside the per-step CUDA events"),
             "pct_of_peak": 100.0 * value / world / peaks["bf16_tflops"],
             "clocks": clocks, "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
-            "cpu_baseline": cpu, "pad_unpad": pad, "kv_cache": cache,
+            "cpu_baseline": cpu, "pad_unpad": pad, "kv_cache": cache, "rotary": rot,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -562,7 +586,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=500)
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-pad-leg", action="store_true", help="skip the padded-batch and kv-cache legs")
+    ap.add_argument("--no-pad-leg", action="store_true", help="skip the padded-batch, kv-cache and rotary legs")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
