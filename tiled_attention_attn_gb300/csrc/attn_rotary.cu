@@ -22,6 +22,7 @@ namespace attn {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kHeadsPerThread = 8;   // heads sharing one thread's sin / cos (vector path)
 
 template <bool BF16>
 __device__ __forceinline__ float ld16(const uint16_t* p) {
@@ -105,6 +106,76 @@ __global__ void __launch_bounds__(kThreads) rotary_kernel(const uint16_t* x, uin
   }
 }
 
+// Vector path (rot_dim a multiple of 16, d a multiple of 8, 16-byte aligned
+// rows): a thread takes one token, one group of 8 pairs and up to 8 heads,
+// forms the 8 (sin, cos) once and applies them to those heads, with 16-byte loads and
+// stores; the pair frequencies come from a table in shared memory.  Tail
+// features are copied 8 at a time.
+template <bool BF16, bool GPTJ>
+__global__ void __launch_bounds__(kThreads) rotary_vec_kernel(const uint16_t* x, uint16_t* y, long long rows, int L,
+                                                              int H, int d, int rot, float log2_base,
+                                                              const int* __restrict__ cu, int B,
+                                                              const int* __restrict__ offset, bool in_place) {
+  __shared__ float theta[256];
+  const int half = rot / 2;
+  for (int i = threadIdx.x; i < half; i += kThreads)
+    theta[i] = exp2f(-2.0f * static_cast<float>(i) / static_cast<float>(rot) * log2_base);
+  __syncthreads();
+  const int pair_groups = half / 8;
+  const int tail_groups = in_place ? 0 : (d - rot) / 8;
+  const int per = pair_groups + tail_groups;
+  const int chunks = (H + kHeadsPerThread - 1) / kHeadsPerThread;
+  const long long items = rows * chunks * per;
+  const long long token_stride = static_cast<long long>(H) * d;
+  for (long long it = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; it < items;
+       it += static_cast<long long>(gridDim.x) * kThreads) {
+    const long long rc = it / per;   // (token, head chunk)
+    const int g = static_cast<int>(it - rc * per);
+    const long long r = rc / chunks;
+    const int h_lo = static_cast<int>(rc - r * chunks) * kHeadsPerThread;
+    const int h_hi = min(h_lo + kHeadsPerThread, H);
+    const uint16_t* xt = x + r * token_stride;
+    uint16_t* yt = y + r * token_stride;
+    if (g >= pair_groups) {
+      const int c0 = rot + (g - pair_groups) * 8;
+      for (int h = h_lo; h < h_hi; ++h)
+        *reinterpret_cast<uint4*>(yt + h * d + c0) = *reinterpret_cast<const uint4*>(xt + h * d + c0);
+      continue;
+    }
+    const float pos = static_cast<float>(position_of(static_cast<int>(r), L, cu, B, offset));
+    float sn[8], cs[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sincosf(pos * theta[8 * g + e], &sn[e], &cs[e]);
+    // the 8 pairs of this group: GPT-NeoX (8g + e, half + 8g + e); GPT-J (16g + 2e, 16g + 2e + 1)
+    const int oa = GPTJ ? 16 * g : 8 * g;
+    const int ob = GPTJ ? 16 * g + 8 : half + 8 * g;
+    for (int h = h_lo; h < h_hi; ++h) {
+      uint16_t va[8], vb[8], ra[8], rb[8];
+      *reinterpret_cast<uint4*>(va) = *reinterpret_cast<const uint4*>(xt + h * d + oa);
+      *reinterpret_cast<uint4*>(vb) = *reinterpret_cast<const uint4*>(xt + h * d + ob);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        // GPT-J: pair e is elements 2e, 2e+1 of the 16 loaded (va holds 0..7, vb 8..15)
+        const uint16_t u1 = GPTJ ? ((2 * e < 8) ? va[2 * e] : vb[2 * e - 8]) : va[e];
+        const uint16_t u2 = GPTJ ? ((2 * e + 1 < 8) ? va[2 * e + 1] : vb[2 * e - 7]) : vb[e];
+        const float x1 = ld16<BF16>(&u1), x2 = ld16<BF16>(&u2);
+        uint16_t o1, o2;
+        st16<BF16>(&o1, x1 * cs[e] - x2 * sn[e]);
+        st16<BF16>(&o2, x1 * sn[e] + x2 * cs[e]);
+        if (GPTJ) {
+          if (2 * e < 8) ra[2 * e] = o1; else rb[2 * e - 8] = o1;
+          if (2 * e + 1 < 8) ra[2 * e + 1] = o2; else rb[2 * e - 7] = o2;
+        } else {
+          ra[e] = o1;
+          rb[e] = o2;
+        }
+      }
+      *reinterpret_cast<uint4*>(yt + h * d + oa) = *reinterpret_cast<const uint4*>(ra);
+      *reinterpret_cast<uint4*>(yt + h * d + ob) = *reinterpret_cast<const uint4*>(rb);
+    }
+  }
+}
+
 }  // namespace
 }  // namespace attn
 
@@ -128,14 +199,25 @@ extern "C" int attn_rotary(const void* x, void* y, int B, int L, int H, int d, i
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return ATTN_ELAUNCH;
   const bool in_place = xa == ya;
-  const long long items = rows * H * ((rot_dim / 2 + 3) / 4 + (in_place ? 0 : (d - rot_dim + 7) / 8));
+  const bool vec = (rot_dim % 16 == 0) && (d % 8 == 0) && rot_dim <= 512 && (xa % 16 == 0) && (ya % 16 == 0);
+  const long long items = vec ? rows * ((H + kHeadsPerThread - 1) / kHeadsPerThread) *
+                                    (rot_dim / 16 + (in_place ? 0 : (d - rot_dim) / 8))
+                              : rows * H * ((rot_dim / 2 + 3) / 4 + (in_place ? 0 : (d - rot_dim + 7) / 8));
   const long long blocks = (items + kThreads - 1) / kThreads;
   const int grid = static_cast<int>(blocks < 8LL * sms ? blocks : 8LL * sms);
   const float lb = std::log2(base);
   auto* xs = static_cast<const uint16_t*>(x);
   auto* ys = static_cast<uint16_t*>(y);
   const int Lr = varlen ? 1 : L;
-  if (fp16 == 0) {
+  if (vec) {
+    if (fp16 == 0) {
+      if (interleaved) rotary_vec_kernel<true, true><<<grid, kThreads, 0, stream>>>(xs, ys, rows, Lr, H, d, rot_dim, lb, cu_seqlens_or_null, B, offsets_or_null, in_place);
+      else rotary_vec_kernel<true, false><<<grid, kThreads, 0, stream>>>(xs, ys, rows, Lr, H, d, rot_dim, lb, cu_seqlens_or_null, B, offsets_or_null, in_place);
+    } else {
+      if (interleaved) rotary_vec_kernel<false, true><<<grid, kThreads, 0, stream>>>(xs, ys, rows, Lr, H, d, rot_dim, lb, cu_seqlens_or_null, B, offsets_or_null, in_place);
+      else rotary_vec_kernel<false, false><<<grid, kThreads, 0, stream>>>(xs, ys, rows, Lr, H, d, rot_dim, lb, cu_seqlens_or_null, B, offsets_or_null, in_place);
+    }
+  } else if (fp16 == 0) {
     if (interleaved) rotary_kernel<true, true><<<grid, kThreads, 0, stream>>>(xs, ys, rows, Lr, H, d, rot_dim, lb, cu_seqlens_or_null, B, offsets_or_null, in_place);
     else rotary_kernel<true, false><<<grid, kThreads, 0, stream>>>(xs, ys, rows, Lr, H, d, rot_dim, lb, cu_seqlens_or_null, B, offsets_or_null, in_place);
   } else {
