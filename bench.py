@@ -456,6 +456,14 @@ def run_ours(args, wl):
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
     flops = workload_flops(wl, inp.lengths)
     stream = torch.cuda.current_stream(device)
+    if args.legs_only:
+        # the padded-batch, kv-cache and rotary legs alone (for profiling them)
+        peaks = measured_peaks()
+        if rank == 0:
+            print(json.dumps({"pad_unpad": pad_leg(attn, device, stream, peaks),
+                              "kv_cache": cache_leg(attn, device, stream, peaks),
+                              "rotary": rotary_leg(attn, device, stream, peaks)}), flush=True)
+        return 0
 
     def call():
         attn.attn_fwd(q, k, v, causal=wl.causal, scale=wl.softmax_scale, cu_seqlens=cu, out=o, lse=lse)
@@ -587,6 +595,7 @@ def main():
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-pad-leg", action="store_true", help="skip the padded-batch, kv-cache and rotary legs")
+    ap.add_argument("--legs-only", action="store_true", help="run only the padded-batch, kv-cache and rotary legs")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
