@@ -57,6 +57,8 @@ def _load(path: str = LIB):
     lib.oracle_attention_rows.restype = I
     lib.oracle_online_rows.argtypes = [dp, dp, dp, u8p, ip, I, dp, dp, I, I, I, I, I, I, I, D, I, I, dp]
     lib.oracle_online_rows.restype = I
+    lib.oracle_attention_backward.argtypes = [dp, dp, dp, dp, u8p, dp, dp, dp, I, I, I, I, I, I, I, D]
+    lib.oracle_attention_backward.restype = I
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = I
     return lib
@@ -138,6 +140,29 @@ def attention(q, k, v, causal: bool = False, scale: Optional[float] = None,
                             B, Hq, Hkv, Lq, Lk, d, int(bool(causal)), float(scale))
     _check(rc, "oracle_attention")
     return (o, lse, p) if with_probs else (o, lse)
+
+
+def attention_backward(q, k, v, dout, causal: bool = False, scale: Optional[float] = None,
+                       key_padding_mask=None, _lib=None):
+    """Gradients (dq, dk, dv) in float64 of sum(dout * O) for the attention
+    above (training page §5.3 recomputes the weights in the backward; the
+    formulas are the chain rule through the definition, see oracle.c).
+    dout is shaped like q; dq like q, dk and dv like k."""
+    L = _lib or lib()
+    q, k, v, dout = f64(q), f64(k), f64(v), f64(dout)
+    B, Hq, Hkv, Lq, Lk, d = _dims(q, k)
+    if dout.shape != q.shape or v.shape != k.shape:
+        raise ValueError("dout must be shaped like q and v like k")
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    kpm = None if key_padding_mask is None else np.ascontiguousarray(np.asarray(key_padding_mask, dtype=np.uint8))
+    dq = np.empty(q.shape, np.float64)
+    dk = np.empty(k.shape, np.float64)
+    dv = np.empty(k.shape, np.float64)
+    rc = L.oracle_attention_backward(_dp(q), _dp(k), _dp(v), _dp(dout), _u8(kpm), _dp(dq), _dp(dk), _dp(dv),
+                                     B, Hq, Hkv, Lq, Lk, d, int(bool(causal)), float(scale))
+    _check(rc, "oracle_attention_backward")
+    return dq, dk, dv
 
 
 def attention_rows(q, k, v, rows: Sequence[Tuple[int, int, int]], causal: bool = False,

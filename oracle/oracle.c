@@ -364,3 +364,94 @@ int oracle_online_rows(const double *q, const double *k, const double *v,
     free(pv);
     return ORACLE_OK;
 }
+
+/*
+ * Backward pass of the same attention (lei6393.com training-integration page,
+ * §5.3: the backward recomputes the attention weights instead of storing the
+ * O(N^2) matrix).  The pages give no formulas; these are the gradients of the
+ * scalar sum(dout * O) with respect to q, k and v, from the chain rule through
+ * the definition at the top of this file:
+ *
+ *   dP_ij = dout_i . v_j                               (O_i = sum_j P_ij v_j)
+ *   dS_ij = P_ij * (dP_ij - sum_{k in J_i} P_ik dP_ik)  (Jacobian of the row softmax)
+ *   dq_i  = scale * sum_j dS_ij k_j                    (s_ij = scale * q_i . k_j)
+ *   dk_j  = scale * sum_{h in group, i} dS_ij q_i
+ *   dv_j  = sum_{h in group, i} P_ij dout_i
+ *
+ * Each P row is materialised by the forward routine, then its dP and dS rows.
+ * One (batch, KV head) pair per OpenMP task, so dk and dv are summed by one
+ * thread.  dout is (B,Lq,Hq,d) like q; dq like q, dk and dv like k.
+ */
+int oracle_attention_backward(const double *q, const double *k, const double *v,
+                              const double *dout,
+                              const unsigned char *key_padding_mask,
+                              double *dq, double *dk, double *dv, int B, int Hq,
+                              int Hkv, int Lq, int Lk, int d, int causal,
+                              double scale)
+{
+    int rc = check_dims(B, Hq, Hkv, Lq, Lk, d);
+    if (rc)
+        return rc;
+    if (key_padding_mask && Lq != Lk)
+        return ORACLE_EINVAL;
+    const int group = Hq / Hkv;
+    memset(dq, 0, sizeof(double) * (size_t)B * Lq * Hq * d);
+    memset(dk, 0, sizeof(double) * (size_t)B * Lk * Hkv * d);
+    memset(dv, 0, sizeof(double) * (size_t)B * Lk * Hkv * d);
+    const long npairs = (long)B * Hkv;
+    int failed = 0;
+#pragma omp parallel
+    {
+        const size_t nk = (size_t)(Lk > 0 ? Lk : 1);
+        double *s = (double *)malloc(sizeof(double) * nk);
+        double *p = (double *)malloc(sizeof(double) * nk);
+        double *prow = (double *)malloc(sizeof(double) * nk);
+        double *dp = (double *)malloc(sizeof(double) * nk);
+        double *orow = (double *)malloc(sizeof(double) * (size_t)d);
+        if (!s || !p || !prow || !dp || !orow) {
+#pragma omp atomic write
+            failed = 1;
+        } else {
+            long r;
+#pragma omp for schedule(dynamic, 1)
+            for (r = 0; r < npairs; ++r) {
+                const int b = (int)(r / Hkv), g = (int)(r % Hkv);
+                for (int h = g * group; h < (g + 1) * group; ++h) {
+                    for (int i = 0; i < Lq; ++i) {
+                        double lse;
+                        attention_row(q, k, v, key_padding_mask, B, Hq, Hkv, Lq, Lk, d,
+                                      causal, scale, b, h, i, s, p, orow, &lse, prow);
+                        /* dP row and the softmax-weighted mean of dP */
+                        double mean_dp = 0.0;
+                        for (int j = 0; j < Lk; ++j) {
+                            dp[j] = 0.0;
+                            if (prow[j] == 0.0)
+                                continue;
+                            double acc = 0.0;
+                            for (int c = 0; c < d; ++c)
+                                acc += dout[qidx(b, i, h, c, Lq, Hq, d)] * v[kidx(b, j, g, c, Lk, Hkv, d)];
+                            dp[j] = acc;
+                            mean_dp += prow[j] * acc;
+                        }
+                        for (int j = 0; j < Lk; ++j) {
+                            if (prow[j] == 0.0)
+                                continue;
+                            const double ds = prow[j] * (dp[j] - mean_dp);
+                            for (int c = 0; c < d; ++c) {
+                                dq[qidx(b, i, h, c, Lq, Hq, d)] += scale * ds * k[kidx(b, j, g, c, Lk, Hkv, d)];
+                                dk[kidx(b, j, g, c, Lk, Hkv, d)] += scale * ds * q[qidx(b, i, h, c, Lq, Hq, d)];
+                                dv[kidx(b, j, g, c, Lk, Hkv, d)] += prow[j] * dout[qidx(b, i, h, c, Lq, Hq, d)];
+                            }
+                        }
+                    }
+                }
+            }
+        }
+        free(s);
+        free(p);
+        free(prow);
+        free(dp);
+        free(orow);
+    }
+    return failed ? ORACLE_ENOMEM : ORACLE_OK;
+}
