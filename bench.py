@@ -440,6 +440,47 @@ def cache_leg(attn, device, stream, peaks, iters: int = 20):
             "flops_per_call": flops, "query_tokens": int(lq.sum()), "key_tokens": int(lk.sum())}
 
 
+BWD_SHAPE = (2, 32, 8, 4096, 128)   # B, Hq, Hkv, L, d of the backward leg (causal, bf16)
+
+
+def bwd_leg(attn, device, stream, peaks, iters: int = 10):
+    """attn_bwd on B 2, Hq 32, Hkv 8, L 4096, d 128, bf16, causal (the
+    grouped-query training shape), after attn_fwd on the same inputs.  FLOPs
+    counted as the five algorithmic contractions of the backward (S, dP, dv,
+    dk, dq: 2.5 x the forward's 4 d per allowed pair, causal half); the
+    kernels execute seven (S and dP are formed once for dk/dv and again for
+    dq), reported beside it.  L2 flushed before every timed call."""
+    B, Hq, Hkv, L, d = BWD_SHAPE
+    g = torch.Generator().manual_seed(77)
+    q = torch.randn(B, L, Hq, d, generator=g).to(torch.bfloat16).to(device)
+    k = torch.randn(B, L, Hkv, d, generator=g).to(torch.bfloat16).to(device)
+    v = torch.randn(B, L, Hkv, d, generator=g).to(torch.bfloat16).to(device)
+    do = torch.randn(B, L, Hq, d, generator=g).to(torch.bfloat16).to(device)
+    o, lse = attn.attn_fwd(q, k, v, causal=True, stream=stream)
+    dq, dk, dv = attn.attn_bwd(q, k, v, o, lse, do, causal=True, stream=stream)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    torch.cuda.synchronize(device)
+    ms = []
+    for _ in range(iters):
+        flush.zero_()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        attn.attn_bwd(q, k, v, o, lse, do, causal=True, dq=dq, dk=dk, dv=dv, stream=stream)
+        e.record(stream)
+        torch.cuda.synchronize(device)
+        ms.append(s.elapsed_time(e))
+    if attn.get_error() != attn.ATTN_OK:
+        raise RuntimeError(f"device error in the backward leg: {attn.last_device_error():#x}")
+    t = statistics.median(ms)
+    fwd_flops = 4.0 * d * Hq * B * L * L / 2
+    flops = 2.5 * fwd_flops
+    tf = flops / (t / 1e3) / 1e12
+    return {"workload": f"backward: B{B} Hq{Hq} Hkv{Hkv} L{L} d{d} bf16 causal", "value": tf, "unit": "TFLOP/s",
+            "frac": tf / peaks["bf16_tflops"], "ms": t, "algorithmic_flops_per_call": flops,
+            "executed_flops_per_call": 3.5 * fwd_flops,
+            "executed_tflops": 3.5 * fwd_flops / (t / 1e3) / 1e12}
+
+
 def run_ours(args, wl):
     from tiled_attention_attn_gb300 import attn, build
 
@@ -462,7 +503,8 @@ def run_ours(args, wl):
         if rank == 0:
             print(json.dumps({"pad_unpad": pad_leg(attn, device, stream, peaks),
                               "kv_cache": cache_leg(attn, device, stream, peaks),
-                              "rotary": rotary_leg(attn, device, stream, peaks)}), flush=True)
+                              "rotary": rotary_leg(attn, device, stream, peaks),
+                              "backward": bwd_leg(attn, device, stream, peaks)}), flush=True)
         return 0
 
     def call():
@@ -554,10 +596,11 @@ def run_ours(args, wl):
         raise RuntimeError(f"device error in the e2e leg: {attn.last_device_error():#x}")
 
     # ---- padded batches: unpad index and row gather / scatter (HBM-bound)
-    pad = cache = rot = None
+    pad = cache = rot = bwd = None
     if not args.no_pad_leg:
         pad = pad_leg(attn, device, stream, peaks)
         cache = cache_leg(attn, device, stream, peaks)
+        bwd = bwd_leg(attn, device, stream, peaks)
         rot = rotary_leg(attn, device, stream, peaks)
 
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1)
@@ -576,7 +619,7 @@ def run_ours(args, wl):
                            l2="256 MiB buffer written before every step, outside the per-step CUDA events"),
             "pct_of_peak": 100.0 * value / world / peaks["bf16_tflops"],
             "clocks": clocks, "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
-            "cpu_baseline": cpu, "pad_unpad": pad, "kv_cache": cache, "rotary": rot,
+            "cpu_baseline": cpu, "pad_unpad": pad, "kv_cache": cache, "rotary": rot, "backward": bwd,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -594,8 +637,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=500)
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-pad-leg", action="store_true", help="skip the padded-batch, kv-cache and rotary legs")
-    ap.add_argument("--legs-only", action="store_true", help="run only the padded-batch, kv-cache and rotary legs")
+    ap.add_argument("--no-pad-leg", action="store_true", help="skip the padded-batch, kv-cache, rotary and backward legs")
+    ap.add_argument("--legs-only", action="store_true", help="run only the padded-batch, kv-cache, rotary and backward legs")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -168,6 +168,38 @@ int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float 
                     const int *cu_seqlens_k, int fp16, cudaStream_t stream);
 
 /*
+ * attn_bwd -- the backward of the dense forward: the gradients of
+ * sum(dout * O) with respect to q, k and v (training page §5.3: the backward
+ * recomputes the attention weights from what the forward kept, and nothing
+ * of size L x L is stored).  With P_ij = exp(scale q_i.k_j - lse_i) (the
+ * forward's weights, recomputed from its lse), dP_ij = dout_i . v_j and
+ * D_i = dout_i . O_i:
+ *     dS_ij = P_ij (dP_ij - D_i)
+ *     dq_i = scale sum_j dS_ij k_j,  dk_j = scale sum_i dS_ij q_i,  dv_j = sum_i P_ij dout_i
+ * with the sums over the keys j that query i sees (the forward's causal
+ * rule) and, for dk and dv, over the query heads that share the KV head.
+ *
+ * q, o, dout, dq: (B, Lq, Hq, d); k, v, dk, dv: (B, Lk, Hkv, d); all
+ * contiguous 16-bit (fp16 = 0: bf16, 1: fp16), 16-byte aligned device
+ * pointers.  lse: (B, Hq, Lq) fp32 as attn_fwd returns it (a row with
+ * lse = -inf gets no gradient).  o and lse must be the forward's outputs for
+ * the same q, k, v, causal and scale.  dq, dk, dv are overwritten (not
+ * accumulated) and must not overlap the inputs.  d in {64, 128}.
+ *
+ * The library keeps one device workspace per device (8 * B * Hq * Lq bytes,
+ * rounded up), grown with cudaMalloc when a larger problem arrives.  Three
+ * kernels run on `stream` (D_i, then dk and dv, then dq); the call returns
+ * without waiting.  Returns ATTN_EINVAL for null or misaligned pointers and
+ * bad sizes, ATTN_EUNSUPPORTED for another d or device, ATTN_ENOMEM when the
+ * workspace cannot grow, ATTN_ELAUNCH on a launch failure; device-side wait
+ * timeouts are reported by attn_get_error as for attn_fwd.  Varlen batches
+ * are not accepted here.
+ */
+int attn_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse, const void *dout,
+             void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int Lq, int Lk, int d, int causal,
+             float scale, int fp16, cudaStream_t stream);
+
+/*
  * attn_rotary -- rotary position embedding of a Q or K tensor (training
  * page §4: rotary dimension, base frequency, GPT-NeoX or GPT-J pairing, and a
  * position offset that starts new tokens at the cache length).  x and y are

@@ -1,0 +1,130 @@
+"""Parity of attn_bwd (dq, dk, dv) with the oracle's fp64 backward.
+
+The forward runs on the GPU (attn_fwd) and its O and lse feed attn_bwd, as in
+training; the oracle gets the same rounded q, k, v, dout and computes the
+exact gradients of sum(dout * O) from the definition.
+
+Bar, per gradient tensor X (derivation: the kernel rounds P and dS to the
+input type before the tensor-core products, 2^-9 relative each for bf16,
+forms D from the rounded O, and rounds X itself; every one of these is a
+relative error of at most a few 2^-9 of the terms it touches, summed with
+random signs):
+    max |X - X_ref|  <= 2^-6 * max |X_ref|
+    rms (X - X_ref)  <= 2^-7 * rms (X_ref)
+A formula mistake (a missing D, scale, mask or head) moves X by O(|X|).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tiled_attention_attn_gb300 import attn
+
+pytestmark = pytest.mark.gpu
+
+MAX_TOL = 2.0 ** -6
+RMS_TOL = 2.0 ** -7
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(attn_lib):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    attn.set_wait_timeout_ns(2_000_000_000)
+    return attn_lib
+
+
+def make(B, Hq, Hkv, Lq, Lk, d, dtype, seed):
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(B, Lq, Hq, d, generator=g).to(dtype)
+    k = torch.randn(B, Lk, Hkv, d, generator=g).to(dtype)
+    v = torch.randn(B, Lk, Hkv, d, generator=g).to(dtype)
+    do = torch.randn(B, Lq, Hq, d, generator=g).to(dtype)
+    return q, k, v, do
+
+
+def gpu_grads(q, k, v, do, causal, scale):
+    dev = torch.device("cuda", 0)
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o, lse = attn.attn_fwd(qd, kd, vd, causal=causal, scale=scale)
+    dq, dk, dv = attn.attn_bwd(qd, kd, vd, o, lse, dod, causal=causal, scale=scale)
+    assert attn.get_error() == attn.ATTN_OK
+    return [t.float().cpu().double().numpy() for t in (dq, dk, dv)]
+
+
+def check(name, x, ref):
+    err = np.abs(x - ref)
+    amax = float(np.abs(ref).max())
+    rms_ref = float(np.sqrt(np.mean(ref ** 2))) if ref.size else 0.0
+    assert np.all(np.isfinite(x)), name
+    assert float(err.max()) <= MAX_TOL * amax + 1e-6, (name, float(err.max()), amax)
+    assert float(np.sqrt(np.mean(err ** 2))) <= RMS_TOL * rms_ref + 1e-7, name
+
+
+CASES = [
+    # B, Hq, Hkv, Lq, Lk, d, causal, dtype
+    (1, 2, 2, 256, 256, 64, False, torch.bfloat16),
+    (1, 2, 1, 300, 300, 128, True, torch.bfloat16),      # GQA, ragged tail
+    (2, 4, 2, 200, 333, 64, True, torch.float16),        # Lq != Lk, causal bottom-right
+    (1, 1, 1, 130, 70, 128, True, torch.bfloat16),       # queries without keys (lse = -inf)
+    (1, 2, 1, 1, 1, 64, False, torch.bfloat16),          # one query, one key
+    (1, 4, 1, 513, 129, 128, False, torch.float16),
+    (2, 2, 2, 640, 640, 128, True, torch.bfloat16),      # several tiles on both sides
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[str(c[:7]) for c in CASES])
+def test_backward_matches_oracle(case):
+    B, Hq, Hkv, Lq, Lk, d, causal, dtype = case
+    q, k, v, do = make(B, Hq, Hkv, Lq, Lk, d, dtype, seed=sum(case[:6]))
+    scale = d ** -0.5
+    dq, dk, dv = gpu_grads(q, k, v, do, causal, scale)
+    rq, rk, rv = oracle.attention_backward(q, k, v, do, causal=causal, scale=scale)
+    check("dq", dq, rq)
+    check("dk", dk, rk)
+    check("dv", dv, rv)
+    if causal and Lq > Lk:
+        # queries that see no key get no gradient
+        blind = np.arange(Lq) + (Lk - Lq) < 0
+        assert np.all(dq[:, blind] == 0.0)
+
+
+def test_backward_is_deterministic():
+    q, k, v, do = make(1, 4, 2, 700, 700, 128, torch.bfloat16, seed=3)
+    a = gpu_grads(q, k, v, do, True, 128 ** -0.5)
+    b = gpu_grads(q, k, v, do, True, 128 ** -0.5)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+
+
+def test_backward_empty_sides_give_zero():
+    dev = torch.device("cuda", 0)
+    for Lq, Lk in ((0, 64), (64, 0)):
+        q, k, v, do = (t.to(dev) for t in make(1, 2, 1, Lq, Lk, 64, torch.bfloat16, seed=1))
+        o = torch.zeros_like(q)
+        lse = torch.full((1, 2, Lq), float("-inf"), device=dev)
+        dq, dk, dv = (torch.full_like(t, 7.0) for t in (q, k, v))
+        attn.attn_bwd(q, k, v, o, lse, do, causal=False, dq=dq, dk=dk, dv=dv)
+        assert attn.get_error() == attn.ATTN_OK
+        for t in (dq, dk, dv):
+            assert torch.count_nonzero(t).item() == 0
+
+
+def test_backward_full_size_group_sample():
+    """The benchmark's backward workload (B2 Hq32 Hkv8 L4096 d128 causal):
+    the whole problem runs on the GPU; the oracle evaluates one (batch, KV
+    head) group, which is a self-contained sub-problem (its four query heads
+    and its keys and values)."""
+    B, Hq, Hkv, L, d = 2, 32, 8, 4096, 128
+    q, k, v, do = make(B, Hq, Hkv, L, L, d, torch.bfloat16, seed=44)
+    scale = d ** -0.5
+    dq, dk, dv = gpu_grads(q, k, v, do, True, scale)
+    G = Hq // Hkv
+    b, g = 1, 5
+    hs = slice(g * G, (g + 1) * G)
+    rq, rk, rv = oracle.attention_backward(q[b:b + 1, :, hs], k[b:b + 1, :, g:g + 1], v[b:b + 1, :, g:g + 1],
+                                           do[b:b + 1, :, hs], causal=True, scale=scale)
+    check("dq", dq[b:b + 1, :, hs], rq)
+    check("dk", dk[b:b + 1, :, g:g + 1], rk)
+    check("dv", dv[b:b + 1, :, g:g + 1], rv)

@@ -61,3 +61,27 @@ def test_empty_query_is_a_no_op(attn_lib):
 def test_timeout_setter_accepts_values(attn_lib):
     attn.set_wait_timeout_ns(10)
     attn.set_wait_timeout_ns(2_000_000_000)
+
+
+def _call_bwd(L, q=16, k=16, v=16, o=16, lse=16, dout=16, dq=16, dk=16, dv=16, B=1, Hq=2, Hkv=1, Lq=8, Lk=8,
+              d=64, causal=0, scale=0.125, fp16=0):
+    return L.attn_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Lq, Lk, d, causal, ctypes.c_float(scale),
+                      fp16, None)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(q=None), dict(k=None), dict(v=None), dict(o=None), dict(lse=None), dict(dout=None),
+    dict(dq=None), dict(dk=None), dict(dv=None),
+    dict(q=8), dict(dout=24), dict(dk=40), dict(lse=2),       # misaligned pointers
+    dict(B=0), dict(Hq=0), dict(Hkv=0), dict(Lq=-1), dict(Lk=-1),
+    dict(Hq=3, Hkv=2), dict(causal=2), dict(fp16=2),
+    dict(scale=float("nan")), dict(scale=-1.0),
+    dict(B=1 << 20, Lq=1 << 12, Hq=1 << 10, Hkv=1 << 10),
+])
+def test_backward_bad_arguments_rejected_on_host(attn_lib, bad):
+    assert _call_bwd(attn_lib, **bad) == attn.ATTN_EINVAL
+
+
+@pytest.mark.parametrize("d", [32, 96, 256])
+def test_backward_unsupported_head_dim(attn_lib, d):
+    assert _call_bwd(attn_lib, d=d) == attn.ATTN_EUNSUPPORTED

@@ -1,5 +1,6 @@
 """GB300 (sm_103a) tiled attention forward: O = softmax(scale * Q K^T [+ causal]) V
-with online-softmax running statistics, behind the C ABI of include/attn.h.
+with online-softmax running statistics, and its backward (dq, dk, dv from the
+kept lse), behind the C ABI of include/attn.h.
 
 The binding loads libattn.so on first use; build it with
 ``tiled_attention_attn_gb300.build.build()``.
@@ -7,6 +8,7 @@ The binding loads libattn.so on first use; build it with
 
 from .attn import (  # noqa: F401
     AttnError,
+    attn_bwd,
     attn_fwd,
     get_error,
     last_device_error,

@@ -100,6 +100,8 @@ def lib(path: Optional[str] = None):
         L.attn_scatter_rows.restype = i
         L.attn_scatter_lse.argtypes = [vp, vp, i, vp, i, i, i, vp, vp]
         L.attn_scatter_lse.restype = i
+        L.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
+        L.attn_bwd.restype = i
         if path is None:
             _lib = L
         return L
@@ -186,6 +188,45 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = F
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd")
     return out, lse
+
+
+def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor, lse: torch.Tensor,
+             dout: torch.Tensor, causal: bool = False, scale: Optional[float] = None,
+             dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None, dv: Optional[torch.Tensor] = None,
+             stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """Gradients (dq, dk, dv) of sum(dout * O) for the dense forward.
+
+    q, out, dout (B, Lq, Hq, d); k, v (B, Lk, Hkv, d); lse (B, Hq, Lq) float32,
+    with out and lse as attn_fwd returned them for the same q, k, v, causal
+    and scale.  dq is shaped like q, dk and dv like k.
+    """
+    ts = (q, k, v, out, dout)
+    if q.dtype not in (torch.bfloat16, torch.float16) or any(t.dtype != q.dtype for t in ts):
+        raise TypeError("q, k, v, out and dout must share one 16-bit dtype")
+    if any(not t.is_cuda or not t.is_contiguous() for t in ts + (lse,)):
+        raise ValueError("tensors must be contiguous CUDA tensors")
+    if q.dim() != 4 or k.dim() != 4 or k.shape != v.shape or out.shape != q.shape or dout.shape != q.shape:
+        raise ValueError("q, out, dout are (B, Lq, Hq, d) and k, v are (B, Lk, Hkv, d)")
+    B, Lq, Hq, d = q.shape
+    _, Lk, Hkv, _ = k.shape
+    if tuple(lse.shape) != (B, Hq, Lq) or lse.dtype != torch.float32:
+        raise ValueError(f"lse must be a float32 tensor of shape {(B, Hq, Lq)}")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for g, ref in ((dq, q), (dk, k), (dv, v)):
+        if g.shape != ref.shape or g.dtype != ref.dtype or not g.is_contiguous() or not g.is_cuda:
+            raise ValueError("dq, dk, dv must be contiguous CUDA tensors shaped like q, k, v")
+    with torch.cuda.device(q.device):
+        rc = lib().attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                            dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), int(B), int(Hq), int(Hkv),
+                            int(Lq), int(Lk), int(d), int(bool(causal)), ctypes.c_float(float(scale)),
+                            int(q.dtype == torch.float16), _stream_handle(q.device, stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_bwd")
+    return dq, dk, dv
 
 
 # ---------------------------------------------------------------------------

@@ -22,7 +22,8 @@ LIB_PATH = os.path.join(PKG, "libattn.so")
 TRACE_LIB_PATH = os.path.join(PKG, "libattn_trace.so")   # phase-trace points compiled in
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["attn_host.cu", "attn_noalloc.cu", "attn_pad.cu", "attn_rotary.cu", "attn_kernels_d64.cu", "attn_kernels_d128.cu", "attn_plan.cpp"]
+SOURCES = ["attn_host.cu", "attn_noalloc.cu", "attn_pad.cu", "attn_rotary.cu", "attn_bwd.cu", "attn_bwd_d64.cu",
+           "attn_bwd_d128.cu", "attn_kernels_d64.cu", "attn_kernels_d128.cu", "attn_plan.cpp"]
 
 
 def nvcc() -> str:

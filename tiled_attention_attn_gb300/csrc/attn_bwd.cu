@@ -1,0 +1,127 @@
+// C ABI of the attention backward: argument checks, the tensor maps, the
+// per-device workspace of the first pass and the three launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+
+#include "attn.h"
+#include "attn_bwd_launch.h"
+#include "attn_internal.h"
+
+namespace attn {
+namespace {
+
+// lse2 and D of the last call's shape, grown on demand and kept per device
+struct BwdWorkspace {
+  float* buf = nullptr;
+  size_t floats = 0;
+};
+std::map<int, BwdWorkspace> g_bwd_ws;
+std::mutex g_bwd_mu;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int bwd(bool bf16, const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+        void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Lq, int Lk, int d, int causal, float scale,
+        cudaStream_t stream) {
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return ATTN_EINVAL;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(dq) ||
+      !aligned16(dk) || !aligned16(dv) || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+    return ATTN_EINVAL;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lq < 0 || Lk < 0 || Hq % Hkv != 0) return ATTN_EINVAL;
+  if (causal != 0 && causal != 1) return ATTN_EINVAL;
+  if (!std::isfinite(scale) || scale < 0.0f) return ATTN_EINVAL;
+  if (d != 64 && d != 128) return ATTN_EUNSUPPORTED;
+  if (static_cast<long long>(B) * Lq * Hq > (1LL << 31) - 1 || static_cast<long long>(B) * Lk * Hkv > (1LL << 31) - 1)
+    return ATTN_EINVAL;
+  if (static_cast<long long>(Lq) + kBM > (1LL << 30) || static_cast<long long>(Lk) + kBN > (1LL << 30))
+    return ATTN_EINVAL;
+  const size_t row_bytes = static_cast<size_t>(d) * 2;
+  if (Lq == 0 || Lk == 0) {
+    // no (query, key) pair: every gradient is zero
+    if (cudaMemsetAsync(dq, 0, static_cast<size_t>(B) * Lq * Hq * row_bytes, stream) != cudaSuccess ||
+        cudaMemsetAsync(dk, 0, static_cast<size_t>(B) * Lk * Hkv * row_bytes, stream) != cudaSuccess ||
+        cudaMemsetAsync(dv, 0, static_cast<size_t>(B) * Lk * Hkv * row_bytes, stream) != cudaSuccess)
+      return ATTN_ELAUNCH;
+    return ATTN_OK;
+  }
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ELAUNCH;
+  DeviceInfo info;
+  int rc = device_info(dev, info);
+  if (rc) return rc;
+  if (!info.supported) return ATTN_EUNSUPPORTED;
+
+  BwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  if ((rc = encode_map(q, bf16, d, Hq, Lq, B, p.tm_q))) return rc;
+  if ((rc = encode_map(dout, bf16, d, Hq, Lq, B, p.tm_do))) return rc;
+  if ((rc = encode_map(k, bf16, d, Hkv, Lk, B, p.tm_k))) return rc;
+  if ((rc = encode_map(v, bf16, d, Hkv, Lk, B, p.tm_v))) return rc;
+  p.n_qt = (Lq + kBM - 1) / kBM;
+  p.n_kt = (Lk + kBN - 1) / kBN;
+  p.Lq_pad = p.n_qt * kBM;
+  if (p.n_qt > 65535 || p.n_kt > 65535) return ATTN_EINVAL;   // grid.y
+  const size_t need = 2 * static_cast<size_t>(B) * Hq * p.Lq_pad;
+
+  std::lock_guard<std::mutex> lock(g_bwd_mu);
+  BwdWorkspace& ws = g_bwd_ws[dev];
+  if (need > ws.floats) {
+    if (ws.buf) cudaFree(ws.buf);
+    ws.buf = nullptr;
+    ws.floats = 0;
+    if (cudaMalloc(&ws.buf, need * sizeof(float)) != cudaSuccess) return ATTN_ENOMEM;
+    ws.floats = need;
+  }
+  p.lse2 = ws.buf;
+  p.dvec = ws.buf + need / 2;
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.err = info.err_word;
+  p.timeout_ns = wait_timeout_ns();
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Lq = Lq;
+  p.Lk = Lk;
+  p.group = Hq / Hkv;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+
+  BwdPrep pr;
+  pr.o = o;
+  pr.dout = dout;
+  pr.lse = lse;
+  const long long threads = static_cast<long long>(B) * Hq * p.Lq_pad * 8;
+  const long long blocks = (threads + 255) / 256;
+  const long long cap = static_cast<long long>(info.sm_count > 0 ? info.sm_count : 1) * 8;
+  pr.grid = static_cast<int>(blocks < cap ? blocks : cap);
+
+  BwdLauncher launch = (d == 64) ? bwd_launcher_d64(bf16, causal != 0) : bwd_launcher_d128(bf16, causal != 0);
+  if (launch(p, pr, stream) != cudaSuccess) return ATTN_ELAUNCH;
+  count_launch();
+  count_launch();
+  count_launch();
+  return ATTN_OK;
+}
+
+}  // namespace
+}  // namespace attn
+
+extern "C" {
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout, void* dq,
+             void* dk, void* dv, int B, int Hq, int Hkv, int Lq, int Lk, int d, int causal, float scale, int fp16,
+             cudaStream_t stream) {
+  if (fp16 != 0 && fp16 != 1) return ATTN_EINVAL;
+  return attn::bwd(fp16 == 0, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Lq, Lk, d, causal, scale, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,611 @@
+// sm_103a attention backward: the gradients dq, dk, dv of sum(dout * O),
+// with the attention weights recomputed tile by tile from q, k and the lse
+// the forward kept (lei6393.com training-integration page, §5.3: nothing of
+// size L x L is stored).  Per (query i, key j) of one head, with scores
+// s_ij = scale q_i.k_j:
+//
+//   P_ij  = exp(s_ij - lse_i)
+//   dP_ij = dout_i . v_j
+//   dS_ij = P_ij (dP_ij - D_i),   D_i = dout_i . O_i   (= sum_j P_ij dP_ij)
+//   dv_j  = sum_i P_ij dout_i,  dk_j = scale sum_i dS_ij q_i,  dq_i = scale sum_j dS_ij k_j
+//
+// Two kernels, each with one contraction direction so that every MMA operand
+// is in a layout the tensor cores read directly and no accumulator is shared
+// between CTAs (no atomics; results are deterministic):
+//   attn_bwd_kv_kernel  one CTA per (batch, KV head, 128-key tile): streams the
+//                       query tiles of every query head of the group, forms
+//                       S^T = K Q^T and dP^T = V dO^T, then P^T and dS^T per key
+//                       row, and accumulates dv += P^T dO, dk += dS^T Q in TMEM.
+//   attn_bwd_q_kernel   one CTA per (batch, query head, 128-query tile): streams
+//                       the key tiles, forms S = Q K^T and dP = dO V^T, then dS
+//                       per query row, and accumulates dq += dS K in TMEM.
+// The second recomputes S and dP (two contractions more than a single pass
+// with shared dq accumulation), in exchange for no atomics.
+//
+// CTA layout (192 threads): warps 0-3 own TMEM lanes 0-127 (one row of the
+// 128-row tile each thread), warp 4 issues TMA, warp 5 allocates TMEM and one
+// thread issues tcgen05.mma.  TMEM columns: S at [0,128), dP at [128,256),
+// the accumulators from 256 on.  The 16-bit P and dS overwrite the first 64
+// columns of S and dP; the MMAs that read them as the A operand are issued
+// before the next tile's S and dP, and the tensor pipe runs them in order.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "attn_params.h"
+#include "ptx.cuh"
+
+namespace attn {
+
+constexpr int kBwdThreads = 192;
+constexpr int kBwdWarpTMA = 4;
+constexpr int kBwdWarpMMA = 5;
+
+struct BwdParams {
+  CUtensorMap tm_q;        // (d, Hq, Lq, B), box 64 x 1 x 128 x 1
+  CUtensorMap tm_k;        // (d, Hkv, Lk, B)
+  CUtensorMap tm_v;
+  CUtensorMap tm_do;       // like q
+  const float* lse2;       // [B][Hq][Lq_pad]: lse * log2(e); +inf for rows with no key and the padding
+  const float* dvec;       // [B][Hq][Lq_pad]: D_i = dout_i . O_i; 0 on the padding
+  void* dq;                // like q
+  void* dk;                // like k
+  void* dv;                // like k
+  int* err;
+  unsigned long long timeout_ns;
+  int B, Hq, Hkv, Lq, Lk, group, Lq_pad, n_qt, n_kt;
+  float scale, scale_log2;
+};
+
+template <int D>
+struct BwdCfg {
+  static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+  static constexpr int kChunks = D / 64;
+  static constexpr int kTile = 128 * D * 2;         // one 128-row tile in smem
+  static constexpr int kNS = (D == 128) ? 2 : 4;    // stages of the streamed operands
+  // kv kernel: K, V resident; stages of (Q, dO, lse2, D)
+  static constexpr int kKvOffStage = 2 * kTile;
+  static constexpr int kKvStageBytes = 2 * kTile;
+  static constexpr int kKvOffVec = kKvOffStage + kNS * kKvStageBytes;   // per stage 128 + 128 floats
+  static constexpr int kKvOffBar = kKvOffVec + kNS * 1024;
+  // q kernel: Q, dO resident; stages of (K, V)
+  static constexpr int kQOffStage = 2 * kTile;
+  static constexpr int kQOffBar = kQOffStage + kNS * 2 * kTile;
+  // barriers: full (resident pair), st_full[NS], st_empty[NS], s_full, p_full, acc_done, drain
+  static constexpr int kNBars = 1 + 2 * kNS + 4;
+  static constexpr int kKvSmem = kKvOffBar + kNBars * 8 + 64 + 1024;
+  static constexpr int kQSmem = kQOffBar + kNBars * 8 + 64 + 1024;
+  static constexpr uint32_t kTmemCols = 512;
+};
+
+template <bool BF16>
+struct BwdIO;
+template <>
+struct BwdIO<true> {
+  using T = __nv_bfloat16;
+};
+template <>
+struct BwdIO<false> {
+  using T = __half;
+};
+
+// Stores 32 fp32 values (times `mul`) of one row as 16-bit, 64 bytes.
+template <bool BF16>
+__device__ __forceinline__ void store_row32(void* dst, const uint32_t (&x)[32], float mul) {
+  uint32_t pk[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) pk[i] = pack2<BF16>(__uint_as_float(x[2 * i]) * mul, __uint_as_float(x[2 * i + 1]) * mul);
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+}
+
+// ---------------------------------------------------------------------------
+// D_i = dout_i . O_i and lse in exp2 units, one (b, i, h) row per 8 threads;
+// rows i in [Lq, Lq_pad) get the padding values.
+// ---------------------------------------------------------------------------
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const void* __restrict__ o, const void* __restrict__ dout,
+                                                            const float* __restrict__ lse, float* __restrict__ lse2,
+                                                            float* __restrict__ dvec, int B, int Hq, int Lq,
+                                                            int Lq_pad) {
+  using T = typename BwdIO<BF16>::T;
+  constexpr int kPer = D / 8;   // elements per thread
+  const long long items = static_cast<long long>(B) * Lq_pad * Hq;
+  const int sub = threadIdx.x & 7;
+  // the loop bound is warp-uniform (the shuffles below need all 32 lanes)
+  const long long stride = (static_cast<long long>(gridDim.x) * blockDim.x) >> 3;
+  for (long long base = (static_cast<long long>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31)) >> 3; base < items;
+       base += stride) {
+    const long long it_raw = base + ((threadIdx.x & 31) >> 3);
+    const bool valid = it_raw < items;
+    const long long it = valid ? it_raw : items - 1;
+    const int h = static_cast<int>(it % Hq);
+    const long long bi = it / Hq;
+    const int i = static_cast<int>(bi % Lq_pad);
+    const int b = static_cast<int>(bi / Lq_pad);
+    float acc = 0.0f;
+    if (valid && i < Lq) {
+      const size_t rb = ((static_cast<size_t>(b) * Lq + i) * Hq + h) * D + sub * kPer;
+      const T* po = reinterpret_cast<const T*>(o) + rb;
+      const T* pd = reinterpret_cast<const T*>(dout) + rb;
+#pragma unroll
+      for (int w = 0; w < kPer / 8; ++w) {
+        const uint4 a = __ldg(reinterpret_cast<const uint4*>(po) + w);
+        const uint4 c = __ldg(reinterpret_cast<const uint4*>(pd) + w);
+        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, cw[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float2 fa, fc;
+          if constexpr (BF16) {
+            fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[e]));
+            fc = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&cw[e]));
+          } else {
+            fa = __half22float2(*reinterpret_cast<const __half2*>(&aw[e]));
+            fc = __half22float2(*reinterpret_cast<const __half2*>(&cw[e]));
+          }
+          acc = fmaf(fa.x, fc.x, acc);
+          acc = fmaf(fa.y, fc.y, acc);
+        }
+      }
+    }
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+    if (valid && sub == 0) {
+      const size_t li = (static_cast<size_t>(b) * Hq + h) * Lq_pad + i;
+      float l2 = INFINITY;
+      if (i < Lq) {
+        const float l = __ldg(lse + (static_cast<size_t>(b) * Hq + h) * Lq + i);
+        l2 = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
+      }
+      lse2[li] = l2;
+      dvec[li] = (i < Lq) ? acc : 0.0f;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// dk, dv: one CTA per (b, g, 128-key tile n); grid (B * Hkv, n_kt)
+// ---------------------------------------------------------------------------
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kv_kernel(const __grid_constant__ BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sK = sbase, sV = sbase + C::kTile;
+  auto sQ = [&](int s) { return sbase + C::kKvOffStage + s * C::kKvStageBytes; };
+  auto sDO = [&](int s) { return sbase + C::kKvOffStage + s * C::kKvStageBytes + C::kTile; };
+  const float* vec = reinterpret_cast<const float*>(smem + C::kKvOffVec);   // [stage][lse2 128 | D 128]
+  const uint32_t bar0 = sbase + C::kKvOffBar;
+  const uint32_t b_kv_full = bar0;
+  auto b_st_full = [&](int s) { return bar0 + 8 + 8 * s; };
+  auto b_st_empty = [&](int s) { return bar0 + 8 + 8 * (C::kNS + s); };
+  const uint32_t b_s_full = bar0 + 8 + 16 * C::kNS;
+  const uint32_t b_p_full = b_s_full + 8;
+  const uint32_t b_acc = b_s_full + 16;
+  const uint32_t b_drain = b_s_full + 24;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kKvOffBar + C::kNBars * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kKvOffBar + C::kNBars * 8 + 4);
+  WaitCtl wc{p.err, abort_flag, p.timeout_ns};
+
+  const int bg = blockIdx.x, n = blockIdx.y;
+  const int b = bg / p.Hkv, g = bg - b * p.Hkv;
+  const int off = p.Lk - p.Lq;   // causal: key j is visible to query i iff j <= i + off
+  int m_first = 0;
+  if constexpr (CAUSAL) {
+    const int first_q = n * kBN - off;   // smallest query that sees key n * 128
+    m_first = first_q <= 0 ? 0 : first_q / kBM;
+  }
+  const int nm = p.n_qt - m_first > 0 ? p.n_qt - m_first : 0;
+  const int n_tiles = p.group * nm;
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    mbar_init(b_kv_full, 1);
+    for (int s = 0; s < C::kNS; ++s) {
+      mbar_init(b_st_full(s), 1);
+      mbar_init(b_st_empty(s), 1);
+    }
+    mbar_init(b_s_full, 1);
+    mbar_init(b_p_full, 4);
+    mbar_init(b_acc, 1);
+    mbar_init(b_drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == kBwdWarpMMA) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kBwdWarpTMA) {
+    if (lane == 0 && n_tiles > 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_do);
+      mbar_arrive_expect_tx(b_kv_full, 2 * C::kTile);
+#pragma unroll
+      for (int c = 0; c < C::kChunks; ++c) {
+        tma_load_4d(sK + c * 16384, &p.tm_k, b_kv_full, c * 64, g, n * kBN, b);
+        tma_load_4d(sV + c * 16384, &p.tm_v, b_kv_full, c * 64, g, n * kBN, b);
+      }
+      int issued = 0;
+      for (int t = 0; t < n_tiles; ++t) {
+        const int st = t % C::kNS;
+        if (!mbar_wait(b_st_empty(st), ((t / C::kNS) & 1) ^ 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKEmpty))) break;
+        const int h = g * p.group + t / nm, m = m_first + t % nm;
+        mbar_arrive_expect_tx(b_st_full(st), 2 * C::kTile + 1024);
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c) {
+          tma_load_4d(sQ(st) + c * 16384, &p.tm_q, b_st_full(st), c * 64, h, m * kBM, b);
+          tma_load_4d(sDO(st) + c * 16384, &p.tm_do, b_st_full(st), c * 64, h, m * kBM, b);
+        }
+        const size_t vi = (static_cast<size_t>(b) * p.Hq + h) * p.Lq_pad + m * kBM;
+        const uint32_t sv = smem_u32(vec + st * 256);
+        bulk_load(sv, p.lse2 + vi, 512, b_st_full(st));
+        bulk_load(sv + 512, p.dvec + vi, 512, b_st_full(st));
+        ++issued;
+      }
+      if (*abort_flag) {
+        // let issued loads land before the CTA exits
+        mbar_wait(b_kv_full, 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteDrain), false);
+        for (int s = 0; s < C::kNS; ++s) {
+          const int cnt = (issued + C::kNS - 1 - s) / C::kNS;
+          if (cnt > 0) mbar_wait(b_st_full(s), (cnt - 1) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteDrain), false);
+        }
+      }
+    }
+  } else if (warp == kBwdWarpMMA) {
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = idesc_f16_f32acc(128, 128, BF16, false);
+      constexpr uint32_t kIdescO = idesc_f16_f32acc(128, D, BF16, true);
+      const uint64_t dk_k = sdesc_sw128(sK, 16, 1024);     // K as A, K-major
+      const uint64_t dv_k = sdesc_sw128(sV, 16, 1024);     // V as A, K-major
+      bool ok = n_tiles > 0 && mbar_wait(b_kv_full, 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteQFull));
+      for (int t = 0; ok && t < n_tiles; ++t) {
+        const int st = t % C::kNS;
+        if (!mbar_wait(b_st_full(st), (t / C::kNS) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull))) break;
+        const uint64_t dq_k = sdesc_sw128(sQ(st), 16, 1024);     // Q as B, K-major
+        const uint64_t ddo_k = sdesc_sw128(sDO(st), 16, 1024);   // dO as B, K-major
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          umma_ss(tmem + 0, dk_k + o, dq_k + o, kIdescS, kk > 0 ? 1u : 0u);     // S^T = K Q^T
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          umma_ss(tmem + 128, dv_k + o, ddo_k + o, kIdescS, kk > 0 ? 1u : 0u);  // dP^T = V dO^T
+        }
+        umma_commit(b_s_full);
+        if (!mbar_wait(b_p_full, t & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSitePFull))) break;
+        tc_fence_after();
+        const uint64_t ddo_mn = sdesc_sw128(sDO(st), 16384, 1024);   // dO as B, MN-major
+        const uint64_t dq_mn = sdesc_sw128(sQ(st), 16384, 1024);     // Q as B, MN-major
+#pragma unroll
+        for (int kk = 0; kk < 128 / 16; ++kk)   // dv += P^T dO
+          umma_ts(tmem + 256, tmem + 0 + kk * 8, ddo_mn + ((kk * 2048) >> 4), kIdescO, (t > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 128 / 16; ++kk)   // dk += dS^T Q
+          umma_ts(tmem + 256 + D, tmem + 128 + kk * 8, dq_mn + ((kk * 2048) >> 4), kIdescO,
+                  (t > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(b_st_empty(st));
+      }
+      umma_commit(b_acc);
+      umma_commit(b_drain);
+      mbar_wait(b_drain, 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteDrain), false);
+    }
+  } else {
+    // ---------------------------------------------------------------- key rows
+    const int quarter = warp;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t t_s = tmem + lane_off, t_dp = tmem + lane_off + 128;
+    const int j = n * kBN + row;
+    const float cl2 = p.scale_log2;
+    bool ok = true;
+    for (int t = 0; t < n_tiles; ++t) {
+      if (!mbar_wait_warp(b_s_full, t & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteSFull))) { ok = false; break; }
+      tc_fence_after();
+      const int st = t % C::kNS, m = m_first + t % nm;
+      // lse2 and D of this stage came by bulk copy: observe its completion
+      // here (the stage cannot be refilled before this warp arrives on p_full)
+      if (!mbar_wait_warp(b_st_full(st), (t / C::kNS) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull))) {
+        ok = false;
+        break;
+      }
+      const float* ls = vec + st * 256;
+      const float* dd = ls + 128;
+      // query column c of this tile is allowed for key j iff cmin <= c < cmax
+      int cmin = CAUSAL ? j - off - m * kBM : 0;
+      const int cmax = p.Lq - m * kBM;
+      if (j >= p.Lk) cmin = 1 << 30;
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t sr[32], dr[32];
+        tmem_ld_32x32b_x32(t_s + ch * 32, sr);
+        tmem_ld_32x32b_x32(t_dp + ch * 32, dr);
+        tmem_wait_ld(sr);
+        tmem_wait_ld(dr);
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(ls + ch * 32 + e);
+          const float4 d4 = *reinterpret_cast<const float4*>(dd + ch * 32 + e);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+          float pp[4], ds[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int c = ch * 32 + e + u;
+            float pr = ex2_approx(fmaf(__uint_as_float(sr[e + u]), cl2, -lv[u]));
+            pr = (c >= cmin && c < cmax) ? pr : 0.0f;
+            pp[u] = pr;
+            ds[u] = pr * (__uint_as_float(dr[e + u]) - dv4[u]);
+          }
+          pk[e / 2] = pack2<BF16>(pp[0], pp[1]);
+          pk[e / 2 + 1] = pack2<BF16>(pp[2], pp[3]);
+          dk[e / 2] = pack2<BF16>(ds[0], ds[1]);
+          dk[e / 2 + 1] = pack2<BF16>(ds[2], ds[3]);
+        }
+        tmem_st_32x32b_x16(t_s + ch * 16, pk);
+        tmem_st_32x32b_x16(t_dp + ch * 16, dk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_p_full);
+    }
+    // epilogue: dv = acc, dk = scale * acc
+    if (ok && (n_tiles == 0 || mbar_wait_warp(b_acc, 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteODone)))) {
+      tc_fence_after();
+      using T = typename BwdIO<BF16>::T;
+      if (j < p.Lk) {
+        const size_t orow = ((static_cast<size_t>(b) * p.Lk + j) * p.Hkv + g) * D;
+        T* dvp = reinterpret_cast<T*>(p.dv) + orow;
+        T* dkp = reinterpret_cast<T*>(p.dk) + orow;
+        if (n_tiles == 0) {
+#pragma unroll
+          for (int i = 0; i < D / 8; ++i) {
+            reinterpret_cast<uint4*>(dvp)[i] = make_uint4(0, 0, 0, 0);
+            reinterpret_cast<uint4*>(dkp)[i] = make_uint4(0, 0, 0, 0);
+          }
+        }
+      }
+      if (n_tiles > 0) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t x[32];
+          tmem_ld_32x32b_x32(tmem + lane_off + 256 + c * 32, x);
+          tmem_wait_ld(x);
+          if (j < p.Lk)
+            store_row32<BF16>(reinterpret_cast<T*>(p.dv) + ((static_cast<size_t>(b) * p.Lk + j) * p.Hkv + g) * D + c * 32,
+                              x, 1.0f);
+        }
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t x[32];
+          tmem_ld_32x32b_x32(tmem + lane_off + 256 + D + c * 32, x);
+          tmem_wait_ld(x);
+          if (j < p.Lk)
+            store_row32<BF16>(reinterpret_cast<T*>(p.dk) + ((static_cast<size_t>(b) * p.Lk + j) * p.Hkv + g) * D + c * 32,
+                              x, p.scale);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kBwdWarpMMA) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// dq: one CTA per (b, h, 128-query tile m); grid (B * Hq, n_qt), heaviest
+// (last) query tiles first
+// ---------------------------------------------------------------------------
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid_constant__ BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sQ = sbase, sDO = sbase + C::kTile;
+  auto sK = [&](int s) { return sbase + C::kQOffStage + s * 2 * C::kTile; };
+  auto sV = [&](int s) { return sbase + C::kQOffStage + s * 2 * C::kTile + C::kTile; };
+  const uint32_t bar0 = sbase + C::kQOffBar;
+  const uint32_t b_q_full = bar0;
+  auto b_st_full = [&](int s) { return bar0 + 8 + 8 * s; };
+  auto b_st_empty = [&](int s) { return bar0 + 8 + 8 * (C::kNS + s); };
+  const uint32_t b_s_full = bar0 + 8 + 16 * C::kNS;
+  const uint32_t b_p_full = b_s_full + 8;
+  const uint32_t b_acc = b_s_full + 16;
+  const uint32_t b_drain = b_s_full + 24;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kQOffBar + C::kNBars * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kQOffBar + C::kNBars * 8 + 4);
+  WaitCtl wc{p.err, abort_flag, p.timeout_ns};
+
+  const int bh = blockIdx.x, m = p.n_qt - 1 - static_cast<int>(blockIdx.y);
+  const int b = bh / p.Hq, h = bh - b * p.Hq, g = h / p.group;
+  const int off = p.Lk - p.Lq;
+  int n_tiles = p.n_kt;
+  if constexpr (CAUSAL) {
+    int last_q = m * kBM + kBM - 1;
+    if (last_q > p.Lq - 1) last_q = p.Lq - 1;
+    const int max_key = last_q + off;
+    n_tiles = max_key < 0 ? 0 : min(p.n_kt, max_key / kBN + 1);
+  }
+
+  if (tid == 0) {
+    *abort_flag = 0;
+    mbar_init(b_q_full, 1);
+    for (int s = 0; s < C::kNS; ++s) {
+      mbar_init(b_st_full(s), 1);
+      mbar_init(b_st_empty(s), 1);
+    }
+    mbar_init(b_s_full, 1);
+    mbar_init(b_p_full, 4);
+    mbar_init(b_acc, 1);
+    mbar_init(b_drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == kBwdWarpMMA) {
+    tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kBwdWarpTMA) {
+    if (lane == 0 && n_tiles > 0) {
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      mbar_arrive_expect_tx(b_q_full, 2 * C::kTile);
+#pragma unroll
+      for (int c = 0; c < C::kChunks; ++c) {
+        tma_load_4d(sQ + c * 16384, &p.tm_q, b_q_full, c * 64, h, m * kBM, b);
+        tma_load_4d(sDO + c * 16384, &p.tm_do, b_q_full, c * 64, h, m * kBM, b);
+      }
+      int issued = 0;
+      for (int t = 0; t < n_tiles; ++t) {
+        const int st = t % C::kNS;
+        if (!mbar_wait(b_st_empty(st), ((t / C::kNS) & 1) ^ 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKEmpty))) break;
+        mbar_arrive_expect_tx(b_st_full(st), 2 * C::kTile);
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c) {
+          tma_load_4d(sK(st) + c * 16384, &p.tm_k, b_st_full(st), c * 64, g, t * kBN, b);
+          tma_load_4d(sV(st) + c * 16384, &p.tm_v, b_st_full(st), c * 64, g, t * kBN, b);
+        }
+        ++issued;
+      }
+      if (*abort_flag) {
+        mbar_wait(b_q_full, 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteDrain), false);
+        for (int s = 0; s < C::kNS; ++s) {
+          const int cnt = (issued + C::kNS - 1 - s) / C::kNS;
+          if (cnt > 0) mbar_wait(b_st_full(s), (cnt - 1) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteDrain), false);
+        }
+      }
+    }
+  } else if (warp == kBwdWarpMMA) {
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = idesc_f16_f32acc(128, 128, BF16, false);
+      constexpr uint32_t kIdescO = idesc_f16_f32acc(128, D, BF16, true);
+      const uint64_t dq_k = sdesc_sw128(sQ, 16, 1024);
+      const uint64_t ddo_k = sdesc_sw128(sDO, 16, 1024);
+      bool ok = n_tiles > 0 && mbar_wait(b_q_full, 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteQFull));
+      for (int t = 0; ok && t < n_tiles; ++t) {
+        const int st = t % C::kNS;
+        if (!mbar_wait(b_st_full(st), (t / C::kNS) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull))) break;
+        const uint64_t dk_k = sdesc_sw128(sK(st), 16, 1024);
+        const uint64_t dv_k = sdesc_sw128(sV(st), 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          umma_ss(tmem + 0, dq_k + o, dk_k + o, kIdescS, kk > 0 ? 1u : 0u);     // S = Q K^T
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          umma_ss(tmem + 128, ddo_k + o, dv_k + o, kIdescS, kk > 0 ? 1u : 0u);  // dP = dO V^T
+        }
+        umma_commit(b_s_full);
+        if (!mbar_wait(b_p_full, t & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSitePFull))) break;
+        tc_fence_after();
+        const uint64_t dk_mn = sdesc_sw128(sK(st), 16384, 1024);   // K as B, MN-major
+#pragma unroll
+        for (int kk = 0; kk < 128 / 16; ++kk)   // dq += dS K
+          umma_ts(tmem + 256, tmem + 0 + kk * 8, dk_mn + ((kk * 2048) >> 4), kIdescO, (t > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(b_st_empty(st));
+      }
+      umma_commit(b_acc);
+      umma_commit(b_drain);
+      mbar_wait(b_drain, 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteDrain), false);
+    }
+  } else {
+    // ---------------------------------------------------------------- query rows
+    const int quarter = warp;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t t_s = tmem + lane_off, t_dp = tmem + lane_off + 128;
+    const int i = m * kBM + row;
+    const float cl2 = p.scale_log2;
+    const size_t vi = (static_cast<size_t>(b) * p.Hq + h) * p.Lq_pad + i;
+    const float l2 = __ldg(p.lse2 + vi);   // i < Lq_pad always
+    const float di = __ldg(p.dvec + vi);
+    int lim_key = p.Lk - 1;
+    if constexpr (CAUSAL) lim_key = min(lim_key, i + off);
+    if (i >= p.Lq) lim_key = -1;
+    bool ok = true;
+    for (int t = 0; t < n_tiles; ++t) {
+      if (!mbar_wait_warp(b_s_full, t & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteSFull))) { ok = false; break; }
+      tc_fence_after();
+      const int lim = lim_key - t * kBN;   // key column c allowed iff c <= lim
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch) {
+        uint32_t sr[32], dr[32];
+        tmem_ld_32x32b_x32(t_s + ch * 32, sr);
+        tmem_ld_32x32b_x32(t_dp + ch * 32, dr);
+        tmem_wait_ld(sr);
+        tmem_wait_ld(dr);
+        uint32_t dk[16];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float ds[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int c = ch * 32 + e + u;
+            float pr = ex2_approx(fmaf(__uint_as_float(sr[e + u]), cl2, -l2));
+            pr = (c <= lim) ? pr : 0.0f;
+            ds[u] = pr * (__uint_as_float(dr[e + u]) - di);
+          }
+          dk[e / 2] = pack2<BF16>(ds[0], ds[1]);
+        }
+        tmem_st_32x32b_x16(t_s + ch * 16, dk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_p_full);
+    }
+    if (ok && (n_tiles == 0 || mbar_wait_warp(b_acc, 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteODone)))) {
+      tc_fence_after();
+      using T = typename BwdIO<BF16>::T;
+      T* dst = reinterpret_cast<T*>(p.dq) + ((static_cast<size_t>(b) * p.Lq + i) * p.Hq + h) * D;
+      if (n_tiles == 0) {
+        if (i < p.Lq) {
+#pragma unroll
+          for (int w = 0; w < D / 8; ++w) reinterpret_cast<uint4*>(dst)[w] = make_uint4(0, 0, 0, 0);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t x[32];
+          tmem_ld_32x32b_x32(tmem + lane_off + 256 + c * 32, x);
+          tmem_wait_ld(x);
+          if (i < p.Lq) store_row32<BF16>(dst + c * 32, x, p.scale);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kBwdWarpMMA) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+}  // namespace attn
