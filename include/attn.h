@@ -184,7 +184,10 @@ int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float 
  * pointers.  lse: (B, Hq, Lq) fp32 as attn_fwd returns it (a row with
  * lse = -inf gets no gradient).  o and lse must be the forward's outputs for
  * the same q, k, v, causal and scale.  dq, dk, dv are overwritten (not
- * accumulated) and must not overlap the inputs.  d in {64, 128}.
+ * accumulated) and must not overlap the inputs.  d in {64, 128}.  With
+ * Lq = 0 the query-side pointers (q, o, lse, dout, dq) may be null and dk,
+ * dv are zeroed; with Lk = 0 the key-side ones (k, v, dk, dv) may be null
+ * and dq is zeroed.
  *
  * The library keeps one device workspace per device (8 * B * Hq * Lq bytes,
  * rounded up), grown with cudaMalloc when a larger problem arrives.  Three

@@ -71,7 +71,7 @@ def _call_bwd(L, q=16, k=16, v=16, o=16, lse=16, dout=16, dq=16, dk=16, dv=16, B
 
 @pytest.mark.parametrize("bad", [
     dict(q=None), dict(k=None), dict(v=None), dict(o=None), dict(lse=None), dict(dout=None),
-    dict(dq=None), dict(dk=None), dict(dv=None),
+    dict(dq=None), dict(dk=None), dict(dv=None), dict(q=None, Lk=0), dict(k=None, Lq=0),
     dict(q=8), dict(dout=24), dict(dk=40), dict(lse=2),       # misaligned pointers
     dict(B=0), dict(Hq=0), dict(Hkv=0), dict(Lq=-1), dict(Lk=-1),
     dict(Hq=3, Hkv=2), dict(causal=2), dict(fp16=2),
@@ -80,6 +80,12 @@ def _call_bwd(L, q=16, k=16, v=16, o=16, lse=16, dout=16, dq=16, dk=16, dv=16, B
 ])
 def test_backward_bad_arguments_rejected_on_host(attn_lib, bad):
     assert _call_bwd(attn_lib, **bad) == attn.ATTN_EINVAL
+
+
+def test_backward_empty_side_accepts_null_pointers(attn_lib):
+    # Lq = 0 and Lk = 0 together: nothing to zero, no CUDA call
+    assert _call_bwd(attn_lib, q=None, o=None, lse=None, dout=None, dq=None, k=None, v=None, dk=None, dv=None,
+                     Lq=0, Lk=0) == attn.ATTN_OK
 
 
 @pytest.mark.parametrize("d", [32, 96, 256])

@@ -29,7 +29,9 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 int bwd(bool bf16, const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
         void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Lq, int Lk, int d, int causal, float scale,
         cudaStream_t stream) {
-  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return ATTN_EINVAL;
+  // a tensor with no elements may be passed as a null pointer
+  if (Lq != 0 && (!q || !o || !lse || !dout || !dq)) return ATTN_EINVAL;
+  if (Lk != 0 && (!k || !v || !dk || !dv)) return ATTN_EINVAL;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(dq) ||
       !aligned16(dk) || !aligned16(dv) || (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
     return ATTN_EINVAL;
@@ -44,9 +46,10 @@ int bwd(bool bf16, const void* q, const void* k, const void* v, const void* o, c
   const size_t row_bytes = static_cast<size_t>(d) * 2;
   if (Lq == 0 || Lk == 0) {
     // no (query, key) pair: every gradient is zero
-    if (cudaMemsetAsync(dq, 0, static_cast<size_t>(B) * Lq * Hq * row_bytes, stream) != cudaSuccess ||
-        cudaMemsetAsync(dk, 0, static_cast<size_t>(B) * Lk * Hkv * row_bytes, stream) != cudaSuccess ||
-        cudaMemsetAsync(dv, 0, static_cast<size_t>(B) * Lk * Hkv * row_bytes, stream) != cudaSuccess)
+    if (Lq != 0 && cudaMemsetAsync(dq, 0, static_cast<size_t>(B) * Lq * Hq * row_bytes, stream) != cudaSuccess)
+      return ATTN_ELAUNCH;
+    if (Lk != 0 && (cudaMemsetAsync(dk, 0, static_cast<size_t>(B) * Lk * Hkv * row_bytes, stream) != cudaSuccess ||
+                    cudaMemsetAsync(dv, 0, static_cast<size_t>(B) * Lk * Hkv * row_bytes, stream) != cudaSuccess))
       return ATTN_ELAUNCH;
     return ATTN_OK;
   }
