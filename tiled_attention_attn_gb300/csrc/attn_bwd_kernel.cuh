@@ -22,12 +22,16 @@
 // The second recomputes S and dP (two contractions more than a single pass
 // with shared dq accumulation), in exchange for no atomics.
 //
-// CTA layout (192 threads): warps 0-3 own TMEM lanes 0-127 (one row of the
-// 128-row tile each thread), warp 4 issues TMA, warp 5 allocates TMEM and one
-// thread issues tcgen05.mma.  TMEM columns: S at [0,128), dP at [128,256),
-// the accumulators from 256 on.  The 16-bit P and dS overwrite the first 64
-// columns of S and dP; the MMAs that read them as the A operand are issued
-// before the next tile's S and dP, and the tensor pipe runs them in order.
+// CTA layout (320 threads): warps 0-7 process rows, warp w owning TMEM lanes
+// 32 (w % 4) .. +31 (one row of the 128-row tile per lane) and columns
+// 64 (w / 4) .. +63 of the 128-wide S and dP tiles; warp 8 issues TMA, warp 9
+// allocates TMEM and one thread issues tcgen05.mma.  TMEM columns: S at
+// [0,128), dP at [128,256), the accumulators from 256 on.  The 16-bit P (kv
+// kernel) and dS of a warp's 64 columns are packed into the first 32 of those
+// columns, so no warp writes where another still reads; the MMAs read the
+// 16-column slices of the A operand from there, and are issued before the
+// next tile's S and dP, which the tensor pipe runs after them.  The row threads signal P and dS separately, so each kernel's
+// next S (and dP) is computed while the rows are still busy with this tile.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -37,9 +41,10 @@
 
 namespace attn {
 
-constexpr int kBwdThreads = 192;
-constexpr int kBwdWarpTMA = 4;
-constexpr int kBwdWarpMMA = 5;
+constexpr int kBwdThreads = 320;
+constexpr int kBwdWarpTMA = 8;
+constexpr int kBwdWarpMMA = 9;
+constexpr int kBwdRowWarps = 8;
 
 struct BwdParams {
   CUtensorMap tm_q;        // (d, Hq, Lq, B), box 64 x 1 x 128 x 1
@@ -71,8 +76,9 @@ struct BwdCfg {
   // q kernel: Q, dO resident; stages of (K, V)
   static constexpr int kQOffStage = 2 * kTile;
   static constexpr int kQOffBar = kQOffStage + kNS * 2 * kTile;
-  // barriers: full (resident pair), st_full[NS], st_empty[NS], s_full, p_full, acc_done, drain
-  static constexpr int kNBars = 1 + 2 * kNS + 4;
+  // barriers: full (resident pair), st_full[NS], st_empty[NS], s_full, dp_full, and two
+  // row-side signals (kv: p_full, ds_full; q: s_free, ds_full), acc_done, drain
+  static constexpr int kNBars = 1 + 2 * kNS + 6;
   static constexpr int kKvSmem = kKvOffBar + kNBars * 8 + 64 + 1024;
   static constexpr int kQSmem = kQOffBar + kNBars * 8 + 64 + 1024;
   static constexpr uint32_t kTmemCols = 512;
@@ -165,6 +171,87 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const void* __restri
   }
 }
 
+// TMEM column of the packed 16-bit A operand's kk-th 16-wide K slice inside a
+// 128-column S or dP region: warp half h packs columns 64h.. into 64h..64h+31.
+__device__ __forceinline__ uint32_t packed_slice_col(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
+
+// kv kernel, one warp's 64 query columns of its 32 key rows: P^T = 2^(S^T c - lse2)
+// (c = scale log2 e), kept in pr and stored packed over the first 32 of its
+// columns.  MASK: query column c is allowed iff c >= cmin (causal).
+template <bool MASK, bool BF16>
+__device__ __forceinline__ void kv_p_half(uint32_t t_s, const float* ls, int cmin, float cl2, float (&pr)[64]) {
+#pragma unroll
+  for (int ch = 0; ch < 2; ++ch) {
+    uint32_t sr[32];
+    tmem_ld_32x32b_x32(t_s + ch * 32, sr);
+    tmem_wait_ld(sr);
+    uint32_t pk[16];
+#pragma unroll
+    for (int e = 0; e < 32; e += 4) {
+      const float4 l4 = *reinterpret_cast<const float4*>(ls + ch * 32 + e);
+      const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int c = ch * 32 + e + u;
+        const float x = ex2_approx(fmaf(__uint_as_float(sr[e + u]), cl2, -lv[u]));
+        pr[c] = (!MASK || c >= cmin) ? x : 0.0f;
+      }
+      pk[e / 2] = pack2<BF16>(pr[ch * 32 + e], pr[ch * 32 + e + 1]);
+      pk[e / 2 + 1] = pack2<BF16>(pr[ch * 32 + e + 2], pr[ch * 32 + e + 3]);
+    }
+    tmem_st_32x32b_x16(t_s + ch * 16, pk);
+  }
+}
+
+// dS = P (dP - D) for one warp's 64 columns, stored packed over the first 32
+// of its dP columns.  dd: D per column (kv kernel), or null with `di` the
+// row's D (q kernel).
+template <bool BF16>
+__device__ __forceinline__ void ds_half(uint32_t t_dp, const float* dd, float di, const float (&pr)[64]) {
+#pragma unroll
+  for (int ch = 0; ch < 2; ++ch) {
+    uint32_t dr[32];
+    tmem_ld_32x32b_x32(t_dp + ch * 32, dr);
+    tmem_wait_ld(dr);
+    uint32_t dk[16];
+#pragma unroll
+    for (int e = 0; e < 32; e += 4) {
+      float dv4[4] = {di, di, di, di};
+      if (dd != nullptr) {
+        const float4 d4 = *reinterpret_cast<const float4*>(dd + ch * 32 + e);
+        dv4[0] = d4.x;
+        dv4[1] = d4.y;
+        dv4[2] = d4.z;
+        dv4[3] = d4.w;
+      }
+      float ds[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) ds[u] = pr[ch * 32 + e + u] * (__uint_as_float(dr[e + u]) - dv4[u]);
+      dk[e / 2] = pack2<BF16>(ds[0], ds[1]);
+      dk[e / 2 + 1] = pack2<BF16>(ds[2], ds[3]);
+    }
+    tmem_st_32x32b_x16(t_dp + ch * 16, dk);
+  }
+}
+
+// q kernel, one warp's 64 key columns of its 32 query rows: P = 2^(S c - lse2_i)
+// kept in pr.  MASK: key column c is allowed iff c <= lim.
+template <bool MASK>
+__device__ __forceinline__ void q_p_half(uint32_t t_s, float l2, int lim, float cl2, float (&pr)[64]) {
+#pragma unroll
+  for (int ch = 0; ch < 2; ++ch) {
+    uint32_t sr[32];
+    tmem_ld_32x32b_x32(t_s + ch * 32, sr);
+    tmem_wait_ld(sr);
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const int c = ch * 32 + e;
+      const float x = ex2_approx(fmaf(__uint_as_float(sr[e]), cl2, -l2));
+      pr[c] = (!MASK || c <= lim) ? x : 0.0f;
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // dk, dv: one CTA per (b, g, 128-key tile n); grid (B * Hkv, n_kt)
 // ---------------------------------------------------------------------------
@@ -183,10 +270,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kv_kernel(const __gri
   const uint32_t b_kv_full = bar0;
   auto b_st_full = [&](int s) { return bar0 + 8 + 8 * s; };
   auto b_st_empty = [&](int s) { return bar0 + 8 + 8 * (C::kNS + s); };
-  const uint32_t b_s_full = bar0 + 8 + 16 * C::kNS;
-  const uint32_t b_p_full = b_s_full + 8;
-  const uint32_t b_acc = b_s_full + 16;
-  const uint32_t b_drain = b_s_full + 24;
+  const uint32_t b_s_full = bar0 + 8 + 16 * C::kNS;   // S^T(t) computed
+  const uint32_t b_dp_full = b_s_full + 8;            // dP^T(t) computed
+  const uint32_t b_p_full = b_s_full + 16;            // P^T(t) stored by the key rows
+  const uint32_t b_ds_full = b_s_full + 24;           // dS^T(t) stored by the key rows
+  const uint32_t b_acc = b_s_full + 32;
+  const uint32_t b_drain = b_s_full + 40;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kKvOffBar + C::kNBars * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kKvOffBar + C::kNBars * 8 + 4);
   WaitCtl wc{p.err, abort_flag, p.timeout_ns};
@@ -210,7 +299,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kv_kernel(const __gri
       mbar_init(b_st_empty(s), 1);
     }
     mbar_init(b_s_full, 1);
-    mbar_init(b_p_full, 4);
+    mbar_init(b_dp_full, 1);
+    mbar_init(b_p_full, kBwdRowWarps);
+    mbar_init(b_ds_full, kBwdRowWarps);
     mbar_init(b_acc, 1);
     mbar_init(b_drain, 1);
     fence_mbar_init();
@@ -266,35 +357,57 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kv_kernel(const __gri
       constexpr uint32_t kIdescO = idesc_f16_f32acc(128, D, BF16, true);
       const uint64_t dk_k = sdesc_sw128(sK, 16, 1024);     // K as A, K-major
       const uint64_t dv_k = sdesc_sw128(sV, 16, 1024);     // V as A, K-major
-      bool ok = n_tiles > 0 && mbar_wait(b_kv_full, 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteQFull));
-      for (int t = 0; ok && t < n_tiles; ++t) {
-        const int st = t % C::kNS;
-        if (!mbar_wait(b_st_full(st), (t / C::kNS) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull))) break;
-        const uint64_t dq_k = sdesc_sw128(sQ(st), 16, 1024);     // Q as B, K-major
-        const uint64_t ddo_k = sdesc_sw128(sDO(st), 16, 1024);   // dO as B, K-major
+      auto issue_s = [&](int st) {   // S^T = K Q^T
+        const uint64_t dq_k = sdesc_sw128(sQ(st), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-          umma_ss(tmem + 0, dk_k + o, dq_k + o, kIdescS, kk > 0 ? 1u : 0u);     // S^T = K Q^T
-        }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-          umma_ss(tmem + 128, dv_k + o, ddo_k + o, kIdescS, kk > 0 ? 1u : 0u);  // dP^T = V dO^T
+          umma_ss(tmem + 0, dk_k + o, dq_k + o, kIdescS, kk > 0 ? 1u : 0u);
         }
         umma_commit(b_s_full);
+      };
+      auto issue_dp = [&](int st) {   // dP^T = V dO^T
+        const uint64_t ddo_k = sdesc_sw128(sDO(st), 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          umma_ss(tmem + 128, dv_k + o, ddo_k + o, kIdescS, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(b_dp_full);
+      };
+      // Order per tile t: dv(t), S^T(t+1), dk(t), dP^T(t+1).  S^T(t+1)
+      // overwrites P^T(t) after dv(t) has been issued, dP^T(t+1) overwrites
+      // dS^T(t) after dk(t); the key rows form P^T(t+1) while dk(t) and
+      // dP^T(t+1) run, and dS^T(t) while dv(t) and S^T(t+1) run.
+      bool ok = n_tiles > 0 && mbar_wait(b_kv_full, 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteQFull)) &&
+                mbar_wait(b_st_full(0), 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull));
+      if (ok) {
+        issue_s(0);
+        issue_dp(0);
+      }
+      for (int t = 0; ok && t < n_tiles; ++t) {
+        const int st = t % C::kNS, st1 = (t + 1) % C::kNS;
+        const bool next = t + 1 < n_tiles;
         if (!mbar_wait(b_p_full, t & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSitePFull))) break;
         tc_fence_after();
         const uint64_t ddo_mn = sdesc_sw128(sDO(st), 16384, 1024);   // dO as B, MN-major
         const uint64_t dq_mn = sdesc_sw128(sQ(st), 16384, 1024);     // Q as B, MN-major
 #pragma unroll
         for (int kk = 0; kk < 128 / 16; ++kk)   // dv += P^T dO
-          umma_ts(tmem + 256, tmem + 0 + kk * 8, ddo_mn + ((kk * 2048) >> 4), kIdescO, (t > 0 || kk > 0) ? 1u : 0u);
+          umma_ts(tmem + 256, tmem + packed_slice_col(kk), ddo_mn + ((kk * 2048) >> 4), kIdescO,
+                  (t > 0 || kk > 0) ? 1u : 0u);
+        if (next) {
+          if (!mbar_wait(b_st_full(st1), ((t + 1) / C::kNS) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull))) break;
+          issue_s(st1);
+        }
+        if (!mbar_wait(b_ds_full, t & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteVFull))) break;
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 128 / 16; ++kk)   // dk += dS^T Q
-          umma_ts(tmem + 256 + D, tmem + 128 + kk * 8, dq_mn + ((kk * 2048) >> 4), kIdescO,
+          umma_ts(tmem + 256 + D, tmem + 128 + packed_slice_col(kk), dq_mn + ((kk * 2048) >> 4), kIdescO,
                   (t > 0 || kk > 0) ? 1u : 0u);
         umma_commit(b_st_empty(st));
+        if (next) issue_dp(st1);
       }
       umma_commit(b_acc);
       umma_commit(b_drain);
@@ -302,10 +415,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kv_kernel(const __gri
     }
   } else {
     // ---------------------------------------------------------------- key rows
-    const int quarter = warp;
+    const int quarter = warp & 3, half = warp >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t t_s = tmem + lane_off, t_dp = tmem + lane_off + 128;
+    const uint32_t t_s = tmem + lane_off + half * 64, t_dp = tmem + lane_off + 128 + half * 64;
     const int j = n * kBN + row;
     const float cl2 = p.scale_log2;
     bool ok = true;
@@ -314,86 +427,63 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kv_kernel(const __gri
       tc_fence_after();
       const int st = t % C::kNS, m = m_first + t % nm;
       // lse2 and D of this stage came by bulk copy: observe its completion
-      // here (the stage cannot be refilled before this warp arrives on p_full)
+      // here (the stage cannot be refilled before this warp arrives on ds_full)
       if (!mbar_wait_warp(b_st_full(st), (t / C::kNS) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull))) {
         ok = false;
         break;
       }
-      const float* ls = vec + st * 256;
-      const float* dd = ls + 128;
-      // query column c of this tile is allowed for key j iff cmin <= c < cmax
-      int cmin = CAUSAL ? j - off - m * kBM : 0;
-      const int cmax = p.Lq - m * kBM;
-      if (j >= p.Lk) cmin = 1 << 30;
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t sr[32], dr[32];
-        tmem_ld_32x32b_x32(t_s + ch * 32, sr);
-        tmem_ld_32x32b_x32(t_dp + ch * 32, dr);
-        tmem_wait_ld(sr);
-        tmem_wait_ld(dr);
-        uint32_t pk[16], dk[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(ls + ch * 32 + e);
-          const float4 d4 = *reinterpret_cast<const float4*>(dd + ch * 32 + e);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-          float pp[4], ds[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int c = ch * 32 + e + u;
-            float pr = ex2_approx(fmaf(__uint_as_float(sr[e + u]), cl2, -lv[u]));
-            pr = (c >= cmin && c < cmax) ? pr : 0.0f;
-            pp[u] = pr;
-            ds[u] = pr * (__uint_as_float(dr[e + u]) - dv4[u]);
-          }
-          pk[e / 2] = pack2<BF16>(pp[0], pp[1]);
-          pk[e / 2 + 1] = pack2<BF16>(pp[2], pp[3]);
-          dk[e / 2] = pack2<BF16>(ds[0], ds[1]);
-          dk[e / 2 + 1] = pack2<BF16>(ds[2], ds[3]);
-        }
-        tmem_st_32x32b_x16(t_s + ch * 16, pk);
-        tmem_st_32x32b_x16(t_dp + ch * 16, dk);
-      }
+      const float* ls = vec + st * 256 + half * 64;
+      const float* dd = vec + st * 256 + 128 + half * 64;
+      // Only tiles crossing the causal diagonal are masked.  Padded query
+      // columns (past Lq) have lse2 = +inf, so P = 0 there; padded key rows
+      // (past Lk) only reach their own rows of dv and dk, which are not stored.
+      float pr[64];
+      if (CAUSAL && n * kBN + kBN - 1 - m * kBM > off)
+        kv_p_half<true, BF16>(t_s, ls, j - off - m * kBM - half * 64, cl2, pr);
+      else
+        kv_p_half<false, BF16>(t_s, ls, 0, cl2, pr);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_p_full);
+      if (!mbar_wait_warp(b_dp_full, t & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteODone))) { ok = false; break; }
+      tc_fence_after();
+      ds_half<BF16>(t_dp, dd, 0.0f, pr);
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_ds_full);
     }
-    // epilogue: dv = acc, dk = scale * acc
+    // epilogue: dv = acc, dk = scale * acc; this warp's half of the columns
     if (ok && (n_tiles == 0 || mbar_wait_warp(b_acc, 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteODone)))) {
       tc_fence_after();
       using T = typename BwdIO<BF16>::T;
-      if (j < p.Lk) {
-        const size_t orow = ((static_cast<size_t>(b) * p.Lk + j) * p.Hkv + g) * D;
-        T* dvp = reinterpret_cast<T*>(p.dv) + orow;
-        T* dkp = reinterpret_cast<T*>(p.dk) + orow;
-        if (n_tiles == 0) {
+      constexpr int kHalf = D / 2;
+      const size_t orow = ((static_cast<size_t>(b) * p.Lk + j) * p.Hkv + g) * D + half * kHalf;
+      T* dvp = reinterpret_cast<T*>(p.dv) + orow;
+      T* dkp = reinterpret_cast<T*>(p.dk) + orow;
+      if (n_tiles == 0) {
+        if (j < p.Lk) {
 #pragma unroll
-          for (int i = 0; i < D / 8; ++i) {
+          for (int i = 0; i < kHalf / 8; ++i) {
             reinterpret_cast<uint4*>(dvp)[i] = make_uint4(0, 0, 0, 0);
             reinterpret_cast<uint4*>(dkp)[i] = make_uint4(0, 0, 0, 0);
           }
         }
-      }
-      if (n_tiles > 0) {
+      } else {
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < kHalf / 32; ++c) {
           uint32_t x[32];
-          tmem_ld_32x32b_x32(tmem + lane_off + 256 + c * 32, x);
+          tmem_ld_32x32b_x32(tmem + lane_off + 256 + half * kHalf + c * 32, x);
           tmem_wait_ld(x);
-          if (j < p.Lk)
-            store_row32<BF16>(reinterpret_cast<T*>(p.dv) + ((static_cast<size_t>(b) * p.Lk + j) * p.Hkv + g) * D + c * 32,
-                              x, 1.0f);
+          if (j < p.Lk) store_row32<BF16>(dvp + c * 32, x, 1.0f);
         }
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < kHalf / 32; ++c) {
           uint32_t x[32];
-          tmem_ld_32x32b_x32(tmem + lane_off + 256 + D + c * 32, x);
+          tmem_ld_32x32b_x32(tmem + lane_off + 256 + D + half * kHalf + c * 32, x);
           tmem_wait_ld(x);
-          if (j < p.Lk)
-            store_row32<BF16>(reinterpret_cast<T*>(p.dk) + ((static_cast<size_t>(b) * p.Lk + j) * p.Hkv + g) * D + c * 32,
-                              x, p.scale);
+          if (j < p.Lk) store_row32<BF16>(dkp + c * 32, x, p.scale);
         }
       }
     }
@@ -426,10 +516,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
   const uint32_t b_q_full = bar0;
   auto b_st_full = [&](int s) { return bar0 + 8 + 8 * s; };
   auto b_st_empty = [&](int s) { return bar0 + 8 + 8 * (C::kNS + s); };
-  const uint32_t b_s_full = bar0 + 8 + 16 * C::kNS;
-  const uint32_t b_p_full = b_s_full + 8;
-  const uint32_t b_acc = b_s_full + 16;
-  const uint32_t b_drain = b_s_full + 24;
+  const uint32_t b_s_full = bar0 + 8 + 16 * C::kNS;   // S(t) computed
+  const uint32_t b_dp_full = b_s_full + 8;            // dP(t) computed
+  const uint32_t b_s_free = b_s_full + 16;            // the query rows have read S(t)
+  const uint32_t b_ds_full = b_s_full + 24;           // dS(t) stored by the query rows
+  const uint32_t b_acc = b_s_full + 32;
+  const uint32_t b_drain = b_s_full + 40;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kQOffBar + C::kNBars * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kQOffBar + C::kNBars * 8 + 4);
   WaitCtl wc{p.err, abort_flag, p.timeout_ns};
@@ -453,7 +545,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
       mbar_init(b_st_empty(s), 1);
     }
     mbar_init(b_s_full, 1);
-    mbar_init(b_p_full, 4);
+    mbar_init(b_dp_full, 1);
+    mbar_init(b_s_free, kBwdRowWarps);
+    mbar_init(b_ds_full, kBwdRowWarps);
     mbar_init(b_acc, 1);
     mbar_init(b_drain, 1);
     fence_mbar_init();
@@ -503,30 +597,50 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
       constexpr uint32_t kIdescO = idesc_f16_f32acc(128, D, BF16, true);
       const uint64_t dq_k = sdesc_sw128(sQ, 16, 1024);
       const uint64_t ddo_k = sdesc_sw128(sDO, 16, 1024);
-      bool ok = n_tiles > 0 && mbar_wait(b_q_full, 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteQFull));
-      for (int t = 0; ok && t < n_tiles; ++t) {
-        const int st = t % C::kNS;
-        if (!mbar_wait(b_st_full(st), (t / C::kNS) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull))) break;
+      auto issue_s = [&](int st) {   // S = Q K^T
         const uint64_t dk_k = sdesc_sw128(sK(st), 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          umma_ss(tmem + 0, dq_k + o, dk_k + o, kIdescS, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(b_s_full);
+      };
+      auto issue_dp = [&](int st) {   // dP = dO V^T
         const uint64_t dv_k = sdesc_sw128(sV(st), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-          umma_ss(tmem + 0, dq_k + o, dk_k + o, kIdescS, kk > 0 ? 1u : 0u);     // S = Q K^T
+          umma_ss(tmem + 128, ddo_k + o, dv_k + o, kIdescS, kk > 0 ? 1u : 0u);
         }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-          umma_ss(tmem + 128, ddo_k + o, dv_k + o, kIdescS, kk > 0 ? 1u : 0u);  // dP = dO V^T
+        umma_commit(b_dp_full);
+      };
+      // Order per tile t: S(t+1) (once the rows have read S(t)), dq(t),
+      // dP(t+1).  dS(t) lives over dP(t)'s first 64 columns, so S(t+1) does
+      // not wait for dq(t); dP(t+1) is issued after dq(t) has been.
+      bool ok = n_tiles > 0 && mbar_wait(b_q_full, 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteQFull)) &&
+                mbar_wait(b_st_full(0), 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull));
+      if (ok) {
+        issue_s(0);
+        issue_dp(0);
+      }
+      for (int t = 0; ok && t < n_tiles; ++t) {
+        const int st = t % C::kNS, st1 = (t + 1) % C::kNS;
+        const bool next = t + 1 < n_tiles;
+        if (next) {
+          if (!mbar_wait(b_s_free, t & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSitePFull))) break;
+          if (!mbar_wait(b_st_full(st1), ((t + 1) / C::kNS) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull))) break;
+          issue_s(st1);
         }
-        umma_commit(b_s_full);
-        if (!mbar_wait(b_p_full, t & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSitePFull))) break;
+        if (!mbar_wait(b_ds_full, t & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteVFull))) break;
         tc_fence_after();
         const uint64_t dk_mn = sdesc_sw128(sK(st), 16384, 1024);   // K as B, MN-major
 #pragma unroll
         for (int kk = 0; kk < 128 / 16; ++kk)   // dq += dS K
-          umma_ts(tmem + 256, tmem + 0 + kk * 8, dk_mn + ((kk * 2048) >> 4), kIdescO, (t > 0 || kk > 0) ? 1u : 0u);
+          umma_ts(tmem + 256, tmem + 128 + packed_slice_col(kk), dk_mn + ((kk * 2048) >> 4), kIdescO,
+                  (t > 0 || kk > 0) ? 1u : 0u);
         umma_commit(b_st_empty(st));
+        if (next) issue_dp(st1);
       }
       umma_commit(b_acc);
       umma_commit(b_drain);
@@ -534,64 +648,53 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
     }
   } else {
     // ---------------------------------------------------------------- query rows
-    const int quarter = warp;
+    const int quarter = warp & 3, half = warp >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t t_s = tmem + lane_off, t_dp = tmem + lane_off + 128;
+    const uint32_t t_s = tmem + lane_off + half * 64, t_dp = tmem + lane_off + 128 + half * 64;
     const int i = m * kBM + row;
     const float cl2 = p.scale_log2;
     const size_t vi = (static_cast<size_t>(b) * p.Hq + h) * p.Lq_pad + i;
-    const float l2 = __ldg(p.lse2 + vi);   // i < Lq_pad always
+    const float l2 = __ldg(p.lse2 + vi);   // i < Lq_pad always; +inf past Lq, so P = 0 there
     const float di = __ldg(p.dvec + vi);
     int lim_key = p.Lk - 1;
     if constexpr (CAUSAL) lim_key = min(lim_key, i + off);
-    if (i >= p.Lq) lim_key = -1;
     bool ok = true;
     for (int t = 0; t < n_tiles; ++t) {
       if (!mbar_wait_warp(b_s_full, t & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteSFull))) { ok = false; break; }
       tc_fence_after();
-      const int lim = lim_key - t * kBN;   // key column c allowed iff c <= lim
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t sr[32], dr[32];
-        tmem_ld_32x32b_x32(t_s + ch * 32, sr);
-        tmem_ld_32x32b_x32(t_dp + ch * 32, dr);
-        tmem_wait_ld(sr);
-        tmem_wait_ld(dr);
-        uint32_t dk[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float ds[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int c = ch * 32 + e + u;
-            float pr = ex2_approx(fmaf(__uint_as_float(sr[e + u]), cl2, -l2));
-            pr = (c <= lim) ? pr : 0.0f;
-            ds[u] = pr * (__uint_as_float(dr[e + u]) - di);
-          }
-          dk[e / 2] = pack2<BF16>(ds[0], ds[1]);
-        }
-        tmem_st_32x32b_x16(t_s + ch * 16, dk);
-      }
+      // masked: tiles crossing the causal diagonal and the ragged last key tile
+      float pr[64];
+      if ((CAUSAL && t * kBN + kBN - 1 > m * kBM + off) || t * kBN + kBN > p.Lk)
+        q_p_half<true>(t_s, l2, lim_key - t * kBN - half * 64, cl2, pr);
+      else
+        q_p_half<false>(t_s, l2, 0, cl2, pr);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_s_free);
+      if (!mbar_wait_warp(b_dp_full, t & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteODone))) { ok = false; break; }
+      tc_fence_after();
+      ds_half<BF16>(t_dp, nullptr, di, pr);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(b_p_full);
+      if (lane == 0) mbar_arrive(b_ds_full);
     }
     if (ok && (n_tiles == 0 || mbar_wait_warp(b_acc, 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteODone)))) {
       tc_fence_after();
       using T = typename BwdIO<BF16>::T;
-      T* dst = reinterpret_cast<T*>(p.dq) + ((static_cast<size_t>(b) * p.Lq + i) * p.Hq + h) * D;
+      constexpr int kHalf = D / 2;
+      T* dst = reinterpret_cast<T*>(p.dq) + ((static_cast<size_t>(b) * p.Lq + i) * p.Hq + h) * D + half * kHalf;
       if (n_tiles == 0) {
         if (i < p.Lq) {
 #pragma unroll
-          for (int w = 0; w < D / 8; ++w) reinterpret_cast<uint4*>(dst)[w] = make_uint4(0, 0, 0, 0);
+          for (int w = 0; w < kHalf / 8; ++w) reinterpret_cast<uint4*>(dst)[w] = make_uint4(0, 0, 0, 0);
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < kHalf / 32; ++c) {
           uint32_t x[32];
-          tmem_ld_32x32b_x32(tmem + lane_off + 256 + c * 32, x);
+          tmem_ld_32x32b_x32(tmem + lane_off + 256 + half * kHalf + c * 32, x);
           tmem_wait_ld(x);
           if (i < p.Lq) store_row32<BF16>(dst + c * 32, x, p.scale);
         }
