@@ -42,7 +42,7 @@ enum TraceTag : int {
 // Wait-site codes (low byte of ATTN_DEVERR_WAIT_TIMEOUT).
 enum WaitSite : int {
   kSiteQEmpty = 1, kSiteKEmpty, kSiteVEmpty, kSiteQFull, kSiteKFull, kSiteVFull,
-  kSiteSFull, kSitePFull, kSiteODone, kSiteDrain, kSiteSelftest
+  kSiteSFull, kSitePFull, kSiteODone, kSiteDrain, kSiteSelftest, kSiteDsFull
 };
 
 struct FwdParams {
