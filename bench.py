@@ -497,6 +497,11 @@ def run_ours(args, wl):
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
     flops = workload_flops(wl, inp.lengths)
     stream = torch.cuda.current_stream(device)
+    if args.bwd_only:
+        # the backward leg alone (for profiling it)
+        if rank == 0:
+            print(json.dumps({"backward": bwd_leg(attn, device, stream, measured_peaks())}), flush=True)
+        return 0
     if args.legs_only:
         # the padded-batch, kv-cache and rotary legs alone (for profiling them)
         peaks = measured_peaks()
@@ -638,6 +643,7 @@ def main():
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-pad-leg", action="store_true", help="skip the padded-batch, kv-cache, rotary and backward legs")
+    ap.add_argument("--bwd-only", action="store_true", help="run only the backward leg")
     ap.add_argument("--legs-only", action="store_true", help="run only the padded-batch, kv-cache, rotary and backward legs")
     args = ap.parse_args()
     if args.warmup < 3:

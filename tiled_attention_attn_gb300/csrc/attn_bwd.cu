@@ -89,6 +89,7 @@ int bwd(bool bf16, const void* q, const void* k, const void* v, const void* o, c
   p.dv = dv;
   p.err = info.err_word;
   p.timeout_ns = wait_timeout_ns();
+  p.trace = trace_buffer(&p.trace_cap);
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;

@@ -58,6 +58,8 @@ struct BwdParams {
   void* dv;                // like k
   int* err;
   unsigned long long timeout_ns;
+  unsigned long long* trace;   // phase trace (traced build, attn_trace_enable), else null
+  int trace_cap;               // events per stream per traced CTA
   int B, Hq, Hkv, Lq, Lk, group, Lq_pad, n_qt, n_kt;
   float scale, scale_log2;
 };
@@ -66,33 +68,49 @@ template <int D>
 struct BwdCfg {
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
   static constexpr int kChunks = D / 64;
-  static constexpr int kTile = 128 * D * 2;   // one 128-row tile in smem
-  // Each streamed operand has its own ring, released after its last reader:
-  // kv kernel: Q (read by S^T and dk, with D) and dO (read by dP^T and dv,
-  // with lse2); q kernel: K (read by S and dq) and V (read by dP only).
-  static constexpr int kNQ = (D == 128) ? 2 : 4;    // kv kernel: Q slots
-  static constexpr int kNO = (D == 128) ? 2 : 4;    // kv kernel: dO slots
-  static constexpr int kNK = (D == 128) ? 3 : 6;    // q kernel: K slots
-  static constexpr int kNV = (D == 128) ? 2 : 4;    // q kernel: V slots
-  // kv kernel: K, V resident, then the Q ring, the dO ring, 512 B of D per
-  // Q slot and 512 B of lse2 per dO slot
-  static constexpr int kKvOffQ = 2 * kTile;
-  static constexpr int kKvOffO = kKvOffQ + kNQ * kTile;
-  static constexpr int kKvOffDvec = kKvOffO + kNO * kTile;
-  static constexpr int kKvOffLvec = kKvOffDvec + kNQ * 512;
-  static constexpr int kKvOffBar = kKvOffLvec + kNO * 512;
-  // barriers: kv_full, q_full/empty[NQ], o_full/empty[NO], s_full, dp_full, p_full, ds_full, acc, drain
-  static constexpr int kKvNBars = 1 + 2 * kNQ + 2 * kNO + 6;
-  static constexpr int kKvSmem = kKvOffBar + kKvNBars * 8 + 64 + 1024;
-  // q kernel: Q, dO resident, then the K ring and the V ring
-  static constexpr int kQOffK = 2 * kTile;
-  static constexpr int kQOffV = kQOffK + kNK * kTile;
-  static constexpr int kQOffBar = kQOffV + kNV * kTile;
-  // barriers: q_full, k_full/empty[NK], v_full/empty[NV], s_full, dp_full, s_free, ds_full, acc, drain
-  static constexpr int kQNBars = 1 + 2 * kNK + 2 * kNV + 6;
-  static constexpr int kQSmem = kQOffBar + kQNBars * 8 + 64 + 1024;
-  static_assert(kKvSmem <= 232448 && kQSmem <= 232448, "shared memory per CTA");
+  static constexpr int kTile = 128 * D * 2;         // one 128-row tile in smem
+  static constexpr int kNS = (D == 128) ? 2 : 4;    // stages of the streamed operands
+  // kv kernel: K, V resident; stages of (Q, dO, lse2, D)
+  static constexpr int kKvOffStage = 2 * kTile;
+  static constexpr int kKvStageBytes = 2 * kTile;
+  static constexpr int kKvOffVec = kKvOffStage + kNS * kKvStageBytes;   // per stage 128 + 128 floats
+  static constexpr int kKvOffBar = kKvOffVec + kNS * 1024;
+  // q kernel: Q, dO resident; stages of (K, V)
+  static constexpr int kQOffStage = 2 * kTile;
+  static constexpr int kQOffBar = kQOffStage + kNS * 2 * kTile;
+  // barriers: full (resident pair), st_full[NS], st_empty[NS], s_full, dp_full, and two
+  // row-side signals (kv: p_full, ds_full; q: s_free, ds_full), acc_done, drain
+  static constexpr int kNBars = 1 + 2 * kNS + 6;
+  static constexpr int kKvSmem = kKvOffBar + kNBars * 8 + 64 + 1024;
+  static constexpr int kQSmem = kQOffBar + kNBars * 8 + 64 + 1024;
   static constexpr uint32_t kTmemCols = 512;
+};
+
+// Phase trace of the first 160 CTAs (linear block id): streams 0-3 for the
+// kv kernel and 4-7 for the q kernel (MMA thread, row warp 0, row warp 4,
+// producer); an event is (tag << 32 | tile) and the SM clock.  Compiled in
+// only when ATTN_TRACE is 1.
+#ifndef ATTN_TRACE
+#define ATTN_TRACE 0
+#endif
+struct BwdTracer {
+  unsigned long long* base;
+  int cap, n;
+  __device__ __forceinline__ void init(const BwdParams& p, int stream, bool on) {
+    const int cta = blockIdx.x + gridDim.x * blockIdx.y;
+    base = (ATTN_TRACE && on && p.trace && cta < 160)
+               ? p.trace + (static_cast<size_t>(cta) * 8 + stream) * p.trace_cap * 2
+               : nullptr;
+    cap = p.trace_cap;
+    n = 0;
+  }
+  __device__ __forceinline__ void rec(int tag, int t) {
+    if (ATTN_TRACE && base != nullptr && n < cap) {
+      base[2 * n] = (static_cast<unsigned long long>(tag) << 32) | static_cast<unsigned>(t);
+      base[2 * n + 1] = clock64();
+      ++n;
+    }
+  }
 };
 
 template <bool BF16>
@@ -274,24 +292,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kv_kernel(const __gri
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sK = sbase, sV = sbase + C::kTile;
-  auto sQ = [&](int s) { return sbase + C::kKvOffQ + s * C::kTile; };
-  auto sDO = [&](int s) { return sbase + C::kKvOffO + s * C::kTile; };
-  const float* dvec_s = reinterpret_cast<const float*>(smem + C::kKvOffDvec);   // [Q slot][128]
-  const float* lvec_s = reinterpret_cast<const float*>(smem + C::kKvOffLvec);   // [dO slot][128]
+  auto sQ = [&](int s) { return sbase + C::kKvOffStage + s * C::kKvStageBytes; };
+  auto sDO = [&](int s) { return sbase + C::kKvOffStage + s * C::kKvStageBytes + C::kTile; };
+  const float* vec = reinterpret_cast<const float*>(smem + C::kKvOffVec);   // [stage][lse2 128 | D 128]
   const uint32_t bar0 = sbase + C::kKvOffBar;
   const uint32_t b_kv_full = bar0;
-  auto b_q_full = [&](int s) { return bar0 + 8 + 8 * s; };
-  auto b_q_empty = [&](int s) { return bar0 + 8 + 8 * (C::kNQ + s); };
-  auto b_o_full = [&](int s) { return bar0 + 8 + 8 * (2 * C::kNQ + s); };
-  auto b_o_empty = [&](int s) { return bar0 + 8 + 8 * (2 * C::kNQ + C::kNO + s); };
-  const uint32_t b_s_full = bar0 + 8 + 16 * (C::kNQ + C::kNO);   // S^T(t) computed
-  const uint32_t b_dp_full = b_s_full + 8;                       // dP^T(t) computed
-  const uint32_t b_p_full = b_s_full + 16;                       // P^T(t) stored by the key rows
-  const uint32_t b_ds_full = b_s_full + 24;                      // dS^T(t) stored by the key rows
+  auto b_st_full = [&](int s) { return bar0 + 8 + 8 * s; };
+  auto b_st_empty = [&](int s) { return bar0 + 8 + 8 * (C::kNS + s); };
+  const uint32_t b_s_full = bar0 + 8 + 16 * C::kNS;   // S^T(t) computed
+  const uint32_t b_dp_full = b_s_full + 8;            // dP^T(t) computed
+  const uint32_t b_p_full = b_s_full + 16;            // P^T(t) stored by the key rows
+  const uint32_t b_ds_full = b_s_full + 24;           // dS^T(t) stored by the key rows
   const uint32_t b_acc = b_s_full + 32;
   const uint32_t b_drain = b_s_full + 40;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kKvOffBar + C::kKvNBars * 8);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kKvOffBar + C::kKvNBars * 8 + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kKvOffBar + C::kNBars * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kKvOffBar + C::kNBars * 8 + 4);
   WaitCtl wc{p.err, abort_flag, p.timeout_ns};
 
   const int bg = blockIdx.x, n = blockIdx.y;
@@ -308,13 +323,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kv_kernel(const __gri
   if (tid == 0) {
     *abort_flag = 0;
     mbar_init(b_kv_full, 1);
-    for (int s = 0; s < C::kNQ; ++s) {
-      mbar_init(b_q_full(s), 1);
-      mbar_init(b_q_empty(s), 1);
-    }
-    for (int s = 0; s < C::kNO; ++s) {
-      mbar_init(b_o_full(s), 1);
-      mbar_init(b_o_empty(s), 1);
+    for (int s = 0; s < C::kNS; ++s) {
+      mbar_init(b_st_full(s), 1);
+      mbar_init(b_st_empty(s), 1);
     }
     mbar_init(b_s_full, 1);
     mbar_init(b_dp_full, 1);
@@ -343,36 +354,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kv_kernel(const __gri
         tma_load_4d(sK + c * 16384, &p.tm_k, b_kv_full, c * 64, g, n * kBN, b);
         tma_load_4d(sV + c * 16384, &p.tm_v, b_kv_full, c * 64, g, n * kBN, b);
       }
-      int nq = 0, no = 0;   // fills issued into the Q and dO rings
+      int issued = 0;
       for (int t = 0; t < n_tiles; ++t) {
+        const int st = t % C::kNS;
+        if (!mbar_wait(b_st_empty(st), ((t / C::kNS) & 1) ^ 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKEmpty))) break;
         const int h = g * p.group + t / nm, m = m_first + t % nm;
+        mbar_arrive_expect_tx(b_st_full(st), 2 * C::kTile + 1024);
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c) {
+          tma_load_4d(sQ(st) + c * 16384, &p.tm_q, b_st_full(st), c * 64, h, m * kBM, b);
+          tma_load_4d(sDO(st) + c * 16384, &p.tm_do, b_st_full(st), c * 64, h, m * kBM, b);
+        }
         const size_t vi = (static_cast<size_t>(b) * p.Hq + h) * p.Lq_pad + m * kBM;
-        const int sq = t % C::kNQ, so = t % C::kNO;
-        if (!mbar_wait(b_q_empty(sq), ((t / C::kNQ) & 1) ^ 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKEmpty))) break;
-        mbar_arrive_expect_tx(b_q_full(sq), C::kTile + 512);
-#pragma unroll
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_4d(sQ(sq) + c * 16384, &p.tm_q, b_q_full(sq), c * 64, h, m * kBM, b);
-        bulk_load(smem_u32(dvec_s + sq * 128), p.dvec + vi, 512, b_q_full(sq));
-        ++nq;
-        if (!mbar_wait(b_o_empty(so), ((t / C::kNO) & 1) ^ 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteVEmpty))) break;
-        mbar_arrive_expect_tx(b_o_full(so), C::kTile + 512);
-#pragma unroll
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_4d(sDO(so) + c * 16384, &p.tm_do, b_o_full(so), c * 64, h, m * kBM, b);
-        bulk_load(smem_u32(lvec_s + so * 128), p.lse2 + vi, 512, b_o_full(so));
-        ++no;
+        const uint32_t sv = smem_u32(vec + st * 256);
+        bulk_load(sv, p.lse2 + vi, 512, b_st_full(st));
+        bulk_load(sv + 512, p.dvec + vi, 512, b_st_full(st));
+        ++issued;
       }
       if (*abort_flag) {
         // let issued loads land before the CTA exits
         mbar_wait(b_kv_full, 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteDrain), false);
-        for (int s = 0; s < C::kNQ; ++s) {
-          const int cnt = (nq + C::kNQ - 1 - s) / C::kNQ;
-          if (cnt > 0) mbar_wait(b_q_full(s), (cnt - 1) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteDrain), false);
-        }
-        for (int s = 0; s < C::kNO; ++s) {
-          const int cnt = (no + C::kNO - 1 - s) / C::kNO;
-          if (cnt > 0) mbar_wait(b_o_full(s), (cnt - 1) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteDrain), false);
+        for (int s = 0; s < C::kNS; ++s) {
+          const int cnt = (issued + C::kNS - 1 - s) / C::kNS;
+          if (cnt > 0) mbar_wait(b_st_full(s), (cnt - 1) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteDrain), false);
         }
       }
     }
@@ -382,8 +386,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kv_kernel(const __gri
       constexpr uint32_t kIdescO = idesc_f16_f32acc(128, D, BF16, true);
       const uint64_t dk_k = sdesc_sw128(sK, 16, 1024);     // K as A, K-major
       const uint64_t dv_k = sdesc_sw128(sV, 16, 1024);     // V as A, K-major
-      auto issue_s = [&](int sq) {   // S^T = K Q^T
-        const uint64_t dq_k = sdesc_sw128(sQ(sq), 16, 1024);
+      auto issue_s = [&](int st) {   // S^T = K Q^T
+        const uint64_t dq_k = sdesc_sw128(sQ(st), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
@@ -391,8 +395,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kv_kernel(const __gri
         }
         umma_commit(b_s_full);
       };
-      auto issue_dp = [&](int so) {   // dP^T = V dO^T
-        const uint64_t ddo_k = sdesc_sw128(sDO(so), 16, 1024);
+      auto issue_dp = [&](int st) {   // dP^T = V dO^T
+        const uint64_t ddo_k = sdesc_sw128(sDO(st), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
@@ -403,41 +407,46 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kv_kernel(const __gri
       // Order per tile t: dv(t), S^T(t+1), dk(t), dP^T(t+1).  S^T(t+1)
       // overwrites P^T(t) after dv(t) has been issued, dP^T(t+1) overwrites
       // dS^T(t) after dk(t); the key rows form P^T(t+1) while dk(t) and
-      // dP^T(t+1) run, and dS^T(t) while dv(t) and S^T(t+1) run.  The dO slot
-      // is released after dv(t), the Q slot after dk(t).
+      // dP^T(t+1) run, and dS^T(t) while dv(t) and S^T(t+1) run.
+      BwdTracer tr;
+      tr.init(p, 0, true);
       bool ok = n_tiles > 0 && mbar_wait(b_kv_full, 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteQFull)) &&
-                mbar_wait(b_q_full(0), 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull));
-      if (ok) issue_s(0);
-      ok = ok && mbar_wait(b_o_full(0), 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteVFull));
-      if (ok) issue_dp(0);
+                mbar_wait(b_st_full(0), 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull));
+      if (ok) {
+        issue_s(0);
+        issue_dp(0);
+      }
       for (int t = 0; ok && t < n_tiles; ++t) {
-        const int sq = t % C::kNQ, so = t % C::kNO;
-        const int sq1 = (t + 1) % C::kNQ, so1 = (t + 1) % C::kNO;
+        const int st = t % C::kNS, st1 = (t + 1) % C::kNS;
         const bool next = t + 1 < n_tiles;
+        tr.rec(1, t);
         if (!mbar_wait(b_p_full, t & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSitePFull))) break;
+        tr.rec(2, t);
         tc_fence_after();
-        const uint64_t ddo_mn = sdesc_sw128(sDO(so), 16384, 1024);   // dO as B, MN-major
+        const uint64_t ddo_mn = sdesc_sw128(sDO(st), 16384, 1024);   // dO as B, MN-major
+        const uint64_t dq_mn = sdesc_sw128(sQ(st), 16384, 1024);     // Q as B, MN-major
 #pragma unroll
         for (int kk = 0; kk < 128 / 16; ++kk)   // dv += P^T dO
           umma_ts(tmem + 256, tmem + packed_slice_col(kk), ddo_mn + ((kk * 2048) >> 4), kIdescO,
                   (t > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(b_o_empty(so));
+        tr.rec(3, t);
         if (next) {
-          if (!mbar_wait(b_q_full(sq1), ((t + 1) / C::kNQ) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull))) break;
-          issue_s(sq1);
+          if (!mbar_wait(b_st_full(st1), ((t + 1) / C::kNS) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull))) break;
+          tr.rec(4, t);
+          issue_s(st1);
+          tr.rec(5, t);
         }
         if (!mbar_wait(b_ds_full, t & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteDsFull))) break;
+        tr.rec(6, t);
         tc_fence_after();
-        const uint64_t dq_mn = sdesc_sw128(sQ(sq), 16384, 1024);     // Q as B, MN-major
 #pragma unroll
         for (int kk = 0; kk < 128 / 16; ++kk)   // dk += dS^T Q
           umma_ts(tmem + 256 + D, tmem + 128 + packed_slice_col(kk), dq_mn + ((kk * 2048) >> 4), kIdescO,
                   (t > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(b_q_empty(sq));
-        if (next) {
-          if (!mbar_wait(b_o_full(so1), ((t + 1) / C::kNO) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteVFull))) break;
-          issue_dp(so1);
-        }
+        umma_commit(b_st_empty(st));
+        tr.rec(7, t);
+        if (next) issue_dp(st1);
+        tr.rec(8, t);
       }
       umma_commit(b_acc);
       umma_commit(b_drain);
@@ -451,41 +460,45 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kv_kernel(const __gri
     const uint32_t t_s = tmem + lane_off + half * 64, t_dp = tmem + lane_off + 128 + half * 64;
     const int j = n * kBN + row;
     const float cl2 = p.scale_log2;
+    BwdTracer tr;
+    tr.init(p, half ? 2 : 1, lane == 0 && quarter == 0);
     bool ok = true;
     for (int t = 0; t < n_tiles; ++t) {
-      const int sq = t % C::kNQ, so = t % C::kNO, m = m_first + t % nm;
+      tr.rec(20, t);
       if (!mbar_wait_warp(b_s_full, t & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteSFull))) { ok = false; break; }
+      tr.rec(21, t);
       tc_fence_after();
-      // lse2 came by bulk copy with dO: observe that slot's completion here
-      // (it is not refilled before dv(t), which waits for this warp's P)
-      if (!mbar_wait_warp(b_o_full(so), (t / C::kNO) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteVFull))) {
+      const int st = t % C::kNS, m = m_first + t % nm;
+      // lse2 and D of this stage came by bulk copy: observe its completion
+      // here (the stage cannot be refilled before this warp arrives on ds_full)
+      if (!mbar_wait_warp(b_st_full(st), (t / C::kNS) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull))) {
         ok = false;
         break;
       }
+      const float* ls = vec + st * 256 + half * 64;
+      const float* dd = vec + st * 256 + 128 + half * 64;
       // Only tiles crossing the causal diagonal are masked.  Padded query
       // columns (past Lq) have lse2 = +inf, so P = 0 there; padded key rows
       // (past Lk) only reach their own rows of dv and dk, which are not stored.
       float pr[64];
       if (CAUSAL && n * kBN + kBN - 1 - m * kBM > off)
-        kv_p_half<true, BF16>(t_s, lvec_s + so * 128 + half * 64, j - off - m * kBM - half * 64, cl2, pr);
+        kv_p_half<true, BF16>(t_s, ls, j - off - m * kBM - half * 64, cl2, pr);
       else
-        kv_p_half<false, BF16>(t_s, lvec_s + so * 128 + half * 64, 0, cl2, pr);
+        kv_p_half<false, BF16>(t_s, ls, 0, cl2, pr);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_p_full);
+      tr.rec(22, t);
       if (!mbar_wait_warp(b_dp_full, t & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteODone))) { ok = false; break; }
+      tr.rec(23, t);
       tc_fence_after();
-      // D came with Q; that slot is not refilled before dk(t), which waits for this warp's dS
-      if (!mbar_wait_warp(b_q_full(sq), (t / C::kNQ) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull))) {
-        ok = false;
-        break;
-      }
-      ds_half<BF16>(t_dp, dvec_s + sq * 128 + half * 64, 0.0f, pr);
+      ds_half<BF16>(t_dp, dd, 0.0f, pr);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_ds_full);
+      tr.rec(24, t);
     }
     // epilogue: dv = acc, dk = scale * acc; this warp's half of the columns
     if (ok && (n_tiles == 0 || mbar_wait_warp(b_acc, 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteODone)))) {
@@ -543,22 +556,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sQ = sbase, sDO = sbase + C::kTile;
-  auto sK = [&](int s) { return sbase + C::kQOffK + s * C::kTile; };
-  auto sV = [&](int s) { return sbase + C::kQOffV + s * C::kTile; };
+  auto sK = [&](int s) { return sbase + C::kQOffStage + s * 2 * C::kTile; };
+  auto sV = [&](int s) { return sbase + C::kQOffStage + s * 2 * C::kTile + C::kTile; };
   const uint32_t bar0 = sbase + C::kQOffBar;
   const uint32_t b_q_full = bar0;
-  auto b_k_full = [&](int s) { return bar0 + 8 + 8 * s; };
-  auto b_k_empty = [&](int s) { return bar0 + 8 + 8 * (C::kNK + s); };
-  auto b_v_full = [&](int s) { return bar0 + 8 + 8 * (2 * C::kNK + s); };
-  auto b_v_empty = [&](int s) { return bar0 + 8 + 8 * (2 * C::kNK + C::kNV + s); };
-  const uint32_t b_s_full = bar0 + 8 + 16 * (C::kNK + C::kNV);   // S(t) computed
-  const uint32_t b_dp_full = b_s_full + 8;                       // dP(t) computed
-  const uint32_t b_s_free = b_s_full + 16;                       // the query rows have read S(t)
-  const uint32_t b_ds_full = b_s_full + 24;                      // dS(t) stored by the query rows
+  auto b_st_full = [&](int s) { return bar0 + 8 + 8 * s; };
+  auto b_st_empty = [&](int s) { return bar0 + 8 + 8 * (C::kNS + s); };
+  const uint32_t b_s_full = bar0 + 8 + 16 * C::kNS;   // S(t) computed
+  const uint32_t b_dp_full = b_s_full + 8;            // dP(t) computed
+  const uint32_t b_s_free = b_s_full + 16;            // the query rows have read S(t)
+  const uint32_t b_ds_full = b_s_full + 24;           // dS(t) stored by the query rows
   const uint32_t b_acc = b_s_full + 32;
   const uint32_t b_drain = b_s_full + 40;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kQOffBar + C::kQNBars * 8);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kQOffBar + C::kQNBars * 8 + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kQOffBar + C::kNBars * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kQOffBar + C::kNBars * 8 + 4);
   WaitCtl wc{p.err, abort_flag, p.timeout_ns};
 
   const int bh = blockIdx.x, m = p.n_qt - 1 - static_cast<int>(blockIdx.y);
@@ -575,13 +586,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
   if (tid == 0) {
     *abort_flag = 0;
     mbar_init(b_q_full, 1);
-    for (int s = 0; s < C::kNK; ++s) {
-      mbar_init(b_k_full(s), 1);
-      mbar_init(b_k_empty(s), 1);
-    }
-    for (int s = 0; s < C::kNV; ++s) {
-      mbar_init(b_v_full(s), 1);
-      mbar_init(b_v_empty(s), 1);
+    for (int s = 0; s < C::kNS; ++s) {
+      mbar_init(b_st_full(s), 1);
+      mbar_init(b_st_empty(s), 1);
     }
     mbar_init(b_s_full, 1);
     mbar_init(b_dp_full, 1);
@@ -610,31 +617,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
         tma_load_4d(sQ + c * 16384, &p.tm_q, b_q_full, c * 64, h, m * kBM, b);
         tma_load_4d(sDO + c * 16384, &p.tm_do, b_q_full, c * 64, h, m * kBM, b);
       }
-      int nk = 0, nv = 0;
+      int issued = 0;
       for (int t = 0; t < n_tiles; ++t) {
-        const int sk = t % C::kNK, sv = t % C::kNV;
-        if (!mbar_wait(b_k_empty(sk), ((t / C::kNK) & 1) ^ 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKEmpty))) break;
-        mbar_arrive_expect_tx(b_k_full(sk), C::kTile);
+        const int st = t % C::kNS;
+        if (!mbar_wait(b_st_empty(st), ((t / C::kNS) & 1) ^ 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKEmpty))) break;
+        mbar_arrive_expect_tx(b_st_full(st), 2 * C::kTile);
 #pragma unroll
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_4d(sK(sk) + c * 16384, &p.tm_k, b_k_full(sk), c * 64, g, t * kBN, b);
-        ++nk;
-        if (!mbar_wait(b_v_empty(sv), ((t / C::kNV) & 1) ^ 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteVEmpty))) break;
-        mbar_arrive_expect_tx(b_v_full(sv), C::kTile);
-#pragma unroll
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_4d(sV(sv) + c * 16384, &p.tm_v, b_v_full(sv), c * 64, g, t * kBN, b);
-        ++nv;
+        for (int c = 0; c < C::kChunks; ++c) {
+          tma_load_4d(sK(st) + c * 16384, &p.tm_k, b_st_full(st), c * 64, g, t * kBN, b);
+          tma_load_4d(sV(st) + c * 16384, &p.tm_v, b_st_full(st), c * 64, g, t * kBN, b);
+        }
+        ++issued;
       }
       if (*abort_flag) {
         mbar_wait(b_q_full, 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteDrain), false);
-        for (int s = 0; s < C::kNK; ++s) {
-          const int cnt = (nk + C::kNK - 1 - s) / C::kNK;
-          if (cnt > 0) mbar_wait(b_k_full(s), (cnt - 1) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteDrain), false);
-        }
-        for (int s = 0; s < C::kNV; ++s) {
-          const int cnt = (nv + C::kNV - 1 - s) / C::kNV;
-          if (cnt > 0) mbar_wait(b_v_full(s), (cnt - 1) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteDrain), false);
+        for (int s = 0; s < C::kNS; ++s) {
+          const int cnt = (issued + C::kNS - 1 - s) / C::kNS;
+          if (cnt > 0) mbar_wait(b_st_full(s), (cnt - 1) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteDrain), false);
         }
       }
     }
@@ -644,8 +643,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
       constexpr uint32_t kIdescO = idesc_f16_f32acc(128, D, BF16, true);
       const uint64_t dq_k = sdesc_sw128(sQ, 16, 1024);
       const uint64_t ddo_k = sdesc_sw128(sDO, 16, 1024);
-      auto issue_s = [&](int sk) {   // S = Q K^T
-        const uint64_t dk_k = sdesc_sw128(sK(sk), 16, 1024);
+      auto issue_s = [&](int st) {   // S = Q K^T
+        const uint64_t dk_k = sdesc_sw128(sK(st), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
@@ -653,44 +652,50 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
         }
         umma_commit(b_s_full);
       };
-      auto issue_dp = [&](int sv) {   // dP = dO V^T; V is read by nothing else
-        const uint64_t dv_k = sdesc_sw128(sV(sv), 16, 1024);
+      auto issue_dp = [&](int st) {   // dP = dO V^T
+        const uint64_t dv_k = sdesc_sw128(sV(st), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
           umma_ss(tmem + 128, ddo_k + o, dv_k + o, kIdescS, kk > 0 ? 1u : 0u);
         }
         umma_commit(b_dp_full);
-        umma_commit(b_v_empty(sv));
       };
       // Order per tile t: S(t+1) (once the rows have read S(t)), dq(t),
-      // dP(t+1).  dS(t) lives over dP(t)'s first columns, so S(t+1) does not
-      // wait for dq(t); dP(t+1) is issued after dq(t) has been.
+      // dP(t+1).  dS(t) lives over dP(t)'s first 64 columns, so S(t+1) does
+      // not wait for dq(t); dP(t+1) is issued after dq(t) has been.
+      BwdTracer tr;
+      tr.init(p, 4, true);
       bool ok = n_tiles > 0 && mbar_wait(b_q_full, 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteQFull)) &&
-                mbar_wait(b_k_full(0), 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull));
-      if (ok) issue_s(0);
-      ok = ok && mbar_wait(b_v_full(0), 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteVFull));
-      if (ok) issue_dp(0);
+                mbar_wait(b_st_full(0), 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull));
+      if (ok) {
+        issue_s(0);
+        issue_dp(0);
+      }
       for (int t = 0; ok && t < n_tiles; ++t) {
-        const int sk = t % C::kNK, sk1 = (t + 1) % C::kNK, sv1 = (t + 1) % C::kNV;
+        const int st = t % C::kNS, st1 = (t + 1) % C::kNS;
         const bool next = t + 1 < n_tiles;
+        tr.rec(1, t);
         if (next) {
           if (!mbar_wait(b_s_free, t & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSitePFull))) break;
-          if (!mbar_wait(b_k_full(sk1), ((t + 1) / C::kNK) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull))) break;
-          issue_s(sk1);
+          tr.rec(2, t);
+          if (!mbar_wait(b_st_full(st1), ((t + 1) / C::kNS) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull))) break;
+          tr.rec(3, t);
+          issue_s(st1);
+          tr.rec(4, t);
         }
         if (!mbar_wait(b_ds_full, t & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteDsFull))) break;
+        tr.rec(6, t);
         tc_fence_after();
-        const uint64_t dk_mn = sdesc_sw128(sK(sk), 16384, 1024);   // K as B, MN-major
+        const uint64_t dk_mn = sdesc_sw128(sK(st), 16384, 1024);   // K as B, MN-major
 #pragma unroll
         for (int kk = 0; kk < 128 / 16; ++kk)   // dq += dS K
           umma_ts(tmem + 256, tmem + 128 + packed_slice_col(kk), dk_mn + ((kk * 2048) >> 4), kIdescO,
                   (t > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(b_k_empty(sk));
-        if (next) {
-          if (!mbar_wait(b_v_full(sv1), ((t + 1) / C::kNV) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteVFull))) break;
-          issue_dp(sv1);
-        }
+        umma_commit(b_st_empty(st));
+        tr.rec(7, t);
+        if (next) issue_dp(st1);
+        tr.rec(8, t);
       }
       umma_commit(b_acc);
       umma_commit(b_drain);
@@ -709,9 +714,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
     const float di = __ldg(p.dvec + vi);
     int lim_key = p.Lk - 1;
     if constexpr (CAUSAL) lim_key = min(lim_key, i + off);
+    BwdTracer tr;
+    tr.init(p, half ? 6 : 5, lane == 0 && quarter == 0);
     bool ok = true;
     for (int t = 0; t < n_tiles; ++t) {
+      tr.rec(20, t);
       if (!mbar_wait_warp(b_s_full, t & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteSFull))) { ok = false; break; }
+      tr.rec(21, t);
       tc_fence_after();
       // masked: tiles crossing the causal diagonal and the ragged last key tile
       float pr[64];
@@ -722,13 +731,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_s_free);
+      tr.rec(22, t);
       if (!mbar_wait_warp(b_dp_full, t & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteODone))) { ok = false; break; }
+      tr.rec(23, t);
       tc_fence_after();
       ds_half<BF16>(t_dp, nullptr, di, pr);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_ds_full);
+      tr.rec(24, t);
     }
     if (ok && (n_tiles == 0 || mbar_wait_warp(b_acc, 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteODone)))) {
       tc_fence_after();

@@ -361,6 +361,11 @@ int encode_map(const void* ptr, bool bf16, int d, int H, int L, int B, CUtensorM
 }
 
 unsigned long long wait_timeout_ns() { return g_timeout_ns.load(); }
+unsigned long long* trace_buffer(int* events_per_stream) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  *events_per_stream = g_trace_cap;
+  return g_trace;
+}
 void count_launch() { g_launches.fetch_add(1); }
 
 cudaError_t launch_selftest_wait(int* err_word, unsigned long long timeout_ns, cudaStream_t stream) {

@@ -21,6 +21,8 @@ int encode_map(const void* ptr, bool bf16, int d, int H, int L, int B, CUtensorM
 
 // Current barrier-wait time limit and the launch counter of attn_launch_count().
 unsigned long long wait_timeout_ns();
+// The phase-trace buffer set by attn_trace_enable (traced build), or null.
+unsigned long long* trace_buffer(int* events_per_stream);
 void count_launch();
 
 }  // namespace attn
