@@ -209,11 +209,12 @@ __device__ __forceinline__ uint32_t packed_slice_col(int kk) { return (kk >> 2) 
 // columns.  MASK: query column c is allowed iff c >= cmin (causal).
 template <bool MASK, bool BF16>
 __device__ __forceinline__ void kv_p_half(uint32_t t_s, const float* ls, int cmin, float cl2, float (&pr)[64]) {
+  uint32_t s64[64];
+  tmem_ld_32x32b_x64(t_s, s64);
+  tmem_wait_ld(s64);
 #pragma unroll
   for (int ch = 0; ch < 2; ++ch) {
-    uint32_t sr[32];
-    tmem_ld_32x32b_x32(t_s + ch * 32, sr);
-    tmem_wait_ld(sr);
+    const uint32_t* sr = s64 + ch * 32;
     uint32_t pk[16];
 #pragma unroll
     for (int e = 0; e < 32; e += 4) {
@@ -263,21 +264,15 @@ __device__ __forceinline__ void ds_half(uint32_t t_dp, const float* dd, float di
   }
 }
 
-// q kernel, one warp's 64 key columns of its 32 query rows: P = 2^(S c - lse2_i)
-// kept in pr.  MASK: key column c is allowed iff c <= lim.
+// q kernel, one warp's 64 key columns of its 32 query rows, from S already
+// in registers: P = 2^(S c - lse2_i) in pr.  MASK: key column c is allowed
+// iff c <= lim.
 template <bool MASK>
-__device__ __forceinline__ void q_p_half(uint32_t t_s, float l2, int lim, float cl2, float (&pr)[64]) {
+__device__ __forceinline__ void q_p_half(const uint32_t (&sr)[64], float l2, int lim, float cl2, float (&pr)[64]) {
 #pragma unroll
-  for (int ch = 0; ch < 2; ++ch) {
-    uint32_t sr[32];
-    tmem_ld_32x32b_x32(t_s + ch * 32, sr);
-    tmem_wait_ld(sr);
-#pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      const int c = ch * 32 + e;
-      const float x = ex2_approx(fmaf(__uint_as_float(sr[e]), cl2, -l2));
-      pr[c] = (!MASK || c <= lim) ? x : 0.0f;
-    }
+  for (int c = 0; c < 64; ++c) {
+    const float x = ex2_approx(fmaf(__uint_as_float(sr[c]), cl2, -l2));
+    pr[c] = (!MASK || c <= lim) ? x : 0.0f;
   }
 }
 
@@ -722,15 +717,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
       if (!mbar_wait_warp(b_s_full, t & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteSFull))) { ok = false; break; }
       tr.rec(21, t);
       tc_fence_after();
-      // masked: tiles crossing the causal diagonal and the ragged last key tile
-      float pr[64];
-      if ((CAUSAL && t * kBN + kBN - 1 > m * kBM + off) || t * kBN + kBN > p.Lk)
-        q_p_half<true>(t_s, l2, lim_key - t * kBN - half * 64, cl2, pr);
-      else
-        q_p_half<false>(t_s, l2, 0, cl2, pr);
+      // S is released as soon as it is in registers; P is formed after
+      uint32_t sr[64];
+      tmem_ld_32x32b_x64(t_s, sr);
+      tmem_wait_ld(sr);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_s_free);
+      // masked: tiles crossing the causal diagonal and the ragged last key tile
+      float pr[64];
+      if ((CAUSAL && t * kBN + kBN - 1 > m * kBM + off) || t * kBN + kBN > p.Lk)
+        q_p_half<true>(sr, l2, lim_key - t * kBN - half * 64, cl2, pr);
+      else
+        q_p_half<false>(sr, l2, 0, cl2, pr);
       tr.rec(22, t);
       if (!mbar_wait_warp(b_dp_full, t & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteODone))) { ok = false; break; }
       tr.rec(23, t);
