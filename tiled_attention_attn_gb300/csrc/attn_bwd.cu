@@ -84,6 +84,8 @@ int bwd(bool bf16, const void* q, const void* k, const void* v, const void* o, c
   }
   p.lse2 = ws.buf;
   p.dvec = ws.buf + need / 2;
+  p.q = q;
+  p.dout = dout;
   p.dq = dq;
   p.dk = dk;
   p.dv = dv;

@@ -51,6 +51,8 @@ struct BwdParams {
   CUtensorMap tm_k;        // (d, Hkv, Lk, B)
   CUtensorMap tm_v;
   CUtensorMap tm_do;       // like q
+  const void* q;           // (B, Lq, Hq, d): the q kernel reads its Q and dO rows directly
+  const void* dout;
   const float* lse2;       // [B][Hq][Lq_pad]: lse * log2(e); +inf for rows with no key and the padding
   const float* dvec;       // [B][Hq][Lq_pad]: D_i = dout_i . O_i; 0 on the padding
   void* dq;                // like q
@@ -75,14 +77,19 @@ struct BwdCfg {
   static constexpr int kKvStageBytes = 2 * kTile;
   static constexpr int kKvOffVec = kKvOffStage + kNS * kKvStageBytes;   // per stage 128 + 128 floats
   static constexpr int kKvOffBar = kKvOffVec + kNS * 1024;
-  // q kernel: Q, dO resident; stages of (K, V)
-  static constexpr int kQOffStage = 2 * kTile;
-  static constexpr int kQOffBar = kQOffStage + kNS * 2 * kTile;
+  // q kernel: Q and dO live in TMEM (the A operands of S and dP), so shared
+  // memory holds only stages of (K, V)
+  static constexpr int kQNS = (D == 128) ? 3 : 6;
+  static constexpr int kQOffStage = 0;
+  static constexpr int kQOffBar = kQOffStage + kQNS * 2 * kTile;
+  static constexpr int kQNBars = 1 + 2 * kQNS + 6;
+  static constexpr uint32_t kColQ = 384;             // Q packed, D/2 columns
+  static constexpr uint32_t kColDO = 384 + D / 2;    // dO packed, D/2 columns
   // barriers: full (resident pair), st_full[NS], st_empty[NS], s_full, dp_full, and two
   // row-side signals (kv: p_full, ds_full; q: s_free, ds_full), acc_done, drain
   static constexpr int kNBars = 1 + 2 * kNS + 6;
   static constexpr int kKvSmem = kKvOffBar + kNBars * 8 + 64 + 1024;
-  static constexpr int kQSmem = kQOffBar + kNBars * 8 + 64 + 1024;
+  static constexpr int kQSmem = kQOffBar + kQNBars * 8 + 64 + 1024;
   static constexpr uint32_t kTmemCols = 512;
 };
 
@@ -209,12 +216,11 @@ __device__ __forceinline__ uint32_t packed_slice_col(int kk) { return (kk >> 2) 
 // columns.  MASK: query column c is allowed iff c >= cmin (causal).
 template <bool MASK, bool BF16>
 __device__ __forceinline__ void kv_p_half(uint32_t t_s, const float* ls, int cmin, float cl2, float (&pr)[64]) {
-  uint32_t s64[64];
-  tmem_ld_32x32b_x64(t_s, s64);
-  tmem_wait_ld(s64);
 #pragma unroll
   for (int ch = 0; ch < 2; ++ch) {
-    const uint32_t* sr = s64 + ch * 32;
+    uint32_t sr[32];
+    tmem_ld_32x32b_x32(t_s + ch * 32, sr);
+    tmem_wait_ld(sr);
     uint32_t pk[16];
 #pragma unroll
     for (int e = 0; e < 32; e += 4) {
@@ -550,21 +556,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t sQ = sbase, sDO = sbase + C::kTile;
   auto sK = [&](int s) { return sbase + C::kQOffStage + s * 2 * C::kTile; };
   auto sV = [&](int s) { return sbase + C::kQOffStage + s * 2 * C::kTile + C::kTile; };
   const uint32_t bar0 = sbase + C::kQOffBar;
-  const uint32_t b_q_full = bar0;
+  const uint32_t b_q_full = bar0;   // the rows have stored Q and dO in TMEM
   auto b_st_full = [&](int s) { return bar0 + 8 + 8 * s; };
-  auto b_st_empty = [&](int s) { return bar0 + 8 + 8 * (C::kNS + s); };
-  const uint32_t b_s_full = bar0 + 8 + 16 * C::kNS;   // S(t) computed
+  auto b_st_empty = [&](int s) { return bar0 + 8 + 8 * (C::kQNS + s); };
+  const uint32_t b_s_full = bar0 + 8 + 16 * C::kQNS;   // S(t) computed
   const uint32_t b_dp_full = b_s_full + 8;            // dP(t) computed
   const uint32_t b_s_free = b_s_full + 16;            // the query rows have read S(t)
   const uint32_t b_ds_full = b_s_full + 24;           // dS(t) stored by the query rows
   const uint32_t b_acc = b_s_full + 32;
   const uint32_t b_drain = b_s_full + 40;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kQOffBar + C::kNBars * 8);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kQOffBar + C::kNBars * 8 + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kQOffBar + C::kQNBars * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kQOffBar + C::kQNBars * 8 + 4);
   WaitCtl wc{p.err, abort_flag, p.timeout_ns};
 
   const int bh = blockIdx.x, m = p.n_qt - 1 - static_cast<int>(blockIdx.y);
@@ -580,8 +585,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
 
   if (tid == 0) {
     *abort_flag = 0;
-    mbar_init(b_q_full, 1);
-    for (int s = 0; s < C::kNS; ++s) {
+    mbar_init(b_q_full, kBwdRowWarps);
+    for (int s = 0; s < C::kQNS; ++s) {
       mbar_init(b_st_full(s), 1);
       mbar_init(b_st_empty(s), 1);
     }
@@ -606,16 +611,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
     if (lane == 0 && n_tiles > 0) {
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
-      mbar_arrive_expect_tx(b_q_full, 2 * C::kTile);
-#pragma unroll
-      for (int c = 0; c < C::kChunks; ++c) {
-        tma_load_4d(sQ + c * 16384, &p.tm_q, b_q_full, c * 64, h, m * kBM, b);
-        tma_load_4d(sDO + c * 16384, &p.tm_do, b_q_full, c * 64, h, m * kBM, b);
-      }
       int issued = 0;
       for (int t = 0; t < n_tiles; ++t) {
-        const int st = t % C::kNS;
-        if (!mbar_wait(b_st_empty(st), ((t / C::kNS) & 1) ^ 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKEmpty))) break;
+        const int st = t % C::kQNS;
+        if (!mbar_wait(b_st_empty(st), ((t / C::kQNS) & 1) ^ 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKEmpty))) break;
         mbar_arrive_expect_tx(b_st_full(st), 2 * C::kTile);
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c) {
@@ -625,9 +624,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
         ++issued;
       }
       if (*abort_flag) {
-        mbar_wait(b_q_full, 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteDrain), false);
-        for (int s = 0; s < C::kNS; ++s) {
-          const int cnt = (issued + C::kNS - 1 - s) / C::kNS;
+        for (int s = 0; s < C::kQNS; ++s) {
+          const int cnt = (issued + C::kQNS - 1 - s) / C::kQNS;
           if (cnt > 0) mbar_wait(b_st_full(s), (cnt - 1) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteDrain), false);
         }
       }
@@ -636,23 +634,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
     if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_f16_f32acc(128, 128, BF16, false);
       constexpr uint32_t kIdescO = idesc_f16_f32acc(128, D, BF16, true);
-      const uint64_t dq_k = sdesc_sw128(sQ, 16, 1024);
-      const uint64_t ddo_k = sdesc_sw128(sDO, 16, 1024);
-      auto issue_s = [&](int st) {   // S = Q K^T
+      auto issue_s = [&](int st) {   // S = Q K^T, Q from TMEM
         const uint64_t dk_k = sdesc_sw128(sK(st), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-          umma_ss(tmem + 0, dq_k + o, dk_k + o, kIdescS, kk > 0 ? 1u : 0u);
+          umma_ts(tmem + 0, tmem + C::kColQ + kk * 8, dk_k + o, kIdescS, kk > 0 ? 1u : 0u);
         }
         umma_commit(b_s_full);
       };
-      auto issue_dp = [&](int st) {   // dP = dO V^T
+      auto issue_dp = [&](int st) {   // dP = dO V^T, dO from TMEM
         const uint64_t dv_k = sdesc_sw128(sV(st), 16, 1024);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-          umma_ss(tmem + 128, ddo_k + o, dv_k + o, kIdescS, kk > 0 ? 1u : 0u);
+          umma_ts(tmem + 128, tmem + C::kColDO + kk * 8, dv_k + o, kIdescS, kk > 0 ? 1u : 0u);
         }
         umma_commit(b_dp_full);
       };
@@ -664,17 +660,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
       bool ok = n_tiles > 0 && mbar_wait(b_q_full, 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteQFull)) &&
                 mbar_wait(b_st_full(0), 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull));
       if (ok) {
+        tc_fence_after();   // Q and dO were written into TMEM by the rows (tcgen05.st)
         issue_s(0);
         issue_dp(0);
       }
       for (int t = 0; ok && t < n_tiles; ++t) {
-        const int st = t % C::kNS, st1 = (t + 1) % C::kNS;
+        const int st = t % C::kQNS, st1 = (t + 1) % C::kQNS;
         const bool next = t + 1 < n_tiles;
         tr.rec(1, t);
         if (next) {
           if (!mbar_wait(b_s_free, t & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSitePFull))) break;
           tr.rec(2, t);
-          if (!mbar_wait(b_st_full(st1), ((t + 1) / C::kNS) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull))) break;
+          if (!mbar_wait(b_st_full(st1), ((t + 1) / C::kQNS) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull))) break;
           tr.rec(3, t);
           issue_s(st1);
           tr.rec(4, t);
@@ -711,6 +708,36 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
     if constexpr (CAUSAL) lim_key = min(lim_key, i + off);
     BwdTracer tr;
     tr.init(p, half ? 6 : 5, lane == 0 && quarter == 0);
+    if (n_tiles > 0) {
+      // this row's Q and dO (half the columns per warp half) into TMEM, packed
+      // two 16-bit values per column in memory order; rows past Lq are zero
+      using T = typename BwdIO<BF16>::T;
+      constexpr int kW = D / 16;   // uint4 words per half row
+      const size_t src = ((static_cast<size_t>(b) * p.Lq + i) * p.Hq + h) * D + half * (D / 2);
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint4* g4 = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(which ? p.dout : p.q) + src);
+        uint32_t w[4 * kW];
+#pragma unroll
+        for (int u = 0; u < kW; ++u) {
+          const uint4 x = (i < p.Lq) ? __ldg(g4 + u) : make_uint4(0, 0, 0, 0);
+          w[4 * u] = x.x;
+          w[4 * u + 1] = x.y;
+          w[4 * u + 2] = x.z;
+          w[4 * u + 3] = x.w;
+        }
+        const uint32_t col = tmem + lane_off + (which ? C::kColDO : C::kColQ) + half * (D / 4);
+        if constexpr (D == 128) {
+          tmem_st_32x32b_x32(col, w);
+        } else {
+          tmem_st_32x32b_x16(col, w);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_q_full);
+    }
     bool ok = true;
     for (int t = 0; t < n_tiles; ++t) {
       tr.rec(20, t);
