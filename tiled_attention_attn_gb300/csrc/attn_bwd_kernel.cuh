@@ -224,13 +224,19 @@ __device__ __forceinline__ void kv_p_half(uint32_t t_s, const float* ls, int cmi
     uint32_t pk[16];
 #pragma unroll
     for (int e = 0; e < 32; e += 4) {
+      // the exponent arguments with packed fp32x2 FMA: scalar FMA streams on
+      // the MMA issuer's sub-partition slow its issue
       const float4 l4 = *reinterpret_cast<const float4*>(ls + ch * 32 + e);
-      const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+      const float2 c2 = make_float2(cl2, cl2);
+      const float2 a0 = ffma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2,
+                              make_float2(-l4.x, -l4.y));
+      const float2 a1 = ffma2(make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), c2,
+                              make_float2(-l4.z, -l4.w));
+      const float xs[4] = {ex2_approx(a0.x), ex2_approx(a0.y), ex2_approx(a1.x), ex2_approx(a1.y)};
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int c = ch * 32 + e + u;
-        const float x = ex2_approx(fmaf(__uint_as_float(sr[e + u]), cl2, -lv[u]));
-        pr[c] = (!MASK || c >= cmin) ? x : 0.0f;
+        pr[c] = (!MASK || c >= cmin) ? xs[u] : 0.0f;
       }
       pk[e / 2] = pack2<BF16>(pr[ch * 32 + e], pr[ch * 32 + e + 1]);
       pk[e / 2 + 1] = pack2<BF16>(pr[ch * 32 + e + 2], pr[ch * 32 + e + 3]);
@@ -260,11 +266,14 @@ __device__ __forceinline__ void ds_half(uint32_t t_dp, const float* dd, float di
         dv4[2] = d4.z;
         dv4[3] = d4.w;
       }
-      float ds[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) ds[u] = pr[ch * 32 + e + u] * (__uint_as_float(dr[e + u]) - dv4[u]);
-      dk[e / 2] = pack2<BF16>(ds[0], ds[1]);
-      dk[e / 2 + 1] = pack2<BF16>(ds[2], ds[3]);
+      const float2 d0 = fmul2(make_float2(pr[ch * 32 + e], pr[ch * 32 + e + 1]),
+                              fadd2(make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])),
+                                    make_float2(-dv4[0], -dv4[1])));
+      const float2 d1 = fmul2(make_float2(pr[ch * 32 + e + 2], pr[ch * 32 + e + 3]),
+                              fadd2(make_float2(__uint_as_float(dr[e + 2]), __uint_as_float(dr[e + 3])),
+                                    make_float2(-dv4[2], -dv4[3])));
+      dk[e / 2] = pack2<BF16>(d0.x, d0.y);
+      dk[e / 2 + 1] = pack2<BF16>(d1.x, d1.y);
     }
     tmem_st_32x32b_x16(t_dp + ch * 16, dk);
   }
@@ -275,10 +284,13 @@ __device__ __forceinline__ void ds_half(uint32_t t_dp, const float* dd, float di
 // iff c <= lim.
 template <bool MASK>
 __device__ __forceinline__ void q_p_half(const uint32_t (&sr)[64], float l2, int lim, float cl2, float (&pr)[64]) {
+  const float2 c2 = make_float2(cl2, cl2), nl = make_float2(-l2, -l2);
 #pragma unroll
-  for (int c = 0; c < 64; ++c) {
-    const float x = ex2_approx(fmaf(__uint_as_float(sr[c]), cl2, -l2));
-    pr[c] = (!MASK || c <= lim) ? x : 0.0f;
+  for (int c = 0; c < 64; c += 2) {
+    const float2 a = ffma2(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), c2, nl);
+    const float x0 = ex2_approx(a.x), x1 = ex2_approx(a.y);
+    pr[c] = (!MASK || c <= lim) ? x0 : 0.0f;
+    pr[c + 1] = (!MASK || c + 1 <= lim) ? x1 : 0.0f;
   }
 }
 
