@@ -70,9 +70,6 @@ typedef struct CUstream_st *cudaStream_t;
                                            low byte names the wait site */
 #define ATTN_DEVERR_BAD_SEQLENS 0x200   /* cu_seqlens not non-decreasing from 0, or its last
                                            entry exceeds the packed length */
-#define ATTN_DEVERR_SMEM_ALIGN 0x300    /* the dynamic shared memory of a kernel that has no
-                                           alignment slack did not start on 1024 bytes; the
-                                           kernel returned without computing */
 
 /*
  * attn_fwd -- attention forward, bf16 inputs and outputs, fp32 accumulation.

@@ -75,17 +75,8 @@ struct BwdCfg {
   // kv kernel: K, V resident; stages of (Q, dO, lse2, D)
   static constexpr int kKvOffStage = 2 * kTile;
   static constexpr int kKvStageBytes = 2 * kTile;
-  // P^T (128 keys x 128 queries, 16-bit) in the 128-byte-swizzled K-major
-  // layout the MMA reads as its A operand: two 16 KB chunks of 64 queries
-  static constexpr int kKvOffPT = kKvOffStage + kNS * kKvStageBytes;
-  static constexpr int kKvOffVec = kKvOffPT + 32768;   // per stage 128 + 128 floats
+  static constexpr int kKvOffVec = kKvOffStage + kNS * kKvStageBytes;   // per stage 128 + 128 floats
   static constexpr int kKvOffBar = kKvOffVec + kNS * 1024;
-  // barriers: kv_full, st_full[NS], st_empty[NS], s_full, dp_full, s_free, p_full, ds_full,
-  // pt_free, acc_done, drain
-  static constexpr int kKvNBars = 1 + 2 * kNS + 8;
-  // no alignment slack (the kernel checks that its dynamic shared memory
-  // starts on 1024 bytes): with d = 128 it needs nearly all 227 KB
-  static constexpr int kKvSmem = kKvOffBar + kKvNBars * 8 + 64;
   // q kernel: Q and dO live in TMEM (the A operands of S and dP), so shared
   // memory holds only stages of (K, V)
   static constexpr int kQNS = (D == 128) ? 3 : 6;
@@ -96,9 +87,10 @@ struct BwdCfg {
   static constexpr uint32_t kColDO = 384 + D / 2;    // dO packed, D/2 columns
   // barriers: full (resident pair), st_full[NS], st_empty[NS], s_full, dp_full, and two
   // row-side signals (kv: p_full, ds_full; q: s_free, ds_full), acc_done, drain
+  static constexpr int kNBars = 1 + 2 * kNS + 6;
+  static constexpr int kKvSmem = kKvOffBar + kNBars * 8 + 64 + 1024;
   static constexpr int kQSmem = kQOffBar + kQNBars * 8 + 64 + 1024;
   static constexpr uint32_t kTmemCols = 512;
-  static_assert(kKvSmem <= 232448 && kQSmem <= 232448, "dynamic shared memory per CTA");
 };
 
 // Phase trace of the first 160 CTAs (linear block id): streams 0-3 for the
@@ -219,23 +211,37 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const void* __restri
 // 128-column S or dP region: warp half h packs columns 64h.. into 64h..64h+31.
 __device__ __forceinline__ uint32_t packed_slice_col(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
 
-// kv kernel, one warp's 64 query columns of its 32 key rows, from S^T in
-// registers: P^T = 2^(S^T c - lse2) in pr.  MASK: query column c is allowed
-// iff c >= cmin (causal).
-template <bool MASK>
-__device__ __forceinline__ void kv_p_regs(const uint32_t (&sr)[64], const float* ls, int cmin, float cl2,
-                                          float (&pr)[64]) {
-  const float2 c2 = make_float2(cl2, cl2);
+// kv kernel, one warp's 64 query columns of its 32 key rows: P^T = 2^(S^T c - lse2)
+// (c = scale log2 e), kept in pr and stored packed over the first 32 of its
+// columns.  MASK: query column c is allowed iff c >= cmin (causal).
+template <bool MASK, bool BF16>
+__device__ __forceinline__ void kv_p_half(uint32_t t_s, const float* ls, int cmin, float cl2, float (&pr)[64]) {
 #pragma unroll
-  for (int e = 0; e < 64; e += 4) {
-    const float4 l4 = *reinterpret_cast<const float4*>(ls + e);
-    const float2 a0 = ffma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2,
-                            make_float2(-l4.x, -l4.y));
-    const float2 a1 = ffma2(make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), c2,
-                            make_float2(-l4.z, -l4.w));
-    const float xs[4] = {ex2_approx(a0.x), ex2_approx(a0.y), ex2_approx(a1.x), ex2_approx(a1.y)};
+  for (int ch = 0; ch < 2; ++ch) {
+    uint32_t sr[32];
+    tmem_ld_32x32b_x32(t_s + ch * 32, sr);
+    tmem_wait_ld(sr);
+    uint32_t pk[16];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) pr[e + u] = (!MASK || e + u >= cmin) ? xs[u] : 0.0f;
+    for (int e = 0; e < 32; e += 4) {
+      // the exponent arguments with packed fp32x2 FMA: scalar FMA streams on
+      // the MMA issuer's sub-partition slow its issue
+      const float4 l4 = *reinterpret_cast<const float4*>(ls + ch * 32 + e);
+      const float2 c2 = make_float2(cl2, cl2);
+      const float2 a0 = ffma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2,
+                              make_float2(-l4.x, -l4.y));
+      const float2 a1 = ffma2(make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), c2,
+                              make_float2(-l4.z, -l4.w));
+      const float xs[4] = {ex2_approx(a0.x), ex2_approx(a0.y), ex2_approx(a1.x), ex2_approx(a1.y)};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int c = ch * 32 + e + u;
+        pr[c] = (!MASK || c >= cmin) ? xs[u] : 0.0f;
+      }
+      pk[e / 2] = pack2<BF16>(pr[ch * 32 + e], pr[ch * 32 + e + 1]);
+      pk[e / 2 + 1] = pack2<BF16>(pr[ch * 32 + e + 2], pr[ch * 32 + e + 3]);
+    }
+    tmem_st_32x32b_x16(t_s + ch * 16, pk);
   }
 }
 
@@ -289,25 +295,18 @@ __device__ __forceinline__ void q_p_half(const uint32_t (&sr)[64], float l2, int
 }
 
 // ---------------------------------------------------------------------------
-// dk, dv: one CTA per (b, g, 128-key tile n); grid (B * Hkv, n_kt).  P^T goes
-// through shared memory, so the next tile's S^T may overwrite S^T in TMEM as
-// soon as the key rows have read it; dv is an smem x smem product.
+// dk, dv: one CTA per (b, g, 128-key tile n); grid (B * Hkv, n_kt)
 // ---------------------------------------------------------------------------
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kv_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  if ((smem_u32(smem_raw) & 1023u) != 0) {   // the layout has no slack to realign
-    if (threadIdx.x == 0) atomicCAS(p.err, 0, ATTN_DEVERR_SMEM_ALIGN);
-    return;
-  }
-  uint8_t* smem = smem_raw;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sK = sbase, sV = sbase + C::kTile;
   auto sQ = [&](int s) { return sbase + C::kKvOffStage + s * C::kKvStageBytes; };
   auto sDO = [&](int s) { return sbase + C::kKvOffStage + s * C::kKvStageBytes + C::kTile; };
-  const uint32_t sPT = sbase + C::kKvOffPT;
   const float* vec = reinterpret_cast<const float*>(smem + C::kKvOffVec);   // [stage][lse2 128 | D 128]
   const uint32_t bar0 = sbase + C::kKvOffBar;
   const uint32_t b_kv_full = bar0;
@@ -315,14 +314,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kv_kernel(const __gri
   auto b_st_empty = [&](int s) { return bar0 + 8 + 8 * (C::kNS + s); };
   const uint32_t b_s_full = bar0 + 8 + 16 * C::kNS;   // S^T(t) computed
   const uint32_t b_dp_full = b_s_full + 8;            // dP^T(t) computed
-  const uint32_t b_s_free = b_s_full + 16;            // the key rows have read S^T(t)
-  const uint32_t b_p_full = b_s_full + 24;            // P^T(t) written to shared memory
-  const uint32_t b_ds_full = b_s_full + 32;           // dS^T(t) stored in TMEM
-  const uint32_t b_pt_free = b_s_full + 40;           // dv(t) has read P^T(t)
-  const uint32_t b_acc = b_s_full + 48;
-  const uint32_t b_drain = b_s_full + 56;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kKvOffBar + C::kKvNBars * 8);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kKvOffBar + C::kKvNBars * 8 + 4);
+  const uint32_t b_p_full = b_s_full + 16;            // P^T(t) stored by the key rows
+  const uint32_t b_ds_full = b_s_full + 24;           // dS^T(t) stored by the key rows
+  const uint32_t b_acc = b_s_full + 32;
+  const uint32_t b_drain = b_s_full + 40;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kKvOffBar + C::kNBars * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kKvOffBar + C::kNBars * 8 + 4);
   WaitCtl wc{p.err, abort_flag, p.timeout_ns};
 
   const int bg = blockIdx.x, n = blockIdx.y;
@@ -345,10 +342,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kv_kernel(const __gri
     }
     mbar_init(b_s_full, 1);
     mbar_init(b_dp_full, 1);
-    mbar_init(b_s_free, kBwdRowWarps);
     mbar_init(b_p_full, kBwdRowWarps);
     mbar_init(b_ds_full, kBwdRowWarps);
-    mbar_init(b_pt_free, 1);
     mbar_init(b_acc, 1);
     mbar_init(b_drain, 1);
     fence_mbar_init();
@@ -404,7 +399,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kv_kernel(const __gri
       constexpr uint32_t kIdescO = idesc_f16_f32acc(128, D, BF16, true);
       const uint64_t dk_k = sdesc_sw128(sK, 16, 1024);     // K as A, K-major
       const uint64_t dv_k = sdesc_sw128(sV, 16, 1024);     // V as A, K-major
-      const uint64_t dpt_k = sdesc_sw128(sPT, 16, 1024);   // P^T as A, K-major (queries)
       auto issue_s = [&](int st) {   // S^T = K Q^T
         const uint64_t dq_k = sdesc_sw128(sQ(st), 16, 1024);
 #pragma unroll
@@ -423,9 +417,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kv_kernel(const __gri
         }
         umma_commit(b_dp_full);
       };
-      // Order per tile t: S^T(t+1) (once the rows have read S^T(t)), dv(t)
-      // (P^T(t) from shared memory), dk(t) (dS^T(t) from TMEM), dP^T(t+1)
-      // (it overwrites dS^T(t), so after dk(t) has been issued).
+      // Order per tile t: dv(t), S^T(t+1), dk(t), dP^T(t+1).  S^T(t+1)
+      // overwrites P^T(t) after dv(t) has been issued, dP^T(t+1) overwrites
+      // dS^T(t) after dk(t); the key rows form P^T(t+1) while dk(t) and
+      // dP^T(t+1) run, and dS^T(t) while dv(t) and S^T(t+1) run.
       BwdTracer tr;
       tr.init(p, 0, true);
       bool ok = n_tiles > 0 && mbar_wait(b_kv_full, 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteQFull)) &&
@@ -438,27 +433,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kv_kernel(const __gri
         const int st = t % C::kNS, st1 = (t + 1) % C::kNS;
         const bool next = t + 1 < n_tiles;
         tr.rec(1, t);
-        if (next) {
-          if (!mbar_wait(b_s_free, t & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteSFull))) break;
-          if (!mbar_wait(b_st_full(st1), ((t + 1) / C::kNS) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull))) break;
-          tr.rec(2, t);
-          issue_s(st1);
-        }
-        tr.rec(3, t);
         if (!mbar_wait(b_p_full, t & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSitePFull))) break;
-        tr.rec(4, t);
+        tr.rec(2, t);
+        tc_fence_after();
         const uint64_t ddo_mn = sdesc_sw128(sDO(st), 16384, 1024);   // dO as B, MN-major
+        const uint64_t dq_mn = sdesc_sw128(sQ(st), 16384, 1024);     // Q as B, MN-major
 #pragma unroll
-        for (int kk = 0; kk < 128 / 16; ++kk) {   // dv += P^T dO
-          const uint32_t o = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-          umma_ss(tmem + 256, dpt_k + o, ddo_mn + ((kk * 2048) >> 4), kIdescO, (t > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 128 / 16; ++kk)   // dv += P^T dO
+          umma_ts(tmem + 256, tmem + packed_slice_col(kk), ddo_mn + ((kk * 2048) >> 4), kIdescO,
+                  (t > 0 || kk > 0) ? 1u : 0u);
+        tr.rec(3, t);
+        if (next) {
+          if (!mbar_wait(b_st_full(st1), ((t + 1) / C::kNS) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull))) break;
+          tr.rec(4, t);
+          issue_s(st1);
+          tr.rec(5, t);
         }
-        umma_commit(b_pt_free);
-        tr.rec(5, t);
         if (!mbar_wait(b_ds_full, t & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteDsFull))) break;
         tr.rec(6, t);
         tc_fence_after();
-        const uint64_t dq_mn = sdesc_sw128(sQ(st), 16384, 1024);     // Q as B, MN-major
 #pragma unroll
         for (int kk = 0; kk < 128 / 16; ++kk)   // dk += dS^T Q
           umma_ts(tmem + 256 + D, tmem + 128 + packed_slice_col(kk), dq_mn + ((kk * 2048) >> 4), kIdescO,
@@ -480,61 +473,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kv_kernel(const __gri
     const uint32_t t_s = tmem + lane_off + half * 64, t_dp = tmem + lane_off + 128 + half * 64;
     const int j = n * kBN + row;
     const float cl2 = p.scale_log2;
-    // this thread's 128-byte row of P^T: chunk `half` (queries 64 half ..),
-    // row j; 16-byte unit u lives at unit u ^ (row % 8) (128-byte swizzle)
-    uint8_t* pt_row = smem + C::kKvOffPT + half * 16384 + row * 128;
     BwdTracer tr;
     tr.init(p, half ? 2 : 1, lane == 0 && quarter == 0);
     bool ok = true;
     for (int t = 0; t < n_tiles; ++t) {
-      const int st = t % C::kNS, m = m_first + t % nm;
       tr.rec(20, t);
       if (!mbar_wait_warp(b_s_full, t & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteSFull))) { ok = false; break; }
       tr.rec(21, t);
       tc_fence_after();
+      const int st = t % C::kNS, m = m_first + t % nm;
       // lse2 and D of this stage came by bulk copy: observe its completion
-      // here (the stage is not refilled before dk(t), which waits for this warp)
+      // here (the stage cannot be refilled before this warp arrives on ds_full)
       if (!mbar_wait_warp(b_st_full(st), (t / C::kNS) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull))) {
         ok = false;
         break;
       }
-      uint32_t sr[64];
-      {
-        uint32_t* s0 = sr;
-        tmem_ld_32x32b_x32(t_s, *reinterpret_cast<uint32_t(*)[32]>(s0));
-        tmem_ld_32x32b_x32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(s0 + 32));
-        tmem_wait_ld(sr);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(b_s_free);
+      const float* ls = vec + st * 256 + half * 64;
+      const float* dd = vec + st * 256 + 128 + half * 64;
       // Only tiles crossing the causal diagonal are masked.  Padded query
       // columns (past Lq) have lse2 = +inf, so P = 0 there; padded key rows
       // (past Lk) only reach their own rows of dv and dk, which are not stored.
-      const float* ls = vec + st * 256 + half * 64;
       float pr[64];
       if (CAUSAL && n * kBN + kBN - 1 - m * kBM > off)
-        kv_p_regs<true>(sr, ls, j - off - m * kBM - half * 64, cl2, pr);
+        kv_p_half<true, BF16>(t_s, ls, j - off - m * kBM - half * 64, cl2, pr);
       else
-        kv_p_regs<false>(sr, ls, 0, cl2, pr);
-      // P^T into shared memory once dv(t-1) has read the previous one
-      if (t > 0 && !mbar_wait_warp(b_pt_free, (t - 1) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteVEmpty))) {
-        ok = false;
-        break;
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        *reinterpret_cast<uint4*>(pt_row + ((u ^ (row & 7)) << 4)) =
-            make_uint4(pack2<BF16>(pr[8 * u], pr[8 * u + 1]), pack2<BF16>(pr[8 * u + 2], pr[8 * u + 3]),
-                       pack2<BF16>(pr[8 * u + 4], pr[8 * u + 5]), pack2<BF16>(pr[8 * u + 6], pr[8 * u + 7]));
-      fence_proxy_async_smem();
+        kv_p_half<false, BF16>(t_s, ls, 0, cl2, pr);
+      tmem_wait_st();
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_p_full);
       tr.rec(22, t);
       if (!mbar_wait_warp(b_dp_full, t & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteODone))) { ok = false; break; }
       tr.rec(23, t);
       tc_fence_after();
-      ds_half<BF16>(t_dp, vec + st * 256 + 128 + half * 64, 0.0f, pr);
+      ds_half<BF16>(t_dp, dd, 0.0f, pr);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();

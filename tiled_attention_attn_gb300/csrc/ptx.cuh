@@ -116,12 +116,6 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// Makes this thread's generic-proxy shared-memory writes visible to the
-// async proxy (tensor-core operand reads, TMA).
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // Contiguous bulk copy global -> shared (no tensor map); both addresses
 // 16-byte aligned and `bytes` a multiple of 16.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
