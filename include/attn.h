@@ -222,6 +222,20 @@ int attn_rotary(const void *x, void *y, int B, int L, int H, int d, int rot_dim,
                 cudaStream_t stream);
 
 /*
+ * attn_rotary_packed -- the same rotation on the packed layouts the training
+ * page's rotary module takes (§4.2: a packed qkv tensor (B, L, 3, H, d), whose
+ * Q and K parts it rotates in place, and Q beside a packed kv tensor
+ * (B, L, 2, H, d), whose K part it rotates).  Every token row holds h_total
+ * heads of d features (3H for qkv, 2H for kv); the first h_rot of them are
+ * rotated (2H for qkv, H for kv).  In place (y == x) the other heads are left
+ * alone; out of place they are copied to y.  Other arguments, layouts and
+ * return codes as attn_rotary; 0 < h_rot <= h_total.
+ */
+int attn_rotary_packed(const void *x, void *y, int B, int L, int h_total, int h_rot, int d, int rot_dim,
+                       float base, int interleaved, const int *cu_seqlens_or_null, int total,
+                       const int *offsets_or_null, int fp16, cudaStream_t stream);
+
+/*
  * Padded batches around the varlen forward (the flash-attention
  * training-integration page, §2.5: drop the padded positions, run the
  * variable-length call, put the outputs back).  Each call enqueues device

@@ -91,3 +91,12 @@ def test_backward_empty_side_accepts_null_pointers(attn_lib):
 @pytest.mark.parametrize("d", [32, 96, 256])
 def test_backward_unsupported_head_dim(attn_lib, d):
     assert _call_bwd(attn_lib, d=d) == attn.ATTN_EUNSUPPORTED
+
+
+@pytest.mark.parametrize("bad", [dict(h_rot=0), dict(h_rot=4, h_total=3), dict(h_total=0), dict(rot=7),
+                                 dict(x=None), dict(fp16=2)])
+def test_rotary_packed_bad_arguments(attn_lib, bad):
+    a = dict(x=16, y=16, B=1, L=4, h_total=3, h_rot=2, d=64, rot=64, fp16=0)
+    a.update(bad)
+    assert attn_lib.attn_rotary_packed(a["x"], a["y"], a["B"], a["L"], a["h_total"], a["h_rot"], a["d"], a["rot"],
+                                       ctypes.c_float(10000.0), 0, None, 0, None, a["fp16"], None) == attn.ATTN_EINVAL

@@ -123,3 +123,49 @@ def test_rotary_rejects_partial_overlap():
     y = buf[64:].view(2, 10, 2, 64)
     with pytest.raises(attn.AttnError):
         attn.rotary(x, out=y)
+
+
+PACKED = [
+    # (B, L, parts, H, d), rot_dim, interleaved, dtype, in_place
+    ((2, 130, 3, 4, 128), 128, False, torch.bfloat16, True),    # qkv in place, as the module does
+    ((1, 77, 3, 2, 64), 64, True, torch.float16, False),        # qkv out of place: v copied
+    ((2, 50, 2, 3, 128), 64, False, torch.bfloat16, False),     # kv: only k rotated
+    ((1, 40, 2, 2, 64), 30, False, torch.bfloat16, True),       # scalar path (rot_dim % 16 != 0)
+]
+
+
+@pytest.mark.parametrize("case", PACKED, ids=[f"packed{i}" for i in range(len(PACKED))])
+def test_rotary_packed_qkv_and_kv(case):
+    shape, rot, inter, dtype, in_place = case
+    B, L, parts, H, d = shape
+    g = torch.Generator().manual_seed(sum(shape) + rot)
+    x = torch.randn(*shape, generator=g).to(dtype)
+    offs = torch.randint(0, 3000, (B,), generator=g, dtype=torch.int32)
+    dev = torch.device("cuda", 0)
+    xd = x.to(dev)
+    y = attn.rotary_packed(xd, rot, 10000.0, inter, offsets=offs.to(dev), out=xd if in_place else None)
+    torch.cuda.synchronize()
+    pos = (np.arange(L)[None, :] + offs.numpy()[:, None]).reshape(-1)
+    y = y.cpu()
+    for part in range(parts):
+        xp = x[:, :, part].reshape(B * L, H, d)
+        yp = y[:, :, part].reshape(B, L, H, d)
+        if part == parts - 1:   # v: untouched, bit for bit
+            assert torch.equal(yp, x[:, :, part])
+            continue
+        ref = oracle.rotary(xp, pos, rot, 10000.0, inter).reshape(B, L, H, d)
+        check_close(yp, ref, dtype, angle_term(xp, pos, rot, inter).reshape(B, L, H, d))
+
+
+def test_rotary_packed_varlen_qkv():
+    lengths = [3, 200, 64]
+    H, d = 2, 128
+    g = torch.Generator().manual_seed(29)
+    x = torch.randn(sum(lengths), 3, H, d, generator=g).to(torch.bfloat16)
+    cu = torch.tensor([0] + np.cumsum(lengths).tolist(), dtype=torch.int32)
+    dev = torch.device("cuda", 0)
+    y = attn.rotary_packed(x.to(dev), cu_seqlens=cu.to(dev)).cpu()
+    pos = np.concatenate([np.arange(n) for n in lengths])
+    for part in range(2):
+        check_close(y[:, part], oracle.rotary(x[:, part], pos, d), torch.bfloat16, angle_term(x[:, part], pos, d, False))
+    assert torch.equal(y[:, 2], x[:, 2])

@@ -100,6 +100,8 @@ def lib(path: Optional[str] = None):
         L.attn_scatter_rows.restype = i
         L.attn_scatter_lse.argtypes = [vp, vp, i, vp, i, i, i, vp, vp]
         L.attn_scatter_lse.restype = i
+        L.attn_rotary_packed.argtypes = [vp, vp, i, i, i, i, i, i, f, i, vp, i, vp, i, vp]
+        L.attn_rotary_packed.restype = i
         L.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
         L.attn_bwd.restype = i
         if path is None:
@@ -375,6 +377,47 @@ def rotary(x: torch.Tensor, rot_dim: Optional[int] = None, base: float = 10000.0
                                int(x.dtype == torch.float16), _stream_handle(x.device, stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_rotary")
+    return out
+
+
+def rotary_packed(x: torch.Tensor, rot_dim: Optional[int] = None, base: float = 10000.0, interleaved: bool = False,
+                  cu_seqlens: Optional[torch.Tensor] = None, offsets: Optional[torch.Tensor] = None,
+                  out: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Rotary embedding of a packed qkv (B, L, 3, H, d) (Q and K rotated) or
+    kv (B, L, 2, H, d) (K rotated) tensor, V untouched; with ``cu_seqlens``
+    the leading (B, L) is packed as (total,).  ``out`` may be x (in place, as
+    the training page's module works); default a new tensor with V copied."""
+    if x.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError("x must be bfloat16 or float16")
+    _check_cuda(x)
+    lead = 1 if cu_seqlens is not None else 2
+    if x.dim() != lead + 3 or x.shape[lead] not in (2, 3):
+        raise ValueError("x is (B, L, 3, H, d) / (B, L, 2, H, d), or (total, 3 | 2, H, d) with cu_seqlens")
+    parts, H, d = x.shape[lead], x.shape[lead + 1], x.shape[lead + 2]
+    rot = d if rot_dim is None else int(rot_dim)
+    if cu_seqlens is not None:
+        _check_cuda(cu_seqlens)
+        B, L, total = cu_seqlens.numel() - 1, 0, x.shape[0]
+    else:
+        B, L, total = x.shape[0], x.shape[1], 0
+    if offsets is not None:
+        _check_cuda(offsets)
+        if offsets.dtype != torch.int32 or offsets.numel() != B:
+            raise ValueError("offsets must be int32 with one entry per sequence")
+    if out is None:
+        out = torch.empty_like(x)
+    if out.shape != x.shape or out.dtype != x.dtype:
+        raise ValueError("out must be shaped like x")
+    _check_cuda(out)
+    h_rot = (parts - 1) * H   # qkv: Q and K; kv: K
+    with torch.cuda.device(x.device):
+        rc = lib().attn_rotary_packed(x.data_ptr(), out.data_ptr(), int(B), int(L), int(parts * H), int(h_rot),
+                                      int(d), rot, ctypes.c_float(float(base)), int(bool(interleaved)),
+                                      cu_seqlens.data_ptr() if cu_seqlens is not None else None, int(total),
+                                      offsets.data_ptr() if offsets is not None else None,
+                                      int(x.dtype == torch.float16), _stream_handle(x.device, stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_rotary_packed")
     return out
 
 

@@ -59,8 +59,9 @@ __device__ __forceinline__ int position_of(int r, int L, const int* cu, int B, c
 // pairs (it loads both members before it stores either), so y == x is safe.
 template <bool BF16, bool GPTJ>
 __global__ void __launch_bounds__(kThreads) rotary_kernel(const uint16_t* x, uint16_t* y,
-                                                          long long rows, int L, int H, int d, int rot,
-                                                          float log2_base, const int* __restrict__ cu, int B,
+                                                          long long rows, long long token_stride, int L, int H,
+                                                          int d, int rot, float log2_base,
+                                                          const int* __restrict__ cu, int B,
                                                           const int* __restrict__ offset, bool in_place) {
   const int half = rot / 2;
   const int pair_groups = (half + 3) / 4;
@@ -72,8 +73,9 @@ __global__ void __launch_bounds__(kThreads) rotary_kernel(const uint16_t* x, uin
     const long long th = it / per;
     const int g = static_cast<int>(it - th * per);
     const long long r = th / H;
-    const uint16_t* xs = x + th * d;
-    uint16_t* ys = y + th * d;
+    const long long at = r * token_stride + (th - r * H) * d;
+    const uint16_t* xs = x + at;
+    uint16_t* ys = y + at;
     if (g >= pair_groups) {   // unrotated features
       const int c0 = rot + (g - pair_groups) * 8;
       for (int c = c0; c < min(c0 + 8, d); ++c) ys[c] = xs[c];
@@ -112,9 +114,9 @@ __global__ void __launch_bounds__(kThreads) rotary_kernel(const uint16_t* x, uin
 // stores; the pair frequencies come from a table in shared memory.  Tail
 // features are copied 8 at a time.
 template <bool BF16, bool GPTJ>
-__global__ void __launch_bounds__(kThreads) rotary_vec_kernel(const uint16_t* x, uint16_t* y, long long rows, int L,
-                                                              int H, int d, int rot, float log2_base,
-                                                              const int* __restrict__ cu, int B,
+__global__ void __launch_bounds__(kThreads) rotary_vec_kernel(const uint16_t* x, uint16_t* y, long long rows,
+                                                              long long token_stride, int L, int H, int d, int rot,
+                                                              float log2_base, const int* __restrict__ cu, int B,
                                                               const int* __restrict__ offset, bool in_place) {
   __shared__ float theta[256];
   const int half = rot / 2;
@@ -126,7 +128,6 @@ __global__ void __launch_bounds__(kThreads) rotary_vec_kernel(const uint16_t* x,
   const int per = pair_groups + tail_groups;
   const int chunks = (H + kHeadsPerThread - 1) / kHeadsPerThread;
   const long long items = rows * chunks * per;
-  const long long token_stride = static_cast<long long>(H) * d;
   for (long long it = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; it < items;
        it += static_cast<long long>(gridDim.x) * kThreads) {
     const long long rc = it / per;   // (token, head chunk)
@@ -179,26 +180,32 @@ __global__ void __launch_bounds__(kThreads) rotary_vec_kernel(const uint16_t* x,
 }  // namespace
 }  // namespace attn
 
-extern "C" int attn_rotary(const void* x, void* y, int B, int L, int H, int d, int rot_dim, float base,
-                           int interleaved, const int* cu_seqlens_or_null, int total, const int* offsets_or_null,
-                           int fp16, cudaStream_t stream) {
-  using namespace attn;
-  if (!x || !y || B <= 0 || H <= 0 || d <= 0 || (fp16 != 0 && fp16 != 1)) return ATTN_EINVAL;
+namespace attn {
+namespace {
+
+// Rotates the first h_rot heads of every token of a tensor whose tokens hold
+// h_total heads of d features; out of place, the other heads are copied.
+int rotary(const void* x, void* y, int B, int L, int h_total, int h_rot, int d, int rot_dim, float base,
+           int interleaved, const int* cu, int total, const int* offsets, int fp16, cudaStream_t stream) {
+  if (!x || !y || B <= 0 || h_total <= 0 || h_rot <= 0 || h_rot > h_total || d <= 0 || (fp16 != 0 && fp16 != 1))
+    return ATTN_EINVAL;
   if (rot_dim <= 0 || rot_dim > d || (rot_dim & 1) || !(base > 1.0f) || !std::isfinite(base)) return ATTN_EINVAL;
   if (interleaved != 0 && interleaved != 1) return ATTN_EINVAL;
-  const bool varlen = cu_seqlens_or_null != nullptr;
+  const bool varlen = cu != nullptr;
   if (varlen ? total < 0 : L < 0) return ATTN_EINVAL;
   const long long rows = varlen ? static_cast<long long>(total) : static_cast<long long>(B) * L;
-  if (rows * H * d > (1LL << 40) || rows > (1LL << 31) - 1) return ATTN_EINVAL;
+  const long long token_stride = static_cast<long long>(h_total) * d;
+  if (rows * token_stride > (1LL << 40) || rows > (1LL << 31) - 1) return ATTN_EINVAL;
   // x and y either the same tensor or disjoint: a partial overlap would race
   const uintptr_t xa = reinterpret_cast<uintptr_t>(x), ya = reinterpret_cast<uintptr_t>(y);
-  const uintptr_t bytes = static_cast<uintptr_t>(rows * H * d * 2);
+  const uintptr_t bytes = static_cast<uintptr_t>(rows * token_stride * 2);
   if (xa != ya && xa < ya + bytes && ya < xa + bytes) return ATTN_EINVAL;
   if (rows == 0) return ATTN_OK;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return ATTN_ELAUNCH;
   const bool in_place = xa == ya;
+  const int H = h_rot;
   const bool vec = (rot_dim % 16 == 0) && (d % 8 == 0) && rot_dim <= 512 && (xa % 16 == 0) && (ya % 16 == 0);
   const long long items = vec ? rows * ((H + kHeadsPerThread - 1) / kHeadsPerThread) *
                                     (rot_dim / 16 + (in_place ? 0 : (d - rot_dim) / 8))
@@ -211,20 +218,48 @@ extern "C" int attn_rotary(const void* x, void* y, int B, int L, int H, int d, i
   const int Lr = varlen ? 1 : L;
   if (vec) {
     if (fp16 == 0) {
-      if (interleaved) rotary_vec_kernel<true, true><<<grid, kThreads, 0, stream>>>(xs, ys, rows, Lr, H, d, rot_dim, lb, cu_seqlens_or_null, B, offsets_or_null, in_place);
-      else rotary_vec_kernel<true, false><<<grid, kThreads, 0, stream>>>(xs, ys, rows, Lr, H, d, rot_dim, lb, cu_seqlens_or_null, B, offsets_or_null, in_place);
+      if (interleaved) rotary_vec_kernel<true, true><<<grid, kThreads, 0, stream>>>(xs, ys, rows, token_stride, Lr, H, d, rot_dim, lb, cu, B, offsets, in_place);
+      else rotary_vec_kernel<true, false><<<grid, kThreads, 0, stream>>>(xs, ys, rows, token_stride, Lr, H, d, rot_dim, lb, cu, B, offsets, in_place);
     } else {
-      if (interleaved) rotary_vec_kernel<false, true><<<grid, kThreads, 0, stream>>>(xs, ys, rows, Lr, H, d, rot_dim, lb, cu_seqlens_or_null, B, offsets_or_null, in_place);
-      else rotary_vec_kernel<false, false><<<grid, kThreads, 0, stream>>>(xs, ys, rows, Lr, H, d, rot_dim, lb, cu_seqlens_or_null, B, offsets_or_null, in_place);
+      if (interleaved) rotary_vec_kernel<false, true><<<grid, kThreads, 0, stream>>>(xs, ys, rows, token_stride, Lr, H, d, rot_dim, lb, cu, B, offsets, in_place);
+      else rotary_vec_kernel<false, false><<<grid, kThreads, 0, stream>>>(xs, ys, rows, token_stride, Lr, H, d, rot_dim, lb, cu, B, offsets, in_place);
     }
   } else if (fp16 == 0) {
-    if (interleaved) rotary_kernel<true, true><<<grid, kThreads, 0, stream>>>(xs, ys, rows, Lr, H, d, rot_dim, lb, cu_seqlens_or_null, B, offsets_or_null, in_place);
-    else rotary_kernel<true, false><<<grid, kThreads, 0, stream>>>(xs, ys, rows, Lr, H, d, rot_dim, lb, cu_seqlens_or_null, B, offsets_or_null, in_place);
+    if (interleaved) rotary_kernel<true, true><<<grid, kThreads, 0, stream>>>(xs, ys, rows, token_stride, Lr, H, d, rot_dim, lb, cu, B, offsets, in_place);
+    else rotary_kernel<true, false><<<grid, kThreads, 0, stream>>>(xs, ys, rows, token_stride, Lr, H, d, rot_dim, lb, cu, B, offsets, in_place);
   } else {
-    if (interleaved) rotary_kernel<false, true><<<grid, kThreads, 0, stream>>>(xs, ys, rows, Lr, H, d, rot_dim, lb, cu_seqlens_or_null, B, offsets_or_null, in_place);
-    else rotary_kernel<false, false><<<grid, kThreads, 0, stream>>>(xs, ys, rows, Lr, H, d, rot_dim, lb, cu_seqlens_or_null, B, offsets_or_null, in_place);
+    if (interleaved) rotary_kernel<false, true><<<grid, kThreads, 0, stream>>>(xs, ys, rows, token_stride, Lr, H, d, rot_dim, lb, cu, B, offsets, in_place);
+    else rotary_kernel<false, false><<<grid, kThreads, 0, stream>>>(xs, ys, rows, token_stride, Lr, H, d, rot_dim, lb, cu, B, offsets, in_place);
   }
   if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
   count_launch();
+  if (!in_place && h_rot < h_total) {
+    // the heads that are not rotated (v of a packed qkv, v of a packed kv)
+    const size_t pitch = static_cast<size_t>(token_stride) * 2;
+    const size_t skip = static_cast<size_t>(h_rot) * d * 2;
+    if (cudaMemcpy2DAsync(static_cast<uint8_t*>(y) + skip, pitch, static_cast<const uint8_t*>(x) + skip, pitch,
+                          pitch - skip, static_cast<size_t>(rows), cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+      return ATTN_ELAUNCH;
+  }
   return ATTN_OK;
 }
+
+}  // namespace
+}  // namespace attn
+
+extern "C" {
+
+int attn_rotary(const void* x, void* y, int B, int L, int H, int d, int rot_dim, float base, int interleaved,
+                const int* cu_seqlens_or_null, int total, const int* offsets_or_null, int fp16, cudaStream_t stream) {
+  return attn::rotary(x, y, B, L, H, H, d, rot_dim, base, interleaved, cu_seqlens_or_null, total, offsets_or_null,
+                      fp16, stream);
+}
+
+int attn_rotary_packed(const void* x, void* y, int B, int L, int h_total, int h_rot, int d, int rot_dim, float base,
+                       int interleaved, const int* cu_seqlens_or_null, int total, const int* offsets_or_null, int fp16,
+                       cudaStream_t stream) {
+  return attn::rotary(x, y, B, L, h_total, h_rot, d, rot_dim, base, interleaved, cu_seqlens_or_null, total,
+                      offsets_or_null, fp16, stream);
+}
+
+}  // extern "C"
