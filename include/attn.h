@@ -203,6 +203,25 @@ int attn_bwd(const void *q, const void *k, const void *v, const void *o, const f
              float scale, int fp16, cudaStream_t stream);
 
 /*
+ * attn_bwd_varlen -- attn_bwd for packed batches, the backward of
+ * attn_fwd_varlen (and of attn_fwd with cu_seqlens, passing the same array
+ * twice).  q, o, dout, dq are (total_q, Hq, d); k, v, dk, dv (total_k, Hkv, d);
+ * lse (Hq, total_q) as the varlen forward returns it; sequence b has queries
+ * cu_seqlens_q[b] .. cu_seqlens_q[b+1] - 1 and keys cu_seqlens_k[b] ..
+ * cu_seqlens_k[b+1] - 1 (device int32 arrays of B+1 entries, 0 first,
+ * non-decreasing, last entry at most the total; checked on the device, a
+ * malformed array is ATTN_DEVERR_BAD_SEQLENS and nothing is computed).
+ * Causal aligns bottom-right per sequence as in attn_fwd_varlen.  Rows of dq,
+ * dk, dv outside every sequence are left unwritten.  The workspace is
+ * 8 * Hq * 128 * (B + total_q / 128 + 1) bytes plus 8 * (B + 1).  Other
+ * arguments and return codes as attn_bwd.
+ */
+int attn_bwd_varlen(const void *q, const void *k, const void *v, const void *o, const float *lse,
+                    const void *dout, void *dq, void *dk, void *dv, int B, int Hq, int Hkv, int total_q,
+                    int total_k, int d, int causal, float scale, const int *cu_seqlens_q,
+                    const int *cu_seqlens_k, int fp16, cudaStream_t stream);
+
+/*
  * attn_rotary -- rotary position embedding of a Q or K tensor (training
  * page §4: rotary dimension, base frequency, GPT-NeoX or GPT-J pairing, and a
  * position offset that starts new tokens at the cache length).  x and y are

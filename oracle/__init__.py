@@ -291,6 +291,31 @@ def varlen_cross_attention(q, k, v, lengths_q: Sequence[int], lengths_k: Sequenc
     return o, lse
 
 
+def varlen_attention_backward(q, k, v, dout, lengths_q: Sequence[int], lengths_k: Sequence[int],
+                              causal: bool = False, scale: Optional[float] = None):
+    """Gradients of a packed batch with per-sequence query and key lengths, one
+    dense backward per sequence (the same composition as
+    varlen_cross_attention).  q, dout (total_q, Hq, d); k, v (total_k, Hkv, d).
+    Returns dq (total_q, Hq, d), dk, dv (total_k, Hkv, d); rows of empty
+    pairings are zero."""
+    q, k, v, dout = f64(q), f64(k), f64(v), f64(dout)
+    dq = np.zeros(q.shape, np.float64)
+    dk = np.zeros(k.shape, np.float64)
+    dv = np.zeros(k.shape, np.float64)
+    oq = ok = 0
+    for nq, nk in zip(lengths_q, lengths_k):
+        nq, nk = int(nq), int(nk)
+        if nq > 0 and nk > 0:
+            a, b_, c = attention_backward(q[None, oq:oq + nq], k[None, ok:ok + nk], v[None, ok:ok + nk],
+                                          dout[None, oq:oq + nq], causal=causal, scale=scale)
+            dq[oq:oq + nq] = a[0]
+            dk[ok:ok + nk] = b_[0]
+            dv[ok:ok + nk] = c[0]
+        oq += nq
+        ok += nk
+    return dq, dk, dv
+
+
 # --------------------------------------------------------------------------
 # padded <-> packed: the unpad / pad steps around the variable-length call
 # (lei6393.com training-integration page, §2.5).  Plain definitions.

@@ -128,3 +128,59 @@ def test_backward_full_size_group_sample():
     check("dq", dq[b:b + 1, :, hs], rq)
     check("dk", dk[b:b + 1, :, g:g + 1], rk)
     check("dv", dv[b:b + 1, :, g:g + 1], rv)
+
+
+def cu_of(lengths):
+    return torch.tensor([0] + np.cumsum(lengths).tolist(), dtype=torch.int32)
+
+
+VARLEN = [
+    # query lengths, key lengths (None: self-attention, one offsets array), Hq, Hkv, d, causal, dtype
+    ([37, 300, 1, 129], None, 4, 2, 64, True, torch.bfloat16),
+    ([64, 200, 5, 256], [764, 233, 1005, 256], 4, 4, 128, True, torch.bfloat16),   # queries after a cache
+    ([300, 20, 130], [100, 0, 130], 2, 1, 64, True, torch.float16),                 # keys < queries, no keys
+    ([0, 17, 0, 400], [50, 3, 0, 300], 2, 2, 128, False, torch.bfloat16),          # empty sequences
+]
+
+
+@pytest.mark.parametrize("case", VARLEN, ids=[f"varlen{i}" for i in range(len(VARLEN))])
+def test_backward_varlen_matches_oracle(case):
+    lq, lk, Hq, Hkv, d, causal, dtype = case
+    self_attn = lk is None
+    lk = lq if self_attn else lk
+    g = torch.Generator().manual_seed(sum(lq) + sum(lk) + d)
+    q = torch.randn(sum(lq), Hq, d, generator=g).to(dtype)
+    k = torch.randn(max(sum(lk), 1), Hkv, d, generator=g).to(dtype)
+    v = torch.randn(max(sum(lk), 1), Hkv, d, generator=g).to(dtype)
+    do = torch.randn(sum(lq), Hq, d, generator=g).to(dtype)
+    dev = torch.device("cuda", 0)
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    cq = cu_of(lq).to(dev)
+    ck = None if self_attn else cu_of(lk).to(dev)
+    scale = d ** -0.5
+    o, lse = attn.attn_fwd(qd, kd, vd, causal=causal, scale=scale, cu_seqlens=cq, cu_seqlens_k=ck)
+    dq, dk, dv = attn.attn_bwd(qd, kd, vd, o, lse, dod, causal=causal, scale=scale, cu_seqlens=cq, cu_seqlens_k=ck)
+    assert attn.get_error() == attn.ATTN_OK
+    rq, rk, rv = oracle.varlen_attention_backward(q, k, v, do, lq, lk, causal=causal, scale=scale)
+    nk = sum(lk)
+    check("dq", dq.float().cpu().double().numpy(), rq)
+    check("dk", dk.float().cpu().double().numpy()[:nk], rk[:nk])
+    check("dv", dv.float().cpu().double().numpy()[:nk], rv[:nk])
+
+
+def test_backward_varlen_equals_dense_for_equal_lengths():
+    """Packed sequences of one length are the dense batch: the results agree
+    bit for bit (the same kernels, the same tiles)."""
+    B, L, Hq, Hkv, d = 3, 300, 4, 2, 128
+    q, k, v, do = make(B, Hq, Hkv, L, L, d, torch.bfloat16, seed=9)
+    dev = torch.device("cuda", 0)
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o, lse = attn.attn_fwd(qd, kd, vd, causal=True)
+    a = attn.attn_bwd(qd, kd, vd, o, lse, dod, causal=True)
+    flat = lambda t: t.reshape(B * L, t.shape[2], d)
+    lse_p = lse.permute(1, 0, 2).reshape(Hq, B * L).contiguous()
+    cu = cu_of([L] * B).to(dev)
+    b = attn.attn_bwd(flat(qd), flat(kd), flat(vd), flat(o), lse_p, flat(dod), causal=True, cu_seqlens=cu)
+    assert attn.get_error() == attn.ATTN_OK
+    for x, y in zip(a, b):
+        assert torch.equal(flat(x), y)

@@ -100,3 +100,10 @@ def test_rotary_packed_bad_arguments(attn_lib, bad):
     a.update(bad)
     assert attn_lib.attn_rotary_packed(a["x"], a["y"], a["B"], a["L"], a["h_total"], a["h_rot"], a["d"], a["rot"],
                                        ctypes.c_float(10000.0), 0, None, 0, None, a["fp16"], None) == attn.ATTN_EINVAL
+
+
+def test_backward_varlen_needs_both_offsets(attn_lib):
+    args = [16] * 9 + [1, 2, 1, 8, 8, 64, 0, ctypes.c_float(0.125)]
+    assert attn_lib.attn_bwd_varlen(*args, None, 16, 0, None) == attn.ATTN_EINVAL
+    assert attn_lib.attn_bwd_varlen(*args, 16, None, 0, None) == attn.ATTN_EINVAL
+    assert attn_lib.attn_bwd_varlen(*args, 16, 16, 2, None) == attn.ATTN_EINVAL

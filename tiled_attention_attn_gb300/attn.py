@@ -104,6 +104,8 @@ def lib(path: Optional[str] = None):
         L.attn_rotary_packed.restype = i
         L.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, vp]
         L.attn_bwd.restype = i
+        L.attn_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp, vp, i, vp]
+        L.attn_bwd_varlen.restype = i
         if path is None:
             _lib = L
         return L
@@ -195,24 +197,42 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = F
 def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor, lse: torch.Tensor,
              dout: torch.Tensor, causal: bool = False, scale: Optional[float] = None,
              dq: Optional[torch.Tensor] = None, dk: Optional[torch.Tensor] = None, dv: Optional[torch.Tensor] = None,
-             stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
-    """Gradients (dq, dk, dv) of sum(dout * O) for the dense forward.
+             stream: Optional[torch.cuda.Stream] = None, cu_seqlens: Optional[torch.Tensor] = None,
+             cu_seqlens_k: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """Gradients (dq, dk, dv) of sum(dout * O) for the forward.
 
-    q, out, dout (B, Lq, Hq, d); k, v (B, Lk, Hkv, d); lse (B, Hq, Lq) float32,
-    with out and lse as attn_fwd returned them for the same q, k, v, causal
-    and scale.  dq is shaped like q, dk and dv like k.
+    Dense: q, out, dout (B, Lq, Hq, d); k, v (B, Lk, Hkv, d); lse (B, Hq, Lq)
+    float32, with out and lse as attn_fwd returned them for the same q, k, v,
+    causal and scale.  Varlen (``cu_seqlens`` given, and ``cu_seqlens_k`` for
+    separate key offsets): q, out, dout (total_q, Hq, d), k, v (total_k, Hkv,
+    d), lse (Hq, total_q).  dq is shaped like q, dk and dv like k.
     """
     ts = (q, k, v, out, dout)
     if q.dtype not in (torch.bfloat16, torch.float16) or any(t.dtype != q.dtype for t in ts):
         raise TypeError("q, k, v, out and dout must share one 16-bit dtype")
     if any(not t.is_cuda or not t.is_contiguous() for t in ts + (lse,)):
         raise ValueError("tensors must be contiguous CUDA tensors")
-    if q.dim() != 4 or k.dim() != 4 or k.shape != v.shape or out.shape != q.shape or dout.shape != q.shape:
-        raise ValueError("q, out, dout are (B, Lq, Hq, d) and k, v are (B, Lk, Hkv, d)")
-    B, Lq, Hq, d = q.shape
-    _, Lk, Hkv, _ = k.shape
-    if tuple(lse.shape) != (B, Hq, Lq) or lse.dtype != torch.float32:
-        raise ValueError(f"lse must be a float32 tensor of shape {(B, Hq, Lq)}")
+    if cu_seqlens_k is not None and cu_seqlens is None:
+        raise ValueError("cu_seqlens_k needs cu_seqlens")
+    varlen = cu_seqlens is not None
+    nd = 3 if varlen else 4
+    if q.dim() != nd or k.dim() != nd or k.shape != v.shape or out.shape != q.shape or dout.shape != q.shape:
+        raise ValueError("q, out, dout are (B, Lq, Hq, d) and k, v are (B, Lk, Hkv, d); packed without B")
+    if varlen:
+        cu_k = cu_seqlens if cu_seqlens_k is None else cu_seqlens_k
+        for c in (cu_seqlens, cu_k):
+            if c.dtype != torch.int32 or not c.is_cuda or c.numel() != cu_seqlens.numel():
+                raise ValueError("cu_seqlens (and cu_seqlens_k) must be int32 CUDA tensors of B+1 entries")
+        B = cu_seqlens.numel() - 1
+        Lq, Hq, d = q.shape
+        Lk, Hkv, _ = k.shape
+        lse_shape = (Hq, Lq)
+    else:
+        B, Lq, Hq, d = q.shape
+        _, Lk, Hkv, _ = k.shape
+        lse_shape = (B, Hq, Lq)
+    if tuple(lse.shape) != lse_shape or lse.dtype != torch.float32:
+        raise ValueError(f"lse must be a float32 tensor of shape {lse_shape}")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     dq = torch.empty_like(q) if dq is None else dq
@@ -222,10 +242,17 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tenso
         if g.shape != ref.shape or g.dtype != ref.dtype or not g.is_contiguous() or not g.is_cuda:
             raise ValueError("dq, dk, dv must be contiguous CUDA tensors shaped like q, k, v")
     with torch.cuda.device(q.device):
-        rc = lib().attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                            dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), int(B), int(Hq), int(Hkv),
-                            int(Lq), int(Lk), int(d), int(bool(causal)), ctypes.c_float(float(scale)),
-                            int(q.dtype == torch.float16), _stream_handle(q.device, stream))
+        if varlen:
+            rc = lib().attn_bwd_varlen(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                       dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), int(B), int(Hq),
+                                       int(Hkv), int(Lq), int(Lk), int(d), int(bool(causal)),
+                                       ctypes.c_float(float(scale)), cu_seqlens.data_ptr(), cu_k.data_ptr(),
+                                       int(q.dtype == torch.float16), _stream_handle(q.device, stream))
+        else:
+            rc = lib().attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), int(B), int(Hq),
+                                int(Hkv), int(Lq), int(Lk), int(d), int(bool(causal)), ctypes.c_float(float(scale)),
+                                int(q.dtype == torch.float16), _stream_handle(q.device, stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_bwd")
     return dq, dk, dv

@@ -26,9 +26,14 @@ std::mutex g_bwd_mu;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Dense (cu_q null): q (B, Lq, Hq, d), k (B, Lk, Hkv, d).  Varlen: Lq and Lk
+// are the packed row counts, q (Lq, Hq, d), k (Lk, Hkv, d), offsets cu_q and
+// cu_k (B+1 each, on the device; never read here).
 int bwd(bool bf16, const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
         void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Lq, int Lk, int d, int causal, float scale,
-        cudaStream_t stream) {
+        const int* cu_q, const int* cu_k, cudaStream_t stream) {
+  const bool varlen = cu_q != nullptr;
+  if (varlen != (cu_k != nullptr)) return ATTN_EINVAL;
   // a tensor with no elements may be passed as a null pointer
   if (Lq != 0 && (!q || !o || !lse || !dout || !dq)) return ATTN_EINVAL;
   if (Lk != 0 && (!k || !v || !dk || !dv)) return ATTN_EINVAL;
@@ -39,17 +44,18 @@ int bwd(bool bf16, const void* q, const void* k, const void* v, const void* o, c
   if (causal != 0 && causal != 1) return ATTN_EINVAL;
   if (!std::isfinite(scale) || scale < 0.0f) return ATTN_EINVAL;
   if (d != 64 && d != 128) return ATTN_EUNSUPPORTED;
-  if (static_cast<long long>(B) * Lq * Hq > (1LL << 31) - 1 || static_cast<long long>(B) * Lk * Hkv > (1LL << 31) - 1)
-    return ATTN_EINVAL;
+  const long long rows_q = varlen ? Lq : static_cast<long long>(B) * Lq;
+  const long long rows_k = varlen ? Lk : static_cast<long long>(B) * Lk;
+  if (rows_q * Hq > (1LL << 31) - 1 || rows_k * Hkv > (1LL << 31) - 1) return ATTN_EINVAL;
   if (static_cast<long long>(Lq) + kBM > (1LL << 30) || static_cast<long long>(Lk) + kBN > (1LL << 30))
     return ATTN_EINVAL;
   const size_t row_bytes = static_cast<size_t>(d) * 2;
   if (Lq == 0 || Lk == 0) {
     // no (query, key) pair: every gradient is zero
-    if (Lq != 0 && cudaMemsetAsync(dq, 0, static_cast<size_t>(B) * Lq * Hq * row_bytes, stream) != cudaSuccess)
+    if (Lq != 0 && cudaMemsetAsync(dq, 0, static_cast<size_t>(rows_q) * Hq * row_bytes, stream) != cudaSuccess)
       return ATTN_ELAUNCH;
-    if (Lk != 0 && (cudaMemsetAsync(dk, 0, static_cast<size_t>(B) * Lk * Hkv * row_bytes, stream) != cudaSuccess ||
-                    cudaMemsetAsync(dv, 0, static_cast<size_t>(B) * Lk * Hkv * row_bytes, stream) != cudaSuccess))
+    if (Lk != 0 && (cudaMemsetAsync(dk, 0, static_cast<size_t>(rows_k) * Hkv * row_bytes, stream) != cudaSuccess ||
+                    cudaMemsetAsync(dv, 0, static_cast<size_t>(rows_k) * Hkv * row_bytes, stream) != cudaSuccess))
       return ATTN_ELAUNCH;
     return ATTN_OK;
   }
@@ -63,15 +69,20 @@ int bwd(bool bf16, const void* q, const void* k, const void* v, const void* o, c
 
   BwdParams p;
   std::memset(&p, 0, sizeof(p));
-  if ((rc = encode_map(q, bf16, d, Hq, Lq, B, p.tm_q))) return rc;
-  if ((rc = encode_map(dout, bf16, d, Hq, Lq, B, p.tm_do))) return rc;
-  if ((rc = encode_map(k, bf16, d, Hkv, Lk, B, p.tm_k))) return rc;
-  if ((rc = encode_map(v, bf16, d, Hkv, Lk, B, p.tm_v))) return rc;
+  const int Bm = varlen ? 1 : B;   // packed tensors are one (total, H, d) batch for TMA
+  if ((rc = encode_map(q, bf16, d, Hq, Lq, Bm, p.tm_q))) return rc;
+  if ((rc = encode_map(dout, bf16, d, Hq, Lq, Bm, p.tm_do))) return rc;
+  if ((rc = encode_map(k, bf16, d, Hkv, Lk, Bm, p.tm_k))) return rc;
+  if ((rc = encode_map(v, bf16, d, Hkv, Lk, Bm, p.tm_v))) return rc;
   p.n_qt = (Lq + kBM - 1) / kBM;
   p.n_kt = (Lk + kBN - 1) / kBN;
   p.Lq_pad = p.n_qt * kBM;
-  if (p.n_qt > 65535 || p.n_kt > 65535) return ATTN_EINVAL;   // grid.y
-  const size_t need = 2 * static_cast<size_t>(B) * Hq * p.Lq_pad;
+  if (!varlen && (p.n_qt > 65535 || p.n_kt > 65535)) return ATTN_EINVAL;   // grid.y
+  // varlen: at most B + total / 128 tiles (each sequence's last tile may be partial)
+  const long long qt_max = static_cast<long long>(B) + p.n_qt, kt_max = static_cast<long long>(B) + p.n_kt;
+  if (varlen && (qt_max * Hq > (1LL << 31) - 1 || kt_max * Hkv > (1LL << 31) - 1)) return ATTN_EINVAL;
+  const size_t vec_floats = varlen ? static_cast<size_t>(Hq) * qt_max * kBM : static_cast<size_t>(B) * Hq * p.Lq_pad;
+  const size_t need = 2 * vec_floats + (varlen ? 2 * static_cast<size_t>(B + 1) : 0);   // + tile tables (ints)
 
   std::lock_guard<std::mutex> lock(g_bwd_mu);
   BwdWorkspace& ws = g_bwd_ws[dev];
@@ -83,7 +94,11 @@ int bwd(bool bf16, const void* q, const void* k, const void* v, const void* o, c
     ws.floats = need;
   }
   p.lse2 = ws.buf;
-  p.dvec = ws.buf + need / 2;
+  p.dvec = ws.buf + vec_floats;
+  int* pref = varlen ? reinterpret_cast<int*>(ws.buf + 2 * vec_floats) : nullptr;
+  p.cu_q = cu_q;
+  p.cu_k = cu_k;
+  p.tile_pref = pref;
   p.q = q;
   p.dout = dout;
   p.dq = dq;
@@ -105,16 +120,18 @@ int bwd(bool bf16, const void* q, const void* k, const void* v, const void* o, c
   pr.o = o;
   pr.dout = dout;
   pr.lse = lse;
-  const long long threads = static_cast<long long>(B) * Hq * p.Lq_pad * 8;
+  pr.pref = pref;
+  const long long threads = static_cast<long long>(vec_floats) * 8;
   const long long blocks = (threads + 255) / 256;
   const long long cap = static_cast<long long>(info.sm_count > 0 ? info.sm_count : 1) * 8;
   pr.grid = static_cast<int>(blocks < cap ? blocks : cap);
+  pr.grid_kv = varlen ? static_cast<int>(kt_max * Hkv) : 0;
+  pr.grid_q = varlen ? static_cast<int>(qt_max * Hq) : 0;
 
-  BwdLauncher launch = (d == 64) ? bwd_launcher_d64(bf16, causal != 0) : bwd_launcher_d128(bf16, causal != 0);
+  BwdLauncher launch = (d == 64) ? bwd_launcher_d64(bf16, causal != 0, varlen)
+                                 : bwd_launcher_d128(bf16, causal != 0, varlen);
   if (launch(p, pr, stream) != cudaSuccess) return ATTN_ELAUNCH;
-  count_launch();
-  count_launch();
-  count_launch();
+  for (int i = 0; i < (varlen ? 4 : 3); ++i) count_launch();
   return ATTN_OK;
 }
 
@@ -127,7 +144,17 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
              void* dk, void* dv, int B, int Hq, int Hkv, int Lq, int Lk, int d, int causal, float scale, int fp16,
              cudaStream_t stream) {
   if (fp16 != 0 && fp16 != 1) return ATTN_EINVAL;
-  return attn::bwd(fp16 == 0, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Lq, Lk, d, causal, scale, stream);
+  return attn::bwd(fp16 == 0, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, Lq, Lk, d, causal, scale, nullptr,
+                   nullptr, stream);
+}
+
+int attn_bwd_varlen(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+                    void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int total_q, int total_k, int d, int causal,
+                    float scale, const int* cu_seqlens_q, const int* cu_seqlens_k, int fp16, cudaStream_t stream) {
+  if (fp16 != 0 && fp16 != 1) return ATTN_EINVAL;
+  if (!cu_seqlens_q || !cu_seqlens_k) return ATTN_EINVAL;
+  return attn::bwd(fp16 == 0, q, k, v, o, lse, dout, dq, dk, dv, B, Hq, Hkv, total_q, total_k, d, causal, scale,
+                   cu_seqlens_q, cu_seqlens_k, stream);
 }
 
 }  // extern "C"

@@ -53,8 +53,12 @@ struct BwdParams {
   CUtensorMap tm_do;       // like q
   const void* q;           // (B, Lq, Hq, d): the q kernel reads its Q and dO rows directly
   const void* dout;
-  const float* lse2;       // [B][Hq][Lq_pad]: lse * log2(e); +inf for rows with no key and the padding
-  const float* dvec;       // [B][Hq][Lq_pad]: D_i = dout_i . O_i; 0 on the padding
+  const float* lse2;       // dense [B][Hq][Lq_pad], varlen [Hq][query tiles][128]: lse * log2(e);
+                           // +inf for rows with no key and on the padding of every tile
+  const float* dvec;       // same layout: D_i = dout_i . O_i; 0 on the padding
+  const int* cu_q;         // varlen: query and key offsets (B+1 each), else null
+  const int* cu_k;
+  const int* tile_pref;    // varlen: query tiles before sequence b (B+1), then key tiles (B+1)
   void* dq;                // like q
   void* dk;                // like k
   void* dv;                // like k
@@ -140,6 +144,141 @@ __device__ __forceinline__ void store_row32(void* dst, const uint32_t (&x)[32], 
   uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
   for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+}
+
+// Largest b with pref[b] <= x (pref non-decreasing, pref[0] = 0 <= x < pref[B]).
+__device__ __forceinline__ int seq_of(const int* pref, int B, int x) {
+  int lo = 0, hi = B;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(pref + mid) <= x) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// ---------------------------------------------------------------------------
+// varlen: validates the offsets and counts 128-row tiles per sequence
+// (pref[b] = query tiles before sequence b, pref[B+1+b] = key tiles before
+// it); one warp.  Malformed offsets set the error word and zero the totals,
+// so the kernels that follow find no work.
+// ---------------------------------------------------------------------------
+static __global__ void __launch_bounds__(32) attn_bwd_tiles_kernel(const int* __restrict__ cu_q, const int* __restrict__ cu_k,
+                                                           int B, int total_q, int total_k, int* __restrict__ pref,
+                                                           int* __restrict__ err) {
+  const int lane = threadIdx.x;
+  bool bad = lane == 0 && (__ldg(cu_q) != 0 || __ldg(cu_k) != 0);
+  int cq = 0, ck = 0;
+  for (int b0 = 0; b0 < B; b0 += 32) {
+    const int b = b0 + lane;
+    int nq = 0, nk = 0;
+    if (b < B) {
+      const int a = __ldg(cu_q + b), e = __ldg(cu_q + b + 1), ak = __ldg(cu_k + b), ek = __ldg(cu_k + b + 1);
+      if (e < a || e > total_q || ek < ak || ek > total_k) bad = true;
+      nq = e > a ? (e - a + kBM - 1) / kBM : 0;
+      nk = ek > ak ? (ek - ak + kBN - 1) / kBN : 0;
+    }
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int yq = __shfl_up_sync(0xffffffffu, nq, o), yk = __shfl_up_sync(0xffffffffu, nk, o);
+      if (lane >= o) {
+        nq += yq;
+        nk += yk;
+      }
+    }
+    if (b < B) {
+      pref[b + 1] = cq + nq;
+      pref[B + 1 + b + 1] = ck + nk;
+    }
+    cq += __shfl_sync(0xffffffffu, nq, 31);
+    ck += __shfl_sync(0xffffffffu, nk, 31);
+  }
+  if (__any_sync(0xffffffffu, bad)) {
+    __syncwarp();
+    if (lane == 0) {
+      pref[B] = 0;
+      pref[2 * B + 1] = 0;
+      atomicCAS(err, 0, ATTN_DEVERR_BAD_SEQLENS);
+    }
+  }
+  if (lane == 0) {
+    pref[0] = 0;
+    pref[B + 1] = 0;
+  }
+}
+
+// Dot product of 8 threads' shares of a 16-bit row pair (D / 8 elements each).
+template <int D, bool BF16>
+__device__ __forceinline__ float row_dot8(const void* o, const void* dout, size_t at, int sub) {
+  using T = typename BwdIO<BF16>::T;
+  constexpr int kPer = D / 8;
+  const T* po = reinterpret_cast<const T*>(o) + at + sub * kPer;
+  const T* pd = reinterpret_cast<const T*>(dout) + at + sub * kPer;
+  float acc = 0.0f;
+#pragma unroll
+  for (int w = 0; w < kPer / 8; ++w) {
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(po) + w);
+    const uint4 c = __ldg(reinterpret_cast<const uint4*>(pd) + w);
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, cw[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      float2 fa, fc;
+      if constexpr (BF16) {
+        fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[e]));
+        fc = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&cw[e]));
+      } else {
+        fa = __half22float2(*reinterpret_cast<const __half2*>(&aw[e]));
+        fc = __half22float2(*reinterpret_cast<const __half2*>(&cw[e]));
+      }
+      acc = fmaf(fa.x, fc.x, acc);
+      acc = fmaf(fa.y, fc.y, acc);
+    }
+  }
+  return acc;
+}
+
+// varlen D_i and lse in exp2 units, one slot (h, query tile, row) per 8
+// threads: slot s is written at index s of [Hq][query tiles][128]; rows past
+// their sequence's end get the padding values.  q, o, dout packed
+// (total_q, Hq, d); lse (Hq, total_q).
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) attn_bwd_prep_varlen_kernel(const void* __restrict__ o,
+                                                                   const void* __restrict__ dout,
+                                                                   const float* __restrict__ lse,
+                                                                   const int* __restrict__ cu_q,
+                                                                   const int* __restrict__ pref, int B, int Hq,
+                                                                   int total_q, float* __restrict__ lse2,
+                                                                   float* __restrict__ dvec) {
+  const long long qt = __ldg(pref + B);
+  const long long slots = static_cast<long long>(Hq) * qt * kBM;
+  const int sub = threadIdx.x & 7;
+  const long long stride = (static_cast<long long>(gridDim.x) * blockDim.x) >> 3;
+  for (long long base = (static_cast<long long>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31)) >> 3; base < slots;
+       base += stride) {   // warp-uniform bound: the shuffles below need all 32 lanes
+    const long long s_raw = base + ((threadIdx.x & 31) >> 3);
+    const bool in = s_raw < slots;
+    const long long sl = in ? s_raw : slots - 1;
+    const int h = static_cast<int>(sl / (qt * kBM));
+    const long long rest = sl - static_cast<long long>(h) * qt * kBM;
+    const int T = static_cast<int>(rest / kBM), rr = static_cast<int>(rest - static_cast<long long>(T) * kBM);
+    const int b = seq_of(pref, B, T);
+    const int q0 = __ldg(cu_q + b), len = __ldg(cu_q + b + 1) - q0;
+    const int i = (T - __ldg(pref + b)) * kBM + rr;
+    const bool valid = in && i < len;
+    const size_t row = static_cast<size_t>(q0) + (valid ? i : 0);
+    float acc = valid ? row_dot8<D, BF16>(o, dout, (row * Hq + h) * D, sub) : 0.0f;
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+    if (in && sub == 0) {
+      float l2 = INFINITY;
+      if (valid) {
+        const float l = __ldg(lse + static_cast<size_t>(h) * total_q + row);
+        l2 = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
+      }
+      lse2[sl] = l2;
+      dvec[sl] = valid ? acc : 0.0f;
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -297,7 +436,7 @@ __device__ __forceinline__ void q_p_half(const uint32_t (&sr)[64], float l2, int
 // ---------------------------------------------------------------------------
 // dk, dv: one CTA per (b, g, 128-key tile n); grid (B * Hkv, n_kt)
 // ---------------------------------------------------------------------------
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kv_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -322,15 +461,46 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kv_kernel(const __gri
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kKvOffBar + C::kNBars * 8 + 4);
   WaitCtl wc{p.err, abort_flag, p.timeout_ns};
 
-  const int bg = blockIdx.x, n = blockIdx.y;
-  const int b = bg / p.Hkv, g = bg - b * p.Hkv;
-  const int off = p.Lk - p.Lq;   // causal: key j is visible to query i iff j <= i + off
+  // this CTA's sequence b, KV head g and key tile n; q_len / k_len its
+  // lengths, rq / rk the global row of its first query / key (dense: b * L)
+  int b, g, n, q_len, k_len, rq, rk, nqt;
+  if constexpr (!VARLEN) {
+    const int bg = blockIdx.x;
+    n = blockIdx.y;
+    b = bg / p.Hkv;
+    g = bg - b * p.Hkv;
+    q_len = p.Lq;
+    k_len = p.Lk;
+    rq = b * p.Lq;
+    rk = b * p.Lk;
+    nqt = p.n_qt;
+  } else {
+    const int* kpref = p.tile_pref + p.B + 1;
+    const int u = blockIdx.x;
+    if (u >= __ldg(kpref + p.B) * p.Hkv) return;   // beyond the work: before any barrier or TMEM use
+    const int nt = u / p.Hkv;
+    g = u - nt * p.Hkv;
+    b = seq_of(kpref, p.B, nt);
+    n = nt - __ldg(kpref + b);
+    rq = __ldg(p.cu_q + b);
+    rk = __ldg(p.cu_k + b);
+    q_len = __ldg(p.cu_q + b + 1) - rq;
+    k_len = __ldg(p.cu_k + b + 1) - rk;
+    nqt = (q_len + kBM - 1) / kBM;
+  }
+  // TMA coordinates: dense maps are (d, H, L, B), packed ones (d, H, total, 1)
+  const int trow_q = VARLEN ? rq : 0, trow_k = VARLEN ? rk : 0, bc = VARLEN ? 0 : b;
+  auto vtile = [&](int h, int m) -> size_t {   // first lse2 / D entry of query tile m of head h
+    return VARLEN ? (static_cast<size_t>(h) * __ldg(p.tile_pref + p.B) + __ldg(p.tile_pref + b) + m) * kBM
+                  : (static_cast<size_t>(b) * p.Hq + h) * p.Lq_pad + static_cast<size_t>(m) * kBM;
+  };
+  const int off = k_len - q_len;   // causal: key j is visible to query i iff j <= i + off
   int m_first = 0;
   if constexpr (CAUSAL) {
     const int first_q = n * kBN - off;   // smallest query that sees key n * 128
     m_first = first_q <= 0 ? 0 : first_q / kBM;
   }
-  const int nm = p.n_qt - m_first > 0 ? p.n_qt - m_first : 0;
+  const int nm = nqt - m_first > 0 ? nqt - m_first : 0;
   const int n_tiles = p.group * nm;
 
   if (tid == 0) {
@@ -364,8 +534,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kv_kernel(const __gri
       mbar_arrive_expect_tx(b_kv_full, 2 * C::kTile);
 #pragma unroll
       for (int c = 0; c < C::kChunks; ++c) {
-        tma_load_4d(sK + c * 16384, &p.tm_k, b_kv_full, c * 64, g, n * kBN, b);
-        tma_load_4d(sV + c * 16384, &p.tm_v, b_kv_full, c * 64, g, n * kBN, b);
+        tma_load_4d(sK + c * 16384, &p.tm_k, b_kv_full, c * 64, g, trow_k + n * kBN, bc);
+        tma_load_4d(sV + c * 16384, &p.tm_v, b_kv_full, c * 64, g, trow_k + n * kBN, bc);
       }
       int issued = 0;
       for (int t = 0; t < n_tiles; ++t) {
@@ -375,10 +545,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kv_kernel(const __gri
         mbar_arrive_expect_tx(b_st_full(st), 2 * C::kTile + 1024);
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_4d(sQ(st) + c * 16384, &p.tm_q, b_st_full(st), c * 64, h, m * kBM, b);
-          tma_load_4d(sDO(st) + c * 16384, &p.tm_do, b_st_full(st), c * 64, h, m * kBM, b);
+          tma_load_4d(sQ(st) + c * 16384, &p.tm_q, b_st_full(st), c * 64, h, trow_q + m * kBM, bc);
+          tma_load_4d(sDO(st) + c * 16384, &p.tm_do, b_st_full(st), c * 64, h, trow_q + m * kBM, bc);
         }
-        const size_t vi = (static_cast<size_t>(b) * p.Hq + h) * p.Lq_pad + m * kBM;
+        const size_t vi = vtile(h, m);
         const uint32_t sv = smem_u32(vec + st * 256);
         bulk_load(sv, p.lse2 + vi, 512, b_st_full(st));
         bulk_load(sv + 512, p.dvec + vi, 512, b_st_full(st));
@@ -518,11 +688,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kv_kernel(const __gri
       tc_fence_after();
       using T = typename BwdIO<BF16>::T;
       constexpr int kHalf = D / 2;
-      const size_t orow = ((static_cast<size_t>(b) * p.Lk + j) * p.Hkv + g) * D + half * kHalf;
+      const size_t orow = ((static_cast<size_t>(rk) + j) * p.Hkv + g) * D + half * kHalf;
       T* dvp = reinterpret_cast<T*>(p.dv) + orow;
       T* dkp = reinterpret_cast<T*>(p.dk) + orow;
       if (n_tiles == 0) {
-        if (j < p.Lk) {
+        if (j < k_len) {
 #pragma unroll
           for (int i = 0; i < kHalf / 8; ++i) {
             reinterpret_cast<uint4*>(dvp)[i] = make_uint4(0, 0, 0, 0);
@@ -535,14 +705,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kv_kernel(const __gri
           uint32_t x[32];
           tmem_ld_32x32b_x32(tmem + lane_off + 256 + half * kHalf + c * 32, x);
           tmem_wait_ld(x);
-          if (j < p.Lk) store_row32<BF16>(dvp + c * 32, x, 1.0f);
+          if (j < k_len) store_row32<BF16>(dvp + c * 32, x, 1.0f);
         }
 #pragma unroll
         for (int c = 0; c < kHalf / 32; ++c) {
           uint32_t x[32];
           tmem_ld_32x32b_x32(tmem + lane_off + 256 + D + half * kHalf + c * 32, x);
           tmem_wait_ld(x);
-          if (j < p.Lk) store_row32<BF16>(dkp + c * 32, x, p.scale);
+          if (j < k_len) store_row32<BF16>(dkp + c * 32, x, p.scale);
         }
       }
     }
@@ -561,7 +731,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kv_kernel(const __gri
 // dq: one CTA per (b, h, 128-query tile m); grid (B * Hq, n_qt), heaviest
 // (last) query tiles first
 // ---------------------------------------------------------------------------
-template <int D, bool BF16, bool CAUSAL>
+template <int D, bool BF16, bool CAUSAL, bool VARLEN>
 __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -584,15 +754,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kQOffBar + C::kQNBars * 8 + 4);
   WaitCtl wc{p.err, abort_flag, p.timeout_ns};
 
-  const int bh = blockIdx.x, m = p.n_qt - 1 - static_cast<int>(blockIdx.y);
-  const int b = bh / p.Hq, h = bh - b * p.Hq, g = h / p.group;
-  const int off = p.Lk - p.Lq;
-  int n_tiles = p.n_kt;
+  // this CTA's sequence b, query head h and query tile m (see the kv kernel)
+  int b, h, m, q_len, k_len, rq, rk, nkt;
+  if constexpr (!VARLEN) {
+    const int bh = blockIdx.x;
+    m = p.n_qt - 1 - static_cast<int>(blockIdx.y);
+    b = bh / p.Hq;
+    h = bh - b * p.Hq;
+    q_len = p.Lq;
+    k_len = p.Lk;
+    rq = b * p.Lq;
+    rk = b * p.Lk;
+    nkt = p.n_kt;
+  } else {
+    const int u = blockIdx.x;
+    if (u >= __ldg(p.tile_pref + p.B) * p.Hq) return;   // beyond the work: before any barrier or TMEM use
+    const int mt = u / p.Hq;
+    h = u - mt * p.Hq;
+    b = seq_of(p.tile_pref, p.B, mt);
+    m = mt - __ldg(p.tile_pref + b);
+    rq = __ldg(p.cu_q + b);
+    rk = __ldg(p.cu_k + b);
+    q_len = __ldg(p.cu_q + b + 1) - rq;
+    k_len = __ldg(p.cu_k + b + 1) - rk;
+    nkt = (k_len + kBN - 1) / kBN;
+  }
+  const int g = h / p.group;
+  const int trow_k = VARLEN ? rk : 0, bc = VARLEN ? 0 : b;
+  const int off = k_len - q_len;
+  int n_tiles = nkt;
   if constexpr (CAUSAL) {
     int last_q = m * kBM + kBM - 1;
-    if (last_q > p.Lq - 1) last_q = p.Lq - 1;
+    if (last_q > q_len - 1) last_q = q_len - 1;
     const int max_key = last_q + off;
-    n_tiles = max_key < 0 ? 0 : min(p.n_kt, max_key / kBN + 1);
+    n_tiles = max_key < 0 ? 0 : min(nkt, max_key / kBN + 1);
   }
 
   if (tid == 0) {
@@ -630,8 +825,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
         mbar_arrive_expect_tx(b_st_full(st), 2 * C::kTile);
 #pragma unroll
         for (int c = 0; c < C::kChunks; ++c) {
-          tma_load_4d(sK(st) + c * 16384, &p.tm_k, b_st_full(st), c * 64, g, t * kBN, b);
-          tma_load_4d(sV(st) + c * 16384, &p.tm_v, b_st_full(st), c * 64, g, t * kBN, b);
+          tma_load_4d(sK(st) + c * 16384, &p.tm_k, b_st_full(st), c * 64, g, trow_k + t * kBN, bc);
+          tma_load_4d(sV(st) + c * 16384, &p.tm_v, b_st_full(st), c * 64, g, trow_k + t * kBN, bc);
         }
         ++issued;
       }
@@ -713,10 +908,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
     const uint32_t t_s = tmem + lane_off + half * 64, t_dp = tmem + lane_off + 128 + half * 64;
     const int i = m * kBM + row;
     const float cl2 = p.scale_log2;
-    const size_t vi = (static_cast<size_t>(b) * p.Hq + h) * p.Lq_pad + i;
-    const float l2 = __ldg(p.lse2 + vi);   // i < Lq_pad always; +inf past Lq, so P = 0 there
+    const size_t vi = VARLEN ? (static_cast<size_t>(h) * __ldg(p.tile_pref + p.B) + __ldg(p.tile_pref + b) + m) * kBM + row
+                             : (static_cast<size_t>(b) * p.Hq + h) * p.Lq_pad + i;
+    const float l2 = __ldg(p.lse2 + vi);   // +inf past the sequence's last query, so P = 0 there
     const float di = __ldg(p.dvec + vi);
-    int lim_key = p.Lk - 1;
+    int lim_key = k_len - 1;
     if constexpr (CAUSAL) lim_key = min(lim_key, i + off);
     BwdTracer tr;
     tr.init(p, half ? 6 : 5, lane == 0 && quarter == 0);
@@ -725,14 +921,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
       // two 16-bit values per column in memory order; rows past Lq are zero
       using T = typename BwdIO<BF16>::T;
       constexpr int kW = D / 16;   // uint4 words per half row
-      const size_t src = ((static_cast<size_t>(b) * p.Lq + i) * p.Hq + h) * D + half * (D / 2);
+      const size_t src = ((static_cast<size_t>(rq) + i) * p.Hq + h) * D + half * (D / 2);
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         const uint4* g4 = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(which ? p.dout : p.q) + src);
         uint32_t w[4 * kW];
 #pragma unroll
         for (int u = 0; u < kW; ++u) {
-          const uint4 x = (i < p.Lq) ? __ldg(g4 + u) : make_uint4(0, 0, 0, 0);
+          const uint4 x = (i < q_len) ? __ldg(g4 + u) : make_uint4(0, 0, 0, 0);
           w[4 * u] = x.x;
           w[4 * u + 1] = x.y;
           w[4 * u + 2] = x.z;
@@ -765,7 +961,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
       if (lane == 0) mbar_arrive(b_s_free);
       // masked: tiles crossing the causal diagonal and the ragged last key tile
       float pr[64];
-      if ((CAUSAL && t * kBN + kBN - 1 > m * kBM + off) || t * kBN + kBN > p.Lk)
+      if ((CAUSAL && t * kBN + kBN - 1 > m * kBM + off) || t * kBN + kBN > k_len)
         q_p_half<true>(sr, l2, lim_key - t * kBN - half * 64, cl2, pr);
       else
         q_p_half<false>(sr, l2, 0, cl2, pr);
@@ -784,9 +980,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
       tc_fence_after();
       using T = typename BwdIO<BF16>::T;
       constexpr int kHalf = D / 2;
-      T* dst = reinterpret_cast<T*>(p.dq) + ((static_cast<size_t>(b) * p.Lq + i) * p.Hq + h) * D + half * kHalf;
+      T* dst = reinterpret_cast<T*>(p.dq) + ((static_cast<size_t>(rq) + i) * p.Hq + h) * D + half * kHalf;
       if (n_tiles == 0) {
-        if (i < p.Lq) {
+        if (i < q_len) {
 #pragma unroll
           for (int w = 0; w < kHalf / 8; ++w) reinterpret_cast<uint4*>(dst)[w] = make_uint4(0, 0, 0, 0);
         }
@@ -796,7 +992,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
           uint32_t x[32];
           tmem_ld_32x32b_x32(tmem + lane_off + 256 + half * kHalf + c * 32, x);
           tmem_wait_ld(x);
-          if (i < p.Lq) store_row32<BF16>(dst + c * 32, x, p.scale);
+          if (i < q_len) store_row32<BF16>(dst + c * 32, x, p.scale);
         }
       }
     }

@@ -6,17 +6,21 @@
 
 namespace attn {
 
-// Inputs of the first pass (D_i = dout_i . O_i and lse in exp2 units).
+// Inputs of the first pass (D_i = dout_i . O_i and lse in exp2 units) and
+// the grids; varlen also fills the tile tables at `pref` first.
 struct BwdPrep {
   const void* o;
   const void* dout;
   const float* lse;
-  int grid;
+  int* pref;          // varlen: p.tile_pref, written by the tile-count kernel
+  int grid;           // first pass
+  int grid_kv;        // varlen: 1-D grids (an upper bound; extra CTAs exit at once)
+  int grid_q;
 };
 
 using BwdLauncher = cudaError_t (*)(const BwdParams& p, const BwdPrep& pr, cudaStream_t stream);
 
-BwdLauncher bwd_launcher_d64(bool bf16, bool causal);
-BwdLauncher bwd_launcher_d128(bool bf16, bool causal);
+BwdLauncher bwd_launcher_d64(bool bf16, bool causal, bool varlen);
+BwdLauncher bwd_launcher_d128(bool bf16, bool causal, bool varlen);
 
 }  // namespace attn
