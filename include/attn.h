@@ -35,12 +35,14 @@
  *     synchronises.  Arguments are validated on the host before anything is
  *     enqueued; a non-zero return means nothing was launched.
  *   - The library allocates, once per device and lazily, its own small
- *     buffers: cached TMA descriptors, a tile schedule per problem shape and
- *     a split-KV workspace that is grown on demand.  These live until the
- *     process exits.
- *   - Calls that share a device may run concurrently on different streams
- *     only if they do not share a problem shape that uses split-KV (the
- *     workspace of a shape is shared).
+ *     buffers: cached TMA descriptors, a tile schedule per problem shape, a
+ *     split-KV workspace for the forward and a D / lse workspace for the
+ *     backward, each grown on demand.  These live until the process exits.
+ *   - Calls that share a device may run concurrently on different streams,
+ *     except that each workspace is one buffer per device: at most one
+ *     forward whose schedule splits the keys (attn_plan reports partials > 0;
+ *     varlen calls never split) and at most one backward may be in flight on
+ *     a device at a time.  Order such calls (one stream, or events).
  */
 #ifndef ATTN_H
 #define ATTN_H
