@@ -25,12 +25,13 @@
 // CTA layout (320 threads): warps 0-7 process rows, warp w owning TMEM lanes
 // 32 (w % 4) .. +31 (one row of the 128-row tile per lane) and columns
 // 64 (w / 4) .. +63 of the 128-wide S and dP tiles; warp 8 issues TMA, warp 9
-// allocates TMEM and one thread issues tcgen05.mma.  TMEM columns: S at
-// [0,128), dP at [128,256), the accumulators from 256 on.  The 16-bit P (kv
-// kernel) and dS of a warp's 64 columns are packed into the first 32 of those
-// columns, so no warp writes where another still reads; the MMAs read the
-// 16-column slices of the A operand from there, and are issued before the
-// next tile's S and dP, which the tensor pipe runs after them.  The row threads signal P and dS separately, so each kernel's
+// allocates TMEM and one thread issues tcgen05.mma.  (Sixteen row warps of 32
+// columns each measured slower: 0.809 against 0.780 ms.)  TMEM
+// columns: S at [0,128), dP at [128,256), the accumulators from 256 on.  The
+// 16-bit P (kv kernel) and dS of a warp's columns are packed into the first
+// half of those columns, so no warp writes where another still reads; the
+// MMAs read the 16-column slices of the A operand from there, and are issued
+// before the next tile's S and dP, which the tensor pipe runs after them.  The row threads signal P and dS separately, so each kernel's
 // next S (and dP) is computed while the rows are still busy with this tile.
 #pragma once
 #include <cuda_bf16.h>
@@ -41,10 +42,14 @@
 
 namespace attn {
 
-constexpr int kBwdThreads = 320;
-constexpr int kBwdWarpTMA = 8;
-constexpr int kBwdWarpMMA = 9;
-constexpr int kBwdRowWarps = 8;
+// Row warps: warp w owns TMEM lanes 32 (w % 4) .. +31 and column part w / 4
+// of the 128-wide S and dP tiles (kBwdCols columns).
+constexpr int kBwdParts = 2;
+constexpr int kBwdCols = 128 / kBwdParts;
+constexpr int kBwdRowWarps = 4 * kBwdParts;
+constexpr int kBwdWarpTMA = kBwdRowWarps;
+constexpr int kBwdWarpMMA = kBwdRowWarps + 1;
+constexpr int kBwdThreads = 32 * (kBwdRowWarps + 2);
 
 struct BwdParams {
   CUtensorMap tm_q;        // (d, Hq, Lq, B), box 64 x 1 x 128 x 1
@@ -281,6 +286,21 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_varlen_kernel(const void* _
   }
 }
 
+// One warp's columns of its 32 lanes in one TMEM load (32 or 64 columns).
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[32]) { tmem_ld_32x32b_x32(taddr, r); }
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[64]) { tmem_ld_32x32b_x64(taddr, r); }
+
+// Stores 16 fp32 values (times `mul`) of one row as 16-bit, 32 bytes.
+template <bool BF16>
+__device__ __forceinline__ void store_row16(void* dst, const uint32_t (&x)[16], float mul) {
+  uint32_t pk[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) pk[i] = pack2<BF16>(__uint_as_float(x[2 * i]) * mul, __uint_as_float(x[2 * i + 1]) * mul);
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+  d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+}
+
 // ---------------------------------------------------------------------------
 // D_i = dout_i . O_i and lse in exp2 units, one (b, i, h) row per 8 threads;
 // rows i in [Lq, Lq_pad) get the padding values.
@@ -347,16 +367,21 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const void* __restri
 }
 
 // TMEM column of the packed 16-bit A operand's kk-th 16-wide K slice inside a
-// 128-column S or dP region: warp half h packs columns 64h.. into 64h..64h+31.
-__device__ __forceinline__ uint32_t packed_slice_col(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
+// 128-column S or dP region: column part c packs its kBwdCols columns into
+// the first kBwdCols / 2 of them.
+__device__ __forceinline__ uint32_t packed_slice_col(int kk) {
+  constexpr int kSlices = kBwdCols / 16;   // K slices per column part
+  return (kk / kSlices) * kBwdCols + (kk % kSlices) * 8;
+}
 
 // kv kernel, one warp's 64 query columns of its 32 key rows: P^T = 2^(S^T c - lse2)
 // (c = scale log2 e), kept in pr and stored packed over the first 32 of its
 // columns.  MASK: query column c is allowed iff c >= cmin (causal).
 template <bool MASK, bool BF16>
-__device__ __forceinline__ void kv_p_half(uint32_t t_s, const float* ls, int cmin, float cl2, float (&pr)[64]) {
+__device__ __forceinline__ void kv_p_half(uint32_t t_s, const float* ls, int cmin, float cl2,
+                                          float (&pr)[kBwdCols]) {
 #pragma unroll
-  for (int ch = 0; ch < 2; ++ch) {
+  for (int ch = 0; ch < kBwdCols / 32; ++ch) {
     uint32_t sr[32];
     tmem_ld_32x32b_x32(t_s + ch * 32, sr);
     tmem_wait_ld(sr);
@@ -388,9 +413,9 @@ __device__ __forceinline__ void kv_p_half(uint32_t t_s, const float* ls, int cmi
 // of its dP columns.  dd: D per column (kv kernel), or null with `di` the
 // row's D (q kernel).
 template <bool BF16>
-__device__ __forceinline__ void ds_half(uint32_t t_dp, const float* dd, float di, const float (&pr)[64]) {
+__device__ __forceinline__ void ds_half(uint32_t t_dp, const float* dd, float di, const float (&pr)[kBwdCols]) {
 #pragma unroll
-  for (int ch = 0; ch < 2; ++ch) {
+  for (int ch = 0; ch < kBwdCols / 32; ++ch) {
     uint32_t dr[32];
     tmem_ld_32x32b_x32(t_dp + ch * 32, dr);
     tmem_wait_ld(dr);
@@ -422,10 +447,11 @@ __device__ __forceinline__ void ds_half(uint32_t t_dp, const float* dd, float di
 // in registers: P = 2^(S c - lse2_i) in pr.  MASK: key column c is allowed
 // iff c <= lim.
 template <bool MASK>
-__device__ __forceinline__ void q_p_half(const uint32_t (&sr)[64], float l2, int lim, float cl2, float (&pr)[64]) {
+__device__ __forceinline__ void q_p_half(const uint32_t (&sr)[kBwdCols], float l2, int lim, float cl2,
+                                         float (&pr)[kBwdCols]) {
   const float2 c2 = make_float2(cl2, cl2), nl = make_float2(-l2, -l2);
 #pragma unroll
-  for (int c = 0; c < 64; c += 2) {
+  for (int c = 0; c < kBwdCols; c += 2) {
     const float2 a = ffma2(make_float2(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), c2, nl);
     const float x0 = ex2_approx(a.x), x1 = ex2_approx(a.y);
     pr[c] = (!MASK || c <= lim) ? x0 : 0.0f;
@@ -637,14 +663,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kv_kernel(const __gri
     }
   } else {
     // ---------------------------------------------------------------- key rows
-    const int quarter = warp & 3, half = warp >> 2;
+    const int quarter = warp & 3, part = warp >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t t_s = tmem + lane_off + half * 64, t_dp = tmem + lane_off + 128 + half * 64;
+    const int c0 = part * kBwdCols;   // this warp's first column of S and dP
+    const uint32_t t_s = tmem + lane_off + c0, t_dp = tmem + lane_off + 128 + c0;
     const int j = n * kBN + row;
     const float cl2 = p.scale_log2;
     BwdTracer tr;
-    tr.init(p, half ? 2 : 1, lane == 0 && quarter == 0);
+    tr.init(p, part == 0 ? 1 : 2, lane == 0 && quarter == 0 && part < 2);
     bool ok = true;
     for (int t = 0; t < n_tiles; ++t) {
       tr.rec(20, t);
@@ -658,14 +685,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kv_kernel(const __gri
         ok = false;
         break;
       }
-      const float* ls = vec + st * 256 + half * 64;
-      const float* dd = vec + st * 256 + 128 + half * 64;
+      const float* ls = vec + st * 256 + c0;
+      const float* dd = vec + st * 256 + 128 + c0;
       // Only tiles crossing the causal diagonal are masked.  Padded query
       // columns (past Lq) have lse2 = +inf, so P = 0 there; padded key rows
       // (past Lk) only reach their own rows of dv and dk, which are not stored.
-      float pr[64];
+      float pr[kBwdCols];
       if (CAUSAL && n * kBN + kBN - 1 - m * kBM > off)
-        kv_p_half<true, BF16>(t_s, ls, j - off - m * kBM - half * 64, cl2, pr);
+        kv_p_half<true, BF16>(t_s, ls, j - off - m * kBM - c0, cl2, pr);
       else
         kv_p_half<false, BF16>(t_s, ls, 0, cl2, pr);
       tmem_wait_st();
@@ -683,12 +710,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kv_kernel(const __gri
       if (lane == 0) mbar_arrive(b_ds_full);
       tr.rec(24, t);
     }
-    // epilogue: dv = acc, dk = scale * acc; this warp's half of the columns
+    // epilogue: dv = acc, dk = scale * acc; this warp's part of the columns
     if (ok && (n_tiles == 0 || mbar_wait_warp(b_acc, 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteODone)))) {
       tc_fence_after();
       using T = typename BwdIO<BF16>::T;
-      constexpr int kHalf = D / 2;
-      const size_t orow = ((static_cast<size_t>(rk) + j) * p.Hkv + g) * D + half * kHalf;
+      constexpr int kHalf = D / kBwdParts;   // accumulator columns per warp
+      const size_t orow = ((static_cast<size_t>(rk) + j) * p.Hkv + g) * D + part * kHalf;
       T* dvp = reinterpret_cast<T*>(p.dv) + orow;
       T* dkp = reinterpret_cast<T*>(p.dk) + orow;
       if (n_tiles == 0) {
@@ -701,18 +728,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kv_kernel(const __gri
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < kHalf / 32; ++c) {
-          uint32_t x[32];
-          tmem_ld_32x32b_x32(tmem + lane_off + 256 + half * kHalf + c * 32, x);
+        for (int c = 0; c < kHalf / 16; ++c) {
+          uint32_t x[16];
+          tmem_ld_32x32b_x16(tmem + lane_off + 256 + part * kHalf + c * 16, x);
           tmem_wait_ld(x);
-          if (j < k_len) store_row32<BF16>(dvp + c * 32, x, 1.0f);
+          if (j < k_len) store_row16<BF16>(dvp + c * 16, x, 1.0f);
         }
 #pragma unroll
-        for (int c = 0; c < kHalf / 32; ++c) {
-          uint32_t x[32];
-          tmem_ld_32x32b_x32(tmem + lane_off + 256 + D + half * kHalf + c * 32, x);
+        for (int c = 0; c < kHalf / 16; ++c) {
+          uint32_t x[16];
+          tmem_ld_32x32b_x16(tmem + lane_off + 256 + D + part * kHalf + c * 16, x);
           tmem_wait_ld(x);
-          if (j < k_len) store_row32<BF16>(dkp + c * 32, x, p.scale);
+          if (j < k_len) store_row16<BF16>(dkp + c * 16, x, p.scale);
         }
       }
     }
@@ -902,10 +929,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
     }
   } else {
     // ---------------------------------------------------------------- query rows
-    const int quarter = warp & 3, half = warp >> 2;
+    const int quarter = warp & 3, part = warp >> 2;
     const int row = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t t_s = tmem + lane_off + half * 64, t_dp = tmem + lane_off + 128 + half * 64;
+    const int c0 = part * kBwdCols;   // this warp's first column of S and dP
+    const uint32_t t_s = tmem + lane_off + c0, t_dp = tmem + lane_off + 128 + c0;
     const int i = m * kBM + row;
     const float cl2 = p.scale_log2;
     const size_t vi = VARLEN ? (static_cast<size_t>(h) * __ldg(p.tile_pref + p.B) + __ldg(p.tile_pref + b) + m) * kBM + row
@@ -915,13 +943,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
     int lim_key = k_len - 1;
     if constexpr (CAUSAL) lim_key = min(lim_key, i + off);
     BwdTracer tr;
-    tr.init(p, half ? 6 : 5, lane == 0 && quarter == 0);
+    tr.init(p, part == 0 ? 5 : 6, lane == 0 && quarter == 0 && part < 2);
     if (n_tiles > 0) {
-      // this row's Q and dO (half the columns per warp half) into TMEM, packed
-      // two 16-bit values per column in memory order; rows past Lq are zero
+      // this row's Q and dO (a quarter of the features per column part) into
+      // TMEM, packed two 16-bit values per column in memory order; rows past
+      // the sequence's end are zero
       using T = typename BwdIO<BF16>::T;
-      constexpr int kW = D / 16;   // uint4 words per half row
-      const size_t src = ((static_cast<size_t>(rq) + i) * p.Hq + h) * D + half * (D / 2);
+      constexpr int kE = D / kBwdParts;   // features per warp
+      constexpr int kW = kE / 8;          // uint4 words per warp's share of a row
+      const size_t src = ((static_cast<size_t>(rq) + i) * p.Hq + h) * D + part * kE;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         const uint4* g4 = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(which ? p.dout : p.q) + src);
@@ -934,11 +964,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
           w[4 * u + 2] = x.z;
           w[4 * u + 3] = x.w;
         }
-        const uint32_t col = tmem + lane_off + (which ? C::kColDO : C::kColQ) + half * (D / 4);
-        if constexpr (D == 128) {
+        const uint32_t col = tmem + lane_off + (which ? C::kColDO : C::kColQ) + part * (kE / 2);
+        if constexpr (kE / 2 == 32) {
           tmem_st_32x32b_x32(col, w);
-        } else {
+        } else if constexpr (kE / 2 == 16) {
           tmem_st_32x32b_x16(col, w);
+        } else {
+          tmem_st_32x32b_x8(col, w);
         }
       }
       tmem_wait_st();
@@ -953,16 +985,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
       tr.rec(21, t);
       tc_fence_after();
       // S is released as soon as it is in registers; P is formed after
-      uint32_t sr[64];
-      tmem_ld_32x32b_x64(t_s, sr);
+      uint32_t sr[kBwdCols];
+      tmem_ld_cols(t_s, sr);
       tmem_wait_ld(sr);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_s_free);
       // masked: tiles crossing the causal diagonal and the ragged last key tile
-      float pr[64];
+      float pr[kBwdCols];
       if ((CAUSAL && t * kBN + kBN - 1 > m * kBM + off) || t * kBN + kBN > k_len)
-        q_p_half<true>(sr, l2, lim_key - t * kBN - half * 64, cl2, pr);
+        q_p_half<true>(sr, l2, lim_key - t * kBN - c0, cl2, pr);
       else
         q_p_half<false>(sr, l2, 0, cl2, pr);
       tr.rec(22, t);
@@ -979,8 +1011,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
     if (ok && (n_tiles == 0 || mbar_wait_warp(b_acc, 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteODone)))) {
       tc_fence_after();
       using T = typename BwdIO<BF16>::T;
-      constexpr int kHalf = D / 2;
-      T* dst = reinterpret_cast<T*>(p.dq) + ((static_cast<size_t>(rq) + i) * p.Hq + h) * D + half * kHalf;
+      constexpr int kHalf = D / kBwdParts;   // accumulator columns per warp
+      T* dst = reinterpret_cast<T*>(p.dq) + ((static_cast<size_t>(rq) + i) * p.Hq + h) * D + part * kHalf;
       if (n_tiles == 0) {
         if (i < q_len) {
 #pragma unroll
@@ -988,11 +1020,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
         }
       } else {
 #pragma unroll
-        for (int c = 0; c < kHalf / 32; ++c) {
-          uint32_t x[32];
-          tmem_ld_32x32b_x32(tmem + lane_off + 256 + half * kHalf + c * 32, x);
+        for (int c = 0; c < kHalf / 16; ++c) {
+          uint32_t x[16];
+          tmem_ld_32x32b_x16(tmem + lane_off + 256 + part * kHalf + c * 16, x);
           tmem_wait_ld(x);
-          if (i < q_len) store_row32<BF16>(dst + c * 32, x, p.scale);
+          if (i < q_len) store_row16<BF16>(dst + c * 16, x, p.scale);
         }
       }
     }
