@@ -26,13 +26,15 @@
 // 32 (w % 4) .. +31 (one row of the 128-row tile per lane) and columns
 // 64 (w / 4) .. +63 of the 128-wide S and dP tiles; warp 8 issues TMA, warp 9
 // allocates TMEM and one thread issues tcgen05.mma.  (Sixteen row warps of 32
-// columns each measured slower: 0.809 against 0.780 ms.)  TMEM
-// columns: S at [0,128), dP at [128,256), the accumulators from 256 on.  The
-// 16-bit P (kv kernel) and dS of a warp's columns are packed into the first
-// half of those columns, so no warp writes where another still reads; the
-// MMAs read the 16-column slices of the A operand from there, and are issued
-// before the next tile's S and dP, which the tensor pipe runs after them.  The row threads signal P and dS separately, so each kernel's
-// next S (and dP) is computed while the rows are still busy with this tile.
+// columns each measured slower: 0.809 against 0.780 ms.)  TMEM columns: S at
+// [0,128), dP at [128,256), the accumulators from 256 on; the q kernel also
+// keeps its Q and dO rows there as the A operands of S and dP.  The 16-bit P
+// (kv kernel) and dS of a warp's columns are packed into the first half of
+// those columns, so no warp writes where another still reads; the MMAs read
+// the 16-column slices of the A operand from there, and are issued before the
+// next tile's S and dP, which the tensor pipe runs after them.  The row
+// threads signal P and dS separately, so each kernel's next S (and dP) is
+// computed while the rows are still busy with this tile.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -374,11 +376,12 @@ __device__ __forceinline__ uint32_t packed_slice_col(int kk) {
   return (kk / kSlices) * kBwdCols + (kk % kSlices) * 8;
 }
 
-// kv kernel, one warp's 64 query columns of its 32 key rows: P^T = 2^(S^T c - lse2)
-// (c = scale log2 e), kept in pr and stored packed over the first 32 of its
-// columns.  MASK: query column c is allowed iff c >= cmin (causal).
+// kv kernel, one warp's kBwdCols query columns of its 32 key rows:
+// P^T = 2^(S^T c - lse2) (c = scale log2 e), kept in pr and stored packed over
+// the first half of its columns.  MASK: query column c is allowed iff
+// c >= cmin (causal).
 template <bool MASK, bool BF16>
-__device__ __forceinline__ void kv_p_half(uint32_t t_s, const float* ls, int cmin, float cl2,
+__device__ __forceinline__ void kv_p_part(uint32_t t_s, const float* ls, int cmin, float cl2,
                                           float (&pr)[kBwdCols]) {
 #pragma unroll
   for (int ch = 0; ch < kBwdCols / 32; ++ch) {
@@ -409,11 +412,11 @@ __device__ __forceinline__ void kv_p_half(uint32_t t_s, const float* ls, int cmi
   }
 }
 
-// dS = P (dP - D) for one warp's 64 columns, stored packed over the first 32
-// of its dP columns.  dd: D per column (kv kernel), or null with `di` the
+// dS = P (dP - D) for one warp's kBwdCols columns, stored packed over the
+// first half of its dP columns.  dd: D per column (kv kernel), or null with `di` the
 // row's D (q kernel).
 template <bool BF16>
-__device__ __forceinline__ void ds_half(uint32_t t_dp, const float* dd, float di, const float (&pr)[kBwdCols]) {
+__device__ __forceinline__ void ds_part(uint32_t t_dp, const float* dd, float di, const float (&pr)[kBwdCols]) {
 #pragma unroll
   for (int ch = 0; ch < kBwdCols / 32; ++ch) {
     uint32_t dr[32];
@@ -443,11 +446,11 @@ __device__ __forceinline__ void ds_half(uint32_t t_dp, const float* dd, float di
   }
 }
 
-// q kernel, one warp's 64 key columns of its 32 query rows, from S already
+// q kernel, one warp's kBwdCols key columns of its 32 query rows, from S already
 // in registers: P = 2^(S c - lse2_i) in pr.  MASK: key column c is allowed
 // iff c <= lim.
 template <bool MASK>
-__device__ __forceinline__ void q_p_half(const uint32_t (&sr)[kBwdCols], float l2, int lim, float cl2,
+__device__ __forceinline__ void q_p_part(const uint32_t (&sr)[kBwdCols], float l2, int lim, float cl2,
                                          float (&pr)[kBwdCols]) {
   const float2 c2 = make_float2(cl2, cl2), nl = make_float2(-l2, -l2);
 #pragma unroll
@@ -692,9 +695,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kv_kernel(const __gri
       // (past Lk) only reach their own rows of dv and dk, which are not stored.
       float pr[kBwdCols];
       if (CAUSAL && n * kBN + kBN - 1 - m * kBM > off)
-        kv_p_half<true, BF16>(t_s, ls, j - off - m * kBM - c0, cl2, pr);
+        kv_p_part<true, BF16>(t_s, ls, j - off - m * kBM - c0, cl2, pr);
       else
-        kv_p_half<false, BF16>(t_s, ls, 0, cl2, pr);
+        kv_p_part<false, BF16>(t_s, ls, 0, cl2, pr);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -703,7 +706,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_kv_kernel(const __gri
       if (!mbar_wait_warp(b_dp_full, t & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteODone))) { ok = false; break; }
       tr.rec(23, t);
       tc_fence_after();
-      ds_half<BF16>(t_dp, dd, 0.0f, pr);
+      ds_part<BF16>(t_dp, dd, 0.0f, pr);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -887,7 +890,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
         umma_commit(b_dp_full);
       };
       // Order per tile t: S(t+1) (once the rows have read S(t)), dq(t),
-      // dP(t+1).  dS(t) lives over dP(t)'s first 64 columns, so S(t+1) does
+      // dP(t+1).  dS(t) lives over dP(t)'s columns, so S(t+1) does
       // not wait for dq(t); dP(t+1) is issued after dq(t) has been.
       BwdTracer tr;
       tr.init(p, 4, true);
@@ -994,14 +997,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1) attn_bwd_q_kernel(const __grid
       // masked: tiles crossing the causal diagonal and the ragged last key tile
       float pr[kBwdCols];
       if ((CAUSAL && t * kBN + kBN - 1 > m * kBM + off) || t * kBN + kBN > k_len)
-        q_p_half<true>(sr, l2, lim_key - t * kBN - c0, cl2, pr);
+        q_p_part<true>(sr, l2, lim_key - t * kBN - c0, cl2, pr);
       else
-        q_p_half<false>(sr, l2, 0, cl2, pr);
+        q_p_part<false>(sr, l2, 0, cl2, pr);
       tr.rec(22, t);
       if (!mbar_wait_warp(b_dp_full, t & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteODone))) { ok = false; break; }
       tr.rec(23, t);
       tc_fence_after();
-      ds_half<BF16>(t_dp, nullptr, di, pr);
+      ds_part<BF16>(t_dp, nullptr, di, pr);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
