@@ -101,9 +101,15 @@ def measured_peaks():
         return dict(FALLBACK_PEAK, bf16_tflops_sustained=1700.0, source="fallback")
 
 
+# the files the forward kernel and its launch are built from (the profile of
+# the forward kernel under profiles/ records their hash)
+FWD_SOURCES = ("attn_kernel.cuh", "attn_kernels.inc", "attn_kernels_d64.cu", "attn_kernels_d128.cu", "attn_params.h",
+               "attn_launch.h", "attn_host.cu", "attn_plan.cpp", "attn_plan.h", "ptx.cuh", "tmem_regs.cuh")
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "tiled_attention_attn_gb300", "csrc", "*"))):
+    for p in sorted(os.path.join(ROOT, "tiled_attention_attn_gb300", "csrc", f) for f in FWD_SOURCES):
         with open(p, "rb") as f:
             h.update(os.path.basename(p).encode())
             h.update(f.read())

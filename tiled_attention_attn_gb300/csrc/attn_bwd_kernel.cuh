@@ -304,7 +304,7 @@ __device__ __forceinline__ void store_row16(void* dst, const uint32_t (&x)[16], 
 }
 
 // ---------------------------------------------------------------------------
-// D_i = dout_i . O_i and lse in exp2 units, one (b, i, h) row per 8 threads;
+// D_i = dout_i . O_i and lse in exp2 units, one (b, h, i) row per 8 threads;
 // rows i in [Lq, Lq_pad) get the padding values.
 // ---------------------------------------------------------------------------
 template <int D, bool BF16>
@@ -323,10 +323,13 @@ __global__ void __launch_bounds__(256) attn_bwd_prep_kernel(const void* __restri
     const long long it_raw = base + ((threadIdx.x & 31) >> 3);
     const bool valid = it_raw < items;
     const long long it = valid ? it_raw : items - 1;
-    const int h = static_cast<int>(it % Hq);
-    const long long bi = it / Hq;
-    const int i = static_cast<int>(bi % Lq_pad);
-    const int b = static_cast<int>(bi / Lq_pad);
+    // (b, h, i) with i fastest: the lse reads and the lse2 / D writes of a
+    // warp are contiguous; each O / dO row is still read as whole 256-byte
+    // segments
+    const int i = static_cast<int>(it % Lq_pad);
+    const long long bh = it / Lq_pad;
+    const int h = static_cast<int>(bh % Hq);
+    const int b = static_cast<int>(bh / Hq);
     float acc = 0.0f;
     if (valid && i < Lq) {
       const size_t rb = ((static_cast<size_t>(b) * Lq + i) * Hq + h) * D + sub * kPer;
