@@ -11,17 +11,10 @@
 //   warps 4-7  softmax warpgroup for query sub-tile 1 (rows 128..255)
 //   warp 8     TMA producer: Q block once per unit, K and V tiles through one ring
 //   warp 9     TMEM allocator and single-thread tcgen05.mma issuer
-// TMEM (512 columns x 128 lanes, fp32): S_t at columns [128t, 128t+128).
-// d = 128: P_t (16-bit, two per column) overwrites the first 64 columns of
-// S_t and the accumulator u_t (= O before normalisation) is at
-// [256+128t, 256+128t+128); the S of tile j+1 is issued after the P.V of tile
-// j has read P.  d = 64: P_t has its own columns [256+64t, 256+64t+64) and u_t
-// is at [384+64t, 384+64t+64), so the S of tile j+1 is issued as soon as the
-// softmax warps have loaded S(j) (barrier s_free), and the softmax of tile
-// j+1 waits for P.V(j) (barrier p_free) only before it writes P and rescales
-// u: the softmax warps run back to back instead of waiting for P.V and the
-// next S at every tile.  Lane i of TMEM is query row i of a sub-tile, owned by
-// one softmax thread.
+// TMEM (512 columns x 128 lanes, fp32): S_t at columns [128t, 128t+128); P_t
+// (16-bit, two per column) overwrites the first 64 columns of S_t; the
+// accumulator u_t (= O before normalisation) at [256+128t, 256+128t+D).
+// Lane i of TMEM is query row i of a sub-tile, owned by one softmax thread.
 //
 // Rescaling of u is skipped while the running max grows by at most 2^8 in
 // exp2 units (the exponentials then stay <= 256); the final O = u / l uses
@@ -52,12 +45,8 @@ struct Cfg {
   static constexpr int kOffV = kOffK + kNS * kTile;
   static constexpr int kOffBar = kOffV + kNS * kTile;
   // barriers: q_full, q_empty, kv_full[NS], kv_empty[NS], s_full[2], p_full[2],
-  //           o_done[2], drain, s_free[2], p_free[2]
-  static constexpr int kNBars = 2 + 2 * kNS + 11;
-  // P in its own TMEM columns (see the file header)
-  static constexpr bool kSplitP = (D == 64);
-  __host__ __device__ static constexpr uint32_t col_p(int t) { return kSplitP ? 256 + 64 * t : 128 * t; }
-  __host__ __device__ static constexpr uint32_t col_o(int t) { return kSplitP ? 384 + 64 * t : 256 + 128 * t; }
+  //           o_done[2], drain
+  static constexpr int kNBars = 2 + 2 * kNS + 7;
   static constexpr int kOffMisc = kOffBar + kNBars * 8;   // tmem slot, abort flag, bad flag
   static constexpr int kOffVarlen = kOffMisc + 64;        // varlen unit prefix table
   static constexpr int kSmemDense = kOffVarlen + 1024;    // + alignment slack
@@ -190,14 +179,9 @@ struct RowState {
 // 2^8, rescales u in TMEM.  The previous tile's P.V has completed by then
 // (the commit that signalled this S was issued after it), and this tile's P.V
 // is issued only after this thread arrives.
-// SPLIT_P (d = 64): S is released (s_free) as soon as it is in registers,
-// and P is written to t_p, after waiting (when `pf_wait`) for the previous
-// P.V to have read the previous P (p_free, parity pf_par); returns false if
-// that wait ran out.  Otherwise t_p is S's own first columns.
-template <bool MASK, bool BF16, int D, bool SPLIT_P>
-__device__ __forceinline__ bool softmax_tile(uint32_t t_s, uint32_t t_p, uint32_t t_o, int lim, float c_log2,
-                                             RowState& st, bool first, uint32_t b_s_free, uint32_t b_p_free,
-                                             bool pf_wait, uint32_t pf_par, const WaitCtl& wc) {
+template <bool MASK, bool BF16, int D>
+__device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, int lim, float c_log2, RowState& st,
+                                             bool first) {
   // S in two halves: the second half loads while the first half's max is
   // taken.  Row max over eight chains of three-input max.
   float s[128];
@@ -226,11 +210,6 @@ __device__ __forceinline__ bool softmax_tile(uint32_t t_s, uint32_t t_p, uint32_
 #pragma unroll
     for (int i = 0; i < 64; ++i) s[64 + i] = __uint_as_float(r2[i]);
   }
-  if constexpr (SPLIT_P) {
-    tc_fence_before();
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(b_s_free);
-  }
   if constexpr (MASK) {
 #pragma unroll
     for (int i = 64; i < 128; ++i) s[i] = (i <= lim) ? s[i] : -INFINITY;
@@ -254,10 +233,6 @@ __device__ __forceinline__ bool softmax_tile(uint32_t t_s, uint32_t t_p, uint32_
   const float2 c2 = make_float2(c_log2, c_log2);
   const float2 nm2 = make_float2(-moff, -moff);
   float2 sum_a = make_float2(0.f, 0.f), sum_b = make_float2(0.f, 0.f);
-  if (SPLIT_P && pf_wait) {   // the previous P.V must have read the previous P (and updated u)
-    if (!mbar_wait_warp(b_p_free, pf_par, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSitePFull))) return false;
-    tc_fence_after();
-  }
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     uint32_t pk[16];
@@ -279,7 +254,7 @@ __device__ __forceinline__ bool softmax_tile(uint32_t t_s, uint32_t t_p, uint32_
       pk[i] = pack2<BF16>(e0.x, e0.y);
       pk[i + 1] = pack2<BF16>(e1.x, e1.y);
     }
-    tmem_st_32x32b_x16(t_p + q * 16, pk);
+    tmem_st_32x32b_x16(t_s + q * 16, pk);
   }
   // rescale l and, when anything is accumulated, u
   const float r = resc ? ((m_old == -INFINITY) ? 0.0f : ex2_approx(m_old - st.m)) : 1.0f;
@@ -297,7 +272,6 @@ __device__ __forceinline__ bool softmax_tile(uint32_t t_s, uint32_t t_p, uint32_
     }
   }
   tmem_wait_st();
-  return true;
 }
 
 // ---------------------------------------------------------------------------
@@ -328,8 +302,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   auto b_p_full = [&](int t) { return bar_sp + 16 + 8 * t; };
   auto b_o_done = [&](int t) { return bar_sp + 32 + 8 * t; };
   const uint32_t b_drain = bar_sp + 48;
-  auto b_s_free = [&](int t) { return bar_sp + 56 + 8 * t; };   // d = 64: the softmax has loaded S_t
-  auto b_p_free = [&](int t) { return bar_sp + 72 + 8 * t; };   // d = 64: P.V_t has read P_t
 
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
@@ -353,10 +325,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       mbar_init(b_o_done(t), 1);
     }
     mbar_init(b_drain, 1);
-    for (int t = 0; t < 2; ++t) {
-      mbar_init(b_s_free(t), kBM / 32);
-      mbar_init(b_p_free(t), 1);
-    }
     fence_mbar_init();
   }
   if (warp == kWarpMMA) {
@@ -489,15 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       tr.rec(kTagStart, 0, 0, 0);
       uint32_t q_cnt = 0, kv_cnt = 0;
       uint32_t p_cnt0 = 0, p_cnt1 = 0;
-      uint32_t sf_n[2] = {0, 0};   // d = 64: S issued per sub-tile so far (s_free phases)
-      auto issue_s = [&](int t, int st) -> bool {
-        if constexpr (C::kSplitP) {   // the softmax must have loaded the previous S_t
-          if (sf_n[t] > 0) {
-            if (!mbar_wait(b_s_free(t), (sf_n[t] - 1) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteSFull))) return false;
-            tc_fence_after();
-          }
-          ++sf_n[t];
-        }
+      auto issue_s = [&](int t, int st) {
         const uint64_t a0 = dq0 + ((t * C::kTile) >> 4);
         const uint64_t b0 = dk0 + ((st * C::kTile) >> 4);
 #pragma unroll
@@ -506,7 +466,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           umma_ss(tmem + t * 128, a0 + off, b0 + off, kIdescS, kk > 0 ? 1u : 0u);
         }
         umma_commit(b_s_full(t));
-        return true;
       };
       bool ok = true;
       for (int u = u_first; u < n_units && ok; u += u_step) {
@@ -521,12 +480,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           const int st = kv_cnt % C::kNS;
           if (!mbar_wait(b_kv_full(st), (kv_cnt / C::kNS) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull))) break;
           tr.rec(kTagKFull, 0, u, U.kv_begin);
-          for (int t = 0; t < kNSub && ok; ++t)
+          for (int t = 0; t < kNSub; ++t)
             if (unit_active(U, t, U.kv_begin)) {
-              ok = issue_s(t, st);
+              issue_s(t, st);
               tr.rec(kTagSIssue, t, u, U.kv_begin);
             }
-          if (!ok) break;
           umma_commit(b_kv_empty(st));
           ++kv_cnt;
         }
@@ -544,43 +502,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           }
           tr.rec(kTagVFull, 0, u, j);
           const bool have_next = j + 1 < U.kv_end;
-          if constexpr (C::kSplitP) {
-            // S_t(j+1) first (P_t(j) has its own columns), then P_t(j) V(j)
-#pragma unroll
-            for (int t = 0; t < kNSub; ++t)
-              if (ok && have_next && unit_active(U, t, j + 1)) {
-                ok = issue_s(t, st);
-                tr.rec(kTagSIssue, t, u, j + 1);
-              }
-            if (!ok) break;
-#pragma unroll
-            for (int t = 0; t < kNSub; ++t) {
-              uint32_t& p_cnt = (t == 0) ? p_cnt0 : p_cnt1;
-              bool& first_pv = (t == 0) ? first_pv0 : first_pv1;
-              if (!unit_active(U, t, j)) continue;
-              tr.rec(kTagPWait, t, u, j);
-              if (!mbar_wait(b_p_full(t), p_cnt & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSitePFull))) {
-                ok = false;
-                break;
-              }
-              ++p_cnt;
-              tc_fence_after();
-              tr.rec(kTagPFull, t, u, j);
-              const uint64_t bv = dv0 + ((st * C::kTile) >> 4);
-#pragma unroll
-              for (int kk = 0; kk < kBN / 16; ++kk)
-                umma_ts(tmem + C::col_o(t), tmem + C::col_p(t) + kk * 8, bv + ((kk * 2048) >> 4), kIdescO,
-                        (first_pv && kk == 0) ? 0u : 1u);
-              umma_commit(b_p_free(t));
-              if (!(have_next && unit_active(U, t, j + 1))) umma_commit(b_o_done(t));
-              tr.rec(kTagPVIssue, t, u, j);
-              first_pv = false;
-            }
-            if (!ok) break;
-            umma_commit(b_kv_empty(st));
-            ++kv_cnt;
-            continue;
-          }
 #pragma unroll
           for (int t = 0; t < kNSub; ++t) {
             uint32_t& p_cnt = (t == 0) ? p_cnt0 : p_cnt1;
@@ -600,14 +521,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
               const uint64_t bv = dv0 + ((st * C::kTile) >> 4);
 #pragma unroll
               for (int kk = 0; kk < kBN / 16; ++kk)
-                umma_ts(tmem + C::col_o(t), tmem + C::col_p(t) + kk * 8, bv + ((kk * 2048) >> 4), kIdescO,
+                umma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8, bv + ((kk * 2048) >> 4), kIdescO,
                         (first_pv && kk == 0) ? 0u : 1u);
               if (!next_s) umma_commit(b_o_done(t));
               tr.rec(kTagPVIssue, t, u, j);
               first_pv = false;
             }
             if (next_s) {
-              issue_s(t, st);   // d = 128: no wait inside, cannot fail
+              issue_s(t, st);
               tr.rec(kTagSIssue, t, u, j + 1);
             }
           }
@@ -631,9 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const int row = quarter * 32 + lane;     // row within the sub-tile
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t t_s = tmem + lane_off + t * 128;
-    const uint32_t t_p = tmem + lane_off + C::col_p(t);
-    const uint32_t t_o = tmem + lane_off + C::col_o(t);
-    uint32_t pf_k = 0;   // tiles this sub-tile's softmax has processed (p_free phases)
+    const uint32_t t_o = tmem + lane_off + 256 + t * 128;
     const float c_log2 = p.scale_log2;
     uint32_t s_cnt = 0, o_cnt = 0;   // s_full phases seen; units with an o_done commit
     T* out = reinterpret_cast<T*>(p.o);
@@ -661,16 +580,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         const int lim = lim_key - j * kBN;
         const bool mask_tile = (j * kBN + kBN - 1 > U.k_len - 1) ||
                                (CAUSAL && j * kBN + kBN - 1 > U.q_row0 + t * kBM + (U.k_len - U.q_len));
-        const bool okp =
-            mask_tile ? softmax_tile<true, BF16, D, C::kSplitP>(t_s, t_p, t_o, lim, c_log2, st, n_act == 0, b_s_free(t),
-                                                                b_p_free(t), pf_k > 0, (pf_k - 1) & 1, wc)
-                      : softmax_tile<false, BF16, D, C::kSplitP>(t_s, t_p, t_o, lim, c_log2, st, n_act == 0,
-                                                                 b_s_free(t), b_p_free(t), pf_k > 0, (pf_k - 1) & 1, wc);
-        if (!okp) {
-          ok = false;
-          break;
-        }
-        ++pf_k;
+        if (mask_tile)
+          softmax_tile<true, BF16, D>(t_s, t_o, lim, c_log2, st, n_act == 0);
+        else
+          softmax_tile<false, BF16, D>(t_s, t_o, lim, c_log2, st, n_act == 0);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(b_p_full(t));
