@@ -184,3 +184,40 @@ def test_backward_varlen_equals_dense_for_equal_lengths():
     assert attn.get_error() == attn.ATTN_OK
     for x, y in zip(a, b):
         assert torch.equal(flat(x), y)
+
+
+def test_autograd_function_matches_oracle():
+    """attn_func under torch.autograd: loss = sum(O * g) gives the oracle's
+    gradients (dense, GQA, causal) and the forward's O."""
+    B, Hq, Hkv, L, d = 1, 4, 2, 300, 64
+    q, k, v, g = make(B, Hq, Hkv, L, L, d, torch.bfloat16, seed=12)
+    dev = torch.device("cuda", 0)
+    qd, kd, vd = (t.to(dev).requires_grad_(True) for t in (q, k, v))
+    o = attn.attn_func(qd, kd, vd, causal=True)
+    (o.float() * g.to(dev).float()).sum().backward()
+    assert attn.get_error() == attn.ATTN_OK
+    rq, rk, rv = oracle.attention_backward(q, k, v, g, causal=True, scale=d ** -0.5)
+    check("dq", qd.grad.float().cpu().double().numpy(), rq)
+    check("dk", kd.grad.float().cpu().double().numpy(), rk)
+    check("dv", vd.grad.float().cpu().double().numpy(), rv)
+    o_ref, _ = oracle.attention(q, k, v, causal=True, scale=d ** -0.5)
+    assert float(np.abs(o.detach().float().cpu().double().numpy() - o_ref).max()) <= 1e-2
+
+
+def test_autograd_function_varlen():
+    lengths = [50, 200, 7]
+    Hq, Hkv, d = 2, 1, 128
+    gen = torch.Generator().manual_seed(13)
+    q = torch.randn(sum(lengths), Hq, d, generator=gen).to(torch.bfloat16)
+    k = torch.randn(sum(lengths), Hkv, d, generator=gen).to(torch.bfloat16)
+    v = torch.randn(sum(lengths), Hkv, d, generator=gen).to(torch.bfloat16)
+    g = torch.randn(sum(lengths), Hq, d, generator=gen).to(torch.bfloat16)
+    dev = torch.device("cuda", 0)
+    qd, kd, vd = (t.to(dev).requires_grad_(True) for t in (q, k, v))
+    o = attn.attn_func(qd, kd, vd, causal=True, cu_seqlens=cu_of(lengths).to(dev))
+    (o.float() * g.to(dev).float()).sum().backward()
+    assert attn.get_error() == attn.ATTN_OK
+    rq, rk, rv = oracle.varlen_attention_backward(q, k, v, g, lengths, lengths, causal=True, scale=d ** -0.5)
+    check("dq", qd.grad.float().cpu().double().numpy(), rq)
+    check("dk", kd.grad.float().cpu().double().numpy(), rk)
+    check("dv", vd.grad.float().cpu().double().numpy(), rv)

@@ -263,6 +263,39 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tenso
 # and the row gather / scatter kernels)
 # ---------------------------------------------------------------------------
 
+class _AttnFunction(torch.autograd.Function):
+    """attn_fwd in the forward, attn_bwd in the backward (the lse the forward
+    returns is what the backward recomputes the weights from)."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, causal, scale, cu_seqlens, cu_seqlens_k):
+        o, lse = attn_fwd(q, k, v, causal=causal, scale=scale, cu_seqlens=cu_seqlens, cu_seqlens_k=cu_seqlens_k)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.causal, ctx.scale, ctx.cu, ctx.cu_k = causal, scale, cu_seqlens, cu_seqlens_k
+        ctx.mark_non_differentiable(lse)
+        return o, lse
+
+    @staticmethod
+    def backward(ctx, do, dlse):
+        q, k, v, o, lse = ctx.saved_tensors
+        dq, dk, dv = attn_bwd(q, k, v, o, lse, do.contiguous(), causal=ctx.causal, scale=ctx.scale,
+                              cu_seqlens=ctx.cu, cu_seqlens_k=ctx.cu_k)
+        return dq, dk, dv, None, None, None, None
+
+
+def attn_func(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+              scale: Optional[float] = None, cu_seqlens: Optional[torch.Tensor] = None,
+              cu_seqlens_k: Optional[torch.Tensor] = None, return_lse: bool = False):
+    """Differentiable attention: O = softmax(scale Q K^T [+ causal]) V with
+    gradients for q, k and v through attn_bwd.  Shapes and arguments as
+    attn_fwd (dense or varlen); returns O, or (O, lse) with ``return_lse``
+    (lse carries no gradient)."""
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    o, lse = _AttnFunction.apply(q, k, v, bool(causal), float(scale), cu_seqlens, cu_seqlens_k)
+    return (o, lse) if return_lse else o
+
+
 def _check_cuda(*ts):
     for t in ts:
         if not t.is_cuda or not t.is_contiguous():
