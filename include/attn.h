@@ -158,7 +158,9 @@ int attn_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float
  * are (total_k, Hkv, d); sequence b has queries cu_seqlens_q[b] ..
  * cu_seqlens_q[b+1] - 1 and keys cu_seqlens_k[b] .. cu_seqlens_k[b+1] - 1 (both
  * device int32 arrays of B+1 entries, 0 first, non-decreasing, last entry
- * at most the total; checked by the kernel as for attn_fwd).  Causal aligns
+ * at most the total; checked by the kernel as for attn_fwd; rows past the
+ * last sequence, up to the next 128-row boundary, are loaded with whole tiles
+ * and weighted by zero, so they must hold finite values).  Causal aligns
  * bottom-right per sequence: query i of a sequence with Lq_b queries and Lk_b
  * keys sees key j iff j <= i + Lk_b - Lq_b (the queries are the last Lq_b
  * positions, as when a cache of Lk_b - Lq_b tokens precedes them); a query
@@ -271,11 +273,14 @@ int attn_rotary_packed(const void *x, void *y, int B, int L, int h_total, int h_
  *   Returns ATTN_EINVAL (null pointer, B or L <= 0, B*L >= 2^31) or
  *   ATTN_ELAUNCH.
  *
- * attn_gather_rows -- dst row r = src row indices[r] for r < min(n_max,
+ * attn_gather_rows -- dst row r = src row indices[r] for r < n = min(n_max,
  *   *n_dev) (n_dev is a DEVICE int, e.g. cu_seqlens + B, so no host sync
- *   is needed; dst must hold n_max rows).  Rows are row_bytes long (a
- *   multiple of 16); src has src_rows rows and an index outside
- *   [0, src_rows) moves nothing.  src and dst 16-byte aligned.
+ *   is needed; dst must hold n_max rows).  Rows n .. n+127 of dst (those
+ *   below n_max) are set to zero: the attention kernels load whole 128-row
+ *   tiles, so the rows just past the last sequence are read (and weighted by
+ *   zero, which needs them finite).  Rows are row_bytes long (a multiple of
+ *   16); src has src_rows rows and an index outside [0, src_rows) moves
+ *   nothing.  src and dst 16-byte aligned.
  *
  * attn_scatter_rows -- dst row indices[r] = src row r for r < min(n_max,
  *   *n_dev); dst has dst_rows rows (indices outside are skipped) and its

@@ -81,16 +81,19 @@ def test_gather_scatter_bitexact(dtype):
 
 
 def test_row_count_comes_from_the_device():
-    # rows at and past the device count are neither read nor written
+    # the row count is read on the device; the gather zeroes the 128 rows
+    # after it (the tile the attention kernels read past the last sequence)
+    # and leaves the rows beyond those alone
     dev = torch.device("cuda", 0)
-    src = torch.arange(64 * 8, dtype=torch.float32, device=dev).view(64, 8)
-    idx = torch.arange(63, -1, -1, dtype=torch.int32, device=dev)
+    src = torch.arange(300 * 8, dtype=torch.float32, device=dev).view(300, 8)
+    idx = torch.arange(299, -1, -1, dtype=torch.int32, device=dev)
     n_dev = torch.tensor([10], dtype=torch.int32, device=dev)
-    out = torch.full((64, 8), -1.0, device=dev)
-    attn.gather_rows(src, idx, n_dev, 64, out=out)
+    out = torch.full((300, 8), -1.0, device=dev)
+    attn.gather_rows(src, idx, n_dev, 300, out=out)
     torch.cuda.synchronize()
-    exp = torch.full((64, 8), -1.0)
-    exp[:10] = src.cpu()[63 - torch.arange(10)]
+    exp = torch.full((300, 8), -1.0)
+    exp[:10] = src.cpu()[299 - torch.arange(10)]
+    exp[10:138] = 0.0
     assert torch.equal(out.cpu(), exp)
     # an index outside the padded side moves nothing
     bad = torch.tensor([0, 70, -3, 5], dtype=torch.int32, device=dev)
@@ -169,3 +172,39 @@ def test_padded_forward_holes_gqa(causal):
     assert attn.get_error() == attn.ATTN_OK
     o_ref, lse_ref = oracle.padded_attention(q, k, v, mask.numpy(), causal=causal)
     check_padded(o, lse, o_ref, lse_ref, mask)
+
+
+def test_padded_autograd_matches_oracle_with_poisoned_memory():
+    """attn_func_padded forward and backward against the oracle's padded
+    attention and backward (key-padding mask), after the caching allocator's
+    memory was filled with NaN: the packed buffers past the kept rows must
+    not leak into the results (the gather zeroes the tile past them)."""
+    dev = torch.device("cuda", 0)
+    poison = torch.full((64 << 20,), float("nan"), dtype=torch.float32, device=dev)
+    del poison
+    B, L, Hq, Hkv, d = 3, 200, 4, 2, 64
+    g = torch.Generator().manual_seed(21)
+    q = torch.randn(B, L, Hq, d, generator=g).to(torch.bfloat16)
+    k = torch.randn(B, L, Hkv, d, generator=g).to(torch.bfloat16)
+    v = torch.randn(B, L, Hkv, d, generator=g).to(torch.bfloat16)
+    go = torch.randn(B, L, Hq, d, generator=g).to(torch.bfloat16)
+    lengths = [200, 131, 57]
+    mask = torch.zeros(B, L, dtype=torch.bool)
+    for b, n in enumerate(lengths):
+        mask[b, :n] = True
+    qd, kd, vd = (t.to(dev).requires_grad_(True) for t in (q, k, v))
+    o = attn.attn_func_padded(qd, kd, vd, mask.to(dev), causal=True)
+    (o.float() * go.to(dev).float()).sum().backward()
+    assert attn.get_error() == attn.ATTN_OK
+    o_ref, _ = oracle.padded_attention(q, k, v, mask.numpy(), causal=True, scale=d ** -0.5)
+    o_np = o.detach().float().cpu().double().numpy()
+    assert np.all(np.isfinite(o_np)) and float(np.abs(o_np - o_ref).max()) <= 1e-2
+    go_masked = go.clone()
+    go_masked[~mask] = 0   # O is zero at padded positions, so they carry no gradient
+    rq, rk, rv = oracle.attention_backward(q, k, v, go_masked, causal=True, scale=d ** -0.5,
+                                           key_padding_mask=mask.numpy().astype(np.uint8))
+    for name, x, r in (("dq", qd.grad, rq), ("dk", kd.grad, rk), ("dv", vd.grad, rv)):
+        x = x.float().cpu().double().numpy()
+        assert np.all(np.isfinite(x)), name
+        assert float(np.abs(x - r).max()) <= 2.0 ** -6 * float(np.abs(r).max()) + 1e-6, name
+        assert np.all(x[~mask.numpy()] == 0.0), name

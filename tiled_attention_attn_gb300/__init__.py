@@ -10,6 +10,7 @@ from .attn import (  # noqa: F401
     AttnError,
     attn_bwd,
     attn_func,
+    attn_func_padded,
     attn_fwd,
     get_error,
     last_device_error,

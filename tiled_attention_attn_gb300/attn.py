@@ -398,6 +398,61 @@ def attn_fwd_padded(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, key_paddi
     return o, lse
 
 
+class _PaddedAttnFunction(torch.autograd.Function):
+    """The padded module's path with gradients (training page §2.5): gather
+    the kept tokens, the varlen forward, scatter O back; the backward
+    gathers dO, runs the varlen backward and scatters dq, dk, dv (zero at
+    padded positions)."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, key_padding_mask, causal, scale):
+        B, L, Hq, d = q.shape
+        Hkv = k.shape[2]
+        cu, idx = unpad_index(key_padding_mask)
+        n_dev = cu[B:]
+        N = B * L
+        qp = gather_rows(q.view(N, Hq, d), idx, n_dev, N)
+        kp = gather_rows(k.view(N, Hkv, d), idx, n_dev, N)
+        vp = gather_rows(v.view(N, Hkv, d), idx, n_dev, N)
+        op, lsep = attn_fwd(qp, kp, vp, causal=causal, scale=scale, cu_seqlens=cu)
+        o = torch.zeros_like(q)
+        scatter_rows(op, idx, n_dev, o.view(N, Hq, d))
+        lse = torch.full((B, Hq, L), float("-inf"), dtype=torch.float32, device=q.device)
+        scatter_lse(lsep, idx, n_dev, lse)
+        ctx.save_for_backward(qp, kp, vp, op, lsep, cu, idx)
+        ctx.causal, ctx.scale, ctx.shape = causal, scale, (B, L, Hq, Hkv, d)
+        ctx.mark_non_differentiable(lse)
+        return o, lse
+
+    @staticmethod
+    def backward(ctx, do, dlse):
+        qp, kp, vp, op, lsep, cu, idx = ctx.saved_tensors
+        B, L, Hq, Hkv, d = ctx.shape
+        N, n_dev = B * L, cu[B:]
+        dop = gather_rows(do.contiguous().view(N, Hq, d), idx, n_dev, N)
+        dqp, dkp, dvp = attn_bwd(qp, kp, vp, op, lsep, dop, causal=ctx.causal, scale=ctx.scale, cu_seqlens=cu)
+        grads = []
+        for gp, H in ((dqp, Hq), (dkp, Hkv), (dvp, Hkv)):
+            g = torch.zeros((B, L, H, d), dtype=gp.dtype, device=gp.device)
+            scatter_rows(gp, idx, n_dev, g.view(N, H, d))
+            grads.append(g)
+        return grads[0], grads[1], grads[2], None, None, None
+
+
+def attn_func_padded(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, key_padding_mask: torch.Tensor,
+                     causal: bool = False, scale: Optional[float] = None, return_lse: bool = False):
+    """attn_fwd_padded with gradients for q, k and v: q (B, L, Hq, d), k, v
+    (B, L, Hkv, d), key_padding_mask (B, L) with True = keep.  Padded
+    positions get O = 0 and no gradient."""
+    B, L, Hq, d = q.shape
+    if k.shape != (B, L, k.shape[2], d) or v.shape != k.shape or tuple(key_padding_mask.shape) != (B, L):
+        raise ValueError("q (B, L, Hq, d), k and v (B, L, Hkv, d), key_padding_mask (B, L)")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o, lse = _PaddedAttnFunction.apply(q, k, v, key_padding_mask, bool(causal), float(scale))
+    return (o, lse) if return_lse else o
+
+
 def rotary(x: torch.Tensor, rot_dim: Optional[int] = None, base: float = 10000.0, interleaved: bool = False,
            cu_seqlens: Optional[torch.Tensor] = None, offsets: Optional[torch.Tensor] = None,
            out: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:

@@ -107,18 +107,25 @@ __global__ void __launch_bounds__(kThreads) index_rows_kernel(const uint8_t* __r
 }
 
 // dst row r = src row idx[r] (gather) or dst row idx[r] = src row r
-// (scatter), for r < min(n_max, *n_dev); rows are `cpr` 16-byte words.  An
-// index outside [0, n_other) (the padded side's row count) moves nothing.
+// (scatter), for r < n = min(n_max, *n_dev); rows are `cpr` 16-byte words.
+// An index outside [0, n_other) (the padded side's row count) moves nothing.
+// The gather also zeroes dst rows n .. n+127 below n_max (a tile's worth past
+// the last packed row, which the attention kernels read and weight by zero).
 template <bool SCATTER>
 __global__ void __launch_bounds__(kThreads) move_rows_kernel(const uint4* __restrict__ src, const int* __restrict__ idx,
                                                              int n_max, const int* __restrict__ n_dev, int n_other,
                                                              int cpr, uint4* __restrict__ dst) {
-  const int n = min(n_max, __ldg(n_dev));
-  const long long words = static_cast<long long>(n) * cpr;
+  const int n = max(0, min(n_max, __ldg(n_dev)));
+  const int n_zero = SCATTER ? n : min(n_max, n + 128);
+  const long long words = static_cast<long long>(n_zero) * cpr;
   for (long long x = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; x < words;
        x += static_cast<long long>(gridDim.x) * kThreads) {
     const long long r = x / cpr;
     const int c = static_cast<int>(x - r * cpr);
+    if (!SCATTER && r >= n) {
+      dst[r * cpr + c] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
     const long long other = __ldg(idx + r);
     if (other < 0 || other >= n_other) continue;
     if (SCATTER)
