@@ -651,6 +651,9 @@ def run_ours(args, wl):
             "config": dict(workload_config(wl, inp.lengths), parallelism=f"replicas x{world}",
                            l2="256 MiB buffer written before every step, outside the per-step CUDA events"),
             "pct_of_peak": 100.0 * value / world / peaks["bf16_tflops"],
+            "pct_of_sustained_peak": 100.0 * value / world / peaks["bf16_tflops_sustained"],
+            "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "mean": total_ms / K,
+                        "per_rank_events": "one CUDA-event pair per step on the launching stream"},
             "clocks": clocks, "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
             "cpu_baseline": cpu, "pad_unpad": pad, "kv_cache": cache, "rotary": rot, "backward": bwd,
         }
