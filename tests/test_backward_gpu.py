@@ -71,6 +71,7 @@ CASES = [
     (1, 2, 1, 1, 1, 64, False, torch.bfloat16),          # one query, one key
     (1, 4, 1, 513, 129, 128, False, torch.float16),
     (2, 2, 2, 640, 640, 128, True, torch.bfloat16),      # several tiles on both sides
+    (1, 8, 1, 200, 200, 64, True, torch.bfloat16),       # eight query heads per KV head
 ]
 
 
@@ -88,6 +89,16 @@ def test_backward_matches_oracle(case):
         # queries that see no key get no gradient
         blind = np.arange(Lq) + (Lk - Lq) < 0
         assert np.all(dq[:, blind] == 0.0)
+
+
+def test_backward_zero_scale():
+    # scale 0: uniform weights; dq and dk vanish, dv spreads dout evenly (a
+    # closed form the oracle is pinned to)
+    q, k, v, do = make(1, 2, 1, 150, 150, 128, torch.bfloat16, seed=8)
+    dq, dk, dv = gpu_grads(q, k, v, do, False, 0.0)
+    rq, rk, rv = oracle.attention_backward(q, k, v, do, causal=False, scale=0.0)
+    assert np.abs(dq).max() == 0.0 and np.abs(dk).max() == 0.0
+    check("dv", dv, rv)
 
 
 def test_backward_is_deterministic():
@@ -140,6 +151,7 @@ VARLEN = [
     ([64, 200, 5, 256], [764, 233, 1005, 256], 4, 4, 128, True, torch.bfloat16),   # queries after a cache
     ([300, 20, 130], [100, 0, 130], 2, 1, 64, True, torch.float16),                 # keys < queries, no keys
     ([0, 17, 0, 400], [50, 3, 0, 300], 2, 2, 128, False, torch.bfloat16),          # empty sequences
+    ([777], None, 2, 2, 64, True, torch.float16),                                   # one sequence
 ]
 
 
