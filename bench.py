@@ -481,10 +481,43 @@ def bwd_leg(attn, device, stream, peaks, iters: int = 10):
     fwd_flops = 4.0 * d * Hq * B * L * L / 2
     flops = 2.5 * fwd_flops
     tf = flops / (t / 1e3) / 1e12
-    return {"workload": f"backward: B{B} Hq{Hq} Hkv{Hkv} L{L} d{d} bf16 causal", "value": tf, "unit": "TFLOP/s",
-            "frac": tf / peaks["bf16_tflops"], "ms": t, "algorithmic_flops_per_call": flops,
-            "executed_flops_per_call": 3.5 * fwd_flops,
-            "executed_tflops": 3.5 * fwd_flops / (t / 1e3) / 1e12}
+    out = {"workload": f"backward: B{B} Hq{Hq} Hkv{Hkv} L{L} d{d} bf16 causal", "value": tf, "unit": "TFLOP/s",
+           "frac": tf / peaks["bf16_tflops"], "ms": t, "algorithmic_flops_per_call": flops,
+           "executed_flops_per_call": 3.5 * fwd_flops,
+           "executed_tflops": 3.5 * fwd_flops / (t / 1e3) / 1e12}
+    del q, k, v, do, o, lse, dq, dk, dv
+    # the packed (varlen) backward: 8 sequences of U[1024, 4096] tokens, same heads and d;
+    # FLOPs 10 d Hq per allowed pair, counted exactly (causal: L_b (L_b + 1) / 2 pairs)
+    lens = torch.randint(1024, 4097, (8,), generator=g)
+    tot = int(lens.sum())
+    qv = torch.randn(tot, Hq, d, generator=g).to(torch.bfloat16).to(device)
+    kv = torch.randn(tot, Hkv, d, generator=g).to(torch.bfloat16).to(device)
+    vv = torch.randn(tot, Hkv, d, generator=g).to(torch.bfloat16).to(device)
+    dov = torch.randn(tot, Hq, d, generator=g).to(torch.bfloat16).to(device)
+    cu = torch.tensor([0] + torch.cumsum(lens, 0).tolist(), dtype=torch.int32, device=device)
+    ov, lsev = attn.attn_fwd(qv, kv, vv, causal=True, cu_seqlens=cu, stream=stream)
+    grads = attn.attn_bwd(qv, kv, vv, ov, lsev, dov, causal=True, cu_seqlens=cu, stream=stream)
+    torch.cuda.synchronize(device)
+    msv = []
+    for _ in range(iters):
+        flush.zero_()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        attn.attn_bwd(qv, kv, vv, ov, lsev, dov, causal=True, cu_seqlens=cu, dq=grads[0], dk=grads[1], dv=grads[2],
+                      stream=stream)
+        e.record(stream)
+        torch.cuda.synchronize(device)
+        msv.append(s.elapsed_time(e))
+    if attn.get_error() != attn.ATTN_OK:
+        raise RuntimeError(f"device error in the varlen backward leg: {attn.last_device_error():#x}")
+    tv = statistics.median(msv)
+    pairs = sum(int(n) * (int(n) + 1) // 2 for n in lens)
+    fv = 10.0 * d * Hq * pairs
+    out["varlen"] = {"workload": f"varlen backward: 8 sequences of U[1024,4096] ({tot} tokens), Hq{Hq} Hkv{Hkv} "
+                                 f"d{d} bf16 causal", "value": fv / (tv / 1e3) / 1e12, "unit": "TFLOP/s",
+                     "frac": fv / (tv / 1e3) / 1e12 / peaks["bf16_tflops"], "ms": tv,
+                     "algorithmic_flops_per_call": fv}
+    return out
 
 
 def run_ours(args, wl):
