@@ -107,3 +107,9 @@ def test_backward_varlen_needs_both_offsets(attn_lib):
     assert attn_lib.attn_bwd_varlen(*args, None, 16, 0, None) == attn.ATTN_EINVAL
     assert attn_lib.attn_bwd_varlen(*args, 16, None, 0, None) == attn.ATTN_EINVAL
     assert attn_lib.attn_bwd_varlen(*args, 16, 16, 2, None) == attn.ATTN_EINVAL
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    # no CPU or library fallback: without the built library the binding raises
+    with pytest.raises(RuntimeError, match="missing"):
+        attn.lib(str(tmp_path / "libattn_absent.so"))
