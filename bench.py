@@ -520,6 +520,45 @@ def bwd_leg(attn, device, stream, peaks, iters: int = 10):
     return out
 
 
+DECODE_SHAPE = (32, 32, 8, 128, 4096)   # B, Hq, Hkv, d, cache length of the decode leg
+
+
+def decode_leg(attn, device, stream, peaks, iters: int = 20):
+    """One new token per sequence over a key/value cache (the generation step
+    of the training page §4.3) through attn_fwd_varlen: B 32 sequences, Hq 32,
+    Hkv 8, d 128, bf16, cache 4096 + the new token, causal (bottom-right).
+    Memory-bound: the reported rate is the cache bytes read (K and V once) per
+    second against the HBM copy peak.  There is no decode-specific kernel: a
+    one-row query runs as a 256-row block, so this measures the general path."""
+    B, Hq, Hkv, d, C = DECODE_SHAPE
+    g = torch.Generator().manual_seed(66)
+    q = torch.randn(B, Hq, d, generator=g).to(torch.bfloat16).to(device)
+    k = torch.randn(B * (C + 1), Hkv, d, generator=g).to(torch.bfloat16).to(device)
+    v = torch.randn(B * (C + 1), Hkv, d, generator=g).to(torch.bfloat16).to(device)
+    cu_q = torch.arange(0, B + 1, dtype=torch.int32, device=device)
+    cu_k = torch.arange(0, B + 1, dtype=torch.int32, device=device) * (C + 1)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    o, lse = attn.attn_fwd(q, k, v, causal=True, cu_seqlens=cu_q, cu_seqlens_k=cu_k, stream=stream)
+    torch.cuda.synchronize(device)
+    ms = []
+    for _ in range(iters):
+        flush.zero_()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        attn.attn_fwd(q, k, v, causal=True, cu_seqlens=cu_q, cu_seqlens_k=cu_k, out=o, lse=lse, stream=stream)
+        e.record(stream)
+        torch.cuda.synchronize(device)
+        ms.append(s.elapsed_time(e))
+    if attn.get_error() != attn.ATTN_OK:
+        raise RuntimeError(f"device error in the decode leg: {attn.last_device_error():#x}")
+    t = statistics.median(ms)
+    kv_bytes = 2 * k.numel() * k.element_size()
+    gbs = kv_bytes / (t / 1e3) / 1e9
+    return {"workload": f"decode: B{B} Hq{Hq} Hkv{Hkv} d{d} bf16, 1 new token over a {C}-token cache",
+            "bound": "hbm", "achieved": gbs, "unit": "GB/s", "peak": peaks["hbm_gbs"],
+            "frac": gbs / peaks["hbm_gbs"], "ms": t, "cache_bytes_per_call": kv_bytes}
+
+
 def run_ours(args, wl):
     from tiled_attention_attn_gb300 import attn, build
 
@@ -548,6 +587,7 @@ def run_ours(args, wl):
             print(json.dumps({"pad_unpad": pad_leg(attn, device, stream, peaks),
                               "kv_cache": cache_leg(attn, device, stream, peaks),
                               "rotary": rotary_leg(attn, device, stream, peaks),
+                              "decode": decode_leg(attn, device, stream, peaks),
                               "backward": bwd_leg(attn, device, stream, peaks)}), flush=True)
         return 0
 
@@ -662,10 +702,11 @@ def run_ours(args, wl):
         raise RuntimeError(f"device error in the e2e leg: {attn.last_device_error():#x}")
 
     # ---- padded batches: unpad index and row gather / scatter (HBM-bound)
-    pad = cache = rot = bwd = None
+    pad = cache = rot = bwd = dec = None
     if not args.no_pad_leg:
         pad = pad_leg(attn, device, stream, peaks)
         cache = cache_leg(attn, device, stream, peaks)
+        dec = decode_leg(attn, device, stream, peaks)
         bwd = bwd_leg(attn, device, stream, peaks)
         rot = rotary_leg(attn, device, stream, peaks)
 
@@ -688,7 +729,7 @@ def run_ours(args, wl):
             "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "mean": total_ms / K,
                         "per_rank_events": "one CUDA-event pair per step on the launching stream"},
             "clocks": clocks, "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
-            "cpu_baseline": cpu, "pad_unpad": pad, "kv_cache": cache, "rotary": rot, "backward": bwd,
+            "cpu_baseline": cpu, "pad_unpad": pad, "kv_cache": cache, "rotary": rot, "backward": bwd, "decode": dec,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
