@@ -166,6 +166,14 @@ int attn_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float
  * positions, as when a cache of Lk_b - Lq_b tokens precedes them); a query
  * that sees no key gives O = 0, lse = -inf.  lse is (Hq, total_q).  fp16 = 0
  * selects bf16 tensors, 1 fp16.  B <= 4096.  Return codes as attn_fwd.
+ *
+ * Grouped heads: when Hq / Hkv is a power of two from 2 to 32, every packed
+ * forward (this entry point and attn_fwd with cu_seqlens) lets the query
+ * heads of one key/value head share a tile: 128 / group positions x group
+ * heads instead of 128 positions of one head.  Each key/value tile is then
+ * read once per group, and a sequence with one new token (decoding) fills
+ * group rows of a tile instead of one.  Every output row is the same
+ * function of its inputs either way.
  */
 int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv,
                     int total_q, int total_k, int d, int causal, float scale, const int *cu_seqlens_q,

@@ -56,6 +56,12 @@ CASES = [
     ([300, 20, 130], [100, 0, 130], 2, 1, 64, True, torch.float16),                   # keys < queries, no keys
     ([0, 17, 0], [50, 3, 0], 2, 2, 128, False, torch.bfloat16),                       # empty sequences
     ([1, 1, 1, 1], [900, 1, 2000, 33], 8, 2, 128, True, torch.bfloat16),              # one new token per sequence
+    # grouped heads sharing a tile (group 2..32: 64..4 queries x group heads per 128 rows)
+    ([1, 2, 17, 16, 33, 0], [1, 700, 17, 300, 4000, 9], 16, 2, 128, True, torch.bfloat16),   # group 8
+    ([5, 8, 9, 0, 70], [300, 8, 1, 40, 70], 32, 2, 64, False, torch.float16),           # group 16, d 64
+    ([1, 3, 4, 5, 130], [2000, 3, 500, 129, 130], 32, 1, 128, True, torch.bfloat16),    # group 32 (one kv head)
+    ([64, 65, 200, 1], [64, 1000, 200, 257], 8, 2, 128, True, torch.bfloat16),         # group 4 over several blocks
+    ([1, 7, 40], [1000, 7, 300], 6, 2, 128, True, torch.bfloat16),                     # group 3: one head per tile
 ]
 
 

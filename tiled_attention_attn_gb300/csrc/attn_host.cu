@@ -82,7 +82,7 @@ bool get_encode() {
   return true;
 }
 
-using MapKey = std::tuple<uintptr_t, int, int, int, int, int>;   // ptr, dtype, d, H, L, B
+using MapKey = std::tuple<uintptr_t, int, int, int, int, int, int>;   // ptr, dtype, d, H, L, B, box heads
 using PlanKey = std::tuple<int, int, int, int, int, int, int>;   // B, Hq, Hkv, Lq, Lk, d, causal
 
 struct DevPlan {
@@ -120,9 +120,10 @@ int init_device(int dev, DevState& st) {
 }
 
 // 4-D map over (d, H, L, B) for a contiguous (B, L, H, d) 16-bit tensor,
-// box 64 x 1 x 128 x 1 (one 128-byte swizzle atom wide, 128 rows high).
-int get_map(DevState& st, const void* ptr, bool bf16, int d, int H, int L, int B, CUtensorMap& out) {
-  const MapKey key{reinterpret_cast<uintptr_t>(ptr), bf16 ? 1 : 0, d, H, L, B};
+// box 64 x box_h x (128 / box_h) x 1: one 128-byte swizzle atom wide and 128
+// shared-memory rows high, rows ordered (position, head) with the head fastest.
+int get_map(DevState& st, const void* ptr, bool bf16, int d, int H, int L, int B, CUtensorMap& out, int box_h = 1) {
+  const MapKey key{reinterpret_cast<uintptr_t>(ptr), bf16 ? 1 : 0, d, H, L, B, box_h};
   auto it = st.maps.find(key);
   if (it != st.maps.end()) {
     out = it->second;
@@ -133,7 +134,7 @@ int get_map(DevState& st, const void* ptr, bool bf16, int d, int H, int L, int B
                               static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(B)};
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(H) * d * 2,
                                  static_cast<cuuint64_t>(L) * H * d * 2};
-  const cuuint32_t box[4] = {64, 1, static_cast<cuuint32_t>(kBM), 1};
+  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_h), static_cast<cuuint32_t>(kBM / box_h), 1};
   const cuuint32_t es[4] = {1, 1, 1, 1};
   const CUresult r = g_encode(&m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
                               const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -248,7 +249,16 @@ int fwd(bool bf16, const void* q, const void* k, const void* v, void* o, float* 
   std::memset(&p, 0, sizeof(p));
   const int Lk_map = Lk > 0 ? Lk : 1;
   const int Bm = varlen ? 1 : B;
-  if ((rc = get_map(st, q, bf16, d, Hq, Lq, Bm, p.tm_q))) return rc;
+  // Packed sequences with grouped heads: the group's query heads share each
+  // tile (128 / group positions x group heads), so a key/value tile is read
+  // once per group instead of once per head, and a short query (one decode
+  // token) fills group rows of the tile instead of one.  Never more units
+  // than one head per tile; a group of 2 to 32 heads, a power of two.
+  const int group = Hq / Hkv;
+  int pack_log2 = 0;
+  if (varlen && group >= 2 && group <= 32 && (group & (group - 1)) == 0)
+    while ((1 << pack_log2) < group) ++pack_log2;
+  if ((rc = get_map(st, q, bf16, d, Hq, Lq, Bm, p.tm_q, 1 << pack_log2))) return rc;
   if ((rc = get_map(st, k, bf16, d, Hkv, Lk_map, Bm, p.tm_k))) return rc;
   if ((rc = get_map(st, v, bf16, d, Hkv, Lk_map, Bm, p.tm_v))) return rc;
   p.o = o;
@@ -264,7 +274,8 @@ int fwd(bool bf16, const void* q, const void* k, const void* v, void* o, float* 
   p.Hkv = Hkv;
   p.Lq = Lq;
   p.Lk = Lk;
-  p.group = Hq / Hkv;
+  p.group = group;
+  p.pack_log2 = pack_log2;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
 
@@ -288,7 +299,8 @@ int fwd(bool bf16, const void* q, const void* k, const void* v, void* o, float* 
     }
     grid = plan->host.n_ctas;
   } else {
-    // units = sum over sequences of Hq * ceil(len / 256) <= Hq * (B + ceil(total / 256))
+    // units = sum over sequences of Hq * ceil(len / 256) <= Hq * (B + ceil(total / 256));
+    // packed heads give (Hq / g) * ceil(len * g / 256), never more
     const long long bound = static_cast<long long>(Hq) * (B + (Lq + kBlockRows - 1) / kBlockRows);
     grid = static_cast<int>(std::min<long long>(st.sm_count, bound));
   }

@@ -105,10 +105,14 @@ __device__ __forceinline__ bool decode_unit(const FwdParams& p, const int* vl_pr
       if (vl_pref[mid] <= u) lo = mid; else hi = mid;
     }
     U.b = lo;
+    // units of a sequence: (query block, head group) with the group fastest;
+    // a group is one head, or the 2^pack_log2 heads sharing a key/value head
+    const int lp = p.pack_log2;
+    const int n_hu = p.Hq >> lp;
     const int local = u - vl_pref[lo];
-    const int mb = local / p.Hq;
-    U.h = local - mb * p.Hq;
-    U.q_row0 = mb * kBlockRows;
+    const int mb = local / n_hu;
+    U.h = (local - mb * n_hu) << lp;   // first query head of the unit
+    U.q_row0 = mb * (kBlockRows >> lp);
     const int s0 = __ldg(p.cu_seqlens + lo);
     const int len = __ldg(p.cu_seqlens + lo + 1) - s0;
     const int s0k = __ldg(p.cu_seqlens_k + lo);
@@ -124,8 +128,9 @@ __device__ __forceinline__ bool decode_unit(const FwdParams& p, const int* vl_pr
     U.kv_end = 0;
   }
   U.g = U.h / p.group;
-  U.kv_last[0] = kv_last_tile(U.q_row0, 0, U.q_len, U.k_len, CAUSAL);
-  U.kv_last[1] = kv_last_tile(U.q_row0, 1, U.q_len, U.k_len, CAUSAL);
+  const int span = VARLEN ? (kBM >> p.pack_log2) : kBM;   // queries per sub-tile
+  U.kv_last[0] = kv_last_tile(U.q_row0, 0, U.q_len, U.k_len, CAUSAL, span);
+  U.kv_last[1] = kv_last_tile(U.q_row0, 1, U.q_len, U.k_len, CAUSAL, span);
   const int end = max(U.kv_last[0], U.kv_last[1]) + 1;
   if constexpr (VARLEN) {
     U.kv_end = end;
@@ -353,7 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           const int ak = __ldg(p.cu_seqlens_k + b), ek = __ldg(p.cu_seqlens_k + b + 1);
           if (e < a || e > p.Lq || ek < ak || ek > p.Lk) bad = true;
           const int len = e - a;
-          cnt = (len > 0) ? ((len + kBlockRows - 1) / kBlockRows) * p.Hq : 0;
+          const int blk = kBlockRows >> p.pack_log2;   // queries per unit
+          cnt = (len > 0) ? ((len + blk - 1) / blk) * (p.Hq >> p.pack_log2) : 0;
         }
         int x = cnt;
 #pragma unroll
@@ -401,12 +407,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         if (U.kv_end <= U.kv_begin) continue;
         if (!mbar_wait(b_q_empty, (q_cnt & 1) ^ 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteQEmpty))) break;
         mbar_arrive_expect_tx(b_q_full, kNSub * C::kTile);
+        // a sub-tile is 128 rows of one head, or (packed) 128 / 2^pack_log2
+        // queries x 2^pack_log2 heads from one box of the same byte count
+        const int q_span = VARLEN ? (kBM >> p.pack_log2) : kBM;
 #pragma unroll
         for (int t = 0; t < kNSub; ++t)
 #pragma unroll
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_4d(sQ + t * C::kTile + c * 16384, &p.tm_q, b_q_full, c * 64, U.h,
-                        U.row_q + U.q_row0 + t * kBM, U.bcoord);
+                        U.row_q + U.q_row0 + t * q_span, U.bcoord);
         tr.rec(kTagQIssue, 0, u, 0);
         ++q_cnt;
         bool ok = true;
@@ -559,10 +568,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     Tracer tr;
     tr.init(p, t == 0 ? kTrSoftmax0 : kTrSoftmax1);
     if (row != 0) tr.off();
+    // packed heads (varlen): TMEM lane `row` is query row >> lp of the
+    // sub-tile, head row & (2^lp - 1) of the unit's group
+    const int lp = VARLEN ? p.pack_log2 : 0;
+    const int span = kBM >> lp;
     for (int u = u_first; u < n_units; u += u_step) {
       Unit U;
       decode_unit<CAUSAL, VARLEN>(p, vl_pref, u, U);
-      const int qrow = U.q_row0 + t * kBM + row;        // query row within the sequence
+      const int q_first = U.q_row0 + t * span;          // first query of the sub-tile
+      const int qrow = q_first + (row >> lp);           // query row within the sequence
+      const int head = U.h + (row & ((1 << lp) - 1));
       const bool row_valid = qrow < U.q_len;
       // allowed keys of this row: key <= lim_key
       int lim_key = U.k_len - 1;
@@ -579,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         tr.rec(kTagSFull, t, u, j);
         const int lim = lim_key - j * kBN;
         const bool mask_tile = (j * kBN + kBN - 1 > U.k_len - 1) ||
-                               (CAUSAL && j * kBN + kBN - 1 > U.q_row0 + t * kBM + (U.k_len - U.q_len));
+                               (CAUSAL && j * kBN + kBN - 1 > q_first + (U.k_len - U.q_len));
         if (mask_tile)
           softmax_tile<true, BF16, D>(t_s, t_o, lim, c_log2, st, n_act == 0);
         else
@@ -603,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         const float inv_l = (st.l > 0.0f) ? 1.0f / st.l : 0.0f;
         const size_t orow = VARLEN ? static_cast<size_t>(U.row_q + qrow)
                                    : static_cast<size_t>(U.b) * p.Lq + qrow;
-        T* dst = out + (orow * p.Hq + U.h) * D;
+        T* dst = out + (orow * p.Hq + head) * D;
         if (n_act > 0) {
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
@@ -627,8 +642,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
         if (row_valid) {
           const float lse = (st.l > 0.0f) ? st.m * 0.69314718055994531f + __logf(st.l) : -INFINITY;
-          const size_t li = VARLEN ? static_cast<size_t>(U.h) * p.Lq + U.row_q + qrow
-                                   : (static_cast<size_t>(U.b) * p.Hq + U.h) * p.Lq + qrow;
+          const size_t li = VARLEN ? static_cast<size_t>(head) * p.Lq + U.row_q + qrow
+                                   : (static_cast<size_t>(U.b) * p.Hq + head) * p.Lq + qrow;
           p.lse[li] = lse;
         }
       } else {

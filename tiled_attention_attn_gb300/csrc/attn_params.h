@@ -47,6 +47,7 @@ enum WaitSite : int {
 
 struct FwdParams {
   CUtensorMap tm_q;            // (d, Hq, L, B) or packed (d, Hq, total, 1); box 64 x 1 x 128 x 1
+                               // (64 x group x 128/group x 1 when pack_log2 > 0)
   CUtensorMap tm_k;            // (d, Hkv, L, B) or packed
   CUtensorMap tm_v;
   void* o;                     // like q
@@ -62,6 +63,11 @@ struct FwdParams {
   int trace_cap;               // events per stream per CTA
   unsigned long long timeout_ns;
   int B, Hq, Hkv, Lq, Lk, group;
+  // varlen only: log2 of the query heads of one key/value group that share a
+  // tile (0: a tile holds 128 rows of one head).  With 2^pack_log2 = group a
+  // tile holds 128 / group tokens x group heads, row r = token r >> pack_log2,
+  // head r & (group - 1), and tm_q's box is 64 x group x (128 / group) x 1.
+  int pack_log2;
   float scale_log2;            // scale * log2(e)
   float scale;
   // A small schedule is copied here so that a CTA learns its first unit from
@@ -82,13 +88,14 @@ struct CombineParams {
 };
 
 // Last 128-key tile (inclusive) that holds an allowed key for query sub-tile
-// `t` of the 256-row block starting at `q_row0`, or -1 if the sub-tile has no
-// valid query row or no allowed key.  Causal keeps key j for query i iff
-// j <= i + (k_len - q_len).
-ATTN_HD inline int kv_last_tile(int q_row0, int t, int q_len, int k_len, bool causal) {
-  const int first = q_row0 + t * kBM;
+// `t` of the block starting at query `q_row0`, each sub-tile covering `span`
+// queries (128, or 128 / group when a group's heads share the tile), or -1 if
+// the sub-tile has no valid query or no allowed key.  Causal keeps key j for
+// query i iff j <= i + (k_len - q_len).
+ATTN_HD inline int kv_last_tile(int q_row0, int t, int q_len, int k_len, bool causal, int span = kBM) {
+  const int first = q_row0 + t * span;
   if (first >= q_len || k_len <= 0) return -1;
-  int last_row = first + kBM - 1;
+  int last_row = first + span - 1;
   if (last_row > q_len - 1) last_row = q_len - 1;
   int last = (k_len + kBN - 1) / kBN - 1;
   if (causal) {
