@@ -62,6 +62,10 @@ CASES = [
     ([1, 3, 4, 5, 130], [2000, 3, 500, 129, 130], 32, 1, 128, True, torch.bfloat16),    # group 32 (one kv head)
     ([64, 65, 200, 1], [64, 1000, 200, 257], 8, 2, 128, True, torch.bfloat16),         # group 4 over several blocks
     ([1, 7, 40], [1000, 7, 300], 6, 2, 128, True, torch.bfloat16),                     # group 3: one head per tile
+    # queries that fill one 128-row sub-tile over several key tiles, where the
+    # first rows see only the first key tile (causal, short cache)
+    ([100, 30, 3], [200, 140, 700], 2, 2, 128, True, torch.bfloat16),
+    ([100, 30, 3], [200, 140, 700], 2, 2, 64, True, torch.float16),
 ]
 
 
