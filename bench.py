@@ -520,17 +520,15 @@ def bwd_leg(attn, device, stream, peaks, iters: int = 10):
     return out
 
 
-DECODE_SHAPE = (32, 32, 8, 128, 4096)   # B, Hq, Hkv, d, cache length of the decode leg
+DECODE_SHAPE = (32, 32, 8, 128, 4096)      # B, Hq, Hkv, d, cache length of the decode leg
+DECODE_LONG_SHAPE = (1, 32, 8, 128, 131072)   # one sequence with a long cache
 
 
-def decode_leg(attn, device, stream, peaks, iters: int = 20):
-    """One new token per sequence over a key/value cache (the generation step
-    of the training page §4.3) through attn_fwd_varlen: B 32 sequences, Hq 32,
-    Hkv 8, d 128, bf16, cache 4096 + the new token, causal (bottom-right).
-    Memory-bound: the reported rate is the cache bytes read (K and V once) per
-    second against the HBM copy peak.  There is no decode-specific kernel: a
-    one-row query runs as a 256-row block, so this measures the general path."""
-    B, Hq, Hkv, d, C = DECODE_SHAPE
+def decode_step_times(attn, device, stream, shape, iters: int = 20):
+    """Median CUDA-event times (ms) of one decoding step, one new token per
+    sequence over a cache of C tokens (+ the new one), through attn_decode
+    and through attn_fwd_varlen; L2 flushed before each call."""
+    B, Hq, Hkv, d, C = shape
     g = torch.Generator().manual_seed(66)
     q = torch.randn(B, Hq, d, generator=g).to(torch.bfloat16).to(device)
     k = torch.randn(B * (C + 1), Hkv, d, generator=g).to(torch.bfloat16).to(device)
@@ -538,25 +536,55 @@ def decode_leg(attn, device, stream, peaks, iters: int = 20):
     cu_q = torch.arange(0, B + 1, dtype=torch.int32, device=device)
     cu_k = torch.arange(0, B + 1, dtype=torch.int32, device=device) * (C + 1)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
-    o, lse = attn.attn_fwd(q, k, v, causal=True, cu_seqlens=cu_q, cu_seqlens_k=cu_k, stream=stream)
-    torch.cuda.synchronize(device)
-    ms = []
-    for _ in range(iters):
-        flush.zero_()
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        s.record(stream)
-        attn.attn_fwd(q, k, v, causal=True, cu_seqlens=cu_q, cu_seqlens_k=cu_k, out=o, lse=lse, stream=stream)
-        e.record(stream)
+
+    def timed(call):
+        call()
         torch.cuda.synchronize(device)
-        ms.append(s.elapsed_time(e))
-    if attn.get_error() != attn.ATTN_OK:
-        raise RuntimeError(f"device error in the decode leg: {attn.last_device_error():#x}")
-    t = statistics.median(ms)
-    kv_bytes = 2 * k.numel() * k.element_size()
-    gbs = kv_bytes / (t / 1e3) / 1e9
-    return {"workload": f"decode: B{B} Hq{Hq} Hkv{Hkv} d{d} bf16, 1 new token over a {C}-token cache",
-            "bound": "hbm", "achieved": gbs, "unit": "GB/s", "peak": peaks["hbm_gbs"],
-            "frac": gbs / peaks["hbm_gbs"], "ms": t, "cache_bytes_per_call": kv_bytes}
+        ms = []
+        for _ in range(iters):
+            flush.zero_()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            call()
+            e.record(stream)
+            torch.cuda.synchronize(device)
+            ms.append(s.elapsed_time(e))
+        if attn.get_error() != attn.ATTN_OK:
+            raise RuntimeError(f"device error in the decode leg: {attn.last_device_error():#x}")
+        return statistics.median(ms)
+
+    o, lse = torch.empty_like(q), torch.empty(Hq, B, dtype=torch.float32, device=device)
+    t_dec = timed(lambda: attn.attn_decode(q, k, v, cu_k, out=o, lse=lse, stream=stream))
+    t_fwd = timed(lambda: attn.attn_fwd(q, k, v, causal=True, cu_seqlens=cu_q, cu_seqlens_k=cu_k, out=o, lse=lse,
+                                        stream=stream))
+    return t_dec, t_fwd, 2 * k.numel() * k.element_size()
+
+
+def decode_leg(attn, device, stream, peaks, iters: int = 20):
+    """One new token per sequence over a key/value cache (the generation step
+    of the training page §4.3), bf16, Hq 32, Hkv 8, d 128.  Memory-bound: the
+    rate is the cache bytes read (K and V once) per second against the HBM
+    copy peak.  Two shapes, each through both entry points: B 32 sequences of
+    4096 + 1 keys, where the packed forward (attn_fwd_varlen: tensor-core
+    tiles, the group's heads sharing a tile) is the faster and is reported
+    first; and one sequence of 131072 + 1 keys (``long``), where the packed
+    forward has only Hkv = 8 units and attn_decode (the key-split CUDA-core
+    path: chunk pass and merge) is the faster."""
+    B, Hq, Hkv, d, C = DECODE_SHAPE
+    t_dec, t_fwd, nbytes = decode_step_times(attn, device, stream, DECODE_SHAPE, iters)
+    gbs = lambda t: nbytes / (t / 1e3) / 1e9
+    out = {"workload": f"decode: B{B} Hq{Hq} Hkv{Hkv} d{d} bf16, 1 new token over a {C}-token cache",
+           "entry": "attn_fwd_varlen", "bound": "hbm", "achieved": gbs(t_fwd), "unit": "GB/s",
+           "peak": peaks["hbm_gbs"], "frac": gbs(t_fwd) / peaks["hbm_gbs"], "ms": t_fwd,
+           "cache_bytes_per_call": nbytes,
+           "attn_decode": {"achieved": gbs(t_dec), "frac": gbs(t_dec) / peaks["hbm_gbs"], "ms": t_dec}}
+    B, Hq, Hkv, d, C = DECODE_LONG_SHAPE
+    t_dec, t_fwd, nbytes = decode_step_times(attn, device, stream, DECODE_LONG_SHAPE, iters)
+    out["long"] = {"workload": f"decode: B{B} Hq{Hq} Hkv{Hkv} d{d} bf16, 1 new token over a {C}-token cache",
+                   "entry": "attn_decode", "achieved": gbs(t_dec), "frac": gbs(t_dec) / peaks["hbm_gbs"],
+                   "ms": t_dec, "cache_bytes_per_call": nbytes,
+                   "attn_fwd_varlen": {"achieved": gbs(t_fwd), "frac": gbs(t_fwd) / peaks["hbm_gbs"], "ms": t_fwd}}
+    return out
 
 
 def run_ours(args, wl):

@@ -180,6 +180,48 @@ int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float 
                     const int *cu_seqlens_k, int fp16, cudaStream_t stream);
 
 /*
+ * attn_decode -- one decoding step: a single new query per sequence against
+ * the sequence's key/value cache (training page §4, generation with a cache
+ * whose length sets the rotary offset; the same exact softmax of page
+ * S23-J17, clxhxhhr.top/posts/5544, §3.1, reached by splitting the keys into
+ * chunks and merging the chunks with the running-max rescaling).  The result
+ * is that of attn_fwd_varlen with cu_seqlens_q = {0, 1, ..., B}: the query is
+ * the last position of its sequence, so causal and non-causal coincide and it
+ * sees all of the sequence's keys.
+ *
+ *   q, o  (B, Hq, d) contiguous, one row per sequence;
+ *   k, v  (total_k, Hkv, d) contiguous, sequence b holding rows
+ *         cu_seqlens_k[b] .. cu_seqlens_k[b+1] - 1 (a device int32 array of
+ *         B+1 entries, 0 first, non-decreasing, last entry at most total_k;
+ *         checked on the device: a malformed array records
+ *         ATTN_DEVERR_BAD_SEQLENS and every row gets O = 0, lse = -inf);
+ *   lse   (Hq, B) float32, natural log; a sequence with no key gives O = 0
+ *         and lse = -inf.
+ *
+ * fp16 = 0 selects bf16 tensors, 1 fp16.  d is 64 or 128 and Hq / Hkv is 1,
+ * 2, 4 or 8 (else ATTN_EUNSUPPORTED; attn_fwd_varlen takes the others).
+ * Pointers 16-byte aligned (lse 4); k and v may be null when total_k is 0.
+ * It runs on the CUDA cores: with one query row per head the products are
+ * matrix-vector and the cache read from HBM bounds the step.  Three launches
+ * on `stream`: a one-warp pass over cu_seqlens_k, one block per chunk of 128
+ * keys and key/value head (the chunk's max, exp-sum and unnormalised
+ * output), and a merge per (sequence, query head).  The chunk results live in
+ * a library workspace (one per device, grown on demand with cudaMalloc):
+ * calls that overlap on the GPU (two streams without ordering) must not share
+ * a device.  Returns ATTN_OK, ATTN_EINVAL, ATTN_EUNSUPPORTED, ATTN_ENOMEM or
+ * ATTN_ELAUNCH.
+ *
+ * Which entry point to use for a decoding step: attn_fwd_varlen does not
+ * split the keys, so it runs B x Hkv units and keeps few SMs busy when that
+ * product is small (one or a few sequences with long caches); attn_decode
+ * splits every cache into 128-key chunks and fills the GPU at any batch
+ * size.  With many sequences (B x Hkv in the hundreds) the packed forward's
+ * tensor-core tiles stream the cache faster.
+ */
+int attn_decode(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv,
+                int total_k, int d, float scale, const int *cu_seqlens_k, int fp16, cudaStream_t stream);
+
+/*
  * attn_bwd -- the backward of the dense forward: the gradients of
  * sum(dout * O) with respect to q, k and v (training page §5.3: the backward
  * recomputes the attention weights from what the forward kept, and nothing

@@ -113,3 +113,24 @@ def test_missing_library_fails_loudly(tmp_path):
     # no CPU or library fallback: without the built library the binding raises
     with pytest.raises(RuntimeError, match="missing"):
         attn.lib(str(tmp_path / "libattn_absent.so"))
+
+
+def _call_decode(L, q=16, k=16, v=16, o=16, lse=16, B=2, Hq=4, Hkv=2, total_k=8, d=64, scale=0.125, cu=16,
+                 fp16=0):
+    return L.attn_decode(q, k, v, o, lse, B, Hq, Hkv, total_k, d, ctypes.c_float(scale), cu, fp16, None)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(q=None), dict(o=None), dict(lse=None), dict(cu=None), dict(k=None), dict(v=None),
+    dict(q=8), dict(k=24), dict(v=40), dict(o=40), dict(lse=2),      # misaligned pointers
+    dict(B=0), dict(Hq=0), dict(Hkv=0), dict(total_k=-1), dict(Hq=3, Hkv=2), dict(fp16=2),
+    dict(scale=float("nan")), dict(scale=-1.0),
+    dict(B=1 << 22, Hq=1 << 10, Hkv=1 << 10),
+])
+def test_decode_bad_arguments_rejected_on_host(attn_lib, bad):
+    assert _call_decode(attn_lib, **bad) == attn.ATTN_EINVAL
+
+
+@pytest.mark.parametrize("shape", [dict(d=32), dict(d=96), dict(d=256), dict(Hq=6, Hkv=2), dict(Hq=16, Hkv=1)])
+def test_decode_unsupported_shapes(attn_lib, shape):
+    assert _call_decode(attn_lib, **shape) == attn.ATTN_EUNSUPPORTED

@@ -9,6 +9,7 @@ The binding loads libattn.so on first use; build it with
 from .attn import (  # noqa: F401
     AttnError,
     attn_bwd,
+    attn_decode,
     attn_func,
     attn_func_padded,
     attn_fwd,

@@ -106,6 +106,8 @@ def lib(path: Optional[str] = None):
         L.attn_bwd.restype = i
         L.attn_bwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, vp, vp, i, vp]
         L.attn_bwd_varlen.restype = i
+        L.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, i, vp]
+        L.attn_decode.restype = i
         if path is None:
             _lib = L
         return L
@@ -256,6 +258,44 @@ def attn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tenso
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_bwd")
     return dq, dk, dv
+
+
+def attn_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cu_seqlens_k: torch.Tensor,
+                scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                lse: Optional[torch.Tensor] = None,
+                stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """One decoding step: q (B, Hq, d) holds one new query per sequence, k
+    and v (total_k, Hkv, d) the packed caches with offsets ``cu_seqlens_k``
+    (int32 on the device, B+1 entries).  Returns O (B, Hq, d) and lse
+    (Hq, B) float32, equal to attn_fwd with cu_seqlens = [0, 1, ..., B] and
+    these key offsets.  Hq / Hkv must be 1, 2, 4 or 8."""
+    if q.dtype not in (torch.bfloat16, torch.float16) or k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must share one 16-bit dtype")
+    if not (q.is_cuda and k.is_cuda and v.is_cuda) or not (q.is_contiguous() and k.is_contiguous()
+                                                            and v.is_contiguous()):
+        raise ValueError("q, k and v must be contiguous CUDA tensors")
+    if q.dim() != 3 or k.dim() != 3 or k.shape != v.shape or k.shape[2] != q.shape[2]:
+        raise ValueError("q is (B, Hq, d) and k, v are (total_k, Hkv, d)")
+    B, Hq, d = q.shape
+    total_k, Hkv, _ = k.shape
+    if cu_seqlens_k.dtype != torch.int32 or not cu_seqlens_k.is_cuda or cu_seqlens_k.numel() != B + 1:
+        raise ValueError("cu_seqlens_k must be an int32 CUDA tensor of B+1 entries")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((Hq, B), dtype=torch.float32, device=q.device) if lse is None else lse
+    if out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor shaped like q")
+    if tuple(lse.shape) != (Hq, B) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError(f"lse must be a contiguous float32 tensor of shape {(Hq, B)}")
+    with torch.cuda.device(q.device):
+        rc = lib().attn_decode(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), int(B),
+                               int(Hq), int(Hkv), int(total_k), int(d), ctypes.c_float(float(scale)),
+                               cu_seqlens_k.data_ptr(), int(q.dtype == torch.float16),
+                               _stream_handle(q.device, stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_decode")
+    return out, lse
 
 
 # ---------------------------------------------------------------------------
