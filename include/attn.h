@@ -34,10 +34,21 @@
  *   - Work is enqueued on `stream`; no entry point except attn_get_error()
  *     synchronises.  Arguments are validated on the host before anything is
  *     enqueued; a non-zero return means nothing was launched.
- *   - The library allocates, once per device and lazily, its own small
- *     buffers: cached TMA descriptors, a tile schedule per problem shape, a
- *     split-KV workspace for the forward and a D / lse workspace for the
- *     backward, each grown on demand.  These live until the process exits.
+ *   - The library allocates, per device and lazily, its own buffers: cached
+ *     TMA descriptors (host memory), a device copy of the tile schedule of
+ *     each dense problem shape whose schedule is too large to travel in the
+ *     kernel parameters, a split-KV workspace for the forward and a D / lse
+ *     workspace for the backward.  For attn_fwd: schedules are cached per
+ *     shape, at most 256 per kernel; the least recently used one is evicted
+ *     and its device copy released with cudaFreeAsync on the calling stream,
+ *     ordered after every launch that read it.  A schedule is written to the
+ *     device by a kernel on the calling stream (its values in the launch
+ *     parameters), so the first call of a shape neither synchronises nor
+ *     copies from pageable memory, and it may be made inside a stream
+ *     capture.  The forward's workspaces grow with cudaMallocAsync; the
+ *     buffer they replace is released with cudaFreeAsync on the calling
+ *     stream.  Schedules and workspaces that a captured graph uses are kept
+ *     until the process exits (a replay reads them).
  *   - Calls that share a device may run concurrently on different streams,
  *     except that each workspace is one buffer per device: at most one
  *     forward whose schedule splits the keys (attn_plan reports partials > 0;
@@ -138,7 +149,9 @@ int attn_fwd_fp16(const void *q, const void *k, const void *v, void *o, float *l
  *     before any stream capture.
  *   - Every call on a device shares the one array and leaves its contents
  *     behind; nothing in it needs to start at zero (every partial is written
- *     before it is read).  Calls whose work overlaps on the GPU (for example
+ *     before it is read).  A schedule too large for the launch parameters
+ *     is written into the array on every call, by a small kernel on
+ *     `stream` ahead of the attention kernels.  Calls whose work overlaps on the GPU (for example
  *     on two streams without an ordering between them) race on the array and
  *     give wrong results: order them.
  *   - A dense problem whose schedule exceeds 4 MiB or whose partials exceed
@@ -352,6 +365,38 @@ int attn_scatter_rows(const void *src, const int *indices, int n_max, const int 
                       int dst_rows, cudaStream_t stream);
 int attn_scatter_lse(const float *src, const int *indices, int n_max, const int *n_dev, int Hq, int B, int L,
                      float *dst, cudaStream_t stream);
+
+/*
+ * attn_set_pair_forward -- selects the kernel of dense head_dim-128 forwards
+ * (attn_fwd, attn_fwd_fp16): 1 runs them on CTA pairs, where one tcgen05
+ * .cta_group::2 MMA spans two SMs (256 query rows against 256 keys) and split
+ * key ranges are merged inside the kernel; 0 (the default) runs them on the
+ * single-CTA kernel with a separate merge pass.  Both compute the same
+ * function.  attn_pair_forward_used(d, varlen) tells which one attn_fwd takes
+ * (1: the pair kernel).  Process-wide; not synchronised with calls in flight.
+ */
+void attn_set_pair_forward(int enable);
+int attn_pair_forward_used(int d, int varlen);
+
+/*
+ * attn_plan_pair -- the CTA-pair kernel's schedule for a dense problem, for
+ * inspection and tests (no GPU needed).  Units as attn_plan's, with m_block a
+ * 256-row query block (128 rows in each CTA of the pair), [kv_begin, kv_end)
+ * counted in 256-key tiles and `cta` the pair that runs the unit;
+ * *n_pairs receives the number of pairs (the grid is twice that).
+ */
+int attn_plan_pair(int B, int Hq, int Hkv, int Lq, int Lk, int causal, int num_pairs, int *units, int max_units,
+                   int *n_units, int *n_pairs, int *n_partials);
+
+/* attn_cache_stats -- the number of schedules cached on the current device
+ * (both kernels) and how many of them a stream capture pinned. */
+int attn_cache_stats(int *plans, int *pinned);
+
+/* attn_selftest_plan_cache -- runs the schedule cache's eviction policy on
+ * host-side entries only (no device memory): n_keys lookups cycling over
+ * 2 * capacity + 7 keys, every pin_every-th new entry pinned (0: none).
+ * Reports the largest number of live entries and how many were released. */
+int attn_selftest_plan_cache(int n_keys, int capacity, int pin_every, int *max_live, int *released);
 
 /* attn_get_error -- synchronises `stream`, then returns ATTN_EDEVICE if any
  * kernel of this library on the current device has reported an error since

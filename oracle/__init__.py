@@ -256,16 +256,6 @@ def varlen_attention(q, k, v, lengths: Sequence[int], causal: bool = False,
     return o_packed, lse_packed
 
 
-def varlen_rows(q, k, v, lengths: Sequence[int], rows: Sequence[Tuple[int, int, int]],
-                causal: bool = False, scale: Optional[float] = None):
-    """Selected (b, h, i) rows of a packed varlen batch, via the padded form."""
-    lengths = [int(n) for n in lengths]
-    qp, mask = pad_packed(q, lengths)
-    kp, _ = pad_packed(k, lengths)
-    vp, _ = pad_packed(v, lengths)
-    return attention_rows(qp, kp, vp, rows, causal=causal, scale=scale, key_padding_mask=mask)
-
-
 def varlen_cross_attention(q, k, v, lengths_q: Sequence[int], lengths_k: Sequence[int], causal: bool = False,
                            scale: Optional[float] = None):
     """Packed varlen attention with separate query and key lengths

@@ -41,15 +41,25 @@ def run(inp, causal, scale=None):
     return o.float().cpu().double().numpy(), lse.cpu().double().numpy()
 
 
-def check(o, lse, o_ref, lse_ref, what=""):
+def check(o, lse, o_ref, lse_ref, what="", o_tol=O_TOL):
+    """Element-wise comparison.  A failure message reports the max-abs error
+    and, separately, how many violating elements have |O_ref| >= 4: there a
+    bf16 output's half-ulp (2^-6) already exceeds the 1e-2 bar, so even a
+    correctly rounded result can miss it.  The bar itself is not relaxed."""
     assert o.shape == o_ref.shape and lse.shape == lse_ref.shape
     inf_ref = np.isneginf(lse_ref)
     assert np.array_equal(np.isneginf(lse), inf_ref), f"{what}: -inf rows differ"
-    err_o = np.max(np.abs(o - o_ref)) if o.size else 0.0
+    dev = np.abs(o - o_ref)
+    err_o = np.max(dev) if o.size else 0.0
     fin = ~inf_ref
     err_l = np.max(np.abs(lse[fin] - lse_ref[fin])) if fin.any() else 0.0
     assert np.all(np.isfinite(o)), f"{what}: non-finite output"
-    assert err_o <= O_TOL, f"{what}: max |dO| = {err_o:.3e}"
+    bar = o_tol if np.isscalar(o_tol) else o_tol
+    bad = dev > bar
+    if np.any(bad):
+        big = bad & (np.abs(o_ref) >= 4.0)
+        raise AssertionError(f"{what}: max |dO| = {err_o:.3e}; {int(bad.sum())} elements over the bar, "
+                             f"{int(big.sum())} of them with |O_ref| >= 4 (bf16 half-ulp > 1e-2 there)")
     assert err_l <= LSE_TOL, f"{what}: max |dlse| = {err_l:.3e}"
     return err_o, err_l
 
@@ -151,10 +161,18 @@ def test_split_kv_small():
     check(o[idx[:, 0], idx[:, 2], idx[:, 1]], lse[idx[:, 0], idx[:, 1], idx[:, 2]], o_ref, lse_ref, "split")
 
 
-def test_split_kv_more_than_one_merge_batch():
-    # a query block split into more than eight pieces: the merge reads pieces
-    # in batches of eight and rescales across batches (single head, causal,
-    # d 128; L = 12288 gives 10-12 pieces for SM counts from 132 to 160)
+@pytest.fixture
+def single_cta():
+    """Dense head_dim-128 forwards on the single-CTA kernel for one test."""
+    attn.set_pair_forward(False)
+    yield
+
+
+def test_split_kv_more_than_one_merge_batch(single_cta):
+    # a query block split into more than eight pieces: the combine pass reads
+    # pieces in batches and rescales across batches (single head, causal,
+    # d 128, single-CTA kernel; L = 12288 gives 10-12 pieces for SM counts
+    # from 132 to 160)
     n_sms = torch.cuda.get_device_properties(0).multi_processor_count
     L = next((x for x in (12288, 14336, 16384) if attn.plan(1, 1, 1, x, x, 128, True, n_sms)[0][:, 5].max() > 8),
              None)
@@ -187,6 +205,44 @@ def test_full_size_sampled(name):
         g = np.arange(wl.Hq) // (wl.Hq // wl.Hkv)
         v0 = inp.v[:, 0].double().numpy()[:, g]
         assert np.array_equal(o[:, 0], v0)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+
+
+# ---------------------------------------------------------------------------
+# value magnitude: the split-KV path must be as exact as the unsplit one
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("pair", [True, False], ids=["pair", "single"])
+@pytest.mark.parametrize("vscale", [1e5, 1e-6])
+@pytest.mark.parametrize("L,split", [(4096, True), (512, False)])
+def test_value_magnitude_split_and_unsplit(L, split, vscale, pair):
+    """bf16 values scaled by 1e5 or 1e-6 (single head, causal, d 128).  A
+    split schedule stores each piece's partial output and merges the pieces;
+    the result must stay finite and as accurate as without splitting.  Bar:
+    the 1e-2 bar of unit-normal values scaled with the values, plus the bf16
+    rounding of O itself (half an ulp, 2^-8 relative); lse does not depend on
+    the values (1e-3)."""
+    n_sms = torch.cuda.get_device_properties(0).multi_processor_count
+    attn.set_pair_forward(pair)
+    try:
+        _magnitude_case(L, split, vscale, n_sms)
+    finally:
+        attn.set_pair_forward(False)
+
+
+def _magnitude_case(L, split, vscale, n_sms):
+    assert attn.fwd_splits(1, 1, 1, L, L, 128, True, n_sms) == split
+    wl = Workload("vmag", B=1, Hq=1, Hkv=1, Lq=L, Lk=L, d=128, dtype="bf16", causal=True, seed=21)
+    inp = generate(wl)
+    g = torch.Generator().manual_seed(22)
+    inp.v = (torch.randn(inp.v.shape, generator=g) * vscale).to(torch.bfloat16)
+    o, lse = run(inp, True)
+    rows = sample_rows(wl, 256)
+    o_ref, lse_ref = oracle.attention_rows(inp.q, inp.k, inp.v, rows, causal=True, scale=wl.softmax_scale)
+    idx = np.array(rows)
+    o_s = o[idx[:, 0], idx[:, 2], idx[:, 1]]
+    tol = 1e-2 * vscale + 2.0 ** -8 * np.abs(o_ref)
+    check(o_s, lse[idx[:, 0], idx[:, 1], idx[:, 2]], o_ref, lse_ref, f"L{L} v x {vscale:g}", o_tol=tol)
     assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
 
 

@@ -102,6 +102,63 @@ def test_noalloc_shape_change_and_varlen():
     assert_close(o, lse, o_ref, lse_ref)
 
 
+def test_noalloc_allocates_nothing():
+    """A call with a shape the entry point has not seen before changes neither
+    the device's free memory nor torch's allocation count.  A first call of
+    another shape that runs the same kernels comes before the measurement,
+    so that loading the library's kernels (which reserves memory for their
+    code) is not counted."""
+    dev = torch.device("cuda", 0)
+    shapes = [(1, 1, 1, 8192, 8192), (1, 2, 1, 6144, 6144)]   # both split, schedules in the array
+    n_sms = torch.cuda.get_device_properties(0).multi_processor_count
+    ins = []
+    for (B, Hq, Hkv, Lq, Lk) in shapes:
+        assert attn.plan(B, Hq, Hkv, Lq, Lk, 128, True, n_sms)[2] > 0
+        wl = Workload("na0", B=B, Hq=Hq, Hkv=Hkv, Lq=Lq, Lk=Lk, d=128, dtype="bf16", causal=True, seed=9)
+        inp = generate(wl)
+        q, k, v = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=dev)
+        ins.append((q, k, v, o, lse, wl))
+    L = attn.lib()
+    stream = torch.cuda.current_stream(dev).cuda_stream
+
+    def call(q, k, v, o, lse, wl):
+        return L.attn_fwd_noalloc(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                  wl.B, wl.Hq, wl.Hkv, wl.Lq, wl.Lk, wl.d, 1, ctypes.c_float(wl.softmax_scale),
+                                  None, stream)
+
+    assert call(*ins[0]) == attn.ATTN_OK
+    torch.cuda.synchronize(dev)
+    free0, _ = torch.cuda.mem_get_info(dev)
+    alloc0 = torch.cuda.memory_allocated(dev)
+    assert call(*ins[1]) == attn.ATTN_OK
+    torch.cuda.synchronize(dev)
+    free1, _ = torch.cuda.mem_get_info(dev)
+    assert torch.cuda.memory_allocated(dev) == alloc0
+    assert free1 == free0
+    assert attn.get_error() == attn.ATTN_OK
+    q, k, v, o, lse, wl = ins[1]
+    o_ref, lse_ref = attn.attn_fwd(q, k, v, causal=True)
+    assert_close(o, lse, o_ref, lse_ref)
+
+
+def test_noalloc_varlen_grouped_heads():
+    """Packed sequences with four query heads per key/value head: attn_fwd
+    lets the group share a tile, the allocation-free entry point does not;
+    both must give the same result."""
+    dev = torch.device("cuda", 0)
+    wl = Workload("na_gqa", B=6, Hq=8, Hkv=2, Lq=0, Lk=0, d=64, dtype="bf16", causal=True, seed=12, varlen=True,
+                  len_lo=1, len_hi=700)
+    inp = generate(wl)
+    q, k, v, cu = inp.q.to(dev), inp.k.to(dev), inp.v.to(dev), inp.cu_seqlens.to(dev)
+    for causal in (True, False):
+        o_ref, lse_ref = attn.attn_fwd(q, k, v, causal=causal, cu_seqlens=cu)
+        o, lse, rc = noalloc(q, k, v, causal, wl.softmax_scale, cu=cu)
+        assert rc == attn.ATTN_OK and attn.get_error() == attn.ATTN_OK
+        assert_close(o, lse, o_ref, lse_ref)
+
+
 def test_noalloc_refuses_problems_beyond_its_array():
     # 133120 one-block units (B 1040, 128 query heads on one KV head, L 256,
     # d 64): the schedule (32 bytes per unit) exceeds the array's 4 MiB

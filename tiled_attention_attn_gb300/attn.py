@@ -108,6 +108,16 @@ def lib(path: Optional[str] = None):
         L.attn_bwd_varlen.restype = i
         L.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, vp, i, vp]
         L.attn_decode.restype = i
+        L.attn_set_pair_forward.argtypes = [i]
+        L.attn_set_pair_forward.restype = None
+        L.attn_pair_forward_used.argtypes = [i, i]
+        L.attn_pair_forward_used.restype = i
+        L.attn_plan_pair.argtypes = [i, i, i, i, i, i, i, ip, i, ip, ip, ip]
+        L.attn_plan_pair.restype = i
+        L.attn_cache_stats.argtypes = [ip, ip]
+        L.attn_cache_stats.restype = i
+        L.attn_selftest_plan_cache.argtypes = [i, i, i, ip, ip]
+        L.attn_selftest_plan_cache.restype = i
         if path is None:
             _lib = L
         return L
@@ -615,6 +625,64 @@ def plan(B: int, Hq: int, Hkv: int, Lq: int, Lk: int, d: int, causal: bool, num_
         raise AttnError(rc, "attn_plan")
     units = torch.tensor(list(buf)[: 8 * n_units.value], dtype=torch.int64).reshape(-1, 8)
     return units, n_ctas.value, n_part.value
+
+
+def plan_pair(B: int, Hq: int, Hkv: int, Lq: int, Lk: int, causal: bool, num_pairs: int):
+    """The CTA-pair kernel's schedule for a dense problem (host only).
+
+    Returns (units, n_pairs, n_partials); units is an (n, 8) int tensor of
+    (b*Hq+h, 256-row block, kv_begin, kv_end, split, n_split, slot, pair)
+    with [kv_begin, kv_end) counted in 256-key tiles."""
+    L = lib()
+    n_units, n_pairs, n_part = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    rc = L.attn_plan_pair(B, Hq, Hkv, Lq, Lk, int(bool(causal)), num_pairs, None, 0,
+                          ctypes.byref(n_units), ctypes.byref(n_pairs), ctypes.byref(n_part))
+    if rc not in (ATTN_OK, ATTN_ENOMEM):
+        raise AttnError(rc, "attn_plan_pair")
+    buf = (ctypes.c_int * (8 * max(n_units.value, 1)))()
+    rc = L.attn_plan_pair(B, Hq, Hkv, Lq, Lk, int(bool(causal)), num_pairs, buf, n_units.value,
+                          ctypes.byref(n_units), ctypes.byref(n_pairs), ctypes.byref(n_part))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_plan_pair")
+    units = torch.tensor(list(buf)[: 8 * n_units.value], dtype=torch.int64).reshape(-1, 8)
+    return units, n_pairs.value, n_part.value
+
+
+def set_pair_forward(enable: bool) -> None:
+    """Dense head_dim-128 forwards on CTA pairs (True) or on the single-CTA
+    kernel (False, the default)."""
+    lib().attn_set_pair_forward(int(bool(enable)))
+
+
+def pair_forward_used(d: int, varlen: bool) -> bool:
+    """Whether attn_fwd runs such a problem on the CTA-pair kernel."""
+    return bool(lib().attn_pair_forward_used(int(d), int(bool(varlen))))
+
+
+def fwd_splits(B: int, Hq: int, Hkv: int, Lq: int, Lk: int, d: int, causal: bool, num_sms: int) -> bool:
+    """Whether the schedule attn_fwd uses for this dense shape splits key ranges."""
+    if pair_forward_used(d, False):
+        return plan_pair(B, Hq, Hkv, Lq, Lk, causal, num_sms // 2)[2] > 0
+    return plan(B, Hq, Hkv, Lq, Lk, d, causal, num_sms)[2] > 0
+
+
+def cache_stats() -> Tuple[int, int]:
+    """(cached schedules, of which pinned by a stream capture) on the current device."""
+    a, b = ctypes.c_int(0), ctypes.c_int(0)
+    rc = lib().attn_cache_stats(ctypes.byref(a), ctypes.byref(b))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_cache_stats")
+    return a.value, b.value
+
+
+def selftest_plan_cache(n_keys: int, capacity: int, pin_every: int = 0) -> Tuple[int, int]:
+    """Runs the schedule cache's eviction policy on host-side entries:
+    (largest number of live entries, entries released)."""
+    a, b = ctypes.c_int(0), ctypes.c_int(0)
+    rc = lib().attn_selftest_plan_cache(int(n_keys), int(capacity), int(pin_every), ctypes.byref(a), ctypes.byref(b))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_selftest_plan_cache")
+    return a.value, b.value
 
 
 def launch_count() -> int:

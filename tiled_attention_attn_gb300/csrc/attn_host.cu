@@ -15,8 +15,10 @@
 #include <vector>
 
 #include "attn.h"
+#include "attn_cache.h"
 #include "attn_internal.h"
 #include "attn_launch.h"
+#include "attn_pair_launch.h"
 #include "attn_params.h"
 #include "attn_plan.h"
 #include "ptx.cuh"
@@ -30,6 +32,7 @@ namespace {
 
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
 std::atomic<unsigned long long> g_launches{0};
+std::atomic<int> g_pair_forward{0};   // attn_set_pair_forward
 unsigned long long* g_trace = nullptr;   // attn_trace_enable (traced build only)
 int g_trace_cap = 0;
 
@@ -82,15 +85,42 @@ bool get_encode() {
   return true;
 }
 
-using MapKey = std::tuple<uintptr_t, int, int, int, int, int, int>;   // ptr, dtype, d, H, L, B, box heads
+using MapKey = std::tuple<uintptr_t, int, int, int, int, int, int, int>;   // ptr, dtype, d, H, L, B, box heads, box rows
 using PlanKey = std::tuple<int, int, int, int, int, int, int>;   // B, Hq, Hkv, Lq, Lk, d, causal
 
+constexpr size_t kMaxPlans = 256;   // schedules cached per device and kernel
+
+// A schedule and its device copy.  The copy is written in stream order by an
+// upload kernel (the values travel in its parameters), so the first call of a
+// shape neither synchronises nor copies from pageable memory.
 struct DevPlan {
   Plan host;
-  std::vector<int> flat_units;   // kUnitInts per unit, the layout the kernel reads
-  int* d_units = nullptr;
-  int* d_cta_off = nullptr;
-  int* d_groups = nullptr;
+  std::vector<int> flat;   // units (kUnitInts each) | CTA or pair offsets | split groups (kGroupInts each)
+  size_t off_cta = 0, off_groups = 0;
+  int* dbuf = nullptr;
+  bool async_alloc = false;   // dbuf from cudaMallocAsync (else cudaMalloc, during a capture)
+  bool pinned = false;        // a captured graph reads dbuf: kept until the process exits
+  bool uploaded = false;      // an upload outside any capture has been enqueued
+  cudaStream_t up_stream = nullptr;
+  cudaEvent_t ready = nullptr;                                // after that upload
+  std::vector<std::pair<cudaStream_t, cudaEvent_t>> uses;     // last launch on each stream
+  uint64_t lru = 0;
+  const int* units() const { return dbuf; }
+  const int* cta_off() const { return dbuf + off_cta; }
+  const int* groups() const { return dbuf + off_groups; }
+};
+
+// A library-owned device buffer grown on demand.  Growth never frees a buffer
+// mid-stream: the old one is released with cudaFreeAsync on the calling
+// stream (ordered after the calls that used it, which the header requires to
+// be ordered before this one), or kept for the life of the process if a
+// captured graph may still use it.
+struct Workspace {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+  bool async_alloc = false;
+  bool pinned = false;
+  std::vector<void*> kept;
 };
 
 struct DevState {
@@ -99,10 +129,12 @@ struct DevState {
   int sm_count = 0;
   int* err_word = nullptr;
   std::map<MapKey, CUtensorMap> maps;
-  std::map<PlanKey, std::unique_ptr<DevPlan>> plans;
-  void* part_o = nullptr;
-  float* part_ml = nullptr;
-  size_t part_o_bytes = 0, part_ml_bytes = 0;
+  LruCache<PlanKey, DevPlan> plans{kMaxPlans};        // single-CTA kernel schedules
+  LruCache<PlanKey, DevPlan> pair_plans{kMaxPlans};   // CTA-pair kernel schedules
+  Workspace part;        // single-CTA split pieces: O_s then (m, l)
+  Workspace pair_part;   // CTA-pair split pieces: u then (m, l)
+  Workspace pair_cnt;    // CTA-pair merge counters (epoch-tagged words, zeroed when allocated)
+  unsigned int epoch = 0;
 };
 
 std::map<int, DevState> g_dev;
@@ -120,10 +152,11 @@ int init_device(int dev, DevState& st) {
 }
 
 // 4-D map over (d, H, L, B) for a contiguous (B, L, H, d) 16-bit tensor,
-// box 64 x box_h x (128 / box_h) x 1: one 128-byte swizzle atom wide and 128
-// shared-memory rows high, rows ordered (position, head) with the head fastest.
-int get_map(DevState& st, const void* ptr, bool bf16, int d, int H, int L, int B, CUtensorMap& out, int box_h = 1) {
-  const MapKey key{reinterpret_cast<uintptr_t>(ptr), bf16 ? 1 : 0, d, H, L, B, box_h};
+// box box_inner x box_h x (box_rows / box_h) x 1, 128-byte swizzle: rows
+// ordered (position, head) with the head fastest.
+int get_map(DevState& st, const void* ptr, bool bf16, int d, int H, int L, int B, CUtensorMap& out, int box_h = 1,
+            int box_rows = kBM, int box_inner = 64) {
+  const MapKey key{reinterpret_cast<uintptr_t>(ptr), bf16 ? 1 : 0, d, H, L, B, box_h, box_rows * 1024 + box_inner};
   auto it = st.maps.find(key);
   if (it != st.maps.end()) {
     out = it->second;
@@ -134,78 +167,247 @@ int get_map(DevState& st, const void* ptr, bool bf16, int d, int H, int L, int B
                               static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(B)};
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(H) * d * 2,
                                  static_cast<cuuint64_t>(L) * H * d * 2};
-  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_h), static_cast<cuuint32_t>(kBM / box_h), 1};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(box_inner), static_cast<cuuint32_t>(box_h),
+                             static_cast<cuuint32_t>(box_rows / box_h), 1};
   const cuuint32_t es[4] = {1, 1, 1, 1};
   const CUresult r = g_encode(&m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
                               const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return ATTN_EINVAL;
-  if (st.maps.size() > 4096) st.maps.clear();
+  if (st.maps.size() > 4096) st.maps.clear();   // host memory only
   st.maps.emplace(key, m);
   out = m;
   return ATTN_OK;
 }
 
-int get_plan(DevState& st, int B, int Hq, int Hkv, int Lq, int Lk, int d, bool causal, cudaStream_t stream,
-             DevPlan*& out) {
-  const PlanKey key{B, Hq, Hkv, Lq, Lk, d, causal ? 1 : 0};
-  auto it = st.plans.find(key);
-  if (it != st.plans.end()) {
-    out = it->second.get();
-    return ATTN_OK;
+// cudaMalloc inside a stream capture: the calling thread's capture mode is
+// relaxed for the call (allocation is otherwise refused under the global
+// mode), then restored.
+cudaError_t malloc_in_capture(void** p, size_t bytes) {
+  cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+  cudaThreadExchangeStreamCaptureMode(&mode);
+  const cudaError_t e = cudaMalloc(p, bytes);
+  cudaThreadExchangeStreamCaptureMode(&mode);
+  return e;
+}
+
+// True while `stream` is being captured into a graph (or when that cannot be
+// told, which is treated the same way: nothing is freed or evicted).
+bool capturing(cudaStream_t stream) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+    cudaGetLastError();
+    return true;
   }
-  auto dp = std::make_unique<DevPlan>();
-  if (!make_plan(B, Hq, Hkv, Lq, Lk, d, causal, st.sm_count, dp->host)) return ATTN_EINVAL;
-  const Plan& pl = dp->host;
-  std::vector<int> units(pl.units.size() * kUnitInts);
-  for (size_t i = 0; i < pl.units.size(); ++i) {
-    const PlanUnit& u = pl.units[i];
-    const int e[kUnitInts] = {u.bh, u.m_block, u.kv_begin, u.kv_end, u.split, u.n_split, u.slot, u.cta};
-    std::memcpy(&units[i * kUnitInts], e, sizeof(e));
+  return cs != cudaStreamCaptureStatusNone;
+}
+
+// ---- stream-ordered upload of int arrays: the values ride in the kernel's
+// parameters (up to 28 KB per launch), so no host buffer has to outlive the
+// call and the copy is captured like any kernel.
+constexpr int kUploadInts = 7168;
+struct UploadParams {
+  int* dst;
+  int n;
+  int data[kUploadInts];
+};
+__global__ void __launch_bounds__(256) upload_kernel(const __grid_constant__ UploadParams p) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < p.n; i += gridDim.x * blockDim.x) p.dst[i] = p.data[i];
+}
+
+}  // namespace
+
+int upload_ints(int* dst, const int* src, size_t n, cudaStream_t stream) {
+  static thread_local UploadParams p;
+  for (size_t off = 0; off < n; off += kUploadInts) {
+    const int cnt = static_cast<int>(std::min<size_t>(kUploadInts, n - off));
+    p.dst = dst + off;
+    p.n = cnt;
+    std::memcpy(p.data, src + off, static_cast<size_t>(cnt) * sizeof(int));
+    upload_kernel<<<(cnt + 255) / 256, 256, 0, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
+    g_launches.fetch_add(1);
   }
-  dp->flat_units = units;
-  std::vector<int> groups(pl.groups.size() * kGroupInts);
-  for (size_t i = 0; i < pl.groups.size(); ++i) {
-    const PlanGroup& g = pl.groups[i];
-    const int e[kGroupInts] = {g.bh, g.m_block, g.slot_base, g.n_split};
-    std::memcpy(&groups[i * kGroupInts], e, sizeof(e));
-  }
-  auto upload = [&](const std::vector<int>& v, int*& dst) -> bool {
-    if (v.empty()) return true;
-    if (cudaMalloc(&dst, v.size() * sizeof(int)) != cudaSuccess) return false;
-    return cudaMemcpy(dst, v.data(), v.size() * sizeof(int), cudaMemcpyHostToDevice) == cudaSuccess;
-  };
-  (void)stream;
-  if (!upload(units, dp->d_units) || !upload(pl.cta_off, dp->d_cta_off) || !upload(groups, dp->d_groups)) {
-    cudaFree(dp->d_units);
-    cudaFree(dp->d_cta_off);
-    cudaFree(dp->d_groups);
-    return ATTN_ENOMEM;
-  }
-  if (st.plans.size() > 256) st.plans.clear();   // bounded cache (device buffers of dropped plans leak)
-  out = dp.get();
-  st.plans.emplace(key, std::move(dp));
   return ATTN_OK;
 }
 
-int ensure_workspace(DevState& st, int n_partials, int d) {
-  const size_t need_o = static_cast<size_t>(n_partials) * kNSub * kBM * d * 2;   // fp16
-  const size_t need_ml = static_cast<size_t>(n_partials) * kNSub * kBM * 2 * sizeof(float);
-  if (need_o > st.part_o_bytes) {
-    if (st.part_o) cudaFree(st.part_o);
-    st.part_o = nullptr;
-    st.part_o_bytes = 0;
-    if (cudaMalloc(&st.part_o, need_o) != cudaSuccess) return ATTN_ENOMEM;
-    st.part_o_bytes = need_o;
+namespace {
+
+void release_plan(DevPlan& pl, cudaStream_t stream) {
+  // the free is ordered after the upload and after every launch that read it
+  if (pl.ready) {
+    cudaStreamWaitEvent(stream, pl.ready, 0);
+    cudaEventDestroy(pl.ready);
   }
-  if (need_ml > st.part_ml_bytes) {
-    if (st.part_ml) cudaFree(st.part_ml);
-    st.part_ml = nullptr;
-    st.part_ml_bytes = 0;
-    if (cudaMalloc(&st.part_ml, need_ml) != cudaSuccess) return ATTN_ENOMEM;
-    st.part_ml_bytes = need_ml;
+  for (auto& u : pl.uses) {
+    cudaStreamWaitEvent(stream, u.second, 0);
+    cudaEventDestroy(u.second);
   }
+  if (pl.dbuf && pl.async_alloc) cudaFreeAsync(pl.dbuf, stream);
+  pl.dbuf = nullptr;
+}
+
+// The device copy of `key`'s schedule, current on `stream` when the call's
+// kernels run.  `make` builds the host plan.
+// A schedule that `inline_ok` accepts travels in the kernel parameters and
+// gets no device copy.
+template <class MakeFn, class InlineFn>
+int get_plan(LruCache<PlanKey, DevPlan>& cache, const PlanKey& key, cudaStream_t stream, MakeFn make,
+             InlineFn inline_ok, DevPlan*& out) {
+  const bool cap = capturing(stream);
+  DevPlan* pl = cache.find(key);
+  if (!pl) {
+    auto dp = std::make_unique<DevPlan>();
+    if (!make(dp->host)) return ATTN_EINVAL;
+    const Plan& h = dp->host;
+    std::vector<int>& f = dp->flat;
+    f.reserve(h.units.size() * kUnitInts + h.cta_off.size() + h.groups.size() * kGroupInts);
+    for (const PlanUnit& u : h.units) {
+      const int e[kUnitInts] = {u.bh, u.m_block, u.kv_begin, u.kv_end, u.split, u.n_split, u.slot, u.cta};
+      f.insert(f.end(), e, e + kUnitInts);
+    }
+    dp->off_cta = f.size();
+    f.insert(f.end(), h.cta_off.begin(), h.cta_off.end());
+    dp->off_groups = f.size();
+    for (const PlanGroup& g : h.groups) {
+      const int e[kGroupInts] = {g.bh, g.m_block, g.slot_base, g.n_split};
+      f.insert(f.end(), e, e + kGroupInts);
+    }
+    const size_t bytes = f.size() * sizeof(int);
+    if (inline_ok(dp->host)) {
+      // no device copy
+    } else if (cap) {
+      if (malloc_in_capture(reinterpret_cast<void**>(&dp->dbuf), bytes) != cudaSuccess) return ATTN_ENOMEM;
+    } else {
+      if (cudaMallocAsync(reinterpret_cast<void**>(&dp->dbuf), bytes, stream) != cudaSuccess) return ATTN_ENOMEM;
+      dp->async_alloc = true;
+    }
+    pl = cache.insert(key, std::move(dp), !cap, [&](DevPlan& v) { release_plan(v, stream); });
+  }
+  if (!pl->dbuf) {
+    // inline schedule
+  } else if (cap) {
+    // the graph carries its own upload, re-run at every replay
+    pl->pinned = true;
+    if (int rc = upload_ints(pl->dbuf, pl->flat.data(), pl->flat.size(), stream)) return rc;
+  } else if (!pl->uploaded) {
+    if (int rc = upload_ints(pl->dbuf, pl->flat.data(), pl->flat.size(), stream)) return rc;
+    if (!pl->ready && cudaEventCreateWithFlags(&pl->ready, cudaEventDisableTiming) != cudaSuccess) return ATTN_ELAUNCH;
+    if (cudaEventRecord(pl->ready, stream) != cudaSuccess) return ATTN_ELAUNCH;
+    pl->uploaded = true;
+    pl->up_stream = stream;
+  } else if (pl->up_stream != stream) {
+    if (cudaStreamWaitEvent(stream, pl->ready, 0) != cudaSuccess) return ATTN_ELAUNCH;
+  }
+  out = pl;
+  return ATTN_OK;
+}
+
+// Records, outside captures, that the kernels just enqueued on `stream` read
+// `pl` (its memory is freed only after them).
+void note_use(DevPlan* pl, cudaStream_t stream) {
+  if (!pl || !pl->dbuf || pl->pinned || capturing(stream)) return;
+  for (auto& u : pl->uses)
+    if (u.first == stream) {
+      cudaEventRecord(u.second, stream);
+      return;
+    }
+  cudaEvent_t e;
+  if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return;
+  cudaEventRecord(e, stream);
+  pl->uses.emplace_back(stream, e);
+}
+
+int ws_ensure(Workspace& w, size_t need, cudaStream_t stream, bool zero) {
+  const bool cap = capturing(stream);
+  if (need <= w.bytes) {
+    if (cap) w.pinned = true;
+    return ATTN_OK;
+  }
+  const size_t nb = std::max(need, 2 * w.bytes);
+  void* np = nullptr;
+  if (cap) {
+    if (malloc_in_capture(&np, nb) != cudaSuccess) return ATTN_ENOMEM;
+  } else {
+    if (cudaMallocAsync(&np, nb, stream) != cudaSuccess) return ATTN_ENOMEM;
+  }
+  if (zero && cudaMemsetAsync(np, 0, nb, stream) != cudaSuccess) return ATTN_ELAUNCH;
+  if (w.ptr) {
+    if (w.pinned || !w.async_alloc || cap)
+      w.kept.push_back(w.ptr);
+    else
+      cudaFreeAsync(w.ptr, stream);
+  }
+  w.ptr = np;
+  w.bytes = nb;
+  w.async_alloc = !cap;
+  w.pinned = cap;
+  return ATTN_OK;
+}
+
+// The dense forward on CTA pairs (head_dim 128): split pieces are merged
+// inside the kernel, so one launch per call.
+int fwd_pair(DevState& st, int dev, bool bf16, const void* q, const void* k, const void* v, void* o, float* lse,
+             int B, int Hq, int Hkv, int Lq, int Lk, int d, bool causal, float scale, cudaStream_t stream) {
+  const PlanKey key{B, Hq, Hkv, Lq, Lk, d, causal ? 1 : 0};
+  auto fits = [](const Plan& h) {
+    return static_cast<int>(h.units.size()) <= kPairInlineUnits && h.n_ctas <= kInlinePairs;
+  };
+  DevPlan* pl = nullptr;
+  int rc = get_plan(
+      st.pair_plans, key, stream,
+      [&](Plan& h) { return make_plan_pair(B, Hq, Hkv, Lq, Lk, causal, st.sm_count / 2, h); }, fits, pl);
+  if (rc) return rc;
+  static thread_local PairParams p;
+  std::memset(&p, 0, sizeof(p));
+  const int Lk_map = Lk > 0 ? Lk : 1;
+  if ((rc = get_map(st, q, bf16, d, Hq, Lq, B, p.tm_q))) return rc;
+  if ((rc = get_map(st, k, bf16, d, Hkv, Lk_map, B, p.tm_k))) return rc;
+  if ((rc = get_map(st, v, bf16, d, Hkv, Lk_map, B, p.tm_v, 1, kPairBN, d / 2))) return rc;
+  if ((rc = get_map(st, o, bf16, d, Hq, Lq, B, p.tm_o))) return rc;
+  p.o = o;
+  p.lse = lse;
+  const Plan& h = pl->host;
+  if (h.n_partials > 0) {
+    const size_t n = static_cast<size_t>(h.n_partials);
+    const size_t u_bytes = n * 2 * kPairRows * d * 4;
+    const size_t ml_bytes = n * 2 * kPairRows * 2 * sizeof(float);
+    if ((rc = ws_ensure(st.pair_part, u_bytes + ml_bytes, stream, false))) return rc;
+    if ((rc = ws_ensure(st.pair_cnt, n * 2 * sizeof(unsigned long long), stream, true))) return rc;
+    p.part_u = static_cast<float*>(st.pair_part.ptr);
+    p.part_ml = reinterpret_cast<float*>(static_cast<char*>(st.pair_part.ptr) + u_bytes);
+    p.counters = static_cast<unsigned long long*>(st.pair_cnt.ptr);
+  }
+  if (++st.epoch == 0) st.epoch = 1;
+  p.epoch = st.epoch;
+  p.err = st.err_word;
+  p.trace = g_trace;
+  p.trace_cap = g_trace_cap;
+  p.timeout_ns = g_timeout_ns.load();
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Lq = Lq;
+  p.Lk = Lk;
+  p.group = Hq / Hkv;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  if (fits(h)) {
+    p.n_inline = 1;
+    std::memcpy(p.units_inline, pl->flat.data(), h.units.size() * kUnitInts * sizeof(int));
+    std::memcpy(p.pair_off_inline, h.cta_off.data(), h.cta_off.size() * sizeof(int));
+  } else {
+    p.units = pl->units();
+    p.pair_off = pl->cta_off();
+  }
+  if (h.n_ctas <= 0) return ATTN_OK;
+  ProfileRec* prof = profile_slot(dev);
+  if (prof && cudaEventRecord(prof->start, stream) != cudaSuccess) return ATTN_ELAUNCH;
+  if (pair_launcher_d128(bf16, causal)(p, h.n_ctas, h.n_partials > 0, stream) != cudaSuccess) return ATTN_ELAUNCH;
+  g_launches.fetch_add(1);
+  note_use(pl, stream);
+  if (prof && (cudaEventRecord(prof->mid, stream) != cudaSuccess || cudaEventRecord(prof->end, stream) != cudaSuccess))
+    return ATTN_ELAUNCH;
   return ATTN_OK;
 }
 
@@ -244,8 +446,10 @@ int fwd(bool bf16, const void* q, const void* k, const void* v, void* o, float* 
   int rc = init_device(dev, st);
   if (rc) return rc;
   if (!st.supported) return ATTN_EUNSUPPORTED;
+  if (!varlen && d == 128 && g_pair_forward.load() != 0 && st.sm_count >= 2)
+    return fwd_pair(st, dev, bf16, q, k, v, o, lse, B, Hq, Hkv, Lq, Lk, d, causal != 0, scale, stream);
 
-  FwdParams p;
+  static thread_local FwdParams p;
   std::memset(&p, 0, sizeof(p));
   const int Lk_map = Lk > 0 ? Lk : 1;
   const int Bm = varlen ? 1 : B;
@@ -284,18 +488,30 @@ int fwd(bool bf16, const void* q, const void* k, const void* v, void* o, float* 
   int grid = 0;
   DevPlan* plan = nullptr;
   if (!varlen) {
-    if ((rc = get_plan(st, B, Hq, Hkv, Lq, Lk, d, causal != 0, stream, plan))) return rc;
+    const PlanKey key{B, Hq, Hkv, Lq, Lk, d, causal};
+    // the combine pass reads the split groups from the device copy
+    auto fits = [](const Plan& h) {
+      return h.groups.empty() && static_cast<int>(h.units.size()) <= kInlineUnits && h.n_ctas <= kInlineCtas;
+    };
+    rc = get_plan(
+        st.plans, key, stream,
+        [&](Plan& h) { return make_plan(B, Hq, Hkv, Lq, Lk, d, causal != 0, st.sm_count, h); }, fits, plan);
+    if (rc) return rc;
     if (plan->host.n_partials > 0) {
-      if ((rc = ensure_workspace(st, plan->host.n_partials, d))) return rc;
-      p.part_o = st.part_o;
-      p.part_ml = st.part_ml;
+      const size_t n = static_cast<size_t>(plan->host.n_partials);
+      const size_t o_bytes = n * kNSub * kBM * d * 4;   // fp32
+      const size_t ml_bytes = n * kNSub * kBM * 2 * sizeof(float);
+      if ((rc = ws_ensure(st.part, o_bytes + ml_bytes, stream, false))) return rc;
+      p.part_o = st.part.ptr;
+      p.part_ml = reinterpret_cast<float*>(static_cast<char*>(st.part.ptr) + o_bytes);
     }
-    p.units = plan->d_units;
-    p.cta_off = plan->d_cta_off;
     if (static_cast<int>(plan->host.units.size()) <= kInlineUnits && plan->host.n_ctas <= kInlineCtas) {
       p.n_inline = 1;
-      std::memcpy(p.units_inline, plan->flat_units.data(), plan->flat_units.size() * sizeof(int));
+      std::memcpy(p.units_inline, plan->flat.data(), plan->host.units.size() * kUnitInts * sizeof(int));
       std::memcpy(p.cta_off_inline, plan->host.cta_off.data(), plan->host.cta_off.size() * sizeof(int));
+    } else {
+      p.units = plan->units();
+      p.cta_off = plan->cta_off();
     }
     grid = plan->host.n_ctas;
   } else {
@@ -312,9 +528,9 @@ int fwd(bool bf16, const void* q, const void* k, const void* v, void* o, float* 
   if (prof && cudaEventRecord(prof->mid, stream) != cudaSuccess) return ATTN_ELAUNCH;
   if (plan && !plan->host.groups.empty()) {
     CombineParams cp;
-    cp.groups = plan->d_groups;
-    cp.part_o = st.part_o;
-    cp.part_ml = st.part_ml;
+    cp.groups = plan->groups();
+    cp.part_o = p.part_o;
+    cp.part_ml = p.part_ml;
     cp.o = o;
     cp.lse = lse;
     cp.Hq = Hq;
@@ -323,6 +539,7 @@ int fwd(bool bf16, const void* q, const void* k, const void* v, void* o, float* 
     if (cl(cp, static_cast<int>(plan->host.groups.size()), stream) != cudaSuccess) return ATTN_ELAUNCH;
     g_launches.fetch_add(1);
   }
+  note_use(plan, stream);
   if (prof && cudaEventRecord(prof->end, stream) != cudaSuccess) return ATTN_ELAUNCH;
   return ATTN_OK;
 }
@@ -503,6 +720,72 @@ int attn_profile_read(float* main_ms, float* call_ms, int max, int* n) {
     if (cudaEventElapsedTime(&call_ms[i], r.start, r.end) != cudaSuccess) return ATTN_ELAUNCH;
   }
   cudaSetDevice(prev);
+  return ATTN_OK;
+}
+
+void attn_set_pair_forward(int enable) { attn::g_pair_forward.store(enable ? 1 : 0); }
+
+int attn_pair_forward_used(int d, int varlen) {
+  return (attn::g_pair_forward.load() != 0 && d == 128 && varlen == 0) ? 1 : 0;
+}
+
+int attn_plan_pair(int B, int Hq, int Hkv, int Lq, int Lk, int causal, int num_pairs, int* units, int max_units,
+                   int* n_units, int* n_pairs, int* n_partials) {
+  if (!n_units || !n_pairs || !n_partials || (max_units > 0 && !units)) return ATTN_EINVAL;
+  if (causal != 0 && causal != 1) return ATTN_EINVAL;
+  attn::Plan pl;
+  if (!attn::make_plan_pair(B, Hq, Hkv, Lq, Lk, causal != 0, num_pairs, pl)) return ATTN_EINVAL;
+  *n_units = static_cast<int>(pl.units.size());
+  *n_pairs = pl.n_ctas;
+  *n_partials = pl.n_partials;
+  if (static_cast<int>(pl.units.size()) > max_units) return ATTN_ENOMEM;
+  for (size_t i = 0; i < pl.units.size(); ++i) {
+    const attn::PlanUnit& u = pl.units[i];
+    const int e[attn::kUnitInts] = {u.bh, u.m_block, u.kv_begin, u.kv_end, u.split, u.n_split, u.slot, u.cta};
+    std::memcpy(units + i * attn::kUnitInts, e, sizeof(e));
+  }
+  return ATTN_OK;
+}
+
+int attn_cache_stats(int* plans, int* pinned) {
+  if (!plans || !pinned) return ATTN_EINVAL;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ELAUNCH;
+  std::lock_guard<std::mutex> lock(attn::g_mu);
+  attn::DevState& st = attn::g_dev[dev];
+  int n = 0, pn = 0;
+  auto count = [&](attn::DevPlan& e) {
+    ++n;
+    if (e.pinned) ++pn;
+  };
+  st.plans.for_each(count);
+  st.pair_plans.for_each(count);
+  *plans = n;
+  *pinned = pn;
+  return ATTN_OK;
+}
+
+int attn_selftest_plan_cache(int n_keys, int capacity, int pin_every, int* max_live, int* released) {
+  // the cache policy alone, with host-side entries: no device memory
+  if (!max_live || !released || n_keys < 0 || capacity <= 0) return ATTN_EINVAL;
+  struct Fake {
+    bool pinned = false;
+    uint64_t lru = 0;
+  };
+  attn::LruCache<int, Fake> c(static_cast<size_t>(capacity));
+  int rel = 0, mx = 0;
+  auto release = [&](Fake&) { ++rel; };
+  for (int i = 0; i < n_keys; ++i) {
+    Fake* f = c.find(i % (2 * capacity + 7));
+    if (!f) {
+      auto e = std::make_unique<Fake>();
+      e->pinned = pin_every > 0 && (i % pin_every) == 0;
+      c.insert(i % (2 * capacity + 7), std::move(e), true, release);
+    }
+    mx = std::max(mx, static_cast<int>(c.size()));
+  }
+  *max_live = mx;
+  *released = rel;
   return ATTN_OK;
 }
 

@@ -19,6 +19,11 @@ int device_info(int dev, DeviceInfo& out);
 // 16-bit tensor, box 64 x 1 x 128 x 1, without caching.  Allocates nothing.
 int encode_map(const void* ptr, bool bf16, int d, int H, int L, int B, CUtensorMap& out);
 
+// Writes n ints from host memory to device memory `dst` in stream order: a
+// small kernel carries the values in its parameters (no pinned buffer, no
+// synchronisation, nothing allocated).  Counts its launches.
+int upload_ints(int* dst, const int* src, size_t n, cudaStream_t stream);
+
 // Current barrier-wait time limit and the launch counter of attn_launch_count().
 unsigned long long wait_timeout_ns();
 // The phase-trace buffer set by attn_trace_enable (traced build), or null.

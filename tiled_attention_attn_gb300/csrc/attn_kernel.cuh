@@ -165,7 +165,7 @@ struct Tracer {
                     (static_cast<unsigned long long>(t & 0xff) << 48) |
                     (static_cast<unsigned long long>(a & 0xffffff) << 24) |
                     static_cast<unsigned long long>(b & 0xffffff);
-      base[2 * n + 1] = clock64();
+      base[2 * n + 1] = (tag >= kTagGEnter) ? global_timer_ns() : clock64();
       ++n;
     }
   }
@@ -568,6 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     Tracer tr;
     tr.init(p, t == 0 ? kTrSoftmax0 : kTrSoftmax1);
     if (row != 0) tr.off();
+    tr.rec(kTagGEnter, t, 0, 0);
     // packed heads (varlen): TMEM lane `row` is query row >> lp of the
     // sub-tile, head row & (2^lp - 1) of the unit's group
     const int lp = VARLEN ? p.pack_log2 : 0;
@@ -647,13 +648,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
           p.lse[li] = lse;
         }
       } else {
-        // split-KV piece: store its own normalised output O_s = u_s / l_s in
-        // fp16 and (m, l) in fp32; the combine pass forms the convex mix
-        // sum_s w_s O_s / sum_s w_s, so the fp16 rounding error stays below
-        // 2^-12 |O|.  Layout [slot][t][D/8][row][8]: a warp's 32 rows of one
-        // 8-column group are 512 contiguous bytes.
-        const size_t pbase = (static_cast<size_t>(U.slot) * kNSub + t) * (D / 8);
-        uint4* po = reinterpret_cast<uint4*>(p.part_o);
+        // split-KV piece: store its own normalised output O_s = u_s / l_s and
+        // (m, l) in fp32; the combine pass forms the convex mix
+        // sum_s w_s O_s / sum_s w_s.  fp32 keeps the range and precision of
+        // the accumulator (a 16-bit copy would overflow or go subnormal on
+        // large- or small-magnitude values that the unsplit path handles).
+        // Layout [slot][t][D/4][row][4]: a warp's 32 rows of one 4-column
+        // group are 512 contiguous bytes.
+        const size_t pbase = (static_cast<size_t>(U.slot) * kNSub + t) * (D / 4);
+        float4* po = reinterpret_cast<float4*>(p.part_o);
         if (n_act > 0) {
           const float inv_l = 1.0f / st.l;
 #pragma unroll
@@ -662,12 +665,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             tmem_ld_32x32b_x32(t_o + c * 32, o);
             tmem_wait_ld(o);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              po[(pbase + c * 4 + i) * kBM + row] =
-                  make_uint4(pack2<false>(__uint_as_float(o[8 * i]) * inv_l, __uint_as_float(o[8 * i + 1]) * inv_l),
-                             pack2<false>(__uint_as_float(o[8 * i + 2]) * inv_l, __uint_as_float(o[8 * i + 3]) * inv_l),
-                             pack2<false>(__uint_as_float(o[8 * i + 4]) * inv_l, __uint_as_float(o[8 * i + 5]) * inv_l),
-                             pack2<false>(__uint_as_float(o[8 * i + 6]) * inv_l, __uint_as_float(o[8 * i + 7]) * inv_l));
+            for (int i = 0; i < 8; ++i)
+              po[(pbase + c * 8 + i) * kBM + row] =
+                  make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
+                              __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
           }
         }
         const size_t prow = (static_cast<size_t>(U.slot) * kNSub + t) * kBM + row;
@@ -679,6 +680,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     }
   }
 
+  if (warp < 8) {
+    Tracer tr;
+    tr.init(p, (warp >> 2) == 0 ? kTrSoftmax0 : kTrSoftmax1);
+    if ((threadIdx.x & 127) != 0) tr.off();
+    tr.n = (ATTN_TRACE && p.trace) ? p.trace_cap - 1 : 0;   // the exit stamp goes in the last slot
+    tr.rec(kTagGExit, 0, 0, 0);
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == kWarpMMA) {
@@ -689,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 }
 
 // ---------------------------------------------------------------------------
-// split-KV combine.  Piece s holds O_s = u_s / l_s (fp16) and (m_s, l_s);
+// split-KV combine.  Piece s holds O_s = u_s / l_s (fp32) and (m_s, l_s);
 // with M = max_s m_s and w_s = 2^(m_s - M) l_s (the same r rescaling as
 // across tiles), O = sum_s w_s O_s / sum_s w_s and lse = M ln 2 + ln sum_s w_s.
 // Grid (groups, 2 sub-tiles, D/16 column blocks), one thread per query row
@@ -708,12 +716,12 @@ __global__ void __launch_bounds__(kBM) attn_combine_kernel(const __grid_constant
   const int b = bh / p.Hq, h = bh - b * p.Hq;
   grid_wait_prerequisites();
   const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
-  const uint4* po = reinterpret_cast<const uint4*>(p.part_o);
+  const float4* po = reinterpret_cast<const float4*>(p.part_o);
   const size_t ml_base = static_cast<size_t>(slot0) * kNSub * kBM + t * kBM + row;
-  const size_t o_base = (static_cast<size_t>(slot0) * kNSub + t) * (D / 8) + cb * 2;
+  const size_t o_base = (static_cast<size_t>(slot0) * kNSub + t) * (D / 4) + cb * 4;
   constexpr size_t kMlStride = kNSub * kBM;      // per piece, in float2
-  constexpr size_t kOStride = kNSub * (D / 8);   // per piece, in 8-column groups
-  // Pieces in batches of eight: every load of a batch ((m, l) and this
+  constexpr size_t kOStride = kNSub * (D / 4);   // per piece, in 4-column groups
+  // Pieces in batches of four: every load of a batch ((m, l) and this
   // thread's 16 columns of O_s) is issued before any is used, so a batch
   // costs one L2 round trip.  Batches merge with a running max, the same
   // r rescaling again.
@@ -721,20 +729,20 @@ __global__ void __launch_bounds__(kBM) attn_combine_kernel(const __grid_constant
   float acc[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
-  for (int s0 = 0; s0 < ns; s0 += 8) {
-    float2 mlv[8];
-    uint4 x[8][2];
+  for (int s0 = 0; s0 < ns; s0 += 4) {
+    float2 mlv[4];
+    float4 x[4][4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < 4; ++i) {
       const bool in = s0 + i < ns;
       mlv[i] = in ? __ldcg(ml + ml_base + (s0 + i) * kMlStride) : make_float2(-INFINITY, 0.0f);
 #pragma unroll
-      for (int c = 0; c < 2; ++c)
-        x[i][c] = in ? __ldcg(po + (o_base + (s0 + i) * kOStride + c) * kBM + row) : make_uint4(0, 0, 0, 0);
+      for (int c = 0; c < 4; ++c)
+        x[i][c] = in ? __ldcg(po + (o_base + (s0 + i) * kOStride + c) * kBM + row) : make_float4(0, 0, 0, 0);
     }
     float mb = M;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) mb = fmaxf(mb, mlv[i].x);
+    for (int i = 0; i < 4; ++i) mb = fmaxf(mb, mlv[i].x);
     if (mb == -INFINITY) continue;   // no piece so far saw a key
     const float r = (M == -INFINITY) ? 0.0f : ex2_approx(M - mb);
     M = mb;
@@ -742,19 +750,16 @@ __global__ void __launch_bounds__(kBM) attn_combine_kernel(const __grid_constant
 #pragma unroll
     for (int i = 0; i < 16; ++i) acc[i] *= r;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < 4; ++i) {
       if (mlv[i].x == -INFINITY) continue;   // an empty piece (its O_s was never written)
       const float w = ex2_approx(mlv[i].x - M) * mlv[i].y;
       L += w;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const uint32_t wds[4] = {x[i][c].x, x[i][c].y, x[i][c].z, x[i][c].w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&wds[k]));
-          acc[8 * c + 2 * k] += w * f.x;
-          acc[8 * c + 2 * k + 1] += w * f.y;
-        }
+      for (int c = 0; c < 4; ++c) {
+        acc[4 * c] += w * x[i][c].x;
+        acc[4 * c + 1] += w * x[i][c].y;
+        acc[4 * c + 2] += w * x[i][c].z;
+        acc[4 * c + 3] += w * x[i][c].w;
       }
     }
   }

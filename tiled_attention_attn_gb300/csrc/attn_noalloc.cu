@@ -41,13 +41,12 @@ struct NoAllocDevice {
   bool ready = false;
   unsigned char* scratch = nullptr;   // device address of g_noalloc_scratch on this device
   DeviceInfo info;
-  // host copy of the last schedule and whether the device array holds it
+  // host copy of the last shape's schedule (rebuilt when the shape changes)
   bool have_plan = false;
   ShapeKey key{};
   Plan plan;
   std::vector<int> units, groups;
   size_t off_cta = 0, off_groups = 0, off_ml = 0;
-  bool loaded = false;
 };
 
 std::mutex g_na_mu;
@@ -102,7 +101,7 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
   if (rc) return rc;
   if (!st.info.supported) return ATTN_EUNSUPPORTED;
 
-  FwdParams p;
+  static thread_local FwdParams p;
   std::memset(&p, 0, sizeof(p));
   const int Lk_map = Lk > 0 ? Lk : 1;
   const int Bm = varlen ? 1 : B;
@@ -130,7 +129,6 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
     const ShapeKey key{B, Hq, Hkv, Lq, Lk, d, causal};
     if (!st.have_plan || st.key != key) {
       st.have_plan = false;
-      st.loaded = false;
       if (!make_plan(B, Hq, Hkv, Lq, Lk, d, causal != 0, st.info.sm_count, st.plan)) return ATTN_EINVAL;
       const Plan& pl = st.plan;
       st.units.assign(pl.units.size() * kUnitInts, 0);
@@ -148,27 +146,33 @@ extern "C" int attn_fwd_noalloc(const void* q, const void* k, const void* v, voi
       st.off_cta = align256(st.units.size() * sizeof(int));
       st.off_groups = st.off_cta + align256(pl.cta_off.size() * sizeof(int));
       const size_t sched = st.off_groups + align256(st.groups.size() * sizeof(int));
-      st.off_ml = align256(static_cast<size_t>(pl.n_partials) * kNSub * kBM * d * 2);   // fp16 partials
+      st.off_ml = align256(static_cast<size_t>(pl.n_partials) * kNSub * kBM * d * 4);   // fp32 partials
       const size_t part = st.off_ml + static_cast<size_t>(pl.n_partials) * kNSub * kBM * 2 * sizeof(float);
       if (sched > kSchedBytes || part > kPartBytes) return ATTN_ETOOLARGE;
       st.key = key;
       st.have_plan = true;
     }
-    if (!st.loaded) {
-      // stream-ordered copies from host memory into the array (no allocation)
-      unsigned char* s = st.scratch;
-      if (cudaMemcpyAsync(s, st.units.data(), st.units.size() * sizeof(int), cudaMemcpyHostToDevice, stream) !=
-              cudaSuccess ||
-          cudaMemcpyAsync(s + st.off_cta, st.plan.cta_off.data(), st.plan.cta_off.size() * sizeof(int),
-                          cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    // The schedule the kernels read: small ones travel in the launch
+    // parameters; larger ones are written into the array on every call, in
+    // stream order just before the kernels (another call with another shape
+    // in between cannot leave a stale schedule behind).
+    const Plan& pl = st.plan;
+    const bool inline_ok = pl.groups.empty() && static_cast<int>(pl.units.size()) <= kInlineUnits &&
+                           pl.n_ctas <= kInlineCtas;
+    if (inline_ok) {
+      p.n_inline = 1;
+      std::memcpy(p.units_inline, st.units.data(), st.units.size() * sizeof(int));
+      std::memcpy(p.cta_off_inline, pl.cta_off.data(), pl.cta_off.size() * sizeof(int));
+    } else {
+      int* s = reinterpret_cast<int*>(st.scratch);
+      if (upload_ints(s, st.units.data(), st.units.size(), stream) ||
+          upload_ints(reinterpret_cast<int*>(st.scratch + st.off_cta), pl.cta_off.data(), pl.cta_off.size(), stream) ||
+          (!st.groups.empty() &&
+           upload_ints(reinterpret_cast<int*>(st.scratch + st.off_groups), st.groups.data(), st.groups.size(), stream)))
         return ATTN_ELAUNCH;
-      if (!st.groups.empty() && cudaMemcpyAsync(s + st.off_groups, st.groups.data(), st.groups.size() * sizeof(int),
-                                                cudaMemcpyHostToDevice, stream) != cudaSuccess)
-        return ATTN_ELAUNCH;
-      st.loaded = true;
+      p.units = reinterpret_cast<const int*>(st.scratch);
+      p.cta_off = reinterpret_cast<const int*>(st.scratch + st.off_cta);
     }
-    p.units = reinterpret_cast<const int*>(st.scratch);
-    p.cta_off = reinterpret_cast<const int*>(st.scratch + st.off_cta);
     p.part_o = st.scratch + kSchedBytes;
     p.part_ml = reinterpret_cast<float*>(st.scratch + kSchedBytes + st.off_ml);
     grid = st.plan.n_ctas;

@@ -37,12 +37,16 @@ enum TraceTag : int {
   kTagQFull = 10, kTagSIssue = 11, kTagPFull = 12, kTagPVIssue = 13, kTagKFull = 14, kTagVFull = 15,
   kTagUnitEnd = 16, kTagVWait = 17, kTagPWait = 18,
   kTagSFull = 20, kTagPArrive = 21, kTagODone = 23, kTagEpiDone = 24, kTagUnitBegin = 25,
+  kTagMaxDone = 26, kTagPvWait = 27, kTagPvDone = 28, kTagSFreeWait = 29,
+  kTagPartDone = 30, kTagSlice = 31, kTagMergeDone = 32, kTagEpiStore = 33,
+  kTagGEnter = 40, kTagGExit = 41,   // the second word holds %globaltimer (ns) instead of the SM clock
 };
 
 // Wait-site codes (low byte of ATTN_DEVERR_WAIT_TIMEOUT).
 enum WaitSite : int {
   kSiteQEmpty = 1, kSiteKEmpty, kSiteVEmpty, kSiteQFull, kSiteKFull, kSiteVFull,
-  kSiteSFull, kSitePFull, kSiteODone, kSiteDrain, kSiteSelftest, kSiteDsFull
+  kSiteSFull, kSitePFull, kSiteODone, kSiteDrain, kSiteSelftest, kSiteDsFull,
+  kSiteSFree, kSitePvDone, kSiteMerge, kSiteXchg
 };
 
 struct FwdParams {
@@ -56,7 +60,7 @@ struct FwdParams {
   const int* cu_seqlens_k;     // varlen only: key row offsets (B+1); the same array for self-attention
   const int* units;            // dense schedule, kUnitInts per unit, grouped by CTA
   const int* cta_off;          // dense: first unit of every CTA, n_ctas + 1 entries
-  void* part_o;                // split-KV partial outputs O_s = u_s / l_s, fp16 [slot][2][D/8][128][8]
+  void* part_o;                // split-KV partial outputs O_s = u_s / l_s, fp32 [slot][2][D/4][128][4]
   float* part_ml;              // split-KV partial (m, l) [slot][2][128][2]
   int* err;                    // device error word
   unsigned long long* trace;   // optional phase trace (traced build, attn_trace_enable), else null
@@ -76,6 +80,49 @@ struct FwdParams {
   int n_inline;
   int cta_off_inline[kInlineCtas + 1];
   int units_inline[kInlineUnits * kUnitInts];
+};
+
+// ---------------------------------------------------------------------------
+// The CTA-pair forward (tcgen05 .cta_group::2): a work unit is a 256-row
+// query block (128 rows in each CTA of the pair) against a range of 256-key
+// tiles; each CTA holds its own query rows, half of every key tile (128 keys)
+// and half of the columns of every value tile (d/2 of 256 keys).
+// ---------------------------------------------------------------------------
+constexpr int kPairThreads = 384;          // 8 softmax warps, TMA warp, two MMA warps, 1 spare warp
+// Registers: launched at 168 per thread (384 x 168 = 64,512); the softmax
+// warpgroups raise theirs to 216 and the third warpgroup lowers its to 72:
+// 256 x 216 + 128 x 72 = 64,512, exactly the launch allocation.
+constexpr int kPairRegsSoftmax = 216;
+constexpr int kPairRegsOther = 72;
+static_assert(256 * kPairRegsSoftmax + 128 * kPairRegsOther <= kPairThreads * 168, "register split");
+constexpr int kPairRows = 128;             // query rows per CTA
+constexpr int kPairBlock = 2 * kPairRows;  // query rows per unit (both CTAs)
+constexpr int kPairBN = 256;               // keys per key tile (128 in each CTA)
+constexpr int kInlinePairs = 80;           // pair schedules up to this many pairs travel inline
+constexpr int kPairInlineUnits = 160;
+
+struct PairParams {
+  CUtensorMap tm_q;            // (d, Hq, Lq, B), box 64 x 1 x 128 x 1
+  CUtensorMap tm_k;            // (d, Hkv, Lk, B), box 64 x 1 x 128 x 1
+  CUtensorMap tm_v;            // (d, Hkv, Lk, B), box d/2 x 1 x 256 x 1
+  CUtensorMap tm_o;            // (d, Hq, Lq, B), box 64 x 1 x 128 x 1 (the epilogue's stores)
+  void* o;                     // (B, Lq, Hq, d)
+  float* lse;                  // (B, Hq, Lq)
+  const int* units;            // kUnitInts per unit, grouped by pair
+  const int* pair_off;         // first unit of every pair, n_pairs + 1 entries
+  float* part_u;               // split pieces: unnormalised u, fp32 [slot][2][d/4][128][4]
+  float* part_ml;              // split pieces: (m, l) [slot][2][128] float2
+  unsigned long long* counters;   // split pieces: one word per (slot, CTA of the pair)
+  unsigned int epoch;          // this call's tag in the counter words
+  int* err;
+  unsigned long long* trace;   // optional phase trace (traced build, attn_trace_enable), else null
+  int trace_cap;               // events per stream per CTA
+  unsigned long long timeout_ns;
+  int B, Hq, Hkv, Lq, Lk, group;
+  float scale_log2;            // scale * log2(e)
+  int n_inline;                // 1: the schedule is in the arrays below
+  int pair_off_inline[kInlinePairs + 1];
+  int units_inline[kPairInlineUnits * kUnitInts];
 };
 
 struct CombineParams {

@@ -181,4 +181,136 @@ bool make_plan(int B, int Hq, int Hkv, int Lq, int Lk, int d, bool causal, int n
   return true;
 }
 
+// ---------------------------------------------------------------------------
+// CTA-pair schedule: a unit is a 256-row query block (128 rows per CTA of the
+// pair) against a range of 256-key tiles; both CTAs run the same tiles, so a
+// unit's cost is its tile count plus a fixed cost per unit (query load,
+// pipeline fill, epilogue) and, for split pieces, the partial write and the
+// share of the merge.
+// ---------------------------------------------------------------------------
+namespace {
+
+struct PairBlock {
+  int bh, mb, n_tiles;
+};
+
+void build_pair_units(const std::vector<PairBlock>& blocks, double target, double c_unit, double c_split,
+                      std::vector<Cand>& units, bool& any_split) {
+  units.clear();
+  any_split = false;
+  for (size_t i = 0; i < blocks.size(); ++i) {
+    const PairBlock& b = blocks[i];
+    int n = 1;
+    if (b.n_tiles > 1 && static_cast<double>(b.n_tiles) > target) {
+      n = static_cast<int>(std::ceil(static_cast<double>(b.n_tiles) / target));
+      n = std::min(n, std::min(b.n_tiles, kMaxSplits));
+    }
+    if (n > 1) any_split = true;
+    for (int s = 0; s < n; ++s) {
+      const int a = static_cast<int>(static_cast<long>(s) * b.n_tiles / n);
+      const int e = static_cast<int>(static_cast<long>(s + 1) * b.n_tiles / n);
+      units.push_back({static_cast<int>(i), a, e, s, n, (e - a) + c_unit + (n > 1 ? c_split : 0.0)});
+    }
+  }
+}
+
+}  // namespace
+
+bool make_plan_pair(int B, int Hq, int Hkv, int Lq, int Lk, bool causal, int num_pairs, Plan& out) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Lq <= 0 || Lk < 0 || num_pairs <= 0) return false;
+  const int group = Hq / Hkv;
+  const int n_mb = (Lq + kPairBlock - 1) / kPairBlock;
+  const long long n_blocks = static_cast<long long>(B) * Hq * n_mb;
+  if (n_blocks > (1LL << 26) || static_cast<long long>(B) * Hq > std::numeric_limits<int>::max()) return false;
+  const int n_kt = (Lk + kPairBN - 1) / kPairBN;
+  std::vector<PairBlock> blocks;
+  blocks.reserve(static_cast<size_t>(n_blocks));
+  long total = 0;
+  int max_tiles = 0;
+  // (batch, KV head, block, query head in group): query heads sharing a KV
+  // head sit side by side
+  for (int b = 0; b < B; ++b)
+    for (int g = 0; g < Hkv; ++g)
+      for (int mb = 0; mb < n_mb; ++mb)
+        for (int hh = 0; hh < group; ++hh) {
+          int nt = n_kt;
+          if (causal) {
+            const int last_row = std::min(mb * kPairBlock + kPairBlock - 1, Lq - 1);
+            const long max_key = static_cast<long>(last_row) + (Lk - Lq);
+            nt = (max_key < 0) ? 0 : std::min<int>(n_kt, static_cast<int>(max_key / kPairBN) + 1);
+          }
+          blocks.push_back({b * Hq + g * group + hh, mb, nt});
+          total += nt;
+          max_tiles = std::max(max_tiles, nt);
+        }
+  const double c_unit = 0.5, c_split = 0.25;
+  const double avg = (static_cast<double>(total) + c_unit * static_cast<double>(blocks.size())) / num_pairs;
+  std::vector<double> targets = {std::numeric_limits<double>::infinity()};
+  if (static_cast<double>(max_tiles) > 0.75 * avg) {
+    for (double f = 0.25; f <= 3.0 + 1e-9; f += 0.03125)
+      if (f * avg >= 1.0) targets.push_back(f * avg);
+  }
+  double best = std::numeric_limits<double>::infinity();
+  std::vector<Cand> best_units;
+  std::vector<int> best_cta;
+  int best_n = 0;
+  for (double tgt : targets) {
+    std::vector<Cand> units;
+    bool any_split = false;
+    build_pair_units(blocks, tgt, c_unit, c_split, units, any_split);
+    std::vector<int> cta_of;
+    int n_workers = 0;
+    const double ms = assign(units, num_pairs, cta_of, n_workers);
+    // the pieces of a split block wait for each other before merging: a
+    // pair runs at most one split piece, as its first unit, so every piece
+    // is running when another waits for it
+    if (any_split) {
+      std::vector<int> n_split_pieces(n_workers, 0);
+      bool ok = true;
+      for (size_t i = 0; i < units.size() && ok; ++i)
+        if (units[i].n_split > 1 && ++n_split_pieces[cta_of[i]] > 1) ok = false;
+      if (!ok) continue;
+    }
+    if (ms < best - 1e-9 || (std::fabs(ms - best) <= 1e-9 && units.size() < best_units.size())) {
+      best = ms;
+      best_units = std::move(units);
+      best_cta = std::move(cta_of);
+      best_n = n_workers;
+    }
+  }
+  out = Plan();
+  std::vector<int> slot_base(blocks.size(), -1);
+  int n_slots = 0;
+  {
+    std::vector<int> nsplit(blocks.size(), 1);
+    for (const Cand& c : best_units) nsplit[c.pair] = c.n_split;
+    for (size_t i = 0; i < blocks.size(); ++i)
+      if (nsplit[i] > 1) {
+        slot_base[i] = n_slots;
+        out.groups.push_back({blocks[i].bh, blocks[i].mb, n_slots, nsplit[i]});
+        n_slots += nsplit[i];
+      }
+  }
+  out.n_ctas = best_n;   // pairs
+  out.n_partials = n_slots;
+  out.makespan = best;
+  std::vector<std::vector<int>> per(best_n);
+  for (size_t i = 0; i < best_units.size(); ++i) per[best_cta[i]].push_back(static_cast<int>(i));
+  out.cta_off.assign(best_n + 1, 0);
+  out.units.reserve(best_units.size());
+  for (int c = 0; c < best_n; ++c) {
+    out.cta_off[c] = static_cast<int>(out.units.size());
+    // the split piece (at most one) first
+    std::stable_partition(per[c].begin(), per[c].end(), [&](int i) { return best_units[i].n_split > 1; });
+    for (int i : per[c]) {
+      const Cand& u = best_units[i];
+      const PairBlock& b = blocks[u.pair];
+      const int slot = (u.n_split > 1) ? slot_base[u.pair] + u.split : -1;
+      out.units.push_back({b.bh, b.mb, u.a, u.e, u.split, u.n_split, slot, c});
+    }
+  }
+  out.cta_off[best_n] = static_cast<int>(out.units.size());
+  return true;
+}
+
 }  // namespace attn

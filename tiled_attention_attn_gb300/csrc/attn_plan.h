@@ -34,4 +34,10 @@ struct Plan {
 // Builds the schedule; returns false on arguments it cannot plan.
 bool make_plan(int B, int Hq, int Hkv, int Lq, int Lk, int d, bool causal, int num_sms, Plan& out);
 
+// The schedule of the CTA-pair forward: units are 256-row query blocks (128
+// rows per CTA) against ranges of 256-key tiles [kv_begin, kv_end), placed on
+// `num_pairs` SM pairs (Plan::n_ctas counts pairs, PlanUnit::cta is the
+// pair).  Split pieces of one block share a group; the kernel merges them.
+bool make_plan_pair(int B, int Hq, int Hkv, int Lq, int Lk, bool causal, int num_pairs, Plan& out);
+
 }  // namespace attn
