@@ -587,6 +587,117 @@ def decode_leg(attn, device, stream, peaks, iters: int = 20):
     return out
 
 
+CONFIG_ORDER = ("mha_l256_d64", "single_head_l8192_d128_causal", "mha_b2_h16_l2048_d64_fp16_causal",
+                "gqa_b2_hq32_hkv8_l4096_d128_causal", "varlen_b16_h12_d64")
+
+
+def configs_leg(attn, device, stream, peaks, flush, iters: int = 40, rows: int = 48):
+    """Every workload of the pages' five configurations through attn_fwd, in
+    the launch configuration of the headline: per call L2 flushed, CUDA events
+    on the launching stream, median of ``iters`` calls.  Reports TFLOP/s
+    (causal-adjusted), its fraction of the measured bf16 peak and the main
+    kernel's median duration (library profiling events).  Also returns, per
+    configuration, the GPU's O and lse on ``rows`` sampled rows (varlen: every
+    row), which the CPU-baseline leg checks against the oracle."""
+    from tiled_attention_attn_gb300.inputs import sample_rows
+
+    out, kept = {}, {}
+    for name in CONFIG_ORDER:
+        wl = WORKLOADS[name]
+        inp = generate(wl)
+        q, k, v = inp.q.to(device), inp.k.to(device), inp.v.to(device)
+        cu = inp.cu_seqlens.to(device) if inp.cu_seqlens is not None else None
+        o, lse = attn.attn_fwd(q, k, v, causal=wl.causal, scale=wl.softmax_scale, cu_seqlens=cu)
+        for _ in range(5):
+            flush.zero_()
+            attn.attn_fwd(q, k, v, causal=wl.causal, scale=wl.softmax_scale, cu_seqlens=cu, out=o, lse=lse)
+        ms = []
+        for _ in range(iters):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            attn.attn_fwd(q, k, v, causal=wl.causal, scale=wl.softmax_scale, cu_seqlens=cu, out=o, lse=lse)
+            b.record(stream)
+            torch.cuda.synchronize(device)
+            ms.append(a.elapsed_time(b))
+        attn.profile_enable(iters)
+        for _ in range(iters):
+            flush.zero_()
+            attn.attn_fwd(q, k, v, causal=wl.causal, scale=wl.softmax_scale, cu_seqlens=cu, out=o, lse=lse)
+        main_ms, _ = attn.profile_read(iters)
+        attn.profile_disable()
+        if attn.get_error() != attn.ATTN_OK:
+            raise RuntimeError(f"device error in the configs leg ({name}): {attn.last_device_error():#x}")
+        t = statistics.median(ms)
+        fl = workload_flops(wl, inp.lengths)
+        on = o.float().cpu().double().numpy()
+        ln = lse.cpu().double().numpy()
+        if wl.varlen:
+            kept[name] = (wl, inp, None, on, ln)
+        else:
+            rs = sample_rows(wl, rows)
+            idx = np.array(rs)
+            kept[name] = (wl, inp, rs, on[idx[:, 0], idx[:, 2], idx[:, 1]], ln[idx[:, 0], idx[:, 1], idx[:, 2]])
+        tf = fl / (t / 1e3) / 1e12
+        out[name] = {"ms_median": t, "ms_min": min(ms), "tflops": tf, "frac": tf / peaks["bf16_tflops"],
+                     "kernel_ms": statistics.median(main_ms),
+                     "kernel_tflops": fl / (statistics.median(main_ms) / 1e3) / 1e12,
+                     "dtype": wl.dtype, "flops": fl}
+        del q, k, v, o, lse
+    return out, kept
+
+
+def configs_oracle_check(cfgs, kept):
+    """CPU-baseline leg for the five configurations: the fp64 oracle on the
+    rows the configs leg kept (timed: its TFLOP/s on those rows is the
+    configuration's CPU baseline), and the largest |O - O_ref|, |lse - lse_ref|
+    of the GPU's outputs on them."""
+    import oracle
+
+    oracle.build()
+    for name, (wl, inp, rs, o_gpu, lse_gpu) in kept.items():
+        t0 = time.perf_counter()
+        if rs is None:
+            o_ref, lse_ref = oracle.varlen_attention(inp.q, inp.k, inp.v, inp.lengths, causal=wl.causal,
+                                                     scale=wl.softmax_scale)
+            fl = workload_flops(wl, inp.lengths)
+            checked = "every row"
+        else:
+            o_ref, lse_ref = oracle.attention_rows(inp.q, inp.k, inp.v, rs, causal=wl.causal, scale=wl.softmax_scale)
+            fl = sample_flops(wl, rs)
+            checked = f"{len(rs)} sampled rows"
+        dt = max(time.perf_counter() - t0, 1e-9)
+        fin = np.isfinite(lse_ref)
+        cfgs[name].update({"max_abs_err_o": float(np.max(np.abs(o_gpu - o_ref))),
+                           "max_abs_err_lse": float(np.max(np.abs(lse_gpu[fin] - lse_ref[fin]))) if fin.any() else 0.0,
+                           "checked": checked, "bar": {"o": 1e-2, "lse": 1e-3},
+                           "cpu_baseline_tflops": fl / dt / 1e12})
+
+
+def pair_headline(attn, wl, q, k, v, o, lse, stream, device, flush, iters: int = 40):
+    """The headline workload on the CTA-pair kernel (attn_set_pair_forward),
+    for comparison with the default single-CTA kernel: median call time."""
+    attn.set_pair_forward(True)
+    try:
+        for _ in range(5):
+            flush.zero_()
+            attn.attn_fwd(q, k, v, causal=wl.causal, scale=wl.softmax_scale, out=o, lse=lse)
+        ms = []
+        for _ in range(iters):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            attn.attn_fwd(q, k, v, causal=wl.causal, scale=wl.softmax_scale, out=o, lse=lse)
+            b.record(stream)
+            torch.cuda.synchronize(device)
+            ms.append(a.elapsed_time(b))
+    finally:
+        attn.set_pair_forward(False)
+    if attn.get_error() != attn.ATTN_OK:
+        raise RuntimeError(f"device error in the pair-kernel leg: {attn.last_device_error():#x}")
+    return statistics.median(ms)
+
+
 def run_ours(args, wl):
     from tiled_attention_attn_gb300 import attn, build
 
@@ -738,17 +849,30 @@ def run_ours(args, wl):
         bwd = bwd_leg(attn, device, stream, peaks)
         rot = rotary_leg(attn, device, stream, peaks)
 
+    # ---- the five configurations, and the headline on the CTA-pair kernel
+    cfgs = pair = kept = None
+    if rank == 0 and not args.no_configs_leg:
+        cfgs, kept = configs_leg(attn, device, stream, peaks, flush)
+        if not wl.varlen and wl.d == 128:
+            t_pair = pair_headline(attn, wl, q, k, v, o, lse, stream, device, flush)
+            pair = {"kernel": "attn_pair_kernel (attn_set_pair_forward(1))", "ms_median": t_pair,
+                    "tflops": flops / (t_pair / 1e3) / 1e12,
+                    "frac": flops / (t_pair / 1e3) / 1e12 / peaks["bf16_tflops"]}
+
     # ---- CPU baseline: the oracle on a bounded sample (rank 0, N = 1)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         tf, dt, n, threads = oracle_sample(wl, inp, args.cpu_budget_s)
         cpu = {"value": tf, "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"{n} random query rows of {wl.name} ({dt:.1f} s), fp64, S and P rows materialised"}
+        if cfgs is not None:
+            configs_oracle_check(cfgs, kept)
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
-            "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "ms_per_step": total_ms / K, "ms_per_step_median": statistics.median(step_ms),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": wl.dtype, "data": "synthetic",
             "config": dict(workload_config(wl, inp.lengths), parallelism=f"replicas x{world}",
                            l2="256 MiB buffer written before every step, outside the per-step CUDA events"),
@@ -757,7 +881,8 @@ def run_ours(args, wl):
             "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "mean": total_ms / K,
                         "per_rank_events": "one CUDA-event pair per step on the launching stream"},
             "clocks": clocks, "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
-            "cpu_baseline": cpu, "pad_unpad": pad, "kv_cache": cache, "rotary": rot, "backward": bwd, "decode": dec,
+            "cpu_baseline": cpu, "configs": cfgs, "pair_kernel_headline": pair,
+            "pad_unpad": pad, "kv_cache": cache, "rotary": rot, "backward": bwd, "decode": dec,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -776,6 +901,7 @@ def main():
     ap.add_argument("--cpu-budget-s", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-pad-leg", action="store_true", help="skip the padded-batch, kv-cache, rotary and backward legs")
+    ap.add_argument("--no-configs-leg", action="store_true", help="skip the five-configuration leg")
     ap.add_argument("--bwd-only", action="store_true", help="run only the backward leg")
     ap.add_argument("--legs-only", action="store_true", help="run only the padded-batch, kv-cache, rotary and backward legs")
     args = ap.parse_args()
