@@ -104,7 +104,8 @@ def measured_peaks():
 # the files the forward kernel and its launch are built from (the profile of
 # the forward kernel under profiles/ records their hash)
 FWD_SOURCES = ("attn_kernel.cuh", "attn_kernels.inc", "attn_kernels_d64.cu", "attn_kernels_d128.cu", "attn_params.h",
-               "attn_launch.h", "attn_host.cu", "attn_plan.cpp", "attn_plan.h", "ptx.cuh", "tmem_regs.cuh")
+               "attn_launch.h", "attn_host.cu", "attn_plan.cpp", "attn_plan.h", "ptx.cuh", "tmem_regs.cuh",
+               "attn_cache.h", "attn_pair_launch.h")
 
 
 def kernel_source_hash() -> str:

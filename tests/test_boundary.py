@@ -134,3 +134,16 @@ def test_decode_bad_arguments_rejected_on_host(attn_lib, bad):
 @pytest.mark.parametrize("shape", [dict(d=32), dict(d=96), dict(d=256), dict(Hq=6, Hkv=2), dict(Hq=16, Hkv=1)])
 def test_decode_unsupported_shapes(attn_lib, shape):
     assert _call_decode(attn_lib, **shape) == attn.ATTN_EUNSUPPORTED
+
+
+def test_schedule_cache_eviction_policy(attn_lib):
+    """The schedule cache's policy on host-side entries: it never holds more
+    unpinned entries than its capacity, evicts the excess, and keeps pinned
+    (captured) entries."""
+    live, released = attn.selftest_plan_cache(300, 256)
+    assert live == 256 and released == 300 - 256
+    live, released = attn.selftest_plan_cache(1000, 256, pin_every=10)
+    assert live <= 256 + 1000 // 10
+    assert released > 0
+    live, released = attn.selftest_plan_cache(100, 256)
+    assert live == 100 and released == 0

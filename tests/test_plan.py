@@ -105,3 +105,44 @@ def test_plan_rejects_bad_shapes(attn_lib):
         attn.plan(1, 3, 2, 128, 128, 64, False, 152)
     with pytest.raises(attn.AttnError):
         attn.plan(1, 2, 2, 128, 128, 96, False, 152)
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 1, 8192, 8192, True), (2, 32, 8, 4096, 4096, True),
+                                   (1, 8, 2, 3000, 3000, True), (3, 4, 4, 700, 900, False),
+                                   (1, 2, 2, 1000, 300, True), (1, 1, 1, 16384, 16384, True)])
+@pytest.mark.parametrize("pairs", [76, 66])
+def test_pair_plan_covers_each_tile_once(attn_lib, shape, pairs):
+    """The CTA-pair schedule: every 256-key tile a 256-row block needs is run
+    by exactly one piece; a pair runs at most one split piece, as its first
+    unit (split pieces wait for each other before merging); split slots of a
+    group are consecutive."""
+    B, Hq, Hkv, Lq, Lk, causal = shape
+    units, n_pairs, n_part = attn.plan_pair(B, Hq, Hkv, Lq, Lk, causal, pairs)
+    assert n_pairs <= pairs
+    n_kt = (Lk + 255) // 256
+    need = {}
+    for bh in range(B * Hq):
+        for mb in range((Lq + 255) // 256):
+            nt = n_kt
+            if causal:
+                last_row = min(mb * 256 + 255, Lq - 1)
+                mk = last_row + (Lk - Lq)
+                nt = 0 if mk < 0 else min(n_kt, mk // 256 + 1)
+            need[(bh, mb)] = nt
+    covered = {}
+    per_pair = {}
+    for u in units.tolist():
+        bh, mb, a, e, split, n_split, slot, p = u
+        for t in range(a, e):
+            assert (bh, mb, t) not in covered
+            covered[(bh, mb, t)] = True
+        per_pair.setdefault(p, []).append(u)
+        if n_split > 1:
+            assert 0 <= slot < n_part
+    for (bh, mb), nt in need.items():
+        for t in range(nt):
+            assert (bh, mb, t) in covered
+    assert len(covered) == sum(need.values())
+    for p, us in per_pair.items():
+        split = [i for i, u in enumerate(us) if u[5] > 1]
+        assert len(split) <= 1 and (not split or split[0] == 0)
