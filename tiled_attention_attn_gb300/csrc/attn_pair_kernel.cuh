@@ -52,6 +52,10 @@
 namespace attn {
 namespace pair {
 
+// warp roles of the pair kernel (its own, independent of the single-CTA kernel's)
+constexpr int kPairWarpTMA = 8;   // TMA producer
+constexpr int kPairWarpMMA = 9;   // S = Q K^T issuer (and TMEM allocator); warp 10 issues P.V
+
 template <int D>
 struct Cfg {
   static_assert(D == 128, "the pair kernel is built for head_dim 128");
@@ -372,11 +376,11 @@ __global__ void __launch_bounds__(kPairThreads, 1) attn_pair_kernel(const __grid
     mbar_init(b_merge, 8);
     fence_mbar_init();
   }
-  if (warp == kWarpMMA) {
+  if (warp == kPairWarpMMA) {
     tmem_alloc_pair(smem_u32(tmem_slot), C::kTmemCols);
     tmem_relinquish_pair();
   }
-  if (warp == kWarpTMA && lane == 0) {
+  if (warp == kPairWarpTMA && lane == 0) {
     tma_prefetch_desc(&p.tm_q);
     tma_prefetch_desc(&p.tm_k);
     tma_prefetch_desc(&p.tm_v);
@@ -395,7 +399,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) attn_pair_kernel(const __grid
   if (warp >= 8) {
     // each register limit governs exactly the code of its warpgroup
     regs_dec<kPairRegsOther>();
-  if (warp == kWarpTMA) {
+  if (warp == kPairWarpTMA) {
     // ------------------------------------------------------------------ TMA producer (both CTAs)
     if (lane == 0) {
       uint32_t q_cnt = 0, k_cnt = 0, v_cnt = 0;
@@ -469,7 +473,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) attn_pair_kernel(const __grid
         }
       }
     }
-  } else if (warp == kWarpMMA && rank == 0 && lane == 0) {
+  } else if (warp == kPairWarpMMA && rank == 0 && lane == 0) {
     // ------------------------------------------------------------------ S = Q K^T issuer (leader CTA)
     constexpr uint32_t kIdescS = idesc_f16_f32acc(2 * kPairRows, kPairBN, BF16, false);
     constexpr uint16_t kBoth = 0x3;
@@ -521,7 +525,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) attn_pair_kernel(const __grid
     // fires (it counts both issuing threads)
     umma_commit_pair(b_drain, 0x1);
     mbar_wait(b_drain, 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteDrain), false);
-  } else if (warp == kWarpMMA + 1 && rank == 0 && lane == 0) {
+  } else if (warp == kPairWarpMMA + 1 && rank == 0 && lane == 0) {
     // ------------------------------------------------------------------ O += P V issuer (leader CTA)
     constexpr uint32_t kIdescO = idesc_f16_f32acc(2 * kPairRows, D, BF16, true);
     constexpr uint16_t kBoth = 0x3;
@@ -851,7 +855,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) attn_pair_kernel(const __grid
   // neither CTA may release TMEM or exit while the pair's MMAs, loads or
   // remote arrivals can still touch the other
   cluster_sync();
-  if (warp == kWarpMMA) {
+  if (warp == kPairWarpMMA) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc_pair(tmem, C::kTmemCols);
