@@ -569,35 +569,38 @@ def decode_step_times(attn, device, stream, shape, iters: int = 20):
 
     o, lse = torch.empty_like(q), torch.empty(Hq, B, dtype=torch.float32, device=device)
     t_dec = timed(lambda: attn.attn_decode(q, k, v, cu_k, out=o, lse=lse, stream=stream))
+    attn.set_decode_path(False)
+    try:
+        t_cc = timed(lambda: attn.attn_decode(q, k, v, cu_k, out=o, lse=lse, stream=stream))
+    finally:
+        attn.set_decode_path(True)
     t_fwd = timed(lambda: attn.attn_fwd(q, k, v, causal=True, cu_seqlens=cu_q, cu_seqlens_k=cu_k, out=o, lse=lse,
                                         stream=stream))
-    return t_dec, t_fwd, 2 * k.numel() * k.element_size()
+    return t_dec, t_cc, t_fwd, 2 * k.numel() * k.element_size()
 
 
 def decode_leg(attn, device, stream, peaks, iters: int = 20):
     """One new token per sequence over a key/value cache (the generation step
     of the training page §4.3), bf16, Hq 32, Hkv 8, d 128.  Memory-bound: the
     rate is the cache bytes read (K and V once) per second against the HBM
-    copy peak.  Two shapes, each through both entry points: B 32 sequences of
-    4096 + 1 keys, where the packed forward (attn_fwd_varlen: tensor-core
-    tiles, the group's heads sharing a tile) is the faster and is reported
-    first; and one sequence of 131072 + 1 keys (``long``), where the packed
-    forward has only Hkv = 8 units and attn_decode (the key-split CUDA-core
-    path: chunk pass and merge) is the faster."""
-    B, Hq, Hkv, d, C = DECODE_SHAPE
-    t_dec, t_fwd, nbytes = decode_step_times(attn, device, stream, DECODE_SHAPE, iters)
-    gbs = lambda t: nbytes / (t / 1e3) / 1e9
-    out = {"workload": f"decode: B{B} Hq{Hq} Hkv{Hkv} d{d} bf16, 1 new token over a {C}-token cache",
-           "entry": "attn_fwd_varlen", "bound": "hbm", "achieved": gbs(t_fwd), "unit": "GB/s",
-           "peak": peaks["hbm_gbs"], "frac": gbs(t_fwd) / peaks["hbm_gbs"], "ms": t_fwd,
-           "cache_bytes_per_call": nbytes,
-           "attn_decode": {"achieved": gbs(t_dec), "frac": gbs(t_dec) / peaks["hbm_gbs"], "ms": t_dec}}
-    B, Hq, Hkv, d, C = DECODE_LONG_SHAPE
-    t_dec, t_fwd, nbytes = decode_step_times(attn, device, stream, DECODE_LONG_SHAPE, iters)
-    out["long"] = {"workload": f"decode: B{B} Hq{Hq} Hkv{Hkv} d{d} bf16, 1 new token over a {C}-token cache",
-                   "entry": "attn_decode", "achieved": gbs(t_dec), "frac": gbs(t_dec) / peaks["hbm_gbs"],
-                   "ms": t_dec, "cache_bytes_per_call": nbytes,
-                   "attn_fwd_varlen": {"achieved": gbs(t_fwd), "frac": gbs(t_fwd) / peaks["hbm_gbs"], "ms": t_fwd}}
+    copy peak.  Two shapes, B 32 sequences of 4096 + 1 keys and one sequence
+    of 131072 + 1 keys (``long``), each through attn_decode on its default
+    route (the packed forward's tensor-core tiles in decode mode, caches cut
+    into pieces when the (sequence, head group) units are few), through
+    attn_decode on its CUDA-core route, and through attn_fwd_varlen (the
+    packed forward without pieces)."""
+    def entry(shape, name):
+        B, Hq, Hkv, d, C = shape
+        t_dec, t_cc, t_fwd, nbytes = decode_step_times(attn, device, stream, shape, iters)
+        gbs = lambda t: nbytes / (t / 1e3) / 1e9
+        return {"workload": f"decode: B{B} Hq{Hq} Hkv{Hkv} d{d} bf16, 1 new token over a {C}-token cache",
+                "entry": "attn_decode (tensor cores)", "bound": "hbm", "achieved": gbs(t_dec), "unit": "GB/s",
+                "peak": peaks["hbm_gbs"], "frac": gbs(t_dec) / peaks["hbm_gbs"], "ms": t_dec,
+                "cache_bytes_per_call": nbytes,
+                "attn_decode_cuda_cores": {"achieved": gbs(t_cc), "frac": gbs(t_cc) / peaks["hbm_gbs"], "ms": t_cc},
+                "attn_fwd_varlen": {"achieved": gbs(t_fwd), "frac": gbs(t_fwd) / peaks["hbm_gbs"], "ms": t_fwd}}
+    out = entry(DECODE_SHAPE, "batch")
+    out["long"] = entry(DECODE_LONG_SHAPE, "long")
     return out
 
 

@@ -214,22 +214,20 @@ int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float 
  * fp16 = 0 selects bf16 tensors, 1 fp16.  d is 64 or 128 and Hq / Hkv is 1,
  * 2, 4 or 8 (else ATTN_EUNSUPPORTED; attn_fwd_varlen takes the others).
  * Pointers 16-byte aligned (lse 4); k and v may be null when total_k is 0.
- * It runs on the CUDA cores: with one query row per head the products are
- * matrix-vector and the cache read from HBM bounds the step.  Three launches
- * on `stream`: a one-warp pass over cu_seqlens_k, one block per chunk of 128
- * keys and key/value head (the chunk's max, exp-sum and unnormalised
- * output), and a merge per (sequence, query head).  The chunk results live in
- * a library workspace (one per device, grown on demand with cudaMalloc):
- * calls that overlap on the GPU (two streams without ordering) must not share
- * a device.  Returns ATTN_OK, ATTN_EINVAL, ATTN_EUNSUPPORTED, ATTN_ENOMEM or
- * ATTN_ELAUNCH.
  *
- * Which entry point to use for a decoding step: attn_fwd_varlen does not
- * split the keys, so it runs B x Hkv units and keeps few SMs busy when that
- * product is small (one or a few sequences with long caches); attn_decode
- * splits every cache into 128-key chunks and fills the GPU at any batch
- * size.  With many sequences (B x Hkv in the hundreds) the packed forward's
- * tensor-core tiles stream the cache faster.
+ * Two routes compute it (attn_set_decode_path).  The default runs the packed
+ * forward kernel in decode mode: TMA tiles and tcgen05 MMAs, the Hq / Hkv
+ * query heads of a key/value head in one tile (the cache is read once per
+ * key/value head), and, when B x Hkv units would leave SMs idle, every cache
+ * cut into pieces of key tiles (about four units per SM) whose fp32 partials
+ * a second launch merges with the running-max rescaling; two launches on
+ * `stream`, partials in the library's stream-ordered split workspace.  The
+ * other route runs on the CUDA cores: a one-warp pass over cu_seqlens_k, one
+ * block per chunk of 128 keys and key/value head, and a merge per (sequence,
+ * query head), with the chunk results in a workspace grown with cudaMalloc
+ * (calls that overlap on the GPU must not share a device); calls with
+ * total_k = 0 or B > 4096 always take it.  Returns ATTN_OK, ATTN_EINVAL,
+ * ATTN_EUNSUPPORTED, ATTN_ENOMEM or ATTN_ELAUNCH.
  */
 int attn_decode(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv,
                 int total_k, int d, float scale, const int *cu_seqlens_k, int fp16, cudaStream_t stream);
@@ -377,6 +375,19 @@ int attn_scatter_lse(const float *src, const int *indices, int n_max, const int 
  */
 void attn_set_pair_forward(int enable);
 int attn_pair_forward_used(int d, int varlen);
+
+/*
+ * attn_set_decode_path -- selects how attn_decode runs: 1 (the default) on
+ * the packed forward's tensor-core tiles, in decode mode (the query heads of
+ * a key/value head share one tile, and each cache is cut into pieces of key
+ * tiles, merged by a second pass, when the (sequence, head group) units
+ * alone would leave SMs idle); 0 on the CUDA-core chunk kernels.  Both
+ * compute the same function.  Calls with total_k = 0 or B > 4096 take the
+ * CUDA-core path either way.  attn_decode_path() returns the setting.
+ * Process-wide; not synchronised with calls in flight.
+ */
+void attn_set_decode_path(int tensor_cores);
+int attn_decode_path(void);
 
 /*
  * attn_plan_pair -- the CTA-pair kernel's schedule for a dense problem, for

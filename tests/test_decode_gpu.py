@@ -1,8 +1,10 @@
 """Parity of attn_decode (one new query per sequence against a packed
 key/value cache) with the oracle's per-sequence dense attention, every
-element compared, and with attn_fwd_varlen on the same inputs.
-Bar: max |O - O_ref| <= 1e-2, max |lse - lse_ref| <= 1e-3; a sequence with
-no key gives O = 0 and lse = -inf on both sides."""
+element compared, and with attn_fwd_varlen on the same inputs, on both of
+its routes: the packed forward's tensor-core tiles in decode mode (caches
+cut into pieces of key tiles whose partials a second launch merges) and the
+CUDA-core chunk kernels.  Bar: max |O - O_ref| <= 1e-2, max |lse - lse_ref|
+<= 1e-3; a sequence with no key gives O = 0 and lse = -inf on both sides."""
 
 import numpy as np
 import pytest
@@ -23,6 +25,14 @@ def _lib(attn_lib):
         pytest.skip("no CUDA device")
     attn.set_wait_timeout_ns(2_000_000_000)
     return attn_lib
+
+
+@pytest.fixture(params=[True, False], ids=["tensor_cores", "cuda_cores"], autouse=True)
+def path(request):
+    attn.set_decode_path(request.param)
+    assert attn.decode_path() == request.param
+    yield request.param
+    attn.set_decode_path(True)
 
 
 def cu_of(lengths):
@@ -57,6 +67,9 @@ CASES = [
     ([300, 513, 1], 4, 2, 64, torch.bfloat16),                  # group 2
     ([2000, 17], 16, 2, 128, torch.float16),                    # group 8
     ([20000, 3], 8, 2, 128, torch.bfloat16),                    # a long cache: 157 chunks to merge
+    ([131072], 32, 8, 128, torch.bfloat16),                     # one sequence, the long decode shape
+    ([5000, 1, 0, 12345, 777, 128, 129], 8, 2, 64, torch.bfloat16),   # pieces, tile edges, an empty cache
+    ([640] * 40, 32, 4, 128, torch.float16),                    # group 8 over many sequences
 ]
 
 

@@ -110,6 +110,10 @@ def lib(path: Optional[str] = None):
         L.attn_decode.restype = i
         L.attn_set_pair_forward.argtypes = [i]
         L.attn_set_pair_forward.restype = None
+        L.attn_set_decode_path.argtypes = [i]
+        L.attn_set_decode_path.restype = None
+        L.attn_decode_path.argtypes = []
+        L.attn_decode_path.restype = i
         L.attn_pair_forward_used.argtypes = [i, i]
         L.attn_pair_forward_used.restype = i
         L.attn_plan_pair.argtypes = [i, i, i, i, i, i, i, ip, i, ip, ip, ip]
@@ -657,6 +661,17 @@ def set_pair_forward(enable: bool) -> None:
 def pair_forward_used(d: int, varlen: bool) -> bool:
     """Whether attn_fwd runs such a problem on the CTA-pair kernel."""
     return bool(lib().attn_pair_forward_used(int(d), int(bool(varlen))))
+
+
+def set_decode_path(tensor_cores: bool) -> None:
+    """attn_decode on the packed forward's tensor-core tiles (True, the
+    default) or on the CUDA-core chunk kernels (False)."""
+    lib().attn_set_decode_path(int(bool(tensor_cores)))
+
+
+def decode_path() -> bool:
+    """True when attn_decode takes the tensor-core route."""
+    return bool(lib().attn_decode_path())
 
 
 def fwd_splits(B: int, Hq: int, Hkv: int, Lq: int, Lk: int, d: int, causal: bool, num_sms: int) -> bool:

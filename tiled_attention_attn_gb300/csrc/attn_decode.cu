@@ -27,6 +27,7 @@
 
 #include "attn.h"
 #include "attn_internal.h"
+#include "attn_params.h"
 
 namespace attn {
 namespace {
@@ -431,6 +432,9 @@ int decode(bool bf16, const void* q, const void* k, const void* v, void* o, floa
   if (static_cast<long long>(B) * Hq > (1LL << 31) - 1 || items_max > (1LL << 31) - 1 ||
       static_cast<long long>(total_k) + kDecChunk > (1LL << 31) - 1)
     return ATTN_EINVAL;
+
+  if (decode_tensor_cores_enabled() && total_k > 0 && B <= kVarlenMaxB)
+    return decode_on_tensor_cores(bf16, q, k, v, o, lse, B, Hq, Hkv, total_k, d, scale, cu_k, stream);
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ELAUNCH;

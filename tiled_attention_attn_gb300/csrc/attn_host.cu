@@ -33,6 +33,7 @@ namespace {
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
 std::atomic<unsigned long long> g_launches{0};
 std::atomic<int> g_pair_forward{0};   // attn_set_pair_forward
+std::atomic<int> g_decode_tc{1};      // attn_set_decode_path
 unsigned long long* g_trace = nullptr;   // attn_trace_enable (traced build only)
 int g_trace_cap = 0;
 
@@ -544,6 +545,113 @@ int fwd(bool bf16, const void* q, const void* k, const void* v, void* o, float* 
   return ATTN_OK;
 }
 
+// One decoding step through the packed forward's tensor-core tiles: decode
+// mode of the varlen kernel (query b at row b, the group's query heads in
+// one tile) with every cache cut into pieces when the (sequence, head group)
+// units alone would leave SMs idle; the pieces' partials are merged by the
+// decode combine.  Arguments are checked by attn_decode.
+int fwd_decode(bool bf16, const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+               int total_k, int d, float scale, const int* cu_k, cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ELAUNCH;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevState& st = g_dev[dev];
+  int rc = init_device(dev, st);
+  if (rc) return rc;
+  if (!st.supported) return ATTN_EUNSUPPORTED;
+  const int group = Hq / Hkv;
+  int lp = 0;
+  while ((1 << lp) < group) ++lp;
+  const int n_hg = Hq >> lp;
+  // Pieces per cache: the units (B x n_hg x pieces) run in rounds of one per
+  // CTA, so with caches of equal length (the host cannot read cu_seqlens_k;
+  // the mean length stands in) the step costs rounds x (tiles per piece +
+  // kDecodeUnitCost), a unit's fixed cost (Q load, pipeline fill, epilogue)
+  // in tile-times.  The piece count that minimises it wins, fewer pieces on
+  // ties; split = 0 leaves every cache whole.  `tiles` bounds the sum over
+  // sequences of their key tiles (a partial tile per sequence at most).
+  const long long units0 = static_cast<long long>(B) * n_hg;
+  const long long tiles = (static_cast<long long>(total_k) + kBN - 1) / kBN + B;
+  const long long t_seq = std::max<long long>(1, ((static_cast<long long>(total_k) + B - 1) / B + kBN - 1) / kBN);
+  const long long grid_max = st.sm_count;
+  constexpr double kDecodeUnitCost = 1.5;
+  long long best_pcs = 1;
+  double best = 1e300;
+  for (long long pcs = 1; pcs <= std::min<long long>(t_seq, 4096); ++pcs) {
+    const long long rounds = (units0 * pcs + grid_max - 1) / grid_max;
+    const double cost = static_cast<double>(rounds) * (static_cast<double>((t_seq + pcs - 1) / pcs) + kDecodeUnitCost);
+    if (cost < best * (1.0 - 1e-9)) {
+      best = cost;
+      best_pcs = pcs;
+    }
+  }
+  const int split = best_pcs > 1 ? static_cast<int>((t_seq + best_pcs - 1) / best_pcs) : 0;
+  const long long max_units = split > 0 ? static_cast<long long>(n_hg) * (tiles / split + 1 + B) : units0;
+  if (max_units > (1LL << 30)) return ATTN_EINVAL;
+
+  static thread_local FwdParams p;
+  std::memset(&p, 0, sizeof(p));
+  if ((rc = get_map(st, q, bf16, d, Hq, B, 1, p.tm_q, 1 << lp))) return rc;
+  if ((rc = get_map(st, k, bf16, d, Hkv, total_k, 1, p.tm_k))) return rc;
+  if ((rc = get_map(st, v, bf16, d, Hkv, total_k, 1, p.tm_v))) return rc;
+  // workspace: the unit prefix and malformed flag (B + 2 ints), then the
+  // pieces' (m, l) and fp32 partial outputs in the forward's slot layout
+  const size_t pref_bytes = (static_cast<size_t>(B + 2) * sizeof(int) + 255) & ~size_t(255);
+  const size_t ml_bytes = split > 0 ? static_cast<size_t>(max_units) * kNSub * kBM * 2 * sizeof(float) : 0;
+  const size_t o_bytes = split > 0 ? static_cast<size_t>(max_units) * kNSub * kBM * d * sizeof(float) : 0;
+  if ((rc = ws_ensure(st.part, pref_bytes + ml_bytes + o_bytes, stream, false))) return rc;
+  char* ws = static_cast<char*>(st.part.ptr);
+  p.vl_pref_out = reinterpret_cast<int*>(ws);
+  p.part_ml = reinterpret_cast<float*>(ws + pref_bytes);
+  p.part_o = ws + pref_bytes + ml_bytes;
+  p.o = o;
+  p.lse = lse;
+  p.cu_seqlens = nullptr;
+  p.cu_seqlens_k = cu_k;
+  p.err = st.err_word;
+  p.trace = g_trace;
+  p.trace_cap = g_trace_cap;
+  p.timeout_ns = g_timeout_ns.load();
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.Lq = B;
+  p.Lk = total_k;
+  p.group = group;
+  p.pack_log2 = lp;
+  p.vl_decode = 1;
+  p.vl_split = split;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  FwdLauncher launch = (d == 64) ? fwd_launcher_d64(bf16, false, true) : fwd_launcher_d128(bf16, false, true);
+  const int grid = static_cast<int>(std::min<long long>(st.sm_count, max_units));
+  ProfileRec* prof = profile_slot(dev);
+  if (prof && cudaEventRecord(prof->start, stream) != cudaSuccess) return ATTN_ELAUNCH;
+  if (launch(p, grid, stream) != cudaSuccess) return ATTN_ELAUNCH;
+  g_launches.fetch_add(1);
+  if (prof && cudaEventRecord(prof->mid, stream) != cudaSuccess) return ATTN_ELAUNCH;
+  if (split > 0) {
+    DecodeCombineParams cp;
+    cp.part_o = p.part_o;
+    cp.part_ml = p.part_ml;
+    cp.pref = p.vl_pref_out;
+    cp.cu_seqlens_k = cu_k;
+    cp.o = o;
+    cp.lse = lse;
+    cp.B = B;
+    cp.Hq = Hq;
+    cp.pack_log2 = lp;
+    cp.split = split;
+    DecodeCombineLauncher cl = (d == 64) ? decode_combine_launcher_d64(bf16) : decode_combine_launcher_d128(bf16);
+    if (cl(cp, B * n_hg, stream) != cudaSuccess) return ATTN_ELAUNCH;
+    g_launches.fetch_add(1);
+  }
+  if (prof && cudaEventRecord(prof->end, stream) != cudaSuccess) return ATTN_ELAUNCH;
+  return ATTN_OK;
+}
+
+bool decode_tensor_cores() { return g_decode_tc.load() != 0; }
+
 __global__ void selftest_wait_kernel(int* err, unsigned long long timeout_ns) {
   __shared__ __align__(8) uint64_t bar;
   __shared__ int abort_flag;
@@ -596,6 +704,12 @@ unsigned long long* trace_buffer(int* events_per_stream) {
   return g_trace;
 }
 void count_launch() { g_launches.fetch_add(1); }
+
+int decode_on_tensor_cores(bool bf16, const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                           int Hkv, int total_k, int d, float scale, const int* cu_k, cudaStream_t stream) {
+  return fwd_decode(bf16, q, k, v, o, lse, B, Hq, Hkv, total_k, d, scale, cu_k, stream);
+}
+bool decode_tensor_cores_enabled() { return decode_tensor_cores(); }
 
 cudaError_t launch_selftest_wait(int* err_word, unsigned long long timeout_ns, cudaStream_t stream) {
   selftest_wait_kernel<<<1, 32, 0, stream>>>(err_word, timeout_ns);
@@ -724,6 +838,9 @@ int attn_profile_read(float* main_ms, float* call_ms, int max, int* n) {
 }
 
 void attn_set_pair_forward(int enable) { attn::g_pair_forward.store(enable ? 1 : 0); }
+
+void attn_set_decode_path(int tensor_cores) { attn::g_decode_tc.store(tensor_cores ? 1 : 0); }
+int attn_decode_path(void) { return attn::g_decode_tc.load(); }
 
 int attn_pair_forward_used(int d, int varlen) {
   return (attn::g_pair_forward.load() != 0 && d == 128 && varlen == 0) ? 1 : 0;

@@ -30,4 +30,12 @@ unsigned long long wait_timeout_ns();
 unsigned long long* trace_buffer(int* events_per_stream);
 void count_launch();
 
+// attn_decode on the packed forward's tensor-core tiles (decode mode of the
+// varlen kernel, caches cut into pieces merged by the decode combine), and
+// whether attn_decode takes that route (attn_set_decode_path, default on).
+// The caller has checked the arguments; needs total_k > 0, B <= kVarlenMaxB.
+int decode_on_tensor_cores(bool bf16, const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                           int Hkv, int total_k, int d, float scale, const int* cu_k, cudaStream_t stream);
+bool decode_tensor_cores_enabled();
+
 }  // namespace attn

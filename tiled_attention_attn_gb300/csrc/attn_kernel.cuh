@@ -110,22 +110,34 @@ __device__ __forceinline__ bool decode_unit(const FwdParams& p, const int* vl_pr
     const int lp = p.pack_log2;
     const int n_hu = p.Hq >> lp;
     const int local = u - vl_pref[lo];
-    const int mb = local / n_hu;
-    U.h = (local - mb * n_hu) << lp;   // first query head of the unit
-    U.q_row0 = mb * (kBlockRows >> lp);
-    const int s0 = __ldg(p.cu_seqlens + lo);
-    const int len = __ldg(p.cu_seqlens + lo + 1) - s0;
     const int s0k = __ldg(p.cu_seqlens_k + lo);
-    U.q_len = len;
     U.k_len = __ldg(p.cu_seqlens_k + lo + 1) - s0k;
-    U.row_q = s0;
     U.row_k = s0k;
     U.bcoord = 0;
-    U.split = 0;
-    U.n_split = 1;
-    U.slot = -1;
     U.kv_begin = 0;
     U.kv_end = 0;
+    if (p.vl_decode) {
+      // one query, row lo of q; units (head group, key piece), piece fastest
+      const int pcs = decode_pieces(U.k_len, p.vl_split);
+      const int hg = local / pcs;
+      U.h = hg << lp;
+      U.q_row0 = 0;
+      U.q_len = 1;
+      U.row_q = lo;
+      U.split = local - hg * pcs;
+      U.n_split = pcs;
+      U.slot = (pcs > 1) ? u : -1;
+    } else {
+      const int mb = local / n_hu;
+      U.h = (local - mb * n_hu) << lp;   // first query head of the unit
+      U.q_row0 = mb * (kBlockRows >> lp);
+      const int s0 = __ldg(p.cu_seqlens + lo);
+      U.q_len = __ldg(p.cu_seqlens + lo + 1) - s0;
+      U.row_q = s0;
+      U.split = 0;
+      U.n_split = 1;
+      U.slot = -1;
+    }
   }
   U.g = U.h / p.group;
   const int span = VARLEN ? (kBM >> p.pack_log2) : kBM;   // queries per sub-tile
@@ -134,6 +146,10 @@ __device__ __forceinline__ bool decode_unit(const FwdParams& p, const int* vl_pr
   const int end = max(U.kv_last[0], U.kv_last[1]) + 1;
   if constexpr (VARLEN) {
     U.kv_end = end;
+    if (U.n_split > 1) {   // a decode piece: its own range of key tiles
+      U.kv_begin = U.split * p.vl_split;
+      U.kv_end = min(end, U.kv_begin + p.vl_split);
+    }
   } else {
     U.kv_end = min(U.kv_end, end);
   }
@@ -349,17 +365,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     if (warp == 0) {
       int carry = 0;
       bool bad = false;
-      if (lane == 0 && (__ldg(p.cu_seqlens) != 0 || __ldg(p.cu_seqlens_k) != 0)) bad = true;
+      if (lane == 0 && ((!p.vl_decode && __ldg(p.cu_seqlens) != 0) || __ldg(p.cu_seqlens_k) != 0)) bad = true;
       for (int b0 = 0; b0 < p.B; b0 += 32) {
         const int b = b0 + lane;
         int cnt = 0;
         if (b < p.B) {
-          const int a = __ldg(p.cu_seqlens + b), e = __ldg(p.cu_seqlens + b + 1);
           const int ak = __ldg(p.cu_seqlens_k + b), ek = __ldg(p.cu_seqlens_k + b + 1);
-          if (e < a || e > p.Lq || ek < ak || ek > p.Lk) bad = true;
-          const int len = e - a;
-          const int blk = kBlockRows >> p.pack_log2;   // queries per unit
-          cnt = (len > 0) ? ((len + blk - 1) / blk) * (p.Hq >> p.pack_log2) : 0;
+          if (ek < ak || ek > p.Lk) bad = true;
+          if (p.vl_decode) {
+            // every head group of every sequence, in pieces of its keys
+            cnt = (p.Hq >> p.pack_log2) * decode_pieces(max(ek - ak, 0), p.vl_split);
+          } else {
+            const int a = __ldg(p.cu_seqlens + b), e = __ldg(p.cu_seqlens + b + 1);
+            if (e < a || e > p.Lq) bad = true;
+            const int len = e - a;
+            const int blk = kBlockRows >> p.pack_log2;   // queries per unit
+            cnt = (len > 0) ? ((len + blk - 1) / blk) * (p.Hq >> p.pack_log2) : 0;
+          }
         }
         int x = cnt;
 #pragma unroll
@@ -388,6 +410,25 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     n_units = (*bad_flag) ? 0 : vl_pref[p.B];
     u_first = blockIdx.x;
     u_step = gridDim.x;
+    if (p.vl_decode) {
+      // the decode combine reads the unit prefix and the malformed flag
+      if (p.vl_pref_out != nullptr && blockIdx.x == 0) {
+        for (int i = tid; i <= p.B; i += kThreads) p.vl_pref_out[i] = vl_pref[i];
+        if (tid == 0) p.vl_pref_out[p.B + 1] = *bad_flag;
+      }
+      // malformed key offsets: every row O = 0, lse = -inf
+      if (*bad_flag) {
+        T* out = reinterpret_cast<T*>(p.o);
+        for (long long r = static_cast<long long>(blockIdx.x) * kThreads + tid; r < static_cast<long long>(p.B) * p.Hq;
+             r += static_cast<long long>(gridDim.x) * kThreads) {
+          uint4* d4 = reinterpret_cast<uint4*>(out + r * D);
+#pragma unroll
+          for (int i = 0; i < D / 8; ++i) d4[i] = make_uint4(0, 0, 0, 0);
+          const long long b = r / p.Hq, h = r - b * p.Hq;
+          p.lse[h * p.B + b] = -INFINITY;
+        }
+      }
+    }
   } else {
     const int* off = p.n_inline ? p.cta_off_inline : p.cta_off;
     u_first = off[blockIdx.x];
@@ -664,16 +705,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             uint32_t o[32];
             tmem_ld_32x32b_x32(t_o + c * 32, o);
             tmem_wait_ld(o);
+            if (row_valid) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              po[(pbase + c * 8 + i) * kBM + row] =
-                  make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
-                              __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
+              for (int i = 0; i < 8; ++i)
+                po[(pbase + c * 8 + i) * kBM + row] =
+                    make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
+                                __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
+            }
           }
         }
-        const size_t prow = (static_cast<size_t>(U.slot) * kNSub + t) * kBM + row;
-        float2* pml = reinterpret_cast<float2*>(p.part_ml) + prow;
-        *pml = make_float2(n_act > 0 ? st.m : -INFINITY, n_act > 0 ? st.l : 0.0f);
+        if (row_valid) {
+          const size_t prow = (static_cast<size_t>(U.slot) * kNSub + t) * kBM + row;
+          float2* pml = reinterpret_cast<float2*>(p.part_ml) + prow;
+          *pml = make_float2(n_act > 0 ? st.m : -INFINITY, n_act > 0 ? st.l : 0.0f);
+        }
       }
       tr.rec(kTagEpiDone, t, u, 0);
       tc_fence_before();
@@ -775,6 +820,91 @@ __global__ void __launch_bounds__(kBM) attn_combine_kernel(const __grid_constant
   if (cb == 0)
     p.lse[(static_cast<size_t>(b) * p.Hq + h) * p.Lq + qrow] =
         (L > 0.0f) ? M * 0.69314718055994531f + __logf(L) : -INFINITY;
+}
+
+
+// ---------------------------------------------------------------------------
+// Merge of decode pieces.  Block (sequence b, head group) x 16-column slice;
+// thread r is query head r of the group (row r of the unit's first sub-tile,
+// the only one a single query fills).  The pieces of (b, group) are the units
+// pref[b] + group * pieces .. + pieces - 1, in key order; the same r-rescale
+// as the split-KV combine above.  Sequences that were not cut (one piece)
+// were written by the forward kernel, and with malformed offsets that kernel
+// has zeroed every row, so those blocks return at once.  Launched as a
+// programmatic dependent of the forward kernel.
+// ---------------------------------------------------------------------------
+template <int D, bool BF16>
+__global__ void __launch_bounds__(32) attn_combine_decode_kernel(const __grid_constant__ DecodeCombineParams p) {
+  using T = typename IO<BF16>::T;
+  const int G = 1 << p.pack_log2;
+  const int n_hg = p.Hq >> p.pack_log2;
+  const int b = blockIdx.x / n_hg, hg = blockIdx.x - b * n_hg;
+  const int cb = blockIdx.y;
+  const int row = threadIdx.x;
+  if (row >= G) return;
+  const int ak = __ldg(p.cu_seqlens_k + b);
+  const int ek = __ldg(p.cu_seqlens_k + b + 1);
+  grid_wait_prerequisites();
+  if (p.pref[p.B + 1] != 0 || ek < ak) return;
+  const int pcs = decode_pieces(ek - ak, p.split);
+  if (pcs <= 1) return;
+  const int slot0 = p.pref[b] + hg * pcs;
+  const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
+  const float4* po = reinterpret_cast<const float4*>(p.part_o);
+  constexpr size_t kMlStride = kNSub * kBM;      // per slot, in float2
+  constexpr size_t kOStride = kNSub * (D / 4);   // per slot, in 4-column groups
+  const size_t ml_base = static_cast<size_t>(slot0) * kMlStride + row;
+  const size_t o_base = static_cast<size_t>(slot0) * kOStride + cb * 4;
+  float M = -INFINITY, L = 0.0f;
+  float acc[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+  for (int s0 = 0; s0 < pcs; s0 += 4) {
+    float2 mlv[4];
+    float4 x[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const bool in = s0 + i < pcs;
+      mlv[i] = in ? __ldcg(ml + ml_base + (s0 + i) * kMlStride) : make_float2(-INFINITY, 0.0f);
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        x[i][c] = in ? __ldcg(po + (o_base + (s0 + i) * kOStride + c) * kBM + row) : make_float4(0, 0, 0, 0);
+    }
+    float mb = M;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) mb = fmaxf(mb, mlv[i].x);
+    if (mb == -INFINITY) continue;
+    const float r = (M == -INFINITY) ? 0.0f : ex2_approx(M - mb);
+    M = mb;
+    L *= r;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] *= r;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (mlv[i].x == -INFINITY) continue;
+      const float w = ex2_approx(mlv[i].x - M) * mlv[i].y;
+      L += w;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        acc[4 * c] += w * x[i][c].x;
+        acc[4 * c + 1] += w * x[i][c].y;
+        acc[4 * c + 2] += w * x[i][c].z;
+        acc[4 * c + 3] += w * x[i][c].w;
+      }
+    }
+  }
+  const float inv = (L > 0.0f) ? 1.0f / L : 0.0f;
+  const int head = hg * G + row;
+  T* dst = reinterpret_cast<T*>(p.o) + (static_cast<size_t>(b) * p.Hq + head) * D + cb * 16;
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+    d4[i] = make_uint4(pack2<BF16>(acc[8 * i] * inv, acc[8 * i + 1] * inv),
+                       pack2<BF16>(acc[8 * i + 2] * inv, acc[8 * i + 3] * inv),
+                       pack2<BF16>(acc[8 * i + 4] * inv, acc[8 * i + 5] * inv),
+                       pack2<BF16>(acc[8 * i + 6] * inv, acc[8 * i + 7] * inv));
+  if (cb == 0)
+    p.lse[static_cast<size_t>(head) * p.B + b] = (L > 0.0f) ? M * 0.69314718055994531f + __logf(L) : -INFINITY;
 }
 
 }  // namespace attn

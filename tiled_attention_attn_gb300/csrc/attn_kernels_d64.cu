@@ -6,4 +6,7 @@ FwdLauncher fwd_launcher_d64(bool bf16, bool causal, bool varlen) { return pick_
 CombineLauncher combine_launcher_d64(bool bf16) {
   return bf16 ? launch_combine<64, true> : launch_combine<64, false>;
 }
+DecodeCombineLauncher decode_combine_launcher_d64(bool bf16) {
+  return bf16 ? launch_combine_decode<64, true> : launch_combine_decode<64, false>;
+}
 }  // namespace attn

@@ -72,6 +72,15 @@ struct FwdParams {
   // tile holds 128 / group tokens x group heads, row r = token r >> pack_log2,
   // head r & (group - 1), and tm_q's box is 64 x group x (128 / group) x 1.
   int pack_log2;
+  // Decode mode (varlen only): one query per sequence, sequence b's query at
+  // row b of q (cu_seqlens unused, may be null).  vl_split > 0 cuts the keys
+  // of every (sequence, head group) into pieces of at most vl_split tiles,
+  // each its own unit writing a partial (slot = unit index) that the decode
+  // combine merges; CTA 0 writes the per-sequence unit prefix (B + 1 ints)
+  // and a malformed-offsets flag to vl_pref_out for that pass.
+  int vl_decode;
+  int vl_split;
+  int* vl_pref_out;
   float scale_log2;            // scale * log2(e)
   float scale;
   // A small schedule is copied here so that a CTA learns its first unit from
@@ -81,6 +90,26 @@ struct FwdParams {
   int cta_off_inline[kInlineCtas + 1];
   int units_inline[kInlineUnits * kUnitInts];
 };
+
+// Merge of the decode mode's split pieces: one block per (sequence, head
+// group) and 16-column slice; rows are the group's query heads.
+struct DecodeCombineParams {
+  const void* part_o;          // fp32 partials, the forward's [slot][2][D/4][128][4] layout
+  const float* part_ml;        // (m, l) per slot, sub-tile and row
+  const int* pref;             // units before each sequence (B + 1), then the malformed flag
+  const int* cu_seqlens_k;
+  void* o;                     // (B, Hq, D)
+  float* lse;                  // (Hq, B)
+  int B, Hq, pack_log2, split;
+};
+
+// Tiles of `split` keys each covering a sequence of k_len keys; a sequence
+// without keys is one (empty) piece.
+ATTN_HD inline int decode_pieces(int k_len, int split) {
+  const int tiles = (k_len + kBN - 1) / kBN;
+  if (split <= 0 || tiles <= split) return 1;
+  return (tiles + split - 1) / split;
+}
 
 // ---------------------------------------------------------------------------
 // The CTA-pair forward (tcgen05 .cta_group::2): a work unit is a 256-row
