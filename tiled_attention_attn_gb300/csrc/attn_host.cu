@@ -591,7 +591,14 @@ int fwd_decode(bool bf16, const void* q, const void* k, const void* v, void* o, 
 
   static thread_local FwdParams p;
   std::memset(&p, 0, sizeof(p));
-  if ((rc = get_map(st, q, bf16, d, Hq, B, 1, p.tm_q, 1 << lp))) return rc;
+  // head_dim 128 runs the transposed decode kernel (keys on the MMA's M
+  // dimension); head_dim 64 the packed forward in decode mode
+  const bool transposed = (d == 128);
+  if (transposed) {
+    if ((rc = get_map(st, q, bf16, d, Hq, B, 1, p.tm_q, group, group))) return rc;
+  } else {
+    if ((rc = get_map(st, q, bf16, d, Hq, B, 1, p.tm_q, 1 << lp))) return rc;
+  }
   if ((rc = get_map(st, k, bf16, d, Hkv, total_k, 1, p.tm_k))) return rc;
   if ((rc = get_map(st, v, bf16, d, Hkv, total_k, 1, p.tm_v))) return rc;
   // workspace: the unit prefix and malformed flag (B + 2 ints), then the
@@ -627,7 +634,12 @@ int fwd_decode(bool bf16, const void* q, const void* k, const void* v, void* o, 
   const int grid = static_cast<int>(std::min<long long>(st.sm_count, max_units));
   ProfileRec* prof = profile_slot(dev);
   if (prof && cudaEventRecord(prof->start, stream) != cudaSuccess) return ATTN_ELAUNCH;
-  if (launch(p, grid, stream) != cudaSuccess) return ATTN_ELAUNCH;
+  const cudaError_t le = transposed
+                             ? launch_decode_tc(p.tm_q, p.tm_k, p.tm_v, o, lse, cu_k, p.vl_pref_out, p.part_o,
+                                                p.part_ml, p.err, p.timeout_ns, B, Hq, Hkv, total_k, split,
+                                                p.scale_log2, bf16, grid, stream)
+                             : launch(p, grid, stream);
+  if (le != cudaSuccess) return ATTN_ELAUNCH;
   g_launches.fetch_add(1);
   if (prof && cudaEventRecord(prof->mid, stream) != cudaSuccess) return ATTN_ELAUNCH;
   if (split > 0) {

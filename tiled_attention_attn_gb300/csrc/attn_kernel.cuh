@@ -117,14 +117,16 @@ __device__ __forceinline__ bool decode_unit(const FwdParams& p, const int* vl_pr
     U.kv_begin = 0;
     U.kv_end = 0;
     if (p.vl_decode) {
-      // one query, row lo of q; units (head group, key piece), piece fastest
+      // one query, row lo of q; units (key piece, head group), the group
+      // fastest (CTAs side by side read the same keys of neighbouring heads)
       const int pcs = decode_pieces(U.k_len, p.vl_split);
-      const int hg = local / pcs;
+      const int piece = local / n_hu;
+      const int hg = local - piece * n_hu;
       U.h = hg << lp;
       U.q_row0 = 0;
       U.q_len = 1;
       U.row_q = lo;
-      U.split = local - hg * pcs;
+      U.split = piece;
       U.n_split = pcs;
       U.slot = (pcs > 1) ? u : -1;
     } else {
@@ -826,8 +828,8 @@ __global__ void __launch_bounds__(kBM) attn_combine_kernel(const __grid_constant
 // ---------------------------------------------------------------------------
 // Merge of decode pieces.  Block (sequence b, head group) x 16-column slice;
 // thread r is query head r of the group (row r of the unit's first sub-tile,
-// the only one a single query fills).  The pieces of (b, group) are the units
-// pref[b] + group * pieces .. + pieces - 1, in key order; the same r-rescale
+// the only one a single query fills).  Piece s of (b, group) is unit
+// pref[b] + s * groups + group, in key order of s; the same r-rescale
 // as the split-KV combine above.  Sequences that were not cut (one piece)
 // were written by the forward kernel, and with malformed offsets that kernel
 // has zeroed every row, so those blocks return at once.  Launched as a
@@ -848,13 +850,14 @@ __global__ void __launch_bounds__(32) attn_combine_decode_kernel(const __grid_co
   if (p.pref[p.B + 1] != 0 || ek < ak) return;
   const int pcs = decode_pieces(ek - ak, p.split);
   if (pcs <= 1) return;
-  const int slot0 = p.pref[b] + hg * pcs;
+  // piece s of (b, group) is unit pref[b] + s * n_hg + hg (the group fastest)
+  const int slot0 = p.pref[b] + hg;
   const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
   const float4* po = reinterpret_cast<const float4*>(p.part_o);
-  constexpr size_t kMlStride = kNSub * kBM;      // per slot, in float2
-  constexpr size_t kOStride = kNSub * (D / 4);   // per slot, in 4-column groups
-  const size_t ml_base = static_cast<size_t>(slot0) * kMlStride + row;
-  const size_t o_base = static_cast<size_t>(slot0) * kOStride + cb * 4;
+  const size_t ml_stride = static_cast<size_t>(n_hg) * kNSub * kBM;      // per piece, in float2
+  const size_t o_stride = static_cast<size_t>(n_hg) * kNSub * (D / 4);   // per piece, in 4-column groups
+  const size_t ml_base = static_cast<size_t>(slot0) * kNSub * kBM + row;
+  const size_t o_base = static_cast<size_t>(slot0) * kNSub * (D / 4) + cb * 4;
   float M = -INFINITY, L = 0.0f;
   float acc[16];
 #pragma unroll
@@ -865,10 +868,10 @@ __global__ void __launch_bounds__(32) attn_combine_decode_kernel(const __grid_co
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const bool in = s0 + i < pcs;
-      mlv[i] = in ? __ldcg(ml + ml_base + (s0 + i) * kMlStride) : make_float2(-INFINITY, 0.0f);
+      mlv[i] = in ? __ldcg(ml + ml_base + (s0 + i) * ml_stride) : make_float2(-INFINITY, 0.0f);
 #pragma unroll
       for (int c = 0; c < 4; ++c)
-        x[i][c] = in ? __ldcg(po + (o_base + (s0 + i) * kOStride + c) * kBM + row) : make_float4(0, 0, 0, 0);
+        x[i][c] = in ? __ldcg(po + (o_base + (s0 + i) * o_stride + c) * kBM + row) : make_float4(0, 0, 0, 0);
     }
     float mb = M;
 #pragma unroll
