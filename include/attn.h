@@ -215,13 +215,17 @@ int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float 
  * 2, 4 or 8 (else ATTN_EUNSUPPORTED; attn_fwd_varlen takes the others).
  * Pointers 16-byte aligned (lse 4); k and v may be null when total_k is 0.
  *
- * Two routes compute it (attn_set_decode_path).  The default runs the packed
- * forward kernel in decode mode: TMA tiles and tcgen05 MMAs, the Hq / Hkv
- * query heads of a key/value head in one tile (the cache is read once per
- * key/value head), and, when B x Hkv units would leave SMs idle, every cache
- * cut into pieces of key tiles (about four units per SM) whose fp32 partials
- * a second launch merges with the running-max rescaling; two launches on
- * `stream`, partials in the library's stream-ordered split workspace.  The
+ * Two routes compute it (attn_set_decode_path).  The default runs on TMA
+ * tiles and tcgen05 MMAs, reading the cache once per key/value head: for
+ * head_dim 128 a decode kernel with the products transposed (S^T = K Q^T,
+ * u^T += V^T P^T: the tile's 128 keys on the TMEM lanes, the group's query
+ * heads on the columns, so each softmax thread owns one key), for head_dim
+ * 64 the packed forward kernel in decode mode (the group's query heads in
+ * one tile).  Units are (sequence, key/value head, piece of the cache): the
+ * caches are cut into pieces of key tiles when that shortens the step (a
+ * cost model over rounds of one unit per SM, with the mean cache length),
+ * and a second launch merges the pieces' fp32 partials with the running-max
+ * rescaling; partials live in the library's stream-ordered split workspace.  The
  * other route runs on the CUDA cores: a one-warp pass over cu_seqlens_k, one
  * block per chunk of 128 keys and key/value head, and a merge per (sequence,
  * query head), with the chunk results in a workspace grown with cudaMalloc
