@@ -157,8 +157,9 @@ __host__ __device__ constexpr uint32_t idesc_a_mn(int M, int N, bool bf16) {
   return idesc_f16_f32acc(M, N, bf16, false) | (1u << 15);
 }
 
-template <int NQ, bool BF16>
+template <int NQ, int GT, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_constant__ Params p) {
+  static_assert(GT >= 1 && GT <= NQ, "query heads per key/value head");
   using C = Cfg<NQ>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -402,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t t_u = tmem + lane_off + 2 * NQ;
     const float c = p.scale_log2;
-    const int G = p.G;
+    constexpr int G = GT;
     uint32_t s_cnt = 0, red_cnt = 0;
     uint32_t free_seen[2] = {0, 0};   // phases of p_free(b) observed
     uint32_t tiles_total = 0;   // P.V products issued so far for this CTA (all units)
@@ -596,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   }
 }
 
-template <int NQ, bool BF16>
+template <int NQ, int GT, bool BF16>
 cudaError_t launch(const Params& p, int grid, cudaStream_t stream) {
   constexpr int smem = Cfg<NQ>::kSmem;
   static bool attr_done[64] = {};
@@ -604,11 +605,11 @@ cudaError_t launch(const Params& p, int grid, cudaStream_t stream) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-    e = cudaFuncSetAttribute(decode_tc_kernel<NQ, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = cudaFuncSetAttribute(decode_tc_kernel<NQ, GT, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[dev] = true;
   }
-  decode_tc_kernel<NQ, BF16><<<grid, kThreads, smem, stream>>>(p);
+  decode_tc_kernel<NQ, GT, BF16><<<grid, kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -637,8 +638,14 @@ cudaError_t launch_decode_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_k, c
   p.G = Hq / Hkv;
   p.split = split;
   p.scale_log2 = scale_log2;
-  if (p.G <= 16) return bf16 ? dtc::launch<16, true>(p, grid, stream) : dtc::launch<16, false>(p, grid, stream);
-  return bf16 ? dtc::launch<32, true>(p, grid, stream) : dtc::launch<32, false>(p, grid, stream);
+  // the query heads per key/value head that attn_decode accepts: 1, 2, 4, 8
+  switch (p.G) {
+    case 1: return bf16 ? dtc::launch<16, 1, true>(p, grid, stream) : dtc::launch<16, 1, false>(p, grid, stream);
+    case 2: return bf16 ? dtc::launch<16, 2, true>(p, grid, stream) : dtc::launch<16, 2, false>(p, grid, stream);
+    case 4: return bf16 ? dtc::launch<16, 4, true>(p, grid, stream) : dtc::launch<16, 4, false>(p, grid, stream);
+    case 8: return bf16 ? dtc::launch<16, 8, true>(p, grid, stream) : dtc::launch<16, 8, false>(p, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace attn
