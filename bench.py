@@ -604,6 +604,58 @@ def decode_leg(attn, device, stream, peaks, iters: int = 20):
     return out
 
 
+def rope_fused_leg(attn, device, stream, peaks, iters: int = 30):
+    """The forward of rotary-embedded q and k (training page §4), three ways,
+    median CUDA-event times with L2 flushed before each call: attn_fwd_rope
+    (Q rotated inside the forward kernel, K by the rotary pass), the unfused
+    route (attn_rotary on q and on k, then attn_fwd) and attn_fwd alone on
+    the same tensors (no rotation: the floor).  GPT-NeoX pairing over the full
+    head dimension, base 10000.  Two shapes: the headline workload and the
+    GQA configuration."""
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def timed(call):
+        call()
+        torch.cuda.synchronize(device)
+        ms = []
+        for _ in range(iters):
+            flush.zero_()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            call()
+            e.record(stream)
+            torch.cuda.synchronize(device)
+            ms.append(s.elapsed_time(e))
+        if attn.get_error() != attn.ATTN_OK:
+            raise RuntimeError(f"device error in the rope leg: {attn.last_device_error():#x}")
+        return statistics.median(ms)
+
+    out = {}
+    for name in ("single_head_l8192_d128_causal", "gqa_b2_hq32_hkv8_l4096_d128_causal"):
+        wl = WORKLOADS[name]
+        inp = generate(wl)
+        q, k, v = inp.q.to(device), inp.k.to(device), inp.v.to(device)
+        o, lse = attn.attn_fwd(q, k, v, causal=wl.causal, scale=wl.softmax_scale)
+        qr, kr = torch.empty_like(q), torch.empty_like(k)
+
+        def fused():
+            attn.attn_fwd_rope(q, k, v, causal=wl.causal, scale=wl.softmax_scale, out=o, lse=lse, stream=stream)
+
+        def unfused():
+            attn.rotary(q, out=qr, stream=stream)
+            attn.rotary(k, out=kr, stream=stream)
+            attn.attn_fwd(qr, kr, v, causal=wl.causal, scale=wl.softmax_scale, out=o, lse=lse, stream=stream)
+
+        def plain():
+            attn.attn_fwd(q, k, v, causal=wl.causal, scale=wl.softmax_scale, out=o, lse=lse, stream=stream)
+
+        t_f, t_u, t_p = timed(fused), timed(unfused), timed(plain)
+        fl = workload_flops(wl, inp.lengths)
+        out[name] = {"fused_ms": t_f, "unfused_ms": t_u, "attn_fwd_only_ms": t_p,
+                     "fused_tflops": fl / (t_f / 1e3) / 1e12, "unfused_tflops": fl / (t_u / 1e3) / 1e12}
+    return out
+
+
 CONFIG_ORDER = ("mha_l256_d64", "single_head_l8192_d128_causal", "mha_b2_h16_l2048_d64_fp16_causal",
                 "gqa_b2_hq32_hkv8_l4096_d128_causal", "varlen_b16_h12_d64")
 
@@ -744,6 +796,7 @@ def run_ours(args, wl):
                               "kv_cache": cache_leg(attn, device, stream, peaks),
                               "rotary": rotary_leg(attn, device, stream, peaks),
                               "decode": decode_leg(attn, device, stream, peaks),
+                              "rope_fused": rope_fused_leg(attn, device, stream, peaks),
                               "backward": bwd_leg(attn, device, stream, peaks)}), flush=True)
         return 0
 
@@ -871,13 +924,14 @@ def run_ours(args, wl):
         raise RuntimeError(f"device error in the e2e leg: {attn.last_device_error():#x}")
 
     # ---- padded batches: unpad index and row gather / scatter (HBM-bound)
-    pad = cache = rot = bwd = dec = None
+    pad = cache = rot = bwd = dec = rope = None
     if not args.no_pad_leg:
         pad = pad_leg(attn, device, stream, peaks)
         cache = cache_leg(attn, device, stream, peaks)
         dec = decode_leg(attn, device, stream, peaks)
         bwd = bwd_leg(attn, device, stream, peaks)
         rot = rotary_leg(attn, device, stream, peaks)
+        rope = rope_fused_leg(attn, device, stream, peaks)
 
     # ---- the five configurations, and the headline on the CTA-pair kernel
     cfgs = pair = kept = None
@@ -913,7 +967,7 @@ def run_ours(args, wl):
                         "per_rank_events": "one CUDA-event pair per step on the launching stream"},
             "clocks": clocks, "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
             "cpu_baseline": cpu, "configs": cfgs, "pair_kernel_headline": pair,
-            "pad_unpad": pad, "kv_cache": cache, "rotary": rot, "backward": bwd, "decode": dec,
+            "pad_unpad": pad, "kv_cache": cache, "rotary": rot, "backward": bwd, "decode": dec, "rope_fused": rope,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:

@@ -381,6 +381,35 @@ void attn_set_pair_forward(int enable);
 int attn_pair_forward_used(int d, int varlen);
 
 /*
+ * attn_fwd_rope -- attn_fwd of rotary-embedded queries and keys (training
+ * page §4: the rotary module, rotary dimension, base frequency, GPT-NeoX or
+ * GPT-J pairing, a position offset for queries that extend a cache):
+ *     O = attention(rope(q, positions q_offset + i), rope(k, positions j), v)
+ * with rope as attn_rotary applies it (pair i of the first rot_dim features
+ * rotated by position * base^(-2 i / rot_dim); interleaved = 1 pairs (2i,
+ * 2i+1), 0 pairs (i, i + rot_dim/2); the rotated values rounded to the
+ * tensors' 16-bit type).  q and k are read, not modified.  Dense layouts as
+ * attn_fwd (no cu_seqlens); d 64 or 128; rot_dim a multiple of 16, at most d;
+ * base > 1; q_offset >= 0 (Lk - Lq places the queries after a cache).
+ *
+ * The rotation of Q is fused into the forward kernel: each softmax thread
+ * rotates its own query row in shared memory after the unit's Q block lands
+ * and before its first S = Q K^T, from a (cos, sin) table the library keeps
+ * (computed once per rotary dimension, base and position count, with the
+ * rotary pass's arithmetic).  K is rotated by the rotary pass into a library
+ * workspace first: a key tile is loaded once per query block, so rotating it
+ * in the tile load would repeat the rotation L / 256 times per key.  Two or
+ * three launches on `stream` (table when new, rotary of K, forward (+ merge));
+ * workspaces are stream-ordered like attn_fwd's.  Return codes as attn_fwd.
+ * Measured on the GB300: the rotation at every unit start delays the unit's
+ * first MMA, so attn_rotary on q and k followed by attn_fwd is faster (e.g.
+ * 44.7 against 48.8 us for one head of 8192 causal tokens at d 128).
+ */
+int attn_fwd_rope(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv, int Lq,
+                  int Lk, int d, int causal, float scale, int rot_dim, float base, int interleaved, int q_offset,
+                  int fp16, cudaStream_t stream);
+
+/*
  * attn_set_decode_path -- selects how attn_decode runs: 1 (the default) on
  * the packed forward's tensor-core tiles, in decode mode (the query heads of
  * a key/value head share one tile, and each cache is cut into pieces of key

@@ -110,6 +110,8 @@ def lib(path: Optional[str] = None):
         L.attn_decode.restype = i
         L.attn_set_pair_forward.argtypes = [i]
         L.attn_set_pair_forward.restype = None
+        L.attn_fwd_rope.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, f, i, i, i, vp]
+        L.attn_fwd_rope.restype = i
         L.attn_set_decode_path.argtypes = [i]
         L.attn_set_decode_path.restype = None
         L.attn_decode_path.argtypes = []
@@ -207,6 +209,47 @@ def attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = F
                     ctypes.c_float(float(scale)), cu_ptr, _stream_handle(q.device, stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd")
+    return out, lse
+
+
+def attn_fwd_rope(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, causal: bool = False,
+                  scale: Optional[float] = None, rot_dim: Optional[int] = None, base: float = 10000.0,
+                  interleaved: bool = False, q_offset: int = 0, out: Optional[torch.Tensor] = None,
+                  lse: Optional[torch.Tensor] = None,
+                  stream: Optional[torch.cuda.Stream] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """attn_fwd of rotary-embedded q and k (dense (B, L, H, d) layouts): query
+    i at position q_offset + i, key j at position j, rotation as ``rotary``;
+    the rotation of q happens inside the forward kernel.  q and k are not
+    modified."""
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError("q, k, v must be bfloat16 or float16")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must share one dtype")
+    for t in (q, k, v):
+        _check_cuda(t)
+    if q.dim() != 4 or k.dim() != 4 or k.shape != v.shape:
+        raise ValueError("dense q is (B, Lq, Hq, d) and k, v are (B, Lk, Hkv, d)")
+    B, Lq, Hq, d = q.shape
+    _, Lk, Hkv, _ = k.shape
+    rot = d if rot_dim is None else int(rot_dim)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Lq), dtype=torch.float32, device=q.device)
+    if out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor shaped like q")
+    if tuple(lse.shape) != (B, Hq, Lq) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError(f"lse must be a contiguous float32 tensor of shape {(B, Hq, Lq)}")
+    with torch.cuda.device(q.device):
+        rc = lib().attn_fwd_rope(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), int(B),
+                                 int(Hq), int(Hkv), int(Lq), int(Lk), int(d), int(bool(causal)),
+                                 ctypes.c_float(float(scale)), rot, ctypes.c_float(float(base)),
+                                 int(bool(interleaved)), int(q_offset), int(q.dtype == torch.float16),
+                                 _stream_handle(q.device, stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_rope")
     return out, lse
 
 

@@ -136,6 +136,10 @@ struct DevState {
   Workspace pair_part;   // CTA-pair split pieces: u then (m, l)
   Workspace pair_cnt;    // CTA-pair merge counters (epoch-tagged words, zeroed when allocated)
   unsigned int epoch = 0;
+  Workspace rope_tab;    // attn_fwd_rope: the (cos, sin) table ...
+  int rope_rot = 0, rope_npos = 0;   // ... for this rotary dimension and positions 0 .. rope_npos - 1
+  float rope_base = 0.0f;
+  Workspace rope_k;      // attn_fwd_rope: the rotated keys
 };
 
 std::map<int, DevState> g_dev;
@@ -414,8 +418,15 @@ int fwd_pair(DevState& st, int dev, bool bf16, const void* q, const void* k, con
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// The rotary embedding of Q applied inside the forward kernel (attn_fwd_rope).
+struct RopeArgs {
+  const float2* cs;   // the (cos, sin) table
+  int rot, gptj, q_offset;
+};
+
 int fwd(bool bf16, const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
-        int Lq, int Lk, int d, int causal, float scale, const int* cu, const int* cu_k, cudaStream_t stream) {
+        int Lq, int Lk, int d, int causal, float scale, const int* cu, const int* cu_k, cudaStream_t stream,
+        const RopeArgs* rope = nullptr) {
   // ---- host-side argument checks (nothing is enqueued on failure)
   if (!q || !k || !v || !o || !lse) return ATTN_EINVAL;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4)) return ATTN_EINVAL;
@@ -447,7 +458,7 @@ int fwd(bool bf16, const void* q, const void* k, const void* v, void* o, float* 
   int rc = init_device(dev, st);
   if (rc) return rc;
   if (!st.supported) return ATTN_EUNSUPPORTED;
-  if (!varlen && d == 128 && g_pair_forward.load() != 0 && st.sm_count >= 2)
+  if (!varlen && !rope && d == 128 && g_pair_forward.load() != 0 && st.sm_count >= 2)
     return fwd_pair(st, dev, bf16, q, k, v, o, lse, B, Hq, Hkv, Lq, Lk, d, causal != 0, scale, stream);
 
   static thread_local FwdParams p;
@@ -486,6 +497,13 @@ int fwd(bool bf16, const void* q, const void* k, const void* v, void* o, float* 
 
   FwdLauncher launch = (d == 64) ? fwd_launcher_d64(bf16, causal != 0, varlen)
                                  : fwd_launcher_d128(bf16, causal != 0, varlen);
+  if (rope) {
+    p.rope_cs = reinterpret_cast<const float*>(rope->cs);
+    p.rope_rot = rope->rot;
+    p.rope_gptj = rope->gptj;
+    p.rope_qoff = rope->q_offset;
+    launch = (d == 64) ? fwd_rope_launcher_d64(bf16, causal != 0) : fwd_rope_launcher_d128(bf16, causal != 0);
+  }
   int grid = 0;
   DevPlan* plan = nullptr;
   if (!varlen) {
@@ -663,6 +681,56 @@ int fwd_decode(bool bf16, const void* q, const void* k, const void* v, void* o, 
 }
 
 bool decode_tensor_cores() { return g_decode_tc.load() != 0; }
+
+// attention(rope(q, q_offset + i), rope(k, j), v): K through the rotary pass
+// into a library workspace, Q rotated by the forward kernel in shared memory
+// at the start of every unit, from a cached (cos, sin) table.
+int fwd_rope(bool bf16, const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+             int Lq, int Lk, int d, int causal, float scale, int rot, float base, int gptj, int q_offset,
+             cudaStream_t stream) {
+  if (!q || !k || !v) return ATTN_EINVAL;
+  if (rot <= 0 || rot > d || rot % 16 != 0 || !(base > 1.0f) || !std::isfinite(base)) return ATTN_EINVAL;
+  if ((gptj != 0 && gptj != 1) || q_offset < 0 || B <= 0 || Hkv <= 0 || Lk < 0 || Lq < 0) return ATTN_EINVAL;
+  if (d != 64 && d != 128) return ATTN_EUNSUPPORTED;
+  if (static_cast<long long>(Lq) + q_offset > (1LL << 30)) return ATTN_EINVAL;
+  if (Lq == 0) return ATTN_OK;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return ATTN_ELAUNCH;
+  const int n_pos = std::max(1, std::max(Lk, Lq + q_offset));
+  const size_t k_bytes = static_cast<size_t>(B) * Lk * Hkv * d * 2;
+  const float2* cs = nullptr;
+  void* k_rot = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    DevState& st = g_dev[dev];
+    int rc = init_device(dev, st);
+    if (rc) return rc;
+    if (!st.supported) return ATTN_EUNSUPPORTED;
+    // the table, recomputed only when the rotation or the positions it covers change
+    if (st.rope_rot != rot || st.rope_base != base || st.rope_npos < n_pos) {
+      const int np = std::max(n_pos, st.rope_rot == rot && st.rope_base == base ? 2 * st.rope_npos : n_pos);
+      if ((rc = ws_ensure(st.rope_tab, static_cast<size_t>(np) * (rot / 2) * sizeof(float2), stream, false))) return rc;
+      if ((rc = rope_table(static_cast<float2*>(st.rope_tab.ptr), np, rot, base, stream))) return rc;
+      st.rope_rot = rot;
+      st.rope_base = base;
+      st.rope_npos = np;
+    } else if (capturing(stream)) {
+      st.rope_tab.pinned = true;
+    }
+    cs = static_cast<const float2*>(st.rope_tab.ptr);
+    if (k_bytes > 0) {
+      if ((rc = ws_ensure(st.rope_k, k_bytes, stream, false))) return rc;
+      k_rot = st.rope_k.ptr;
+    }
+  }
+  if (k_bytes > 0) {
+    const int rc = attn_rotary(k, k_rot, B, Lk, Hkv, d, rot, base, gptj, nullptr, 0, nullptr, bf16 ? 0 : 1, stream);
+    if (rc) return rc;
+  }
+  const RopeArgs ra{cs, rot, gptj, q_offset};
+  return fwd(bf16, q, k_bytes > 0 ? k_rot : k, v, o, lse, B, Hq, Hkv, Lq, Lk, d, causal, scale, nullptr, nullptr,
+             stream, &ra);
+}
 
 __global__ void selftest_wait_kernel(int* err, unsigned long long timeout_ns) {
   __shared__ __align__(8) uint64_t bar;
@@ -850,6 +918,14 @@ int attn_profile_read(float* main_ms, float* call_ms, int max, int* n) {
 }
 
 void attn_set_pair_forward(int enable) { attn::g_pair_forward.store(enable ? 1 : 0); }
+
+int attn_fwd_rope(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Lq,
+                  int Lk, int d, int causal, float scale, int rot_dim, float base, int interleaved, int q_offset,
+                  int fp16, cudaStream_t stream) {
+  if (fp16 != 0 && fp16 != 1) return ATTN_EINVAL;
+  return attn::fwd_rope(fp16 == 0, q, k, v, o, lse, B, Hq, Hkv, Lq, Lk, d, causal, scale, rot_dim, base, interleaved,
+                        q_offset, stream);
+}
 
 void attn_set_decode_path(int tensor_cores) { attn::g_decode_tc.store(tensor_cores ? 1 : 0); }
 int attn_decode_path(void) { return attn::g_decode_tc.load(); }

@@ -38,4 +38,8 @@ int decode_on_tensor_cores(bool bf16, const void* q, const void* k, const void* 
                            int Hkv, int total_k, int d, float scale, const int* cu_k, cudaStream_t stream);
 bool decode_tensor_cores_enabled();
 
+// Writes cs[pos * rot / 2 + i] = (cos, sin) of pos * base^(-2 i / rot) for
+// pos < n_pos with the arithmetic of the rotary pass (one launch on stream).
+int rope_table(float2* cs, int n_pos, int rot, float base, cudaStream_t stream);
+
 }  // namespace attn

@@ -45,8 +45,8 @@ struct Cfg {
   static constexpr int kOffV = kOffK + kNS * kTile;
   static constexpr int kOffBar = kOffV + kNS * kTile;
   // barriers: q_full, q_empty, kv_full[NS], kv_empty[NS], s_full[2], p_full[2],
-  //           o_done[2], drain
-  static constexpr int kNBars = 2 + 2 * kNS + 7;
+  //           o_done[2], drain, q_rot
+  static constexpr int kNBars = 2 + 2 * kNS + 8;   // + q_rot (rotary variant)
   static constexpr int kOffMisc = kOffBar + kNBars * 8;   // tmem slot, abort flag, bad flag
   static constexpr int kOffVarlen = kOffMisc + 64;        // varlen unit prefix table
   static constexpr int kSmemDense = kOffVarlen + 1024;    // + alignment slack
@@ -297,11 +297,80 @@ __device__ __forceinline__ void softmax_tile(uint32_t t_s, uint32_t t_o, int lim
   tmem_wait_st();
 }
 
+// Rotary embedding of one 128-byte-swizzled Q row in shared memory (row
+// `row` of a 128-row sub-tile starting at `tile`, D/64 chunks of 64 columns,
+// 16 KB apart): pair (x1, x2) -> (x1 cos a - x2 sin a, x1 sin a + x2 cos a)
+// with (cos a, sin a) = p.rope_cs[pos * rot / 2 + i], computed and rounded
+// as the standalone rotary pass does; 8 pairs per step with 16-byte accesses.
+template <int D, bool BF16>
+__device__ __forceinline__ void rope_row(uint8_t* tile, int row, const FwdParams& p, int pos) {
+  const int half = p.rope_rot >> 1;
+  const float2* cs = reinterpret_cast<const float2*>(p.rope_cs) + static_cast<size_t>(pos) * half;
+  auto at = [&](int col) -> uint4* {   // the 16-byte granule holding columns col .. col + 7
+    return reinterpret_cast<uint4*>(tile + (col >> 6) * 16384 + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4));
+  };
+  auto unpack = [](uint32_t w, float& lo, float& hi) {
+    if constexpr (BF16) {
+      lo = __uint_as_float(w << 16);
+      hi = __uint_as_float(w & 0xffff0000u);
+    } else {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w));
+      lo = f.x;
+      hi = f.y;
+    }
+  };
+  for (int g = 0; g < half; g += 8) {
+    float c[8], s[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const float2 v = __ldg(cs + g + e);
+      c[e] = v.x;
+      s[e] = v.y;
+    }
+    if (p.rope_gptj) {
+      // pairs (2i, 2i+1): columns 2g .. 2g + 15 in two granules
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        uint4* gp = at(2 * g + 8 * k);
+        uint4 w = *gp;
+        uint32_t* ww = reinterpret_cast<uint32_t*>(&w);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float x1, x2;
+          unpack(ww[e], x1, x2);
+          const int i = 4 * k + e;
+          ww[e] = pack2<BF16>(x1 * c[i] - x2 * s[i], x1 * s[i] + x2 * c[i]);
+        }
+        *gp = w;
+      }
+    } else {
+      // pairs (i, i + rot/2): columns g .. g + 7 and g + half .. g + half + 7
+      uint4* ga = at(g);
+      uint4* gb = at(g + half);
+      uint4 wa = *ga, wb = *gb;
+      uint32_t* a = reinterpret_cast<uint32_t*>(&wa);
+      uint32_t* b = reinterpret_cast<uint32_t*>(&wb);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float a0, a1, b0, b1;
+        unpack(a[e], a0, a1);
+        unpack(b[e], b0, b1);
+        const int i = 2 * e;
+        a[e] = pack2<BF16>(a0 * c[i] - b0 * s[i], a1 * c[i + 1] - b1 * s[i + 1]);
+        b[e] = pack2<BF16>(a0 * s[i] + b0 * c[i], a1 * s[i + 1] + b1 * c[i + 1]);
+      }
+      *ga = wa;
+      *gb = wb;
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <int D, bool BF16, bool CAUSAL, bool VARLEN>
+template <int D, bool BF16, bool CAUSAL, bool VARLEN, bool ROPE = false>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
+  static_assert(!(ROPE && VARLEN), "the rotary variant is dense only");
   using C = Cfg<D>;
   using T = typename IO<BF16>::T;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -325,6 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   auto b_p_full = [&](int t) { return bar_sp + 16 + 8 * t; };
   auto b_o_done = [&](int t) { return bar_sp + 32 + 8 * t; };
   const uint32_t b_drain = bar_sp + 48;
+  const uint32_t b_q_rot = bar_sp + 56;   // rotary variant: the unit's Q rotated in place
 
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
@@ -348,6 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       mbar_init(b_o_done(t), 1);
     }
     mbar_init(b_drain, 1);
+    mbar_init(b_q_rot, 2 * kBM / 32);   // one arrival per softmax warp
     fence_mbar_init();
   }
   if (warp == kWarpMMA) {
@@ -524,7 +595,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         Unit U;
         decode_unit<CAUSAL, VARLEN>(p, vl_pref, u, U);
         if (U.kv_end <= U.kv_begin) continue;
-        if (!mbar_wait(b_q_full, q_cnt & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteQFull))) break;
+        // (rotary variant: the softmax threads have rotated the Q block in place)
+        if (!mbar_wait(ROPE ? b_q_rot : b_q_full, q_cnt & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteQFull))) break;
         tr.rec(kTagQFull, 0, u, 0);
         bool first_pv0 = true, first_pv1 = true;
         // first stage use: K of the first tile, S for it
@@ -607,6 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const uint32_t t_o = tmem + lane_off + 256 + t * 128;
     const float c_log2 = p.scale_log2;
     uint32_t s_cnt = 0, o_cnt = 0;   // s_full phases seen; units with an o_done commit
+    uint32_t qr_cnt = 0;             // rotary variant: q_full phases seen
     T* out = reinterpret_cast<T*>(p.o);
     Tracer tr;
     tr.init(p, t == 0 ? kTrSoftmax0 : kTrSoftmax1);
@@ -629,6 +702,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       RowState st{-INFINITY, 0.0f};
       int n_act = 0;
       bool ok = true;
+      if constexpr (ROPE) {
+        // rotary embedding of this thread's Q row, in shared memory, before
+        // the unit's first S = Q K^T (the MMA issuer waits for q_rot)
+        if (U.kv_end > U.kv_begin) {
+          if (!mbar_wait_warp(b_q_full, qr_cnt & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteQFull))) break;
+          ++qr_cnt;
+          rope_row<D, BF16>(smem + C::kOffQ + t * C::kTile, row, p, min(q_first + row, p.Lq - 1) + p.rope_qoff);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(b_q_rot);
+        }
+      }
       tr.rec(kTagUnitBegin, t, u, 0);
       for (int j = U.kv_begin; j < U.kv_end; ++j) {
         if (!unit_active(U, t, j)) break;

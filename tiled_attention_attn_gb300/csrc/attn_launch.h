@@ -13,6 +13,10 @@ using DecodeCombineLauncher = cudaError_t (*)(const DecodeCombineParams& p, int 
 
 FwdLauncher fwd_launcher_d64(bool bf16, bool causal, bool varlen);
 FwdLauncher fwd_launcher_d128(bool bf16, bool causal, bool varlen);
+// The dense forward with the rotary embedding of Q applied in the kernel
+// (FwdParams::rope_cs and its companions set).
+FwdLauncher fwd_rope_launcher_d64(bool bf16, bool causal);
+FwdLauncher fwd_rope_launcher_d128(bool bf16, bool causal);
 CombineLauncher combine_launcher_d64(bool bf16);
 CombineLauncher combine_launcher_d128(bool bf16);
 DecodeCombineLauncher decode_combine_launcher_d64(bool bf16);

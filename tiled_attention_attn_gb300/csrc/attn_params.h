@@ -81,6 +81,14 @@ struct FwdParams {
   int vl_decode;
   int vl_split;
   int* vl_pref_out;
+  // Rotary embedding of Q inside the kernel (the ROPE instantiations, dense
+  // only): rope_cs[pos * rot / 2 + i] = (cos, sin) of pos * base^(-2 i / rot);
+  // query row i of a sequence has position i + rope_qoff; GPT-J pairs
+  // (2i, 2i+1) when rope_gptj, else GPT-NeoX pairs (i, i + rot/2).
+  const float* rope_cs;   // float2 pairs
+  int rope_rot;
+  int rope_gptj;
+  int rope_qoff;
   float scale_log2;            // scale * log2(e)
   float scale;
   // A small schedule is copied here so that a CTA learns its first unit from

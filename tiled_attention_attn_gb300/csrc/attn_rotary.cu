@@ -12,6 +12,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 
@@ -244,7 +245,35 @@ int rotary(const void* x, void* y, int B, int L, int h_total, int h_rot, int d, 
   return ATTN_OK;
 }
 
+// (cos, sin) of pos * theta_i for pos < n_pos and i < rot / 2, computed as
+// the rotary kernels above compute them, for the forward kernel's in-kernel
+// rotation of Q.
+__global__ void rope_table_kernel(float2* cs, int n_pos, int rot, float log2_base) {
+  const int half = rot / 2;
+  const long long n = static_cast<long long>(n_pos) * half;
+  for (long long it = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; it < n;
+       it += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int pos = static_cast<int>(it / half);
+    const int i = static_cast<int>(it - static_cast<long long>(pos) * half);
+    const float theta = exp2f(-2.0f * static_cast<float>(i) / static_cast<float>(rot) * log2_base);
+    float sn, c;
+    sincosf(static_cast<float>(pos) * theta, &sn, &c);
+    cs[it] = make_float2(c, sn);
+  }
+}
+
 }  // namespace
+
+int rope_table(float2* cs, int n_pos, int rot, float base, cudaStream_t stream) {
+  if (!cs || n_pos <= 0 || rot <= 0 || (rot & 1) || !(base > 1.0f)) return ATTN_EINVAL;
+  const long long n = static_cast<long long>(n_pos) * (rot / 2);
+  const int grid = static_cast<int>(std::min<long long>((n + 255) / 256, 1024));
+  rope_table_kernel<<<grid, 256, 0, stream>>>(cs, n_pos, rot, std::log2(base));
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ELAUNCH;
+  count_launch();
+  return ATTN_OK;
+}
+
 }  // namespace attn
 
 extern "C" {
