@@ -406,6 +406,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   if (tid == 0) {
     *abort_flag = 0;
     *bad_flag = 0;
+  }
+  // The producer thread initialises the barriers, so that (dense schedules)
+  // it can issue the first unit's Q block and first key tile before the
+  // set-up barrier: the first loads after an L2 flush take microseconds, and
+  // they then overlap the TMEM allocation and the set-up.
+  bool early = false;
+  if (warp == kWarpTMA && lane == 0) {
     mbar_init(b_q_full, 1);
     mbar_init(b_q_empty, 1);
     for (int s = 0; s < C::kNS; ++s) {
@@ -420,15 +427,35 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     mbar_init(b_drain, 1);
     mbar_init(b_q_rot, 2 * kBM / 32);   // one arrival per softmax warp
     fence_mbar_init();
+    tma_prefetch_desc(&p.tm_q);
+    tma_prefetch_desc(&p.tm_k);
+    tma_prefetch_desc(&p.tm_v);
+    if constexpr (!VARLEN) {
+      const int* off = p.n_inline ? p.cta_off_inline : p.cta_off;
+      if (off[blockIdx.x] < off[blockIdx.x + 1]) {
+        Unit U;
+        decode_unit<CAUSAL, VARLEN>(p, nullptr, off[blockIdx.x], U);
+        if (U.kv_end > U.kv_begin) {
+          // the producer loop below skips exactly these two issues
+          mbar_arrive_expect_tx(b_q_full, kNSub * C::kTile);
+#pragma unroll
+          for (int t = 0; t < kNSub; ++t)
+#pragma unroll
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_4d(sQ + t * C::kTile + c * 16384, &p.tm_q, b_q_full, c * 64, U.h, U.row_q + U.q_row0 + t * kBM,
+                          U.bcoord);
+          mbar_arrive_expect_tx(b_kv_full(0), C::kTile);
+#pragma unroll
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_4d(sK + c * 16384, &p.tm_k, b_kv_full(0), c * 64, U.g, U.row_k + U.kv_begin * kBN, U.bcoord);
+          early = true;
+        }
+      }
+    }
   }
   if (warp == kWarpMMA) {
     tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
     tmem_relinquish();
-  }
-  if (warp == kWarpTMA && lane == 0) {
-    tma_prefetch_desc(&p.tm_q);
-    tma_prefetch_desc(&p.tm_k);
-    tma_prefetch_desc(&p.tm_v);
   }
 
   // varlen: validate cu_seqlens (queries) and cu_seqlens_k (keys) and build
@@ -519,23 +546,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         Unit U;
         decode_unit<CAUSAL, VARLEN>(p, vl_pref, u, U);
         if (U.kv_end <= U.kv_begin) continue;
-        if (!mbar_wait(b_q_empty, (q_cnt & 1) ^ 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteQEmpty))) break;
-        mbar_arrive_expect_tx(b_q_full, kNSub * C::kTile);
+        const bool pre = early;   // this unit's Q and first key tile were issued before the set-up barrier
+        early = false;
+        if (!pre && !mbar_wait(b_q_empty, (q_cnt & 1) ^ 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteQEmpty))) break;
+        if (!pre) mbar_arrive_expect_tx(b_q_full, kNSub * C::kTile);
         // a sub-tile is 128 rows of one head, or (packed) 128 / 2^pack_log2
         // queries x 2^pack_log2 heads from one box of the same byte count
         const int q_span = VARLEN ? (kBM >> p.pack_log2) : kBM;
+        if (!pre) {
 #pragma unroll
-        for (int t = 0; t < kNSub; ++t)
+          for (int t = 0; t < kNSub; ++t)
 #pragma unroll
-          for (int c = 0; c < C::kChunks; ++c)
-            tma_load_4d(sQ + t * C::kTile + c * 16384, &p.tm_q, b_q_full, c * 64, U.h,
-                        U.row_q + U.q_row0 + t * q_span, U.bcoord);
+            for (int c = 0; c < C::kChunks; ++c)
+              tma_load_4d(sQ + t * C::kTile + c * 16384, &p.tm_q, b_q_full, c * 64, U.h,
+                          U.row_q + U.q_row0 + t * q_span, U.bcoord);
+        }
         tr.rec(kTagQIssue, 0, u, 0);
         ++q_cnt;
         bool ok = true;
         const int n = U.kv_end - U.kv_begin;
         for (int i = 0; i <= n; ++i) {
           const int st = kv_cnt % C::kNS;
+          if (pre && i == 0) {   // stage 0 holds the first key tile already
+            ++kv_cnt;
+            continue;
+          }
           if (!mbar_wait(b_kv_empty(st), ((kv_cnt / C::kNS) & 1) ^ 1, wc,
                          ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKEmpty))) { ok = false; break; }
           const bool hk = i < n, hv = i > 0;
