@@ -783,7 +783,56 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         const size_t orow = VARLEN ? static_cast<size_t>(U.row_q + qrow)
                                    : static_cast<size_t>(U.b) * p.Lq + qrow;
         T* dst = out + (orow * p.Hq + head) * D;
-        if (n_act > 0) {
+        if (n_act > 0 && D == 64) {
+          // The 128-byte rows are transposed within groups of 8 lanes by
+          // three xor-shuffle stages: afterwards lane 8g + j holds 16-byte
+          // chunk j of rows 8g .. 8g + 7, so one warp store writes 4 whole
+          // rows, where a store of each thread's own row would write a
+          // 16-byte piece of 32 rows (32 cache lines).  (For head_dim 128 the
+          // shuffles cost more than they save: measured slower.)
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c) {
+            uint4 a[8];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              uint32_t o[32];
+              tmem_ld_32x32b_x32(t_o + c * 64 + h * 32, o);
+              tmem_wait_ld(o);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                a[4 * h + i] = make_uint4(
+                    pack2<BF16>(__uint_as_float(o[8 * i + 0]) * inv_l, __uint_as_float(o[8 * i + 1]) * inv_l),
+                    pack2<BF16>(__uint_as_float(o[8 * i + 2]) * inv_l, __uint_as_float(o[8 * i + 3]) * inv_l),
+                    pack2<BF16>(__uint_as_float(o[8 * i + 4]) * inv_l, __uint_as_float(o[8 * i + 5]) * inv_l),
+                    pack2<BF16>(__uint_as_float(o[8 * i + 6]) * inv_l, __uint_as_float(o[8 * i + 7]) * inv_l));
+            }
+#pragma unroll
+            for (int m = 4; m >= 1; m >>= 1) {
+              const bool up = (lane & m) != 0;
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                if (k & m) continue;
+                const uint4 snd = up ? a[k] : a[k | m];
+                uint4 rcv;
+                rcv.x = __shfl_xor_sync(0xffffffffu, snd.x, m);
+                rcv.y = __shfl_xor_sync(0xffffffffu, snd.y, m);
+                rcv.z = __shfl_xor_sync(0xffffffffu, snd.z, m);
+                rcv.w = __shfl_xor_sync(0xffffffffu, snd.w, m);
+                if (up) a[k] = rcv; else a[k | m] = rcv;
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int rr = quarter * 32 + (lane & ~7) + i;   // row of the sub-tile
+              const int qr = q_first + (rr >> lp);
+              if (qr < U.q_len) {
+                const int hd = U.h + (rr & ((1 << lp) - 1));
+                const size_t orr = VARLEN ? static_cast<size_t>(U.row_q + qr) : static_cast<size_t>(U.b) * p.Lq + qr;
+                *reinterpret_cast<uint4*>(out + (orr * p.Hq + hd) * D + c * 64 + (lane & 7) * 8) = a[i];
+              }
+            }
+          }
+        } else if (n_act > 0) {
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
