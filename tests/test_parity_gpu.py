@@ -307,3 +307,35 @@ def test_forward_is_bitwise_reproducible():
     o2, l2 = attn.attn_fwd(q, k, v, causal=True)
     assert attn.get_error() == attn.ATTN_OK
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_output_alignment_16_and_32_bytes_agree(d):
+    """The epilogue stores whole 32-byte pieces where the output pointer is
+    32-byte aligned and 16-byte pieces otherwise; both give the same bits,
+    and both match the oracle (dense and packed varlen)."""
+    dev = torch.device("cuda", 0)
+    g = torch.Generator().manual_seed(40 + d)
+    q = torch.randn(1, 300, 4, d, generator=g).to(torch.bfloat16)
+    k = torch.randn(1, 300, 2, d, generator=g).to(torch.bfloat16)
+    v = torch.randn(1, 300, 2, d, generator=g).to(torch.bfloat16)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    o1, l1 = attn.attn_fwd(qd, kd, vd, causal=True)
+    buf = torch.zeros(o1.numel() + 8, dtype=o1.dtype, device=dev)   # 8 elements = 16 bytes off
+    o2 = buf[8:].view_as(o1)
+    assert o2.data_ptr() % 32 == 16
+    l2 = torch.empty_like(l1)
+    attn.attn_fwd(qd, kd, vd, causal=True, out=o2, lse=l2)
+    assert attn.get_error() == attn.ATTN_OK
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    o_ref, lse_ref = oracle.attention(q, k, v, causal=True, scale=d ** -0.5)
+    assert np.max(np.abs(o1.float().cpu().double().numpy() - o_ref)) <= O_TOL
+    # packed varlen, two sequences
+    cu = torch.tensor([0, 130, 300], dtype=torch.int32, device=dev)
+    o3, l3 = attn.attn_fwd(qd[0], kd[0], vd[0], causal=True, cu_seqlens=cu)
+    buf = torch.zeros(o3.numel() + 8, dtype=o3.dtype, device=dev)
+    o4 = buf[8:].view_as(o3)
+    l4 = torch.empty_like(l3)
+    attn.attn_fwd(qd[0], kd[0], vd[0], causal=True, cu_seqlens=cu, out=o4, lse=l4)
+    assert attn.get_error() == attn.ATTN_OK
+    assert torch.equal(o3, o4) and torch.equal(l3, l4)

@@ -33,14 +33,19 @@ long piece_cost(const Pair& p, int a, int e) {
 }
 
 // Fixed per-unit cost in tile pairs (Q load, pipeline fill and drain,
-// epilogue), the extra store of a split piece, and the combine pass.
+// epilogue), the extra store of a split piece, the combine pass, and the
+// lone tail of a causal block's last piece: its last key tile has only the
+// second sub-tile active, so that tile's softmax -> P.V chain runs with no
+// other sub-tile's MMAs beside it (per-CTA phase traces of the L = 8192,
+// d = 128 causal forward: pieces ending on the diagonal take 1.4-2.9 us more
+// than their tile count predicts, ~2.5 tile pairs).
 struct CostModel {
-  double unit, split_extra, combine;
+  double unit, split_extra, combine, tail;
 };
 
 CostModel cost_model(int d) {
-  if (d == 128) return {2.0, 1.0, 3.0};
-  return {4.0, 2.0, 6.0};
+  if (d == 128) return {2.0, 1.0, 3.0, 2.5};
+  return {4.0, 2.0, 6.0, 0.0};
 }
 
 double assign(std::vector<Cand>& units, int num_sms, std::vector<int>& cta_of, int& n_ctas) {
@@ -74,10 +79,27 @@ void build_units(const std::vector<Pair>& pairs, double target, const CostModel&
       n = std::min(n, std::min(p.kv_end, kMaxSplits));
     }
     if (n > 1) any_split = true;
+    const double tail = (p.kl0 != p.kl1) ? cm.tail : 0.0;
+    // the last piece ends on the block's last key tile and carries the lone
+    // tail: it starts where its cost comes closest to an equal share, and the
+    // tiles before it are cut into n - 1 equal pieces
+    int a_last = static_cast<int>(static_cast<long>(n - 1) * p.kv_end / n);
+    if (n > 1 && tail > 0.0) {
+      const double share = (static_cast<double>(piece_cost(p, 0, p.kv_end)) + tail) / n;
+      double best_gap = std::numeric_limits<double>::infinity();
+      for (int a = n - 1; a < p.kv_end; ++a) {
+        const double gap = std::fabs(static_cast<double>(piece_cost(p, a, p.kv_end)) + tail - share);
+        if (gap < best_gap) {
+          best_gap = gap;
+          a_last = a;
+        }
+      }
+    }
     for (int s = 0; s < n; ++s) {
-      const int a = static_cast<int>(static_cast<long>(s) * p.kv_end / n);
-      const int e = static_cast<int>(static_cast<long>(s + 1) * p.kv_end / n);
-      const double c = static_cast<double>(piece_cost(p, a, e)) + cm.unit + (n > 1 ? cm.split_extra : 0.0);
+      const int a = (s == n - 1) ? a_last : static_cast<int>(static_cast<long>(s) * a_last / (n - 1));
+      const int e = (s == n - 1) ? p.kv_end : static_cast<int>(static_cast<long>(s + 1) * a_last / (n - 1));
+      const double c = static_cast<double>(piece_cost(p, a, e)) + cm.unit + (n > 1 ? cm.split_extra : 0.0) +
+                       (e == p.kv_end ? tail : 0.0);
       units.push_back({static_cast<int>(i), a, e, s, n, c});
     }
   }

@@ -142,6 +142,12 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 }
 // Waits until every committed bulk group of this thread has completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// 256-bit global store (sm_100 and later); `p` must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* v) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]), "r"(v[1]), "r"(v[2]),
+               "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy accesses (a TMA store reading them).
 __device__ __forceinline__ void fence_proxy_async_smem() {
