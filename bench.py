@@ -538,10 +538,9 @@ DECODE_SHAPE = (32, 32, 8, 128, 4096)      # B, Hq, Hkv, d, cache length of the 
 DECODE_LONG_SHAPE = (1, 32, 8, 128, 131072)   # one sequence with a long cache
 
 
-def decode_step_times(attn, device, stream, shape, iters: int = 20):
-    """Median CUDA-event times (ms) of one decoding step, one new token per
-    sequence over a cache of C tokens (+ the new one), through attn_decode
-    and through attn_fwd_varlen; L2 flushed before each call."""
+def decode_inputs(device, shape):
+    """q (B, Hq, d), packed caches k, v (B (C + 1), Hkv, d) bf16 N(0, 1), and
+    the query and key offsets of a decoding step of ``shape``."""
     B, Hq, Hkv, d, C = shape
     g = torch.Generator().manual_seed(66)
     q = torch.randn(B, Hq, d, generator=g).to(torch.bfloat16).to(device)
@@ -549,6 +548,15 @@ def decode_step_times(attn, device, stream, shape, iters: int = 20):
     v = torch.randn(B * (C + 1), Hkv, d, generator=g).to(torch.bfloat16).to(device)
     cu_q = torch.arange(0, B + 1, dtype=torch.int32, device=device)
     cu_k = torch.arange(0, B + 1, dtype=torch.int32, device=device) * (C + 1)
+    return q, k, v, cu_q, cu_k
+
+
+def decode_step_times(attn, device, stream, shape, iters: int = 20):
+    """Median CUDA-event times (ms) of one decoding step, one new token per
+    sequence over a cache of C tokens (+ the new one), through attn_decode
+    and through attn_fwd_varlen; L2 flushed before each call."""
+    B, Hq, Hkv, d, C = shape
+    q, k, v, cu_q, cu_k = decode_inputs(device, shape)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
 
     def timed(call):
@@ -803,6 +811,19 @@ def run_ours(args, wl):
     def call():
         attn.attn_fwd(q, k, v, causal=wl.causal, scale=wl.softmax_scale, cu_seqlens=cu, out=o, lse=lse)
 
+    if args.profile_decode > 0:
+        # attn_decode calls of the decode leg's batch shape (for profiling)
+        dq, dk, dv, _, dcu = decode_inputs(device, DECODE_SHAPE)
+        do = torch.empty_like(dq)
+        dl = torch.empty(DECODE_SHAPE[1], DECODE_SHAPE[0], dtype=torch.float32, device=device)
+        for _ in range(args.profile_decode):
+            flush.zero_()
+            attn.attn_decode(dq, dk, dv, dcu, out=do, lse=dl, stream=stream)
+        torch.cuda.synchronize(device)
+        if attn.get_error() != attn.ATTN_OK:
+            raise RuntimeError(f"device error: {attn.last_device_error():#x}")
+        print(f"{args.profile_decode} attn_decode calls of B{DECODE_SHAPE[0]} x {DECODE_SHAPE[4]}")
+        return 0
     if args.profile_calls > 0:
         attn.set_pair_forward(args.pair)
         for _ in range(args.profile_calls):
@@ -992,6 +1013,9 @@ def main():
     ap.add_argument("--profile-calls", type=int, default=0,
                     help="only make this many attn_fwd calls of --workload (L2 flushed before each) and exit: "
                          "the program the ncu summaries capture")
+    ap.add_argument("--profile-decode", type=int, default=0,
+                    help="only make this many attn_decode calls of the decode leg's batch shape "
+                         "(L2 flushed before each) and exit")
     ap.add_argument("--pair", action="store_true", help="with --profile-calls: run the CTA-pair kernel")
     args = ap.parse_args()
     if args.warmup < 3:
