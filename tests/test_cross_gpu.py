@@ -68,6 +68,21 @@ CASES = [
     ([100, 30, 3], [200, 140, 700], 2, 2, 64, True, torch.float16),
 ]
 
+# Up to 32 sequences are placed in order of their key counts (ties by index);
+# more keep their order.  32 and 33 sequences with repeated lengths and empty
+# ones, and a kv-cache-like mix.
+_rng = np.random.default_rng(123)
+_lq32 = _rng.integers(0, 300, 32).tolist()
+_lq32[5] = 0
+_lk32 = [a + int(c) for a, c in zip(_lq32, _rng.choice([0, 64, 500, 1500], 32))]
+_lq33 = _rng.integers(1, 200, 33).tolist()
+CASES += [
+    (_lq32, _lk32, 8, 2, 128, True, torch.bfloat16),
+    (_lq32, _lq32, 4, 4, 64, False, torch.bfloat16),
+    (_lq33, [a + 100 for a in _lq33], 8, 2, 128, True, torch.bfloat16),
+    ([300] * 12, [300, 800, 300, 2000, 300, 800, 300, 2000, 300, 800, 300, 2000], 2, 2, 64, True, torch.float16),
+]
+
 
 @pytest.mark.parametrize("case", CASES, ids=[f"case{i}" for i in range(len(CASES))])
 def test_cross_varlen(case):

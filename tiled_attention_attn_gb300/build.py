@@ -24,7 +24,7 @@ TRACE_LIB_PATH = os.path.join(PKG, "libattn_trace.so")   # phase-trace points co
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["attn_host.cu", "attn_noalloc.cu", "attn_pad.cu", "attn_rotary.cu", "attn_bwd.cu", "attn_bwd_d64.cu",
            "attn_bwd_d128.cu", "attn_kernels_d64.cu", "attn_kernels_d128.cu", "attn_plan.cpp", "attn_decode.cu",
-           "attn_pair_d128.cu", "attn_decode_tc.cu", "attn_kernels_rope.cu"]
+           "attn_pair_d128.cu", "attn_decode_tc.cu", "attn_kernels_rope.cu", "attn_kernels_sorted.cu"]
 
 
 def nvcc() -> str:

@@ -437,6 +437,9 @@ int fwd(bool bf16, const void* q, const void* k, const void* v, void* o, float* 
   if (d != 64 && d != 128) return ATTN_EUNSUPPORTED;
   const bool varlen = cu != nullptr;
   if (!varlen && cu_k != nullptr) return ATTN_EINVAL;
+  // queries with their own key offsets (cross-attention, a key/value cache):
+  // key counts may differ widely between sequences
+  const bool own_keys = varlen && cu_k != nullptr && cu_k != cu;
   if (varlen) {
     // one offsets array serves queries and keys (self-attention) unless the
     // keys have their own (cross-attention, a key/value cache)
@@ -497,6 +500,8 @@ int fwd(bool bf16, const void* q, const void* k, const void* v, void* o, float* 
 
   FwdLauncher launch = (d == 64) ? fwd_launcher_d64(bf16, causal != 0, varlen)
                                  : fwd_launcher_d128(bf16, causal != 0, varlen);
+  if (own_keys && B <= kVarlenSortMax)
+    launch = (d == 64) ? fwd_sorted_launcher_d64(bf16, causal != 0) : fwd_sorted_launcher_d128(bf16, causal != 0);
   if (rope) {
     p.rope_cs = reinterpret_cast<const float*>(rope->cs);
     p.rope_rot = rope->rot;

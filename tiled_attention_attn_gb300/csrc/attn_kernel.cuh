@@ -51,6 +51,9 @@ struct Cfg {
   static constexpr int kOffVarlen = kOffMisc + 64;        // varlen unit prefix table
   static constexpr int kSmemDense = kOffVarlen + 1024;    // + alignment slack
   static constexpr int kSmemVarlen = kOffVarlen + 4 * (kVarlenMaxB + 1) + 1024;
+  // the sorting variant: the sequence of each rank after the prefix table
+  static constexpr int kOffOrder = kOffVarlen + 4 * (kVarlenMaxB + 1);
+  static constexpr int kSmemVarlenSorted = kOffOrder + 4 * kVarlenSortMax + 1024;
   static constexpr uint32_t kTmemCols = 512;
 };
 
@@ -79,8 +82,13 @@ struct Unit {
   int kv_last[2];
 };
 
-template <bool CAUSAL, bool VARLEN>
-__device__ __forceinline__ bool decode_unit(const FwdParams& p, const int* vl_pref, int u, Unit& U) {
+// SORT (varlen, the sorting variant) with `sorted` set by its prefix pass:
+// the sequences are numbered by rank, most keys first (the prefix table is
+// over ranks; the sequence of rank i follows it, at vl_pref[kVarlenMaxB + 1 +
+// i]), and `u`, the CTA's loop index, is permuted into snake order.
+template <bool CAUSAL, bool VARLEN, bool SORT = false>
+__device__ __forceinline__ bool decode_unit(const FwdParams& p, const int* vl_pref, int u, Unit& U,
+                                            bool sorted = false) {
   if constexpr (!VARLEN) {
     const int* e = (p.n_inline ? p.units_inline : p.units) + u * kUnitInts;
     const int bh = e[0];
@@ -98,6 +106,15 @@ __device__ __forceinline__ bool decode_unit(const FwdParams& p, const int* vl_pr
     U.row_k = 0;
     U.bcoord = U.b;
   } else {
+    if constexpr (SORT) {
+      if (sorted) {
+        // odd rounds of gridDim.x units reversed (a last, partial round
+        // keeps its order, so every unit is still visited once): the CTA
+        // that takes a long unit in one round takes a short one in the next
+        const int G = gridDim.x, r = u / G;
+        if ((r & 1) && (r + 1) * G <= vl_pref[p.B]) u = r * G + (G - 1) - (u - r * G);
+      }
+    }
     // binary search: largest b with vl_pref[b] <= u
     int lo = 0, hi = p.B;   // vl_pref[0] = 0 <= u < vl_pref[B]
     while (hi - lo > 1) {
@@ -110,6 +127,12 @@ __device__ __forceinline__ bool decode_unit(const FwdParams& p, const int* vl_pr
     const int lp = p.pack_log2;
     const int n_hu = p.Hq >> lp;
     const int local = u - vl_pref[lo];
+    if constexpr (SORT) {
+      if (sorted) {
+        lo = vl_pref[kVarlenMaxB + 1 + lo];
+        U.b = lo;
+      }
+    }
     const int s0k = __ldg(p.cu_seqlens_k + lo);
     U.k_len = __ldg(p.cu_seqlens_k + lo + 1) - s0k;
     U.row_k = s0k;
@@ -368,9 +391,92 @@ __device__ __forceinline__ void rope_row(uint8_t* tile, int row, const FwdParams
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <int D, bool BF16, bool CAUSAL, bool VARLEN, bool ROPE = false>
+// The sorting variant's prefix pass (packed varlen forwards with their own
+// key offsets: cross-attention, a key/value cache), by one warp: validates
+// cu_seqlens (queries) and cu_seqlens_k (keys), writes the prefix table of
+// units per sequence (vl_pref[0..B]) and sets *bad_flag on malformed offsets,
+// as the kernel's own pass does; and sets *sort_flag when it numbers the
+// sequences by rank instead.
+// ---------------------------------------------------------------------------
+static __device__ __noinline__ void varlen_prefix_pass_sorted(const FwdParams& p, int* vl_pref, volatile int* bad_flag,
+                                                       volatile int* sort_flag) {
+  const int lane = threadIdx.x & 31;
+  int carry = 0;
+  bool bad = false;
+  if (lane == 0 && ((!p.vl_decode && __ldg(p.cu_seqlens) != 0) || __ldg(p.cu_seqlens_k) != 0)) bad = true;
+  for (int b0 = 0; b0 < p.B; b0 += 32) {
+    const int b = b0 + lane;
+    int cnt = 0;
+    int key = -1;   // sort key: the sequence's key count
+    if (b < p.B) {
+      const int ak = __ldg(p.cu_seqlens_k + b), ek = __ldg(p.cu_seqlens_k + b + 1);
+      if (ek < ak || ek > p.Lk) bad = true;
+      key = max(ek - ak, 0);
+      if (p.vl_decode) {
+        // every head group of every sequence, in pieces of its keys
+        cnt = (p.Hq >> p.pack_log2) * decode_pieces(max(ek - ak, 0), p.vl_split);
+      } else {
+        const int a = __ldg(p.cu_seqlens + b), e = __ldg(p.cu_seqlens + b + 1);
+        if (e < a || e > p.Lq) bad = true;
+        const int len = e - a;
+        const int blk = kBlockRows >> p.pack_log2;   // queries per unit
+        cnt = (len > 0) ? ((len + blk - 1) / blk) * (p.Hq >> p.pack_log2) : 0;
+      }
+    }
+    // At most kVarlenSortMax sequences (one pass; not decoding steps) whose
+    // key counts (over the sequences with queries) differ by more than 4x:
+    // number the sequences by rank, most keys first, and place the units in
+    // snake order (decode_unit), so a CTA that takes a long unit in one
+    // round takes a short one in the next.
+    bool sort = false;
+    if (!p.vl_decode && p.B <= kVarlenSortMax) {
+      int kmax = (cnt > 0) ? key : 0, kmin = (cnt > 0) ? key : 0x7fffffff;
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+        kmin = min(kmin, __shfl_xor_sync(0xffffffffu, kmin, o));
+      }
+      sort = kmin != 0x7fffffff && static_cast<long long>(kmax) > 4LL * kmin;
+      if (lane == 0) *sort_flag = sort ? 1 : 0;
+    }
+    if (sort) {
+      // rank of this sequence: more keys first, then the lower index
+      int rank = 0;
+#pragma unroll 8
+      for (int j = 0; j < 32; ++j) {
+        const int kj = __shfl_sync(0xffffffffu, key, j);
+        rank += (kj > key || (kj == key && j < lane)) ? 1 : 0;
+      }
+      int* order = vl_pref + kVarlenMaxB + 1;
+      if (b < p.B) {
+        order[rank] = b;
+        vl_pref[rank + 1] = cnt;   // scratch: unit count by rank
+      }
+      __syncwarp();
+      cnt = (lane < p.B) ? vl_pref[lane + 1] : 0;
+      __syncwarp();
+    }
+    int x = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (b < p.B) vl_pref[b + 1] = carry + x;
+    carry += __shfl_sync(0xffffffffu, x, 31);
+  }
+  if (lane == 0) vl_pref[0] = 0;
+  if (__any_sync(0xffffffffu, bad) && lane == 0) {
+    *bad_flag = 1;
+    atomicCAS(p.err, 0, ATTN_DEVERR_BAD_SEQLENS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+template <int D, bool BF16, bool CAUSAL, bool VARLEN, bool ROPE = false, bool SORT = false>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ FwdParams p) {
   static_assert(!(ROPE && VARLEN), "the rotary variant is dense only");
+  static_assert(!SORT || VARLEN, "the sorting variant is varlen only");
   using C = Cfg<D>;
   using T = typename IO<BF16>::T;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -399,6 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
   volatile int* bad_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 8);
+  volatile int* sort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 12);   // SORT
   int* vl_pref = reinterpret_cast<int*>(smem + C::kOffVarlen);
 
   WaitCtl wc{p.err, abort_flag, p.timeout_ns};
@@ -406,6 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   if (tid == 0) {
     *abort_flag = 0;
     *bad_flag = 0;
+    if constexpr (SORT) *sort_flag = 0;
   }
   // The producer thread initialises the barriers, so that (dense schedules)
   // it can issue the first unit's Q block and first key tile before the
@@ -461,7 +569,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   // varlen: validate cu_seqlens (queries) and cu_seqlens_k (keys) and build
   // the prefix table of units per sequence
   int n_units = 0, u_first = 0, u_step = 1;
-  if constexpr (VARLEN) {
+  if constexpr (SORT) {
+    if (warp == 0) varlen_prefix_pass_sorted(p, vl_pref, bad_flag, sort_flag);
+  } else if constexpr (VARLEN) {
     if (warp == 0) {
       int carry = 0;
       bool bad = false;
@@ -535,6 +645,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     n_units = off[blockIdx.x + 1];
     u_step = 1;
   }
+  bool snake = false;   // the sorting variant's units in rank and snake order
+  if constexpr (SORT) snake = *sort_flag != 0;
 
   if (warp == kWarpTMA) {
     // ------------------------------------------------------------------ TMA producer
@@ -544,7 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       uint32_t q_cnt = 0, kv_cnt = 0;
       for (int u = u_first; u < n_units; u += u_step) {
         Unit U;
-        decode_unit<CAUSAL, VARLEN>(p, vl_pref, u, U);
+        decode_unit<CAUSAL, VARLEN, SORT>(p, vl_pref, u, U, snake);
         if (U.kv_end <= U.kv_begin) continue;
         const bool pre = early;   // this unit's Q and first key tile were issued before the set-up barrier
         early = false;
@@ -628,7 +740,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
       bool ok = true;
       for (int u = u_first; u < n_units && ok; u += u_step) {
         Unit U;
-        decode_unit<CAUSAL, VARLEN>(p, vl_pref, u, U);
+        decode_unit<CAUSAL, VARLEN, SORT>(p, vl_pref, u, U, snake);
         if (U.kv_end <= U.kv_begin) continue;
         // (rotary variant: the softmax threads have rotated the Q block in place)
         if (!mbar_wait(ROPE ? b_q_rot : b_q_full, q_cnt & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteQFull))) break;
@@ -726,7 +838,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const int span = kBM >> lp;
     for (int u = u_first; u < n_units; u += u_step) {
       Unit U;
-      decode_unit<CAUSAL, VARLEN>(p, vl_pref, u, U);
+      decode_unit<CAUSAL, VARLEN, SORT>(p, vl_pref, u, U, snake);
       const int q_first = U.q_row0 + t * span;          // first query of the sub-tile
       const int qrow = q_first + (row >> lp);           // query row within the sequence
       const int head = U.h + (row & ((1 << lp) - 1));

@@ -17,6 +17,11 @@ FwdLauncher fwd_launcher_d128(bool bf16, bool causal, bool varlen);
 // (FwdParams::rope_cs and its companions set).
 FwdLauncher fwd_rope_launcher_d64(bool bf16, bool causal);
 FwdLauncher fwd_rope_launcher_d128(bool bf16, bool causal);
+// Packed varlen forwards whose keys have their own offsets: when the
+// sequences (at most kVarlenSortMax) have key counts more than 4x apart, the
+// kernel numbers them by key count and places the units in snake order.
+FwdLauncher fwd_sorted_launcher_d64(bool bf16, bool causal);
+FwdLauncher fwd_sorted_launcher_d128(bool bf16, bool causal);
 CombineLauncher combine_launcher_d64(bool bf16);
 CombineLauncher combine_launcher_d128(bool bf16);
 DecodeCombineLauncher decode_combine_launcher_d64(bool bf16);

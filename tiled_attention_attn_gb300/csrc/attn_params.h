@@ -23,6 +23,7 @@ constexpr int kThreads = 320;   // 8 softmax warps + 1 TMA warp + 1 MMA warp
 constexpr int kWarpTMA = 8;
 constexpr int kWarpMMA = 9;
 constexpr int kVarlenMaxB = 4096;   // sequences per varlen call (prefix table in smem)
+constexpr int kVarlenSortMax = 32;  // the sorting varlen variant ranks at most this many sequences
 constexpr int kUnitInts = 8;        // ints per scheduled work unit
 constexpr int kGroupInts = 4;       // ints per split-KV group
 constexpr int kMaxSplits = 64;      // split pieces per group
