@@ -187,6 +187,13 @@ int attn_fwd_noalloc(const void *q, const void *k, const void *v, void *o, float
  * read once per group, and a sequence with one new token (decoding) fills
  * group rows of a tile instead of one.  Every output row is the same
  * function of its inputs either way.
+ *
+ * Scheduling: the kernel builds its work list from the offsets on the
+ * device.  With separate key offsets, up to 32 sequences whose key counts
+ * differ by more than 4x are numbered by key count (most first) and the work
+ * units placed on the CTAs in snake order, so long and short units share
+ * CTAs; otherwise the units go round-robin in sequence order.  The results do
+ * not depend on the placement.
  */
 int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float *lse, int B, int Hq, int Hkv,
                     int total_q, int total_k, int d, int causal, float scale, const int *cu_seqlens_q,
