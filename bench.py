@@ -612,6 +612,49 @@ def decode_leg(attn, device, stream, peaks, iters: int = 20):
     return out
 
 
+def cluster_merge_leg(attn, device, stream, peaks, iters: int = 30):
+    """Split key ranges merged two ways (page S23-J17 §3.1's rescaling across
+    pieces): the default combine pass (pieces of planned lengths, fp32
+    partials in a workspace) against the in-cluster merge
+    (attn_set_cluster_merge: equal pieces of every query block as one
+    cluster, partials merged over distributed shared memory), median
+    CUDA-event times with L2 flushed before each call, bf16, non-causal."""
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    def timed(call):
+        call()
+        torch.cuda.synchronize(device)
+        ms = []
+        for _ in range(iters):
+            flush.zero_()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            call()
+            e.record(stream)
+            torch.cuda.synchronize(device)
+            ms.append(s.elapsed_time(e))
+        if attn.get_error() != attn.ATTN_OK:
+            raise RuntimeError(f"device error in the cluster-merge leg: {attn.last_device_error():#x}")
+        return statistics.median(ms)
+
+    out = {}
+    try:
+        for (B, H, L, d) in ((1, 1, 8192, 128), (1, 4, 4096, 64)):
+            g = torch.Generator().manual_seed(21)
+            q, k, v = (torch.randn(B, L, H, d, generator=g).to(torch.bfloat16).to(device) for _ in range(3))
+            o, lse = attn.attn_fwd(q, k, v, causal=False)
+            fl = 4.0 * d * B * H * L * L
+            entry = {}
+            for cs in (0, 2, 4, 8):
+                attn.set_cluster_merge(cs)
+                t = timed(lambda: attn.attn_fwd(q, k, v, causal=False, out=o, lse=lse, stream=stream))
+                entry["combine_pass" if cs == 0 else f"cluster_{cs}"] = {"ms": t, "tflops": fl / (t / 1e3) / 1e12}
+            out[f"B{B} H{H} L{L} d{d} non-causal"] = entry
+    finally:
+        attn.set_cluster_merge(0)
+    return out
+
+
 def rope_fused_leg(attn, device, stream, peaks, iters: int = 30):
     """The forward of rotary-embedded q and k (training page §4), three ways,
     median CUDA-event times with L2 flushed before each call: attn_fwd_rope
@@ -805,6 +848,7 @@ def run_ours(args, wl):
                               "rotary": rotary_leg(attn, device, stream, peaks),
                               "decode": decode_leg(attn, device, stream, peaks),
                               "rope_fused": rope_fused_leg(attn, device, stream, peaks),
+                              "cluster_merge": cluster_merge_leg(attn, device, stream, peaks),
                               "backward": bwd_leg(attn, device, stream, peaks)}), flush=True)
         return 0
 
@@ -945,7 +989,7 @@ def run_ours(args, wl):
         raise RuntimeError(f"device error in the e2e leg: {attn.last_device_error():#x}")
 
     # ---- padded batches: unpad index and row gather / scatter (HBM-bound)
-    pad = cache = rot = bwd = dec = rope = None
+    pad = cache = rot = bwd = dec = rope = cmerge = None
     if not args.no_pad_leg:
         pad = pad_leg(attn, device, stream, peaks)
         cache = cache_leg(attn, device, stream, peaks)
@@ -953,6 +997,7 @@ def run_ours(args, wl):
         bwd = bwd_leg(attn, device, stream, peaks)
         rot = rotary_leg(attn, device, stream, peaks)
         rope = rope_fused_leg(attn, device, stream, peaks)
+        cmerge = cluster_merge_leg(attn, device, stream, peaks)
 
     # ---- the five configurations, and the headline on the CTA-pair kernel
     cfgs = pair = kept = None
@@ -988,7 +1033,7 @@ def run_ours(args, wl):
                         "per_rank_events": "one CUDA-event pair per step on the launching stream"},
             "clocks": clocks, "e2e": e2e, "gpu_launches": launches, "roofline": roofline,
             "cpu_baseline": cpu, "configs": cfgs, "pair_kernel_headline": pair,
-            "pad_unpad": pad, "kv_cache": cache, "rotary": rot, "backward": bwd, "decode": dec, "rope_fused": rope,
+            "pad_unpad": pad, "kv_cache": cache, "rotary": rot, "backward": bwd, "decode": dec, "rope_fused": rope, "cluster_merge": cmerge,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:

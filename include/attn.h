@@ -388,6 +388,23 @@ void attn_set_pair_forward(int enable);
 int attn_pair_forward_used(int d, int varlen);
 
 /*
+ * attn_set_cluster_merge -- how dense forwards on the single-CTA kernel merge
+ * split key ranges (the r = exp(m_s - M) rescaling of page S23-J17 §3.1,
+ * applied across pieces).  0 (the default): the host plans
+ * pieces of any length where they balance the load, the pieces write fp32
+ * partials to a workspace and a separate combine pass merges them.  2, 4 or
+ * 8: every 256-row query block is split into that many pieces of equal key
+ * ranges, the pieces of a block run as one thread-block cluster, keep their
+ * partials in shared memory and merge them over distributed shared memory
+ * inside the kernel (no workspace, no combine pass).  Both compute the same
+ * function; the second suits shapes whose blocks all have the same key range
+ * (non-causal).  Other values are ignored.  attn_cluster_merge() returns the
+ * setting.  Process-wide; not synchronised with calls in flight.
+ */
+void attn_set_cluster_merge(int cluster_size);
+int attn_cluster_merge(void);
+
+/*
  * attn_fwd_rope -- attn_fwd of rotary-embedded queries and keys (training
  * page §4: the rotary module, rotary dimension, base frequency, GPT-NeoX or
  * GPT-J pairing, a position offset for queries that extend a cache):

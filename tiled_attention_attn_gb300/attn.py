@@ -110,6 +110,10 @@ def lib(path: Optional[str] = None):
         L.attn_decode.restype = i
         L.attn_set_pair_forward.argtypes = [i]
         L.attn_set_pair_forward.restype = None
+        L.attn_set_cluster_merge.argtypes = [i]
+        L.attn_set_cluster_merge.restype = None
+        L.attn_cluster_merge.argtypes = []
+        L.attn_cluster_merge.restype = i
         L.attn_fwd_rope.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, f, i, i, i, vp]
         L.attn_fwd_rope.restype = i
         L.attn_set_decode_path.argtypes = [i]
@@ -699,6 +703,18 @@ def set_pair_forward(enable: bool) -> None:
     """Dense head_dim-128 forwards on CTA pairs (True) or on the single-CTA
     kernel (False, the default)."""
     lib().attn_set_pair_forward(int(bool(enable)))
+
+
+def set_cluster_merge(cluster_size: int) -> None:
+    """attn_set_cluster_merge: 0 merges split key ranges in a combine pass,
+    2, 4 or 8 splits every query block into that many pieces that run as one
+    cluster and merge over distributed shared memory."""
+    lib().attn_set_cluster_merge(int(cluster_size))
+
+
+def cluster_merge() -> int:
+    """attn_cluster_merge: the current setting."""
+    return int(lib().attn_cluster_merge())
 
 
 def pair_forward_used(d: int, varlen: bool) -> bool:

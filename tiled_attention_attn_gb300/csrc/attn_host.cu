@@ -33,6 +33,7 @@ namespace {
 std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
 std::atomic<unsigned long long> g_launches{0};
 std::atomic<int> g_pair_forward{0};   // attn_set_pair_forward
+std::atomic<int> g_cluster_merge{0};  // attn_set_cluster_merge: 0, 2, 4 or 8
 std::atomic<int> g_decode_tc{1};      // attn_set_decode_path
 unsigned long long* g_trace = nullptr;   // attn_trace_enable (traced build only)
 int g_trace_cap = 0;
@@ -132,6 +133,7 @@ struct DevState {
   std::map<MapKey, CUtensorMap> maps;
   LruCache<PlanKey, DevPlan> plans{kMaxPlans};        // single-CTA kernel schedules
   LruCache<PlanKey, DevPlan> pair_plans{kMaxPlans};   // CTA-pair kernel schedules
+  LruCache<PlanKey, DevPlan> cluster_plans{kMaxPlans};   // in-cluster merge schedules (causal + 2 * cluster size)
   Workspace part;        // single-CTA split pieces: O_s then (m, l)
   Workspace pair_part;   // CTA-pair split pieces: u then (m, l)
   Workspace pair_cnt;    // CTA-pair merge counters (epoch-tagged words, zeroed when allocated)
@@ -511,7 +513,28 @@ int fwd(bool bf16, const void* q, const void* k, const void* v, void* o, float* 
   }
   int grid = 0;
   DevPlan* plan = nullptr;
-  if (!varlen) {
+  const int cs = (!varlen && !rope) ? g_cluster_merge.load() : 0;
+  if (cs > 0) {
+    // in-cluster merge: equal pieces, one per CTA of a cluster of cs
+    const PlanKey key{B, Hq, Hkv, Lq, Lk, d, causal + 2 * cs};
+    auto fits = [](const Plan& h) {
+      return static_cast<int>(h.units.size()) <= kInlineUnits && h.n_ctas <= kInlineCtas;
+    };
+    rc = get_plan(
+        st.cluster_plans, key, stream,
+        [&](Plan& h) { return make_plan_cluster(B, Hq, Hkv, Lq, Lk, causal != 0, cs, h); }, fits, plan);
+    if (rc) return rc;
+    if (fits(plan->host)) {
+      p.n_inline = 1;
+      std::memcpy(p.units_inline, plan->flat.data(), plan->host.units.size() * kUnitInts * sizeof(int));
+      std::memcpy(p.cta_off_inline, plan->host.cta_off.data(), plan->host.cta_off.size() * sizeof(int));
+    } else {
+      p.units = plan->units();
+      p.cta_off = plan->cta_off();
+    }
+    p.cluster_merge = cs;
+    grid = plan->host.n_ctas;
+  } else if (!varlen) {
     const PlanKey key{B, Hq, Hkv, Lq, Lk, d, causal};
     // the combine pass reads the split groups from the device copy
     auto fits = [](const Plan& h) {
@@ -923,6 +946,12 @@ int attn_profile_read(float* main_ms, float* call_ms, int max, int* n) {
 }
 
 void attn_set_pair_forward(int enable) { attn::g_pair_forward.store(enable ? 1 : 0); }
+
+void attn_set_cluster_merge(int cluster_size) {
+  if (cluster_size == 0 || cluster_size == 2 || cluster_size == 4 || cluster_size == 8)
+    attn::g_cluster_merge.store(cluster_size);
+}
+int attn_cluster_merge(void) { return attn::g_cluster_merge.load(); }
 
 int attn_fwd_rope(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv, int Lq,
                   int Lk, int d, int causal, float scale, int rot_dim, float base, int interleaved, int q_offset,

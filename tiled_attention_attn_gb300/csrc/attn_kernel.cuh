@@ -46,7 +46,7 @@ struct Cfg {
   static constexpr int kOffBar = kOffV + kNS * kTile;
   // barriers: q_full, q_empty, kv_full[NS], kv_empty[NS], s_full[2], p_full[2],
   //           o_done[2], drain, q_rot
-  static constexpr int kNBars = 2 + 2 * kNS + 8;   // + q_rot (rotary variant)
+  static constexpr int kNBars = 2 + 2 * kNS + 10;   // + q_rot (rotary variant), in-cluster merge ready / done
   static constexpr int kOffMisc = kOffBar + kNBars * 8;   // tmem slot, abort flag, bad flag
   static constexpr int kOffVarlen = kOffMisc + 64;        // varlen unit prefix table
   static constexpr int kSmemDense = kOffVarlen + 1024;    // + alignment slack
@@ -501,6 +501,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   auto b_o_done = [&](int t) { return bar_sp + 32 + 8 * t; };
   const uint32_t b_drain = bar_sp + 48;
   const uint32_t b_q_rot = bar_sp + 56;   // rotary variant: the unit's Q rotated in place
+  // in-cluster merge: every softmax warp of every CTA of the cluster has
+  // staged its rows (ready) / has finished reading the peers (done)
+  const uint32_t b_cready = bar_sp + 64;
+  const uint32_t b_cdone = bar_sp + 72;
 
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
@@ -534,6 +538,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     }
     mbar_init(b_drain, 1);
     mbar_init(b_q_rot, 2 * kBM / 32);   // one arrival per softmax warp
+    mbar_init(b_cready, (2 * kBM / 32) * max(p.cluster_merge, 1));
+    mbar_init(b_cdone, (2 * kBM / 32) * max(p.cluster_merge, 1));
     fence_mbar_init();
     tma_prefetch_desc(&p.tm_q);
     tma_prefetch_desc(&p.tm_k);
@@ -612,6 +618,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // in-cluster merge: the peers' barriers are initialised before any remote
+  // arrival (CTAs of a cluster are co-scheduled, so this wait ends)
+  if (!VARLEN && p.cluster_merge > 0) cluster_sync();
   const uint32_t tmem = *tmem_slot;
   // the combine pass of split pieces may be scheduled now; it waits for this grid
   grid_launch_dependents();
@@ -985,32 +994,136 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         // large- or small-magnitude values that the unsplit path handles).
         // Layout [slot][t][D/4][row][4]: a warp's 32 rows of one 4-column
         // group are 512 contiguous bytes.
-        const size_t pbase = (static_cast<size_t>(U.slot) * kNSub + t) * (D / 4);
-        float4* po = reinterpret_cast<float4*>(p.part_o);
-        if (n_act > 0) {
-          const float inv_l = 1.0f / st.l;
+        if (!VARLEN && p.cluster_merge > 0) {
+          // in-cluster merge: O_s and (m, l) of this row stay in this CTA's
+          // shared memory, over the unit's K/V ring and Q block; layout
+          // [t][D/4][row][4].  They are free once the unit's last MMA has
+          // completed (the q_empty commit; one unit per CTA, so the loads
+          // are all consumed too) - the other sub-tile's MMAs may still be
+          // reading them when this sub-tile's o_done arrives.
+          const bool idle = (U.kv_end <= U.kv_begin) ||   // an empty piece issued nothing
+                            mbar_wait_warp(b_q_empty, 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteMerge));
+          tc_fence_after();
+          if (idle) {
+            float4* so = reinterpret_cast<float4*>(smem + C::kOffK);
+            float2* sml = reinterpret_cast<float2*>(smem + C::kOffQ);
+            const float inv_l = (n_act > 0) ? 1.0f / st.l : 0.0f;
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld_32x32b_x32(t_o + c * 32, o);
-            tmem_wait_ld(o);
-            if (row_valid) {
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              if (n_act > 0) {
+                tmem_ld_32x32b_x32(t_o + c * 32, o);
+                tmem_wait_ld(o);
+              } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] = 0u;
+              }
 #pragma unroll
               for (int i = 0; i < 8; ++i)
-                po[(pbase + c * 8 + i) * kBM + row] =
+                so[(t * (D / 4) + c * 8 + i) * kBM + row] =
                     make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
                                 __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
             }
+            sml[t * kBM + row] = make_float2(n_act > 0 ? st.m : -INFINITY, n_act > 0 ? st.l : 0.0f);
+            fence_acq_rel_cluster();
+            __syncwarp();
+            if (lane == 0)
+              for (int r = 0; r < p.cluster_merge; ++r) mbar_arrive_remote_release(mapa_shared(b_cready, r));
           }
-        }
-        if (row_valid) {
-          const size_t prow = (static_cast<size_t>(U.slot) * kNSub + t) * kBM + row;
-          float2* pml = reinterpret_cast<float2*>(p.part_ml) + prow;
-          *pml = make_float2(n_act > 0 ? st.m : -INFINITY, n_act > 0 ? st.l : 0.0f);
+        } else {
+          const size_t pbase = (static_cast<size_t>(U.slot) * kNSub + t) * (D / 4);
+          float4* po = reinterpret_cast<float4*>(p.part_o);
+          if (n_act > 0) {
+            const float inv_l = 1.0f / st.l;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t o[32];
+              tmem_ld_32x32b_x32(t_o + c * 32, o);
+              tmem_wait_ld(o);
+              if (row_valid) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                  po[(pbase + c * 8 + i) * kBM + row] =
+                      make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
+                                  __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
+              }
+            }
+          }
+          if (row_valid) {
+            const size_t prow = (static_cast<size_t>(U.slot) * kNSub + t) * kBM + row;
+            float2* pml = reinterpret_cast<float2*>(p.part_ml) + prow;
+            *pml = make_float2(n_act > 0 ? st.m : -INFINITY, n_act > 0 ? st.l : 0.0f);
+          }
         }
       }
       tr.rec(kTagEpiDone, t, u, 0);
       tc_fence_before();
+    }
+    if constexpr (!VARLEN) {
+      if (p.cluster_merge > 0 && u_first < n_units) {
+        // In-cluster merge: once all cluster_merge pieces of the block are
+        // staged, cluster rank s merges rows [256 s / n, 256 (s + 1) / n) of
+        // the block, reading every piece's O_s and (m, l) from its CTA's
+        // shared memory (the combine pass's arithmetic: M = max m_s, w_s =
+        // 2^(m_s - M) l_s, O = sum w_s O_s / sum w_s, lse = M ln 2 + ln sum
+        // w_s); then every warp tells every peer that it has finished
+        // reading, and no CTA leaves before all have.
+        const int n = p.cluster_merge;
+        const uint32_t rank = cluster_ctarank();
+        Unit U;
+        decode_unit<CAUSAL, VARLEN>(p, vl_pref, u_first, U);
+        const bool ready = mbar_wait_acq_cluster(b_cready, 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteMerge));
+        if (ready) {
+          const uint32_t so0 = smem_u32(smem + C::kOffK), sml0 = smem_u32(smem + C::kOffQ);
+          const int r0 = static_cast<int>(rank) * kBlockRows / n, r1 = (static_cast<int>(rank) + 1) * kBlockRows / n;
+          const int R = r1 - r0;
+          for (int idx = warp * 32 + lane; idx < R * (D / 16); idx += 2 * kBM) {
+            const int rr = r0 + idx % R, cb = idx / R;
+            const int qr = U.q_row0 + rr;
+            if (qr >= p.Lq) continue;
+            const int tt = rr / kBM, rw = rr % kBM;
+            float M = -INFINITY, L = 0.0f;
+            float acc[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+            for (int sp = 0; sp < n; ++sp) {
+              const float2 ml = ld_dsmem_f2(mapa_shared(sml0 + (tt * kBM + rw) * 8, sp));
+              float4 x[4];
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+                x[c] = ld_dsmem_f4(mapa_shared(so0 + ((tt * (D / 4) + cb * 4 + c) * kBM + rw) * 16, sp));
+              if (ml.x == -INFINITY) continue;   // a piece that saw no key
+              const float mn = fmaxf(M, ml.x);
+              const float r = (M == -INFINITY) ? 0.0f : ex2_approx(M - mn);
+              const float w = ex2_approx(ml.x - mn) * ml.y;
+              M = mn;
+              L = L * r + w;
+#pragma unroll
+              for (int c = 0; c < 4; ++c) {
+                acc[4 * c] = acc[4 * c] * r + w * x[c].x;
+                acc[4 * c + 1] = acc[4 * c + 1] * r + w * x[c].y;
+                acc[4 * c + 2] = acc[4 * c + 2] * r + w * x[c].z;
+                acc[4 * c + 3] = acc[4 * c + 3] * r + w * x[c].w;
+              }
+            }
+            const float inv = (L > 0.0f) ? 1.0f / L : 0.0f;
+            uint4* d4 = reinterpret_cast<uint4*>(out + ((static_cast<size_t>(U.b) * p.Lq + qr) * p.Hq + U.h) * D + cb * 16);
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+              d4[i] = make_uint4(pack2<BF16>(acc[8 * i] * inv, acc[8 * i + 1] * inv),
+                                 pack2<BF16>(acc[8 * i + 2] * inv, acc[8 * i + 3] * inv),
+                                 pack2<BF16>(acc[8 * i + 4] * inv, acc[8 * i + 5] * inv),
+                                 pack2<BF16>(acc[8 * i + 6] * inv, acc[8 * i + 7] * inv));
+            if (cb == 0)
+              p.lse[(static_cast<size_t>(U.b) * p.Hq + U.h) * p.Lq + qr] =
+                  (L > 0.0f) ? M * 0.69314718055994531f + __logf(L) : -INFINITY;
+          }
+        }
+        __syncwarp();
+        if (lane == 0)
+          for (int r = 0; r < n; ++r) mbar_arrive_remote_release(mapa_shared(b_cdone, r));
+        mbar_wait_acq_cluster(b_cdone, 0, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteMerge));
+      }
     }
   }
 

@@ -63,6 +63,11 @@ struct FwdParams {
   const int* cta_off;          // dense: first unit of every CTA, n_ctas + 1 entries
   void* part_o;                // split-KV partial outputs O_s = u_s / l_s, fp32 [slot][2][D/4][128][4]
   float* part_ml;              // split-KV partial (m, l) [slot][2][128][2]
+  // In-cluster merge (dense): a cluster of cluster_merge CTAs holds the
+  // cluster_merge pieces of one query block, piece s on cluster rank s, one
+  // unit per CTA; the pieces' partials stay in shared memory and are merged
+  // over distributed shared memory (no workspace, no combine pass).  0: off.
+  int cluster_merge;
   int* err;                    // device error word
   unsigned long long* trace;   // optional phase trace (traced build, attn_trace_enable), else null
   int trace_cap;               // events per stream per CTA

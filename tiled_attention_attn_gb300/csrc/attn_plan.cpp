@@ -335,4 +335,35 @@ bool make_plan_pair(int B, int Hq, int Hkv, int Lq, int Lk, bool causal, int num
   return true;
 }
 
+bool make_plan_cluster(int B, int Hq, int Hkv, int Lq, int Lk, bool causal, int cs, Plan& out) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Lq <= 0 || Lk < 0) return false;
+  if (cs != 2 && cs != 4 && cs != 8) return false;
+  const int group = Hq / Hkv;
+  const int n_mb = (Lq + kBlockRows - 1) / kBlockRows;
+  const long long n_ctas = static_cast<long long>(B) * Hq * n_mb * cs;
+  if (n_ctas > (1LL << 24)) return false;
+  out = Plan();
+  out.units.reserve(static_cast<size_t>(n_ctas));
+  int c = 0;
+  for (int b = 0; b < B; ++b)
+    for (int g = 0; g < Hkv; ++g)
+      for (int mb = 0; mb < n_mb; ++mb)
+        for (int hh = 0; hh < group; ++hh) {
+          const int kl0 = kv_last_tile(mb * kBlockRows, 0, Lq, Lk, causal);
+          const int kl1 = kv_last_tile(mb * kBlockRows, 1, Lq, Lk, causal);
+          const int T = std::max(kl0, kl1) + 1;
+          for (int s = 0; s < cs; ++s, ++c) {
+            const int a = static_cast<int>(static_cast<long>(s) * T / cs);
+            const int e = static_cast<int>(static_cast<long>(s + 1) * T / cs);
+            out.units.push_back({b * Hq + g * group + hh, mb, a, e, s, cs, -1, c});
+            out.cta_off.push_back(c);
+            out.makespan = std::max(out.makespan, static_cast<double>(e - a));
+          }
+        }
+  out.cta_off.push_back(c);
+  out.n_ctas = c;
+  out.n_partials = 0;
+  return true;
+}
+
 }  // namespace attn

@@ -40,4 +40,10 @@ bool make_plan(int B, int Hq, int Hkv, int Lq, int Lk, int d, bool causal, int n
 // pair).  Split pieces of one block share a group; the kernel merges them.
 bool make_plan_pair(int B, int Hq, int Hkv, int Lq, int Lk, bool causal, int num_pairs, Plan& out);
 
+// The schedule of the in-cluster merge: every 256-row query block split
+// into `cs` key-range pieces of equal tile counts (a block with fewer tiles
+// than cs has empty pieces), piece s of block g on CTA g * cs + s, one unit
+// per CTA; no workspace slots and no combine groups.
+bool make_plan_cluster(int B, int Hq, int Hkv, int Lq, int Lk, bool causal, int cs, Plan& out);
+
 }  // namespace attn

@@ -288,6 +288,44 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
   return false;
 }
 
+// Arrival on an mbarrier of any CTA of the cluster (`cbar` a shared::cluster
+// address) that releases this thread's earlier memory operations at cluster
+// scope: a peer that acquires the barrier's phase sees them.
+__device__ __forceinline__ void mbar_arrive_remote_release(uint32_t cbar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" :: "r"(cbar) : "memory");
+}
+// Bounded wait on this CTA's mbarrier with acquire at cluster scope (the
+// arrivals came from peer CTAs, see mbar_arrive_remote_release).
+__device__ __forceinline__ bool mbar_wait_acq_cluster(uint32_t bar, uint32_t parity, const WaitCtl& w, int code) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 0;; ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    if (ok) return true;
+    if ((it & 63u) == 63u && global_timer_ns() - t0 > w.timeout_ns) {
+      report_error(w, code);
+      return false;
+    }
+  }
+}
+// Loads from the shared memory of a CTA of the cluster (shared::cluster address).
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ float2 ld_dsmem_f2(uint32_t a) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+
 // 4-D tiled load into this CTA's shared memory whose completion (bytes) is
 // signalled on an mbarrier of either CTA of the pair (`cbar` is a
 // shared::cluster address): the peer CTA's loads report to the leader.
