@@ -98,3 +98,14 @@ def test_cross_needs_both_offsets_and_matching_counts():
         attn.attn_fwd(q, q, q, cu_seqlens_k=cu)
     with pytest.raises(ValueError):
         attn.attn_fwd(q, q, q, cu_seqlens=cu, cu_seqlens_k=torch.tensor([0, 5, 10], dtype=torch.int32, device=dev))
+
+
+def test_cross_varlen_maximum_sequence_count():
+    # 4096 sequences (the most one call takes): the kernel's prefix table of
+    # units per sequence is full; short sequences, some empty on either side.
+    # fp16: with a handful of keys per row O is not averaged down, and bf16's
+    # rounding of P and O alone can pass 1e-2 where |O| approaches 4
+    rng = np.random.default_rng(4096)
+    lq = rng.integers(0, 9, 4096).tolist()
+    lk = [a + int(c) for a, c in zip(lq, rng.integers(0, 6, 4096))]
+    run_case(lq, lk, 4, 2, 64, True, torch.float16, seed=4096)

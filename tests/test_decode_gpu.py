@@ -128,3 +128,18 @@ def test_decode_unsupported_group_raises():
     k = torch.randn(10, 2, 64, device=dev, dtype=torch.bfloat16)
     with pytest.raises(attn.AttnError):
         attn.attn_decode(q, k, k, torch.tensor([0, 10], dtype=torch.int32, device=dev))
+
+
+def test_decode_maximum_sequence_count(path):
+    # 4096 sequences, one new query each, caches of 1 to 40 keys (fp16: with
+    # so few keys per row O is not averaged down, and bf16's rounding of P
+    # and O alone can pass 1e-2 where |O| approaches 4)
+    rng = np.random.default_rng(7)
+    lk = rng.integers(1, 41, 4096).tolist()
+    q, k, v = make(lk, 8, 2, 128, torch.float16, seed=7)
+    dev = torch.device("cuda", 0)
+    scale = 128 ** -0.5
+    o, lse = attn.attn_decode(q.to(dev), k.to(dev), v.to(dev), cu_of(lk).to(dev), scale=scale)
+    assert attn.get_error() == attn.ATTN_OK
+    o_ref, lse_ref = oracle.varlen_cross_attention(q, k, v, [1] * len(lk), lk, causal=False, scale=scale)
+    check(o, lse, o_ref, lse_ref)
