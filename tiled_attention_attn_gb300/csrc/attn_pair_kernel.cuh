@@ -185,7 +185,7 @@ __device__ __forceinline__ bool group_wait(const unsigned long long* c, unsigned
 __device__ __forceinline__ bool warp_handshake(uint32_t bar, uint32_t& cnt, const WaitCtl& wc) {
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-  const bool ok = mbar_wait_lane0(bar, cnt & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteXchg));
+  const bool ok = mbar_wait_warp(bar, cnt & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteXchg));
   ++cnt;
   return ok;
 }
@@ -611,7 +611,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) attn_pair_kernel(const __grid
       float m = -INFINITY, l = 0.0f;
       bool ok = true;
       for (int j = U.kv_begin; j < U.kv_end; ++j) {
-        if (!mbar_wait_lane0(b_s_full, s_cnt & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteSFull))) { ok = false; break; }
+        if (!mbar_wait_warp(b_s_full, s_cnt & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteSFull))) { ok = false; break; }
         tr.rec(kTagSFull, half, u, j);
         ++s_cnt;
         tc_fence_after();
@@ -638,7 +638,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) attn_pair_kernel(const __grid
         if (!first) {
           // the previous tile's P.V has read P and updated u
           tr.rec(kTagPvWait, half, u, j);
-          if (!mbar_wait_lane0(b_pv_done, pv_cnt & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSitePvDone))) {
+          if (!mbar_wait_warp(b_pv_done, pv_cnt & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSitePvDone))) {
             ok = false;
             break;
           }
@@ -679,7 +679,7 @@ __global__ void __launch_bounds__(kPairThreads, 1) attn_pair_kernel(const __grid
       }
       if (!ok) break;
       // the unit's last P.V
-      if (!mbar_wait_lane0(b_pv_done, pv_cnt & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSitePvDone))) break;
+      if (!mbar_wait_warp(b_pv_done, pv_cnt & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSitePvDone))) break;
       tr.rec(kTagODone, half, u, 0);
       ++pv_cnt;
       tc_fence_after();
