@@ -16,6 +16,12 @@
 // the A operand in its natural (keys x d) layout, read MN-major; P^T is
 // written by the softmax threads into shared memory as the K-major B operand.
 //
+// Head dimension DA = 128 or 64.  The shared-memory tiles keep the 128-column
+// layout for both: with DA = 64 the TMA fills only the first 64-column chunk
+// of each Q, K and V tile and the second stays zero (written once), so S^T
+// takes only the first half of its K dimension and u^T's rows d >= 64 are
+// zero and never stored; the bytes streamed are the 64-column rows.
+//
 // Work units are (sequence, key/value head, piece of the cache), the same
 // schedule as the packed forward's decode mode, run round-robin over the
 // CTAs; a cut cache's pieces leave fp32 partials that the decode combine
@@ -42,7 +48,7 @@ constexpr int kThreads = 192;
 constexpr int kWarpTMA = 0;
 constexpr int kWarpMMA = 1;
 constexpr int kKeys = 128;   // keys per tile
-constexpr int kD = 128;      // head dimension
+constexpr int kD = 128;      // head dimension of the shared-memory tiles (the largest DA)
 
 template <int NQ>
 struct Cfg {
@@ -157,7 +163,7 @@ __host__ __device__ constexpr uint32_t idesc_a_mn(int M, int N, bool bf16) {
   return idesc_f16_f32acc(M, N, bf16, false) | (1u << 15);
 }
 
-template <int NQ, int GT, bool BF16>
+template <int NQ, int GT, bool BF16, int DA>
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_constant__ Params p) {
   static_assert(GT >= 1 && GT <= NQ, "query heads per key/value head");
   using C = Cfg<NQ>;
@@ -214,6 +220,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     tma_prefetch_desc(&p.tm_k);
     tma_prefetch_desc(&p.tm_v);
   }
+  if constexpr (DA < kD) {
+    // the second 64-column chunk of every K and V stage and of both Q slots
+    // stays zero: the MMAs that read it see zeros, the TMA never writes it
+    if (warp >= 3) {
+      const int t3 = tid - 3 * 32;   // 0 .. 95
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      for (int s = 0; s < C::kStages; ++s)
+        for (int i = t3; i < 16384 / 16; i += 3 * 32) {
+          reinterpret_cast<uint4*>(smem + C::kOffK + s * C::kTile + 16384)[i] = z;
+          reinterpret_cast<uint4*>(smem + C::kOffV + s * C::kTile + 16384)[i] = z;
+        }
+      for (int qs = 0; qs < 2; ++qs)
+        for (int i = t3; i < C::kQChunk / 16; i += 3 * 32)
+          reinterpret_cast<uint4*>(smem + C::kOffQ + qs * C::kQ + C::kQChunk)[i] = z;
+      fence_proxy_async_smem();   // before the MMAs (async proxy) read them
+    }
+  }
   if (warp == 2) {
     // validate cu_seqlens_k and build the unit prefix: sequence b has
     // Hkv x pieces(b) units
@@ -258,9 +281,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     T* out = reinterpret_cast<T*>(p.o);
     for (long long r = static_cast<long long>(blockIdx.x) * kThreads + tid; r < static_cast<long long>(p.B) * p.Hq;
          r += static_cast<long long>(gridDim.x) * kThreads) {
-      uint4* d4 = reinterpret_cast<uint4*>(out + r * kD);
+      uint4* d4 = reinterpret_cast<uint4*>(out + r * DA);
 #pragma unroll
-      for (int i = 0; i < kD / 8; ++i) d4[i] = make_uint4(0, 0, 0, 0);
+      for (int i = 0; i < DA / 8; ++i) d4[i] = make_uint4(0, 0, 0, 0);
       const long long b = r / p.Hq, h = r - b * p.Hq;
       p.lse[h * p.B + b] = -INFINITY;
     }
@@ -277,16 +300,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         if (U.t1 <= U.t0) continue;
         const int qs = q_cnt & 1;
         if (!mbar_wait(b_q_empty(qs), ((q_cnt >> 1) & 1) ^ 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteQEmpty))) break;
-        mbar_arrive_expect_tx(b_q_full(qs), 2 * p.G * 128);
-        for (int c = 0; c < 2; ++c)
+        mbar_arrive_expect_tx(b_q_full(qs), (DA / 64) * p.G * 128);
+        for (int c = 0; c < DA / 64; ++c)
           tma_load_4d(sQ + qs * C::kQ + c * C::kQChunk, &p.tm_q, b_q_full(qs), c * 64, U.g * p.G, U.b, 0);
         ++q_cnt;
         for (int t = U.t0; t < U.t1; ++t) {
           const int st = kv_cnt % C::kStages;
           if (!mbar_wait(b_kv_empty(st), ((kv_cnt / C::kStages) & 1) ^ 1, wc,
                          ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKEmpty))) { ok = false; break; }
-          mbar_arrive_expect_tx(b_kv_full(st), 2 * C::kTile);
-          for (int c = 0; c < 2; ++c) {
+          mbar_arrive_expect_tx(b_kv_full(st), 2 * C::kTile * DA / kD);
+          for (int c = 0; c < DA / 64; ++c) {
             tma_load_4d(sK + st * C::kTile + c * 16384, &p.tm_k, b_kv_full(st), c * 64, U.g, U.row_k + t * kKeys, 0);
             tma_load_4d(sV + st * C::kTile + c * 16384, &p.tm_v, b_kv_full(st), c * 64, U.g, U.row_k + t * kKeys, 0);
           }
@@ -368,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
           // back) were consumed, since this thread has waited for that tile's P
           const int sb = s_cnt & 1;
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) {
+          for (int kk = 0; kk < DA / 16; ++kk) {
             const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
             const uint32_t offq = ((qs * C::kQ + (kk >> 2) * C::kQChunk + (kk & 3) * 32) >> 4);
             umma_ss(tmem + sb * NQ, dk0 + ((st * C::kTile) >> 4) + off, dq0 + offq, kIdescS, kk > 0 ? 1u : 0u);
@@ -465,7 +488,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       if (U.t1 <= U.t0) {
         // a sequence without keys: O = 0, lse = -inf
         T* dst = reinterpret_cast<T*>(p.o);
-        for (int h = 0; h < G; ++h) dst[(orow0 + h) * kD + lrow] = T(0.0f);
+        if (lrow < DA)
+          for (int h = 0; h < G; ++h) dst[(orow0 + h) * DA + lrow] = T(0.0f);
         if (sw == 0 && lane < G) p.lse[static_cast<size_t>(U.g * G + lane) * p.B + U.b] = -INFINITY;
         continue;
       }
@@ -551,8 +575,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         T* dst = reinterpret_cast<T*>(p.o);
 #pragma unroll
         for (int h = 0; h < NQ; ++h) {
-          if (h >= G) break;
-          dst[(orow0 + h) * kD + lrow] = T((l[h] > 0.0f) ? o[h] / l[h] : 0.0f);
+          if (h >= G || lrow >= DA) break;
+          dst[(orow0 + h) * DA + lrow] = T((l[h] > 0.0f) ? o[h] / l[h] : 0.0f);
         }
         if (sw == 0 && lane < G) {
           float lv = 0.0f, mv = 0.0f;
@@ -568,10 +592,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       } else {
         // a piece: O_s = u^T / l in fp32 and (m, l), rows = heads of the group
         float* po = reinterpret_cast<float*>(p.part_o);
-        const size_t pbase = static_cast<size_t>(U.slot) * kNSub * (kD / 4);
+        const size_t pbase = static_cast<size_t>(U.slot) * kNSub * (DA / 4);
 #pragma unroll
         for (int h = 0; h < NQ; ++h) {
-          if (h >= G) break;
+          if (h >= G || lrow >= DA) break;
           po[((pbase + (lrow >> 2)) * kBM + h) * 4 + (lrow & 3)] = (l[h] > 0.0f) ? o[h] / l[h] : 0.0f;
         }
         if (sw == 0 && lane < G) {
@@ -597,19 +621,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   }
 }
 
-template <int NQ, int GT, bool BF16>
+template <int NQ, int GT, bool BF16, int DA>
 cudaError_t launch(const Params& p, int grid, cudaStream_t stream) {
   constexpr int smem = Cfg<NQ>::kSmem;
-  static bool attr_done[64] = {};
+  static bool attr_done[64] = {};   // per instantiation
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-    e = cudaFuncSetAttribute(decode_tc_kernel<NQ, GT, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    e = cudaFuncSetAttribute(decode_tc_kernel<NQ, GT, BF16, DA>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) attr_done[dev] = true;
   }
-  decode_tc_kernel<NQ, GT, BF16><<<grid, kThreads, smem, stream>>>(p);
+  decode_tc_kernel<NQ, GT, BF16, DA><<<grid, kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -618,7 +642,7 @@ cudaError_t launch(const Params& p, int grid, cudaStream_t stream) {
 cudaError_t launch_decode_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v, void* o,
                              float* lse, const int* cu_k, int* pref_out, void* part_o, float* part_ml, int* err,
                              unsigned long long timeout_ns, int B, int Hq, int Hkv, int total_k, int split,
-                             float scale_log2, bool bf16, int grid, cudaStream_t stream) {
+                             float scale_log2, bool bf16, int d, int grid, cudaStream_t stream) {
   dtc::Params p;
   p.tm_q = tm_q;
   p.tm_k = tm_k;
@@ -639,11 +663,21 @@ cudaError_t launch_decode_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_k, c
   p.split = split;
   p.scale_log2 = scale_log2;
   // the query heads per key/value head that attn_decode accepts: 1, 2, 4, 8
+  if (d == 64) {
+    switch (p.G) {
+      case 1: return bf16 ? dtc::launch<16, 1, true, 64>(p, grid, stream) : dtc::launch<16, 1, false, 64>(p, grid, stream);
+      case 2: return bf16 ? dtc::launch<16, 2, true, 64>(p, grid, stream) : dtc::launch<16, 2, false, 64>(p, grid, stream);
+      case 4: return bf16 ? dtc::launch<16, 4, true, 64>(p, grid, stream) : dtc::launch<16, 4, false, 64>(p, grid, stream);
+      case 8: return bf16 ? dtc::launch<16, 8, true, 64>(p, grid, stream) : dtc::launch<16, 8, false, 64>(p, grid, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  if (d != 128) return cudaErrorInvalidValue;
   switch (p.G) {
-    case 1: return bf16 ? dtc::launch<16, 1, true>(p, grid, stream) : dtc::launch<16, 1, false>(p, grid, stream);
-    case 2: return bf16 ? dtc::launch<16, 2, true>(p, grid, stream) : dtc::launch<16, 2, false>(p, grid, stream);
-    case 4: return bf16 ? dtc::launch<16, 4, true>(p, grid, stream) : dtc::launch<16, 4, false>(p, grid, stream);
-    case 8: return bf16 ? dtc::launch<16, 8, true>(p, grid, stream) : dtc::launch<16, 8, false>(p, grid, stream);
+    case 1: return bf16 ? dtc::launch<16, 1, true, 128>(p, grid, stream) : dtc::launch<16, 1, false, 128>(p, grid, stream);
+    case 2: return bf16 ? dtc::launch<16, 2, true, 128>(p, grid, stream) : dtc::launch<16, 2, false, 128>(p, grid, stream);
+    case 4: return bf16 ? dtc::launch<16, 4, true, 128>(p, grid, stream) : dtc::launch<16, 4, false, 128>(p, grid, stream);
+    case 8: return bf16 ? dtc::launch<16, 8, true, 128>(p, grid, stream) : dtc::launch<16, 8, false, 128>(p, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -637,9 +637,9 @@ int fwd_decode(bool bf16, const void* q, const void* k, const void* v, void* o, 
 
   static thread_local FwdParams p;
   std::memset(&p, 0, sizeof(p));
-  // head_dim 128 runs the transposed decode kernel (keys on the MMA's M
-  // dimension); head_dim 64 the packed forward in decode mode
-  const bool transposed = (d == 128);
+  // head_dim 64 and 128 run the transposed decode kernel (keys on the MMA's
+  // M dimension); any other head dim the packed forward in decode mode
+  const bool transposed = (d == 64 || d == 128);
   if (transposed) {
     if ((rc = get_map(st, q, bf16, d, Hq, B, 1, p.tm_q, group, group))) return rc;
   } else {
@@ -683,7 +683,7 @@ int fwd_decode(bool bf16, const void* q, const void* k, const void* v, void* o, 
   const cudaError_t le = transposed
                              ? launch_decode_tc(p.tm_q, p.tm_k, p.tm_v, o, lse, cu_k, p.vl_pref_out, p.part_o,
                                                 p.part_ml, p.err, p.timeout_ns, B, Hq, Hkv, total_k, split,
-                                                p.scale_log2, bf16, grid, stream)
+                                                p.scale_log2, bf16, d, grid, stream)
                              : launch(p, grid, stream);
   if (le != cudaSuccess) return ATTN_ELAUNCH;
   g_launches.fetch_add(1);
