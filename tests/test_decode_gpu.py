@@ -70,6 +70,12 @@ CASES = [
     ([131072], 32, 8, 128, torch.bfloat16),                     # one sequence, the long decode shape
     ([5000, 1, 0, 12345, 777, 128, 129], 8, 2, 64, torch.bfloat16),   # pieces, tile edges, an empty cache
     ([640] * 40, 32, 4, 128, torch.float16),                    # group 8 over many sequences
+    # head_dim 64: steps of two key tiles, a last step of one tile (128, 257),
+    # pieces of whole steps merged
+    ([128, 257, 256, 1, 384], 16, 4, 64, torch.bfloat16),
+    ([20000, 3], 8, 2, 64, torch.float16),
+    ([131072], 32, 8, 64, torch.bfloat16),                      # the long decode shape at d 64
+    ([640] * 40, 32, 4, 64, torch.float16),
 ]
 
 
@@ -130,15 +136,18 @@ def test_decode_unsupported_group_raises():
         attn.attn_decode(q, k, k, torch.tensor([0, 10], dtype=torch.int32, device=dev))
 
 
-def test_decode_maximum_sequence_count(path):
-    # 4096 sequences, one new query each, caches of 1 to 40 keys (fp16: with
-    # so few keys per row O is not averaged down, and bf16's rounding of P
-    # and O alone can pass 1e-2 where |O| approaches 4)
+@pytest.mark.parametrize("B,d", [(4096, 128), (4096, 64), (3399, 64), (3400, 64)])
+def test_decode_maximum_sequence_count(path, B, d):
+    # up to 4096 sequences, one new query each, caches of 1 to 40 keys (fp16:
+    # with so few keys per row O is not averaged down, and bf16's rounding of
+    # P and O alone can pass 1e-2 where |O| approaches 4).  At head_dim 64 the
+    # transposed kernel's prefix table holds 3399 sequences; more take the
+    # packed forward's decode mode.
     rng = np.random.default_rng(7)
-    lk = rng.integers(1, 41, 4096).tolist()
-    q, k, v = make(lk, 8, 2, 128, torch.float16, seed=7)
+    lk = rng.integers(1, 41, B).tolist()
+    q, k, v = make(lk, 8, 2, d, torch.float16, seed=7)
     dev = torch.device("cuda", 0)
-    scale = 128 ** -0.5
+    scale = d ** -0.5
     o, lse = attn.attn_decode(q.to(dev), k.to(dev), v.to(dev), cu_of(lk).to(dev), scale=scale)
     assert attn.get_error() == attn.ATTN_OK
     o_ref, lse_ref = oracle.varlen_cross_attention(q, k, v, [1] * len(lk), lk, causal=False, scale=scale)

@@ -16,11 +16,17 @@
 // the A operand in its natural (keys x d) layout, read MN-major; P^T is
 // written by the softmax threads into shared memory as the K-major B operand.
 //
-// Head dimension DA = 128 or 64.  The shared-memory tiles keep the 128-column
-// layout for both: with DA = 64 the TMA fills only the first 64-column chunk
-// of each Q, K and V tile and the second stays zero (written once), so S^T
-// takes only the first half of its K dimension and u^T's rows d >= 64 are
-// zero and never stored; the bytes streamed are the 64-column rows.
+// Head dimension DA = 128 or 64.  A ring stage holds two 64-column chunks of
+// K and of V (128-byte rows, 128-byte swizzle): with DA = 128 the two column
+// halves of one 128-key tile, with DA = 64 two consecutive 128-key tiles, so
+// that one softmax step (one max exchange across the four warps, the step's
+// fixed cost) covers 256 keys.  At DA = 64 each tile has its own S^T
+// columns, and one P.V serves both tiles: V read MN-major with M = 128 spans
+// the stage's two chunks (rows 0-63 = d of tile a, rows 64-127 = d of tile
+// b), and P^T has 2 x 16 rows (tile a's heads, then tile b's), so the
+// product's diagonal blocks are u_a (lanes 0-63, columns 0-15) and u_b
+// (lanes 64-127, columns 16-31); the off-diagonal blocks are never read.
+// u = u_a + u_b is summed through shared memory at the unit's end.
 //
 // Work units are (sequence, key/value head, piece of the cache), the same
 // schedule as the packed forward's decode mode, run round-robin over the
@@ -50,28 +56,36 @@ constexpr int kWarpMMA = 1;
 constexpr int kKeys = 128;   // keys per tile
 constexpr int kD = 128;      // head dimension of the shared-memory tiles (the largest DA)
 
-template <int NQ>
+template <int NQ, int DA>
 struct Cfg {
+  static constexpr int kTPS = kD / DA;                 // 128-key tiles per softmax step
   static constexpr int kStages = (NQ == 16) ? 3 : 2;   // key/value ring (shared memory bounds it)
-  static constexpr int kTile = kKeys * kD * 2;       // one K or V tile, bytes
+  static constexpr int kTile = kKeys * kD * 2;       // one stage of K or of V (two 64-column chunks), bytes
   static constexpr int kQChunk = NQ * 128;           // one 64-column chunk of the Q tile (NQ rows x 128 B)
-  static constexpr int kQ = 2 * kQChunk;             // the Q tile (NQ rows x 128 columns)
-  static constexpr int kPChunk = NQ * 128;           // one 64-key chunk of P^T
-  static constexpr int kP = 2 * kPChunk;             // P^T (NQ rows x 128 keys)
+  static constexpr int kQ = (DA / 64) * kQChunk;     // the Q tile (NQ rows x DA columns)
+  static constexpr int kRows = kTPS * NQ;            // P^T rows of a step (the P.V's N)
+  static constexpr int kPChunk = kRows * 128;        // one 64-key chunk of P^T
+  static constexpr int kP = 2 * kPChunk;             // P^T of a step (kRows rows x 128 keys)
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kOffK + kStages * kTile;
   static constexpr int kOffQ = kOffV + kStages * kTile;   // two Q slots
   static constexpr int kOffP = kOffQ + 2 * kQ;            // two P^T buffers
   static constexpr int kOffRed = kOffP + 2 * kP;          // [parity][warp][NQ] floats
   // barriers: kv_full[S], kv_empty[S], q_full[2], q_empty[2], s_full[2],
-  // p_full[2], p_free[2], o_free, red, drain
+  // p_full[2], p_free[2], o_free, red, drain, xch
   static constexpr int kOffBar = kOffRed + 2 * 4 * NQ * 4;
-  static constexpr int kNBars = 2 * kStages + 13;
+  static constexpr int kNBars = 2 * kStages + 14;
   static constexpr int kOffMisc = kOffBar + kNBars * 8;   // tmem slot, abort flag, bad flag
   static constexpr int kOffPref = kOffMisc + 64;          // units before each sequence (B + 1 ints)
-  static constexpr int kSmem = kOffPref + 4 * (kVarlenMaxB + 1) + 1024;
-  static_assert(kSmem <= 227 * 1024, "shared memory");
-  static constexpr uint32_t kTmemCols = (3 * NQ <= 64) ? 64 : 128;   // S^T x 2, u^T
+  // sequences per call: the prefix table takes what shared memory leaves
+  static constexpr int kMaxB = (227 * 1024 - 1024 - kOffPref) / 4 - 1 < kVarlenMaxB
+                                   ? (227 * 1024 - 1024 - kOffPref) / 4 - 1
+                                   : kVarlenMaxB;
+  static constexpr int kSmem = kOffPref + 4 * (kMaxB + 1) + 1024;
+  static_assert(kSmem <= 227 * 1024 && kMaxB >= 1024, "shared memory");
+  // S^T: two buffers of kTPS tiles, then u^T (kRows columns)
+  static constexpr int kUsedCols = 3 * kTPS * NQ;
+  static constexpr uint32_t kTmemCols = kUsedCols <= 64 ? 64 : kUsedCols <= 128 ? 128 : 256;
 };
 
 struct Params {
@@ -166,7 +180,9 @@ __host__ __device__ constexpr uint32_t idesc_a_mn(int M, int N, bool bf16) {
 template <int NQ, int GT, bool BF16, int DA>
 __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_constant__ Params p) {
   static_assert(GT >= 1 && GT <= NQ, "query heads per key/value head");
-  using C = Cfg<NQ>;
+  using C = Cfg<NQ, DA>;
+  static_assert(DA == 128 || DA == 64, "head dimension");
+  constexpr int kTPS = C::kTPS;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -186,6 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
   const uint32_t b_o_free = bar1 + 8 * 10;
   const uint32_t b_red = bar1 + 8 * 11;
   const uint32_t b_drain = bar1 + 8 * 12;
+  const uint32_t b_xch = bar1 + 8 * 13;   // u_b handed over (head_dim 64)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
   volatile int* bad_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 8);
@@ -209,6 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     mbar_init(b_o_free, 4);
     mbar_init(b_red, 4);
     mbar_init(b_drain, 1);
+    mbar_init(b_xch, 2);
     fence_mbar_init();
   }
   if (warp == kWarpMMA) {
@@ -220,21 +238,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     tma_prefetch_desc(&p.tm_k);
     tma_prefetch_desc(&p.tm_v);
   }
-  if constexpr (DA < kD) {
-    // the second 64-column chunk of every K and V stage and of both Q slots
-    // stays zero: the MMAs that read it see zeros, the TMA never writes it
+  if constexpr (kTPS == 2) {
+    // a step with one tile leaves V's chunk 1 as it was and multiplies it by
+    // P = 0: before its first load it must hold finite values
     if (warp >= 3) {
-      const int t3 = tid - 3 * 32;   // 0 .. 95
       const uint4 z = make_uint4(0, 0, 0, 0);
-      for (int s = 0; s < C::kStages; ++s)
-        for (int i = t3; i < 16384 / 16; i += 3 * 32) {
-          reinterpret_cast<uint4*>(smem + C::kOffK + s * C::kTile + 16384)[i] = z;
-          reinterpret_cast<uint4*>(smem + C::kOffV + s * C::kTile + 16384)[i] = z;
-        }
-      for (int qs = 0; qs < 2; ++qs)
-        for (int i = t3; i < C::kQChunk / 16; i += 3 * 32)
-          reinterpret_cast<uint4*>(smem + C::kOffQ + qs * C::kQ + C::kQChunk)[i] = z;
-      fence_proxy_async_smem();   // before the MMAs (async proxy) read them
+      for (int st = 0; st < C::kStages; ++st)
+        for (int i = tid - 96; i < 16384 / 16; i += 96)
+          reinterpret_cast<uint4*>(smem + C::kOffV + st * C::kTile + 16384)[i] = z;
+      fence_proxy_async_smem();
     }
   }
   if (warp == 2) {
@@ -304,14 +316,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         for (int c = 0; c < DA / 64; ++c)
           tma_load_4d(sQ + qs * C::kQ + c * C::kQChunk, &p.tm_q, b_q_full(qs), c * 64, U.g * p.G, U.b, 0);
         ++q_cnt;
-        for (int t = U.t0; t < U.t1; ++t) {
+        for (int t = U.t0; t < U.t1; t += kTPS) {
           const int st = kv_cnt % C::kStages;
           if (!mbar_wait(b_kv_empty(st), ((kv_cnt / C::kStages) & 1) ^ 1, wc,
                          ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKEmpty))) { ok = false; break; }
-          mbar_arrive_expect_tx(b_kv_full(st), 2 * C::kTile * DA / kD);
-          for (int c = 0; c < DA / 64; ++c) {
-            tma_load_4d(sK + st * C::kTile + c * 16384, &p.tm_k, b_kv_full(st), c * 64, U.g, U.row_k + t * kKeys, 0);
-            tma_load_4d(sV + st * C::kTile + c * 16384, &p.tm_v, b_kv_full(st), c * 64, U.g, U.row_k + t * kKeys, 0);
+          // chunk c: columns 64c.. of tile t (DA = 128) or tile t + c (DA = 64;
+          // a piece's odd last tile leaves chunk 1 as it was)
+          const int nc = (kTPS == 1) ? 2 : min(2, U.t1 - t);
+          mbar_arrive_expect_tx(b_kv_full(st), nc * 2 * 16384);
+          for (int c = 0; c < nc; ++c) {
+            const int col = (kTPS == 1) ? c * 64 : 0, row = U.row_k + (kTPS == 1 ? t : t + c) * kKeys;
+            tma_load_4d(sK + st * C::kTile + c * 16384, &p.tm_k, b_kv_full(st), col, U.g, row, 0);
+            tma_load_4d(sV + st * C::kTile + c * 16384, &p.tm_v, b_kv_full(st), col, U.g, row, 0);
           }
           ++kv_cnt;
         }
@@ -332,12 +348,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdescS = idesc_f16_f32acc(kKeys, NQ, BF16, false);   // A = K, B = Q: both K-major
-      constexpr uint32_t kIdescO = idesc_a_mn(kD, NQ, BF16);                  // A = V read MN-major, B = P^T
+      constexpr uint32_t kIdescO = idesc_a_mn(kD, C::kRows, BF16);            // A = V read MN-major, B = P^T
       const uint64_t dq0 = sdesc_sw128(sQ, 16, 1024);
       const uint64_t dk0 = sdesc_sw128(sK, 16, 1024);
       const uint64_t dv0 = sdesc_sw128(sV, 16384, 1024);
       const uint64_t dp0 = sdesc_sw128(sP, 16, 1024);
-      const uint32_t t_u = tmem + 2 * NQ;   // u^T columns
+      const uint32_t t_u = tmem + 2 * kTPS * NQ;   // u^T columns
       uint32_t q_cnt = 0, kv_cnt = 0, s_cnt = 0, p_cnt = 0, units_done = 0;
       bool ok = true;
       auto issue_pv = [&](int st, int pb, bool first) {   // stage st, P^T buffer pb
@@ -379,22 +395,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
           return true;
         };
         int prev_st = -1;
-        for (int t = U.t0; t < U.t1; ++t) {
+        for (int t = U.t0; t < U.t1; t += kTPS) {
           const int st = kv_cnt % C::kStages;
+          const int nt = min(kTPS, U.t1 - t);
           if (!mbar_wait(b_kv_full(st), (kv_cnt / C::kStages) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKFull))) {
             ok = false;
             break;
           }
           ++kv_cnt;
           tc_fence_after();
-          // S^T(t) into buffer s_cnt & 1: its previous contents (two tiles
-          // back) were consumed, since this thread has waited for that tile's P
+          // S^T of the step's tiles into buffer s_cnt & 1: its previous
+          // contents (two steps back) were consumed, since this thread has
+          // waited for that step's P
           const int sb = s_cnt & 1;
+          for (int x = 0; x < nt; ++x) {
 #pragma unroll
-          for (int kk = 0; kk < DA / 16; ++kk) {
-            const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-            const uint32_t offq = ((qs * C::kQ + (kk >> 2) * C::kQChunk + (kk & 3) * 32) >> 4);
-            umma_ss(tmem + sb * NQ, dk0 + ((st * C::kTile) >> 4) + off, dq0 + offq, kIdescS, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < DA / 16; ++kk) {
+              const uint32_t off = ((x + (kk >> 2)) * 16384 + (kk & 3) * 32) >> 4;
+              const uint32_t offq = ((qs * C::kQ + (kk >> 2) * C::kQChunk + (kk & 3) * 32) >> 4);
+              umma_ss(tmem + (sb * kTPS + x) * NQ, dk0 + ((st * C::kTile) >> 4) + off, dq0 + offq, kIdescS,
+                      kk > 0 ? 1u : 0u);
+            }
           }
           umma_commit(b_s_full(sb));
           ++s_cnt;
@@ -409,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
           prev_pb = sb;
         }
         if (!ok) break;
-        // the unit's last tile
+        // the unit's last step
         if (!do_pv(prev_st, prev_pb, first_pv)) break;
         umma_commit(b_q_empty(qs));
         ++units_done;
@@ -424,12 +445,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     const int quarter = warp & 3;                  // TMEM lane quarter this warp may address
     const int lrow = quarter * 32 + lane;          // TMEM lane: key of the tile (S^T), d (u^T)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t t_u = tmem + lane_off + 2 * NQ;
+    // u^T columns this thread's lane holds: at DA = 64 lanes 64-127 keep u_b
+    const uint32_t t_u = tmem + lane_off + 2 * kTPS * NQ + ((kTPS == 2 && lrow >= 64) ? NQ : 0);
     const float c = p.scale_log2;
     constexpr int G = GT;
-    uint32_t s_cnt = 0, red_cnt = 0;
+    uint32_t s_cnt = 0, red_cnt = 0, xch_cnt = 0;
     uint32_t free_seen[2] = {0, 0};   // phases of p_free(b) observed
-    uint32_t tiles_total = 0;   // P.V products issued so far for this CTA (all units)
+    uint32_t tiles_total = 0;   // steps (P^T buffer uses) so far for this CTA (all units)
     bool ok = true;
     // reduces v over the 128 softmax threads (max or sum), all get the result:
     // within a warp by redux.sync (max) or shuffles (sum), then across the
@@ -500,8 +522,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         l[h] = 0.0f;
       }
       const uint32_t tile0 = tiles_total;
-      for (int t = U.t0; t < U.t1; ++t) {
-        const uint32_t i = tiles_total - tile0;   // tile within the unit
+      for (int t = U.t0; t < U.t1; t += kTPS) {
+        const uint32_t i = tiles_total - tile0;   // step within the unit
         const int sb = s_cnt & 1;
         if (!mbar_wait_warp(b_s_full(sb), (s_cnt >> 1) & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteSFull))) {
           ok = false;
@@ -509,12 +531,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
         }
         ++s_cnt;
         tc_fence_after();
-        float s[NQ];
-        tld<NQ>(tmem + lane_off + sb * NQ, s);
-        const bool valid = t * kKeys + lrow < U.k_len;
+        // this thread's key in each tile of the step
+        float s[kTPS][NQ];
+        bool valid[kTPS];
+#pragma unroll
+        for (int y = 0; y < kTPS; ++y) {
+          tld<NQ>(tmem + lane_off + (sb * kTPS + y) * NQ, s[y]);
+          valid[y] = t + y < U.t1 && (t + y) * kKeys + lrow < U.k_len;
+        }
         float x[NQ];
 #pragma unroll
-        for (int h = 0; h < NQ; ++h) x[h] = valid ? s[h] : -INFINITY;
+        for (int h = 0; h < NQ; ++h) {
+          x[h] = valid[0] ? s[0][h] : -INFINITY;
+#pragma unroll
+          for (int y = 1; y < kTPS; ++y) x[h] = fmaxf(x[h], valid[y] ? s[y][h] : -INFINITY);
+        }
         if (!reduce(x, true)) { ok = false; break; }
         // running max (scaled units) with the stale-max rule of the forward
         // kernel: rescale only when the max grows by more than 2^8
@@ -531,19 +562,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
             any_resc = true;
           }
         }
-        // P^T of this key into buffer sb, once the P.V that read it two
-        // tiles back (this CTA's tile tiles_total - 2) has completed
+        // P^T of these keys into buffer sb, once the P.V that read it two
+        // steps back (this CTA's step tiles_total - 2) has completed
         if (tiles_total >= 2 && !pv_wait(tiles_total - 2)) { ok = false; break; }
-        uint8_t* pbuf = smem + C::kOffP + sb * C::kP + (lrow >> 6) * C::kPChunk;
 #pragma unroll
         for (int h = 0; h < NQ; ++h) {
           if (h >= G) break;
-          const float e = valid ? ex2_approx(s[h] * c - ((m[h] == -INFINITY) ? 0.0f : m[h])) : 0.0f;
-          l[h] = l[h] * r[h] + e;
-          T pv = T(e);
-          *reinterpret_cast<T*>(pbuf + sw128(h, lrow & 63)) = pv;
+          const float mh = (m[h] == -INFINITY) ? 0.0f : m[h];
+          float e_sum = 0.0f;
+#pragma unroll
+          for (int y = 0; y < kTPS; ++y) {
+            const float e = valid[y] ? ex2_approx(s[y][h] * c - mh) : 0.0f;
+            e_sum += e;
+            uint8_t* pbuf = smem + C::kOffP + sb * C::kP + (lrow >> 6) * C::kPChunk;
+            *reinterpret_cast<T*>(pbuf + sw128(y * NQ + h, lrow & 63)) = T(e);
+          }
+          l[h] = l[h] * r[h] + e_sum;
         }
-        // u^T rescale (rare): needs the previous tile's P.V complete.  m is
+        // u^T rescale (rare): needs the previous step's P.V complete.  m is
         // the same in every thread, so the decision is too; the vote keeps the
         // warp-collective TMEM accesses below uniform regardless.
         any_resc = __any_sync(0xffffffffu, any_resc);
@@ -571,6 +607,26 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_o_free);   // u^T may be overwritten by the next unit
+      if constexpr (kTPS == 2) {
+        // u = u_a + u_b: lanes 64-127 hand u_b over through the first P^T
+        // buffer, idle now that every P.V so far has completed; the next
+        // P^T write follows the next max exchange, which all four warps
+        // reach only after this
+        float* xch = reinterpret_cast<float*>(smem + C::kOffP);
+        if (lrow >= 64) {
+#pragma unroll
+          for (int h = 0; h < NQ; ++h)
+            if (h < G) xch[h * 64 + (lrow - 64)] = o[h];
+          __syncwarp();
+          if (lane == 0) mbar_arrive(b_xch);
+        } else {
+          if (!mbar_wait_warp(b_xch, xch_cnt & 1, wc, ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteXchg))) break;
+#pragma unroll
+          for (int h = 0; h < NQ; ++h)
+            if (h < G) o[h] += xch[h * 64 + lrow];
+        }
+        ++xch_cnt;
+      }
       if (U.n_split <= 1) {
         T* dst = reinterpret_cast<T*>(p.o);
 #pragma unroll
@@ -623,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
 
 template <int NQ, int GT, bool BF16, int DA>
 cudaError_t launch(const Params& p, int grid, cudaStream_t stream) {
-  constexpr int smem = Cfg<NQ>::kSmem;
+  constexpr int smem = Cfg<NQ, DA>::kSmem;
   static bool attr_done[64] = {};   // per instantiation
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -638,6 +694,8 @@ cudaError_t launch(const Params& p, int grid, cudaStream_t stream) {
 }
 
 }  // namespace dtc
+
+int decode_tc_max_b(int d) { return d == 64 ? dtc::Cfg<16, 64>::kMaxB : dtc::Cfg<16, 128>::kMaxB; }
 
 cudaError_t launch_decode_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v, void* o,
                              float* lse, const int* cu_k, int* pref_out, void* part_o, float* part_ml, int* err,

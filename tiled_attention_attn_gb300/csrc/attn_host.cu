@@ -609,16 +609,24 @@ int fwd_decode(bool bf16, const void* q, const void* k, const void* v, void* o, 
   int lp = 0;
   while ((1 << lp) < group) ++lp;
   const int n_hg = Hq >> lp;
+  // head_dim 64 and 128 run the transposed decode kernel (keys on the MMA's
+  // M dimension); other head dims, or more sequences than its prefix table
+  // holds, the packed forward in decode mode.  The transposed kernel's
+  // softmax step covers 256 keys at head_dim 64, 128 otherwise.
+  const bool transposed = (d == 64 || d == 128) && B <= decode_tc_max_b(d);
+  const long long step_keys = (transposed && d == 64) ? 2 * kBN : kBN;
   // Pieces per cache: the units (B x n_hg x pieces) run in rounds of one per
   // CTA, so with caches of equal length (the host cannot read cu_seqlens_k;
-  // the mean length stands in) the step costs rounds x (tiles per piece +
+  // the mean length stands in) the call costs rounds x (steps per piece +
   // kDecodeUnitCost), a unit's fixed cost (Q load, pipeline fill, epilogue)
-  // in tile-times.  The piece count that minimises it wins, fewer pieces on
-  // ties; split = 0 leaves every cache whole.  `tiles` bounds the sum over
-  // sequences of their key tiles (a partial tile per sequence at most).
+  // in step-times.  The piece count that minimises it wins, fewer pieces on
+  // ties; split = 0 leaves every cache whole, else it counts key tiles (whole
+  // steps).  `tiles` bounds the sum over sequences of their key tiles (a
+  // partial tile per sequence at most).
   const long long units0 = static_cast<long long>(B) * n_hg;
   const long long tiles = (static_cast<long long>(total_k) + kBN - 1) / kBN + B;
-  const long long t_seq = std::max<long long>(1, ((static_cast<long long>(total_k) + B - 1) / B + kBN - 1) / kBN);
+  const long long t_seq =
+      std::max<long long>(1, ((static_cast<long long>(total_k) + B - 1) / B + step_keys - 1) / step_keys);
   const long long grid_max = st.sm_count;
   constexpr double kDecodeUnitCost = 1.5;
   long long best_pcs = 1;
@@ -631,15 +639,12 @@ int fwd_decode(bool bf16, const void* q, const void* k, const void* v, void* o, 
       best_pcs = pcs;
     }
   }
-  const int split = best_pcs > 1 ? static_cast<int>((t_seq + best_pcs - 1) / best_pcs) : 0;
+  const int split = best_pcs > 1 ? static_cast<int>((t_seq + best_pcs - 1) / best_pcs * (step_keys / kBN)) : 0;
   const long long max_units = split > 0 ? static_cast<long long>(n_hg) * (tiles / split + 1 + B) : units0;
   if (max_units > (1LL << 30)) return ATTN_EINVAL;
 
   static thread_local FwdParams p;
   std::memset(&p, 0, sizeof(p));
-  // head_dim 64 and 128 run the transposed decode kernel (keys on the MMA's
-  // M dimension); any other head dim the packed forward in decode mode
-  const bool transposed = (d == 64 || d == 128);
   if (transposed) {
     if ((rc = get_map(st, q, bf16, d, Hq, B, 1, p.tm_q, group, group))) return rc;
   } else {

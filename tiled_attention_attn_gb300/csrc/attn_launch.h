@@ -29,12 +29,17 @@ DecodeCombineLauncher decode_combine_launcher_d128(bool bf16);
 
 // The transposed decode kernel (head_dim 64 or 128, d): S^T = K Q^T and u^T += V^T P^T
 // with the keys, then d, on the TMEM lanes; same units, pieces and partial
-// layout as the packed forward's decode mode.  tm_q: q (B, Hq, 128) as
+// layout as the packed forward's decode mode.  With d = 64 a softmax step
+// covers two key tiles: split must then be even (pieces of whole steps) for
+// full steps, though any split gives the right result.  tm_q: q (B, Hq, 128) as
 // (d, Hq, B, 1) with box 64 x G x 1 x 1; tm_k, tm_v: (d, Hkv, total_k, 1).
 cudaError_t launch_decode_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v, void* o,
                              float* lse, const int* cu_k, int* pref_out, void* part_o, float* part_ml, int* err,
                              unsigned long long timeout_ns, int B, int Hq, int Hkv, int total_k, int split,
                              float scale_log2, bool bf16, int d, int grid, cudaStream_t stream);
+// Sequences per call that launch_decode_tc takes for head_dim d (its shared
+// memory holds a prefix table of B + 1 ints).
+int decode_tc_max_b(int d);
 
 // Test kernel: waits on a barrier that never completes, under `timeout_ns`.
 cudaError_t launch_selftest_wait(int* err_word, unsigned long long timeout_ns, cudaStream_t stream);
