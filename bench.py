@@ -536,6 +536,7 @@ def bwd_leg(attn, device, stream, peaks, iters: int = 10):
 
 DECODE_SHAPE = (32, 32, 8, 128, 4096)      # B, Hq, Hkv, d, cache length of the decode leg
 DECODE_LONG_SHAPE = (1, 32, 8, 128, 131072)   # one sequence with a long cache
+DECODE_D64_SHAPES = ((32, 32, 8, 64, 4096), (1, 32, 8, 64, 131072))   # the same at head_dim 64
 
 
 def decode_inputs(device, shape):
@@ -551,10 +552,14 @@ def decode_inputs(device, shape):
     return q, k, v, cu_q, cu_k
 
 
-def decode_step_times(attn, device, stream, shape, iters: int = 20):
+def decode_step_times(attn, device, stream, shape, iters: int = 20, no_flush: bool = False):
     """Median CUDA-event times (ms) of one decoding step, one new token per
     sequence over a cache of C tokens (+ the new one), through attn_decode
-    and through attn_fwd_varlen; L2 flushed before each call."""
+    and through attn_fwd_varlen; L2 flushed before each call.  With
+    ``no_flush`` also the time of attn_decode in back-to-back calls with no
+    flush between them (the caches are larger than L2), as a fifth value: the
+    flush leaves up to L2's size of dirty lines whose write-back the next
+    kernel shares HBM with."""
     B, Hq, Hkv, d, C = shape
     q, k, v, cu_q, cu_k = decode_inputs(device, shape)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
@@ -584,31 +589,50 @@ def decode_step_times(attn, device, stream, shape, iters: int = 20):
         attn.set_decode_path(True)
     t_fwd = timed(lambda: attn.attn_fwd(q, k, v, causal=True, cu_seqlens=cu_q, cu_seqlens_k=cu_k, out=o, lse=lse,
                                         stream=stream))
-    return t_dec, t_cc, t_fwd, 2 * k.numel() * k.element_size()
+    if not no_flush:
+        return t_dec, t_cc, t_fwd, 2 * k.numel() * k.element_size()
+    runs = []
+    for _ in range(5):
+        torch.cuda.synchronize(device)
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        for _ in range(iters):
+            attn.attn_decode(q, k, v, cu_k, out=o, lse=lse, stream=stream)
+        e.record(stream)
+        torch.cuda.synchronize(device)
+        runs.append(s.elapsed_time(e) / iters)
+    if attn.get_error() != attn.ATTN_OK:
+        raise RuntimeError(f"device error in the decode leg: {attn.last_device_error():#x}")
+    return t_dec, t_cc, t_fwd, 2 * k.numel() * k.element_size(), statistics.median(runs)
 
 
 def decode_leg(attn, device, stream, peaks, iters: int = 20):
     """One new token per sequence over a key/value cache (the generation step
-    of the training page §4.3), bf16, Hq 32, Hkv 8, d 128.  Memory-bound: the
-    rate is the cache bytes read (K and V once) per second against the HBM
-    copy peak.  Two shapes, B 32 sequences of 4096 + 1 keys and one sequence
-    of 131072 + 1 keys (``long``), each through attn_decode on its default
-    route (the packed forward's tensor-core tiles in decode mode, caches cut
-    into pieces when the (sequence, head group) units are few), through
-    attn_decode on its CUDA-core route, and through attn_fwd_varlen (the
-    packed forward without pieces)."""
-    def entry(shape, name):
+    of the training page §4.3), bf16, Hq 32, Hkv 8, d 128 and d 64.
+    Memory-bound: the rate is the cache bytes read (K and V once) per second
+    against the HBM copy peak.  Two shapes per head dim, B 32 sequences of
+    4096 + 1 keys and one sequence of 131072 + 1 keys (``long``), each
+    through attn_decode on its default route (the transposed tensor-core
+    decode kernel, caches cut into pieces when the (sequence, head group)
+    units are few), through attn_decode on its CUDA-core route, and through
+    attn_fwd_varlen (the packed forward without pieces).  L2 is flushed (a
+    256 MiB write) before each call; ``no_flush`` is attn_decode in
+    back-to-back calls, the caches (268-537 MB) being larger than L2."""
+    def entry(shape):
         B, Hq, Hkv, d, C = shape
-        t_dec, t_cc, t_fwd, nbytes = decode_step_times(attn, device, stream, shape, iters)
+        t_dec, t_cc, t_fwd, nbytes, t_nf = decode_step_times(attn, device, stream, shape, iters, no_flush=True)
         gbs = lambda t: nbytes / (t / 1e3) / 1e9
         return {"workload": f"decode: B{B} Hq{Hq} Hkv{Hkv} d{d} bf16, 1 new token over a {C}-token cache",
                 "entry": "attn_decode (tensor cores)", "bound": "hbm", "achieved": gbs(t_dec), "unit": "GB/s",
                 "peak": peaks["hbm_gbs"], "frac": gbs(t_dec) / peaks["hbm_gbs"], "ms": t_dec,
                 "cache_bytes_per_call": nbytes,
+                "no_flush": {"achieved": gbs(t_nf), "frac": gbs(t_nf) / peaks["hbm_gbs"], "ms": t_nf},
                 "attn_decode_cuda_cores": {"achieved": gbs(t_cc), "frac": gbs(t_cc) / peaks["hbm_gbs"], "ms": t_cc},
                 "attn_fwd_varlen": {"achieved": gbs(t_fwd), "frac": gbs(t_fwd) / peaks["hbm_gbs"], "ms": t_fwd}}
-    out = entry(DECODE_SHAPE, "batch")
-    out["long"] = entry(DECODE_LONG_SHAPE, "long")
+    out = entry(DECODE_SHAPE)
+    out["long"] = entry(DECODE_LONG_SHAPE)
+    out["d64"] = entry(DECODE_D64_SHAPES[0])
+    out["d64"]["long"] = entry(DECODE_D64_SHAPES[1])
     return out
 
 
@@ -857,16 +881,17 @@ def run_ours(args, wl):
 
     if args.profile_decode > 0:
         # attn_decode calls of the decode leg's batch shape (for profiling)
-        dq, dk, dv, _, dcu = decode_inputs(device, DECODE_SHAPE)
+        shape = DECODE_SHAPE if args.decode_d == 128 else DECODE_D64_SHAPES[0]
+        dq, dk, dv, _, dcu = decode_inputs(device, shape)
         do = torch.empty_like(dq)
-        dl = torch.empty(DECODE_SHAPE[1], DECODE_SHAPE[0], dtype=torch.float32, device=device)
+        dl = torch.empty(shape[1], shape[0], dtype=torch.float32, device=device)
         for _ in range(args.profile_decode):
             flush.zero_()
             attn.attn_decode(dq, dk, dv, dcu, out=do, lse=dl, stream=stream)
         torch.cuda.synchronize(device)
         if attn.get_error() != attn.ATTN_OK:
             raise RuntimeError(f"device error: {attn.last_device_error():#x}")
-        print(f"{args.profile_decode} attn_decode calls of B{DECODE_SHAPE[0]} x {DECODE_SHAPE[4]}")
+        print(f"{args.profile_decode} attn_decode calls of B{shape[0]} x {shape[4]}, d {shape[3]}")
         return 0
     if args.profile_calls > 0:
         attn.set_pair_forward(args.pair)
@@ -1061,6 +1086,8 @@ def main():
     ap.add_argument("--profile-decode", type=int, default=0,
                     help="only make this many attn_decode calls of the decode leg's batch shape "
                          "(L2 flushed before each) and exit")
+    ap.add_argument("--decode-d", type=int, default=128, choices=[64, 128],
+                    help="with --profile-decode: the head dim of the decode shape")
     ap.add_argument("--pair", action="store_true", help="with --profile-calls: run the CTA-pair kernel")
     args = ap.parse_args()
     if args.warmup < 3:
