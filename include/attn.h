@@ -223,12 +223,13 @@ int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float 
  * Pointers 16-byte aligned (lse 4); k and v may be null when total_k is 0.
  *
  * Two routes compute it (attn_set_decode_path).  The default runs on TMA
- * tiles and tcgen05 MMAs, reading the cache once per key/value head: for
- * head_dim 128 a decode kernel with the products transposed (S^T = K Q^T,
- * u^T += V^T P^T: the tile's 128 keys on the TMEM lanes, the group's query
- * heads on the columns, so each softmax thread owns one key), for head_dim
- * 64 the packed forward kernel in decode mode (the group's query heads in
- * one tile).  Units are (sequence, key/value head, piece of the cache): the
+ * tiles and tcgen05 MMAs, reading the cache once per key/value head: a
+ * decode kernel with the products transposed (S^T = K Q^T, u^T += V^T P^T:
+ * the tile's 128 keys on the TMEM lanes, the group's query heads on the
+ * columns, so each softmax thread owns one key); at head_dim 64 each softmax
+ * step takes two key tiles.  With head_dim 64 and more than 3399 sequences
+ * the packed forward kernel in decode mode (the group's query heads in one
+ * tile) runs instead.  Units are (sequence, key/value head, piece of the cache): the
  * caches are cut into pieces of key tiles when that shortens the step (a
  * cost model over rounds of one unit per SM, with the mean cache length),
  * and a second launch merges the pieces' fp32 partials with the running-max
@@ -435,9 +436,9 @@ int attn_fwd_rope(const void *q, const void *k, const void *v, void *o, float *l
 
 /*
  * attn_set_decode_path -- selects how attn_decode runs: 1 (the default) on
- * the packed forward's tensor-core tiles, in decode mode (the query heads of
- * a key/value head share one tile, and each cache is cut into pieces of key
- * tiles, merged by a second pass, when the (sequence, head group) units
+ * tensor cores, the transposed decode kernel (the query heads of a
+ * key/value head are the MMA's columns, and each cache is cut into pieces of
+ * key tiles, merged by a second pass, when the (sequence, head group) units
  * alone would leave SMs idle); 0 on the CUDA-core chunk kernels.  Both
  * compute the same function.  Calls with total_k = 0 or B > 4096 take the
  * CUDA-core path either way.  attn_decode_path() returns the setting.

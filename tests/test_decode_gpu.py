@@ -1,9 +1,10 @@
 """Parity of attn_decode (one new query per sequence against a packed
 key/value cache) with the oracle's per-sequence dense attention, every
 element compared, and with attn_fwd_varlen on the same inputs, on both of
-its routes: the packed forward's tensor-core tiles in decode mode (caches
-cut into pieces of key tiles whose partials a second launch merges) and the
-CUDA-core chunk kernels.  Bar: max |O - O_ref| <= 1e-2, max |lse - lse_ref|
+its routes: the transposed tensor-core decode kernel (caches cut into
+pieces of key tiles whose partials a second launch merges; at head_dim 64
+steps of two key tiles, and the packed forward's decode mode above 3399
+sequences) and the CUDA-core chunk kernels.  Bar: max |O - O_ref| <= 1e-2, max |lse - lse_ref|
 <= 1e-3; a sequence with no key gives O = 0 and lse = -inf on both sides."""
 
 import numpy as np
