@@ -227,7 +227,7 @@ int attn_fwd_varlen(const void *q, const void *k, const void *v, void *o, float 
  * decode kernel with the products transposed (S^T = K Q^T, u^T += V^T P^T:
  * the tile's 128 keys on the TMEM lanes, the group's query heads on the
  * columns, so each softmax thread owns one key); at head_dim 64 each softmax
- * step takes two key tiles.  With head_dim 64 and more than 3399 sequences
+ * step takes two key tiles.  With head_dim 64 and more than 3143 sequences
  * the packed forward kernel in decode mode (the group's query heads in one
  * tile) runs instead.  Units are (sequence, key/value head, piece of the cache): the
  * caches are cut into pieces of key tiles when that shortens the step (a

@@ -3,7 +3,7 @@ key/value cache) with the oracle's per-sequence dense attention, every
 element compared, and with attn_fwd_varlen on the same inputs, on both of
 its routes: the transposed tensor-core decode kernel (caches cut into
 pieces of key tiles whose partials a second launch merges; at head_dim 64
-steps of two key tiles, and the packed forward's decode mode above 3399
+steps of two key tiles, and the packed forward's decode mode above 3143
 sequences) and the CUDA-core chunk kernels.  Bar: max |O - O_ref| <= 1e-2, max |lse - lse_ref|
 <= 1e-3; a sequence with no key gives O = 0 and lse = -inf on both sides."""
 
@@ -137,12 +137,12 @@ def test_decode_unsupported_group_raises():
         attn.attn_decode(q, k, k, torch.tensor([0, 10], dtype=torch.int32, device=dev))
 
 
-@pytest.mark.parametrize("B,d", [(4096, 128), (4096, 64), (3399, 64), (3400, 64)])
+@pytest.mark.parametrize("B,d", [(4096, 128), (4096, 64), (3143, 64), (3144, 64)])
 def test_decode_maximum_sequence_count(path, B, d):
     # up to 4096 sequences, one new query each, caches of 1 to 40 keys (fp16:
     # with so few keys per row O is not averaged down, and bf16's rounding of
     # P and O alone can pass 1e-2 where |O| approaches 4).  At head_dim 64 the
-    # transposed kernel's prefix table holds 3399 sequences; more take the
+    # transposed kernel's prefix table holds 3143 sequences; more take the
     # packed forward's decode mode.
     rng = np.random.default_rng(7)
     lk = rng.integers(1, 41, B).tolist()

@@ -77,9 +77,11 @@ struct Cfg {
   static constexpr int kNBars = 2 * kStages + 14;
   static constexpr int kOffMisc = kOffBar + kNBars * 8;   // tmem slot, abort flag, bad flag
   static constexpr int kOffPref = kOffMisc + 64;          // units before each sequence (B + 1 ints)
-  // sequences per call: the prefix table takes what shared memory leaves
-  static constexpr int kMaxB = (227 * 1024 - 1024 - kOffPref) / 4 - 1 < kVarlenMaxB
-                                   ? (227 * 1024 - 1024 - kOffPref) / 4 - 1
+  // sequences per call: the prefix table takes what shared memory leaves,
+  // less 1 KB so that the merge pass's blocks (a programmatic dependent
+  // launch) fit beside the CTA and wait there
+  static constexpr int kMaxB = (227 * 1024 - 2048 - kOffPref) / 4 - 1 < kVarlenMaxB
+                                   ? (227 * 1024 - 2048 - kOffPref) / 4 - 1
                                    : kVarlenMaxB;
   static constexpr int kSmem = kOffPref + 4 * (kMaxB + 1) + 1024;
   static_assert(kSmem <= 227 * 1024 && kMaxB >= 1024, "shared memory");

@@ -1226,31 +1226,31 @@ __global__ void __launch_bounds__(kBM) attn_combine_kernel(const __grid_constant
 
 
 // ---------------------------------------------------------------------------
-// Merge of decode pieces.  Block (sequence b, head group) x 16-column slice;
-// thread r is query head r of the group (row r of the unit's first sub-tile,
-// the only one a single query fills).  Piece s of (b, group) is unit
-// pref[b] + s * groups + group, in key order of s; the same r-rescale
-// as the split-KV combine above.  Sequences that were not cut (one piece)
-// were written by the forward kernel, and with malformed offsets that kernel
-// has zeroed every row, so those blocks return at once.  Launched as a
-// programmatic dependent of the forward kernel.
+// Merge of decode pieces.  Block (sequence b, head group) x 16-column slice,
+// one warp per query head r of the group (row r of the pieces' first
+// sub-tile, the only one a single query fills); lane s takes piece s of each
+// chunk of 32, so a chunk's loads ((m, l) and 16 columns of O_s) are one L2
+// round trip, and the warp reduces across its lanes with the same r-rescale
+// as the split-KV combine above: M = max_s m_s, w_s = 2^(m_s - M) l_s.
+// Piece s of (b, group) is unit pref[b] + s * groups + group, in key order of
+// s.  Sequences that were not cut (one piece) were written by the decode
+// kernel, and with malformed offsets that kernel has zeroed every row, so
+// those blocks return at once.  Launched as a programmatic dependent of the
+// decode kernel.
 // ---------------------------------------------------------------------------
 template <int D, bool BF16>
-__global__ void __launch_bounds__(32) attn_combine_decode_kernel(const __grid_constant__ DecodeCombineParams p) {
+__global__ void __launch_bounds__(256) attn_combine_decode_kernel(const __grid_constant__ DecodeCombineParams p) {
   using T = typename IO<BF16>::T;
-  const int G = 1 << p.pack_log2;
   const int n_hg = p.Hq >> p.pack_log2;
   const int b = blockIdx.x / n_hg, hg = blockIdx.x - b * n_hg;
   const int cb = blockIdx.y;
-  const int row = threadIdx.x;
-  if (row >= G) return;
+  const int row = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int ak = __ldg(p.cu_seqlens_k + b);
   const int ek = __ldg(p.cu_seqlens_k + b + 1);
   grid_wait_prerequisites();
   if (p.pref[p.B + 1] != 0 || ek < ak) return;
   const int pcs = decode_pieces(ek - ak, p.split);
   if (pcs <= 1) return;
-  // piece s of (b, group) is unit pref[b] + s * n_hg + hg (the group fastest)
   const int slot0 = p.pref[b] + hg;
   const float2* ml = reinterpret_cast<const float2*>(p.part_ml);
   const float4* po = reinterpret_cast<const float4*>(p.part_o);
@@ -1262,42 +1262,45 @@ __global__ void __launch_bounds__(32) attn_combine_decode_kernel(const __grid_co
   float acc[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
-  for (int s0 = 0; s0 < pcs; s0 += 4) {
-    float2 mlv[4];
-    float4 x[4][4];
+  for (int s0 = 0; s0 < pcs; s0 += 32) {
+    const int s = s0 + lane;
+    const bool in = s < pcs;
+    float2 mlv = in ? __ldcg(ml + ml_base + s * ml_stride) : make_float2(-INFINITY, 0.0f);
+    float4 x[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const bool in = s0 + i < pcs;
-      mlv[i] = in ? __ldcg(ml + ml_base + (s0 + i) * ml_stride) : make_float2(-INFINITY, 0.0f);
+    for (int c = 0; c < 4; ++c)
+      x[c] = in ? __ldcg(po + (o_base + s * o_stride + c) * kBM + row) : make_float4(0, 0, 0, 0);
+    float mc = mlv.x;
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-        x[i][c] = in ? __ldcg(po + (o_base + (s0 + i) * o_stride + c) * kBM + row) : make_float4(0, 0, 0, 0);
+    for (int o = 16; o > 0; o >>= 1) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, o));
+    if (mc == -INFINITY) continue;   // no piece of this chunk saw a key
+    const float mn = fmaxf(M, mc);
+    const float r = (M == -INFINITY) ? 0.0f : ex2_approx(M - mn);
+    M = mn;
+    // an empty piece's O_s was never written: weight 0 and its values dropped
+    const bool live = mlv.x != -INFINITY;
+    float w = live ? ex2_approx(mlv.x - M) * mlv.y : 0.0f;
+    float v[16];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      v[4 * c] = live ? w * x[c].x : 0.0f;
+      v[4 * c + 1] = live ? w * x[c].y : 0.0f;
+      v[4 * c + 2] = live ? w * x[c].z : 0.0f;
+      v[4 * c + 3] = live ? w * x[c].w : 0.0f;
     }
-    float mb = M;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) mb = fmaxf(mb, mlv[i].x);
-    if (mb == -INFINITY) continue;
-    const float r = (M == -INFINITY) ? 0.0f : ex2_approx(M - mb);
-    M = mb;
-    L *= r;
+    for (int o = 16; o > 0; o >>= 1) {
+      w += __shfl_xor_sync(0xffffffffu, w, o);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) acc[i] *= r;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if (mlv[i].x == -INFINITY) continue;
-      const float w = ex2_approx(mlv[i].x - M) * mlv[i].y;
-      L += w;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        acc[4 * c] += w * x[i][c].x;
-        acc[4 * c + 1] += w * x[i][c].y;
-        acc[4 * c + 2] += w * x[i][c].z;
-        acc[4 * c + 3] += w * x[i][c].w;
-      }
+      for (int i = 0; i < 16; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], o);
     }
+    L = L * r + w;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) acc[i] = acc[i] * r + v[i];
   }
+  if (lane != 0) return;
   const float inv = (L > 0.0f) ? 1.0f / L : 0.0f;
-  const int head = hg * G + row;
+  const int head = (hg << p.pack_log2) + row;
   T* dst = reinterpret_cast<T*>(p.o) + (static_cast<size_t>(b) * p.Hq + head) * D + cb * 16;
   uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll

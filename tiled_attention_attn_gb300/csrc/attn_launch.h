@@ -8,7 +8,7 @@ namespace attn {
 
 using FwdLauncher = cudaError_t (*)(const FwdParams& p, int grid, cudaStream_t stream);
 using CombineLauncher = cudaError_t (*)(const CombineParams& p, int n_groups, cudaStream_t stream);
-// grid: one block per (sequence, head group) x 16-column slice
+// grid: one block per (sequence, head group) x 16-column slice, one warp per query head
 using DecodeCombineLauncher = cudaError_t (*)(const DecodeCombineParams& p, int n_groups, cudaStream_t stream);
 
 FwdLauncher fwd_launcher_d64(bool bf16, bool causal, bool varlen);
