@@ -240,17 +240,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
     tma_prefetch_desc(&p.tm_k);
     tma_prefetch_desc(&p.tm_v);
   }
-  if constexpr (kTPS == 2) {
-    // a step with one tile leaves V's chunk 1 as it was and multiplies it by
-    // P = 0: before its first load it must hold finite values
-    if (warp >= 3) {
-      const uint4 z = make_uint4(0, 0, 0, 0);
-      for (int st = 0; st < C::kStages; ++st)
-        for (int i = tid - 96; i < 16384 / 16; i += 96)
-          reinterpret_cast<uint4*>(smem + C::kOffV + st * C::kTile + 16384)[i] = z;
-      fence_proxy_async_smem();
-    }
-  }
   if (warp == 2) {
     // validate cu_seqlens_k and build the unit prefix: sequence b has
     // Hkv x pieces(b) units
@@ -322,15 +311,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_tc_kernel(const __grid_con
           const int st = kv_cnt % C::kStages;
           if (!mbar_wait(b_kv_empty(st), ((kv_cnt / C::kStages) & 1) ^ 1, wc,
                          ATTN_DEVERR_WAIT_TIMEOUT_SITE(kSiteKEmpty))) { ok = false; break; }
-          // chunk c: columns 64c.. of tile t (DA = 128) or tile t + c (DA = 64;
-          // a piece's odd last tile leaves chunk 1 as it was)
+          // chunk c: columns 64c.. of tile t (DA = 128) or tile t + c (DA = 64).
+          // A segment's odd last tile at DA = 64 loads no K chunk 1 (its S^T is
+          // not computed) and a V chunk 1 of zeros, from rows past total_k
+          // (the fill value): the step's P.V multiplies that chunk by P = 0
           const int nc = (kTPS == 1) ? 2 : min(2, U.t1 - t);
-          mbar_arrive_expect_tx(b_kv_full(st), nc * 2 * 16384);
+          mbar_arrive_expect_tx(b_kv_full(st), (2 * nc + (nc < 2 ? 1 : 0)) * 16384);
           for (int c = 0; c < nc; ++c) {
             const int col = (kTPS == 1) ? c * 64 : 0, row = U.row_k + (kTPS == 1 ? t : t + c) * kKeys;
             tma_load_4d(sK + st * C::kTile + c * 16384, &p.tm_k, b_kv_full(st), col, U.g, row, 0);
             tma_load_4d(sV + st * C::kTile + c * 16384, &p.tm_v, b_kv_full(st), col, U.g, row, 0);
           }
+          if (nc < 2) tma_load_4d(sV + st * C::kTile + 16384, &p.tm_v, b_kv_full(st), 0, U.g, p.total_k, 0);
           ++kv_cnt;
         }
       }
