@@ -117,6 +117,17 @@ def test_decode_no_keys_at_all():
     assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_every_cache_empty_with_keys_present(d):
+    # valid offsets that give every sequence zero keys while k and v hold rows
+    dev = torch.device("cuda", 0)
+    q = torch.randn(3, 8, d, device=dev, dtype=torch.bfloat16)
+    k = torch.randn(300, 2, d, device=dev, dtype=torch.bfloat16)
+    o, lse = attn.attn_decode(q, k, k, torch.zeros(4, dtype=torch.int32, device=dev))
+    assert attn.get_error() == attn.ATTN_OK
+    assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
+
+
 def test_decode_malformed_offsets_reported():
     dev = torch.device("cuda", 0)
     q = torch.randn(3, 4, 64, device=dev, dtype=torch.bfloat16)
