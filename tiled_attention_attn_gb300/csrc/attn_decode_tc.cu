@@ -11,8 +11,9 @@
 //   u^T += V^T P^T (M = d = 128, N = the head columns, K = 128 keys)
 // so the tile's keys sit on the 128 TMEM lanes and each softmax thread owns
 // one key: G exponentials per tile instead of 128.  The tile's max over keys
-// is a reduction across threads (shuffles, then four warps through shared
-// memory); the exp-sum is kept per thread and reduced once per unit.  V is
+// is a reduction across threads (redux.sync within a warp, then the four
+// warps through shared memory); the exp-sum is kept per thread and reduced
+// once per unit.  V is
 // the A operand in its natural (keys x d) layout, read MN-major; P^T is
 // written by the softmax threads into shared memory as the K-major B operand.
 //
