@@ -164,3 +164,41 @@ def test_decode_maximum_sequence_count(path, B, d):
     assert attn.get_error() == attn.ATTN_OK
     o_ref, lse_ref = oracle.varlen_cross_attention(q, k, v, [1] * len(lk), lk, causal=False, scale=scale)
     check(o, lse, o_ref, lse_ref)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_merge_of_more_than_32_pieces(d):
+    # one key/value head with eight query heads: one (sequence, head group)
+    # unit, so the cache is cut into as many pieces as there are SMs and the
+    # merge takes them in chunks of 32
+    lk = [65536]
+    q, k, v = make(lk, 8, 1, d, torch.bfloat16, seed=31 + d)
+    dev = torch.device("cuda", 0)
+    scale = d ** -0.5
+    o, lse = attn.attn_decode(q.to(dev), k.to(dev), v.to(dev), cu_of(lk).to(dev), scale=scale)
+    assert attn.get_error() == attn.ATTN_OK
+    o_ref, lse_ref = oracle.varlen_cross_attention(q, k, v, [1], lk, causal=False, scale=scale)
+    check(o, lse, o_ref, lse_ref)
+
+
+@pytest.mark.parametrize("vscale", [1e5, 1e-6])
+@pytest.mark.parametrize("d", [64, 128])
+def test_decode_value_magnitude_through_pieces(d, vscale):
+    # bf16 values scaled by 1e5 or 1e-6 on caches that are cut into pieces
+    # (fp32 partials, then the merge): the result stays finite and as accurate
+    # as unit-normal values, the bar scaled with the values plus half a bf16
+    # ulp of O; lse does not depend on the values
+    lk = [20000, 3, 9000]
+    q, k, v = make(lk, 8, 2, d, torch.bfloat16, seed=41)
+    g = torch.Generator().manual_seed(42)
+    v = (torch.randn(v.shape, generator=g) * vscale).to(torch.bfloat16)
+    dev = torch.device("cuda", 0)
+    scale = d ** -0.5
+    o, lse = attn.attn_decode(q.to(dev), k.to(dev), v.to(dev), cu_of(lk).to(dev), scale=scale)
+    assert attn.get_error() == attn.ATTN_OK
+    o_ref, lse_ref = oracle.varlen_cross_attention(q, k, v, [1] * len(lk), lk, causal=False, scale=scale)
+    on = o.float().cpu().double().numpy()
+    assert np.all(np.isfinite(on)) and np.all(np.isfinite(lse.cpu().numpy()))
+    tol = 1e-2 * vscale + 2.0 ** -8 * np.abs(o_ref)
+    assert np.all(np.abs(on - o_ref) <= tol)
+    assert float(np.abs(lse.cpu().double().numpy() - lse_ref).max()) <= LSE_TOL
